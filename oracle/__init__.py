@@ -1,0 +1,160 @@
+"""CPU oracle for DSA candidate-block selection (ctypes over plain C).
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import this package. The
+product path (``deepseek_sparse_attention_row_gb300``) never imports it and
+shares no code with it.
+
+``dsa_oracle.c`` states the definition each function follows and the
+readings taken where the pages are silent. Every function here is pinned by
+``tests/test_oracle_pins.py`` and ``tests/test_oracle_golden.py``.
+
+``build()`` compiles ``dsa_oracle.c`` with gcc into ``oracle/_build``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dsa_oracle.c")
+_HDR = os.path.join(_HERE, "dsa_oracle.h")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libdsa_oracle.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (portable C, no target-specific flags)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    fresh = (os.path.exists(_LIB_PATH)
+             and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
+                                                    os.path.getmtime(_HDR)))
+    if fresh and not force:
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-Wall", "-Wextra",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def bind(path: str):
+    """Load an oracle library built from ``dsa_oracle.c`` and declare its
+    entry points."""
+    lib = ctypes.CDLL(path)
+    i64, i32, p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    lib.dsa_oracle_block_scores.argtypes = [p, i64, i64, i64, p, p, i32, i32, i32, p, i64]
+    lib.dsa_oracle_select.argtypes = [p, i64, i64, i64, p, p, i32, i32, i32, i32, p, i64, p, i64]
+    lib.dsa_oracle_select_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32, i32, i32,
+                                              p, i64, p, i64]
+    for f in (lib.dsa_oracle_block_scores, lib.dsa_oracle_select,
+              lib.dsa_oracle_select_sharded):
+        f.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = bind(build())
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def _f32(a):
+    a = np.asarray(a, dtype=np.float32)
+    assert a.flags.c_contiguous
+    return a
+
+
+def _i32(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def nblocks(width: int, block_size: int) -> int:
+    return -(-width // block_size)
+
+
+def block_scores(logits: np.ndarray, row_ks, row_ke, block_size: int,
+                 row_repeat: int = 1, pin_newest: bool = True,
+                 width: Optional[int] = None) -> np.ndarray:
+    """Block scores ``[rows, ceil(width / block_size)]`` (fp32).
+
+    ``logits`` is ``[rows, ld]``; ``width`` (default ``ld``) is the logical
+    row length."""
+    logits = _f32(logits)
+    rows, ld = logits.shape
+    width = ld if width is None else width
+    ks, ke = _i32(row_ks), _i32(row_ke)
+    nb = nblocks(width, block_size)
+    scores = np.zeros((rows, nb), dtype=np.float32)
+    rc = _load().dsa_oracle_block_scores(_ptr(logits), rows, width, ld, _ptr(ks), _ptr(ke),
+                                         block_size, row_repeat, int(pin_newest),
+                                         _ptr(scores), nb)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return scores
+
+
+def select(logits: np.ndarray, row_ks, row_ke, topk_blocks: int, block_size: int,
+           row_repeat: int = 1, pin_newest: bool = True,
+           width: Optional[int] = None, want_scores: bool = True):
+    """Ordered candidate ids ``[rows, topk_blocks]`` (int32, -1 padded) and,
+    when ``want_scores``, the block scores they were ranked by."""
+    logits = _f32(logits)
+    rows, ld = logits.shape
+    width = ld if width is None else width
+    ks, ke = _i32(row_ks), _i32(row_ke)
+    nb = nblocks(width, block_size)
+    out = np.full((rows, topk_blocks), -7, dtype=np.int32)
+    scores = np.zeros((rows, nb), dtype=np.float32) if want_scores and nb else None
+    rc = _load().dsa_oracle_select(_ptr(logits), rows, width, ld, _ptr(ks), _ptr(ke),
+                                   topk_blocks, block_size, row_repeat, int(pin_newest),
+                                   _ptr(out), topk_blocks, _ptr(scores), max(nb, 1))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return out, scores
+
+
+def select_sharded(logits: np.ndarray, global_row_ke, global_block_size: int,
+                   max_global_blocks: int, topk_blocks: int, row_repeat: int = 1,
+                   want_scores: bool = True):
+    """Ordered candidate ids for a ``[shards, rows, local_width]`` DCP layout,
+    and the merged global block scores ``[rows, max(max_global_blocks, 1)]``."""
+    logits = _f32(logits)
+    shards, rows, lw = logits.shape
+    gke = _i32(global_row_ke)
+    nbg = max(int(max_global_blocks), 1)
+    out = np.full((rows, topk_blocks), -7, dtype=np.int32)
+    scores = np.zeros((rows, nbg), dtype=np.float32) if want_scores else None
+    rc = _load().dsa_oracle_select_sharded(_ptr(logits), shards, rows, lw, lw, rows * lw,
+                                           _ptr(gke), global_block_size, max_global_blocks,
+                                           row_repeat, topk_blocks, _ptr(out), topk_blocks,
+                                           _ptr(scores), nbg)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return out, scores
+
+
+def run_workload(wl, want_scores: bool = True):
+    """Run the oracle on a ``workloads.Workload`` or ``ShardedWorkload``."""
+    if hasattr(wl, "global_row_ke"):
+        return select_sharded(wl.logits, wl.global_row_ke, wl.global_block_size,
+                              wl.max_global_blocks, wl.topk_blocks, wl.row_repeat,
+                              want_scores=want_scores)
+    return select(wl.logits, wl.row_ks, wl.row_ke, wl.topk_blocks, wl.block_size,
+                  wl.row_repeat, wl.pin_newest, width=wl.width,
+                  want_scores=want_scores)

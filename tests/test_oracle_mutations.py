@@ -1,0 +1,92 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case below plants one mistake in a temporary copy of ``oracle/dsa_oracle.c``
+(the committed source is never touched), builds it with gcc, and runs the
+golden fixtures, the brute-force comparisons and the interleave identity
+against the planted copy. At least one of them has to fail; a mistake that
+passes every pin would mean the pins do not constrain that part of the
+oracle. Only in-bounds mistakes are planted, so a planted copy cannot crash
+the test process.
+"""
+
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_golden as golden
+import test_oracle_pins as pins
+
+MUTATIONS = [
+    ("absolute block origin", "int64_t lo = s + b * bs;", "int64_t lo = b * bs;"),
+    ("pin uses the absolute end", "score[(e - s - 1) / bs] = INFINITY;",
+     "score[(e - 1) / bs] = INFINITY;"),
+    ("NaN ranks lowest", "return a_nan - b_nan;", "return b_nan - a_nan;"),
+    ("-0 ranks above +0", "return b_neg - a_neg;", "return a_neg - b_neg;"),
+    ("ties rank the higher id first", "return (a->id > b->id) - (a->id < b->id);",
+     "return (a->id < b->id) - (a->id > b->id);"),
+    ("-inf blocks are emitted", "int keep = j < k && total_cmp(tmp[j].v, -INFINITY) > 0;",
+     "int keep = j < k;"),
+    ("starts ignored", "int64_t ks = row_ks ? (int64_t)row_ks[g] : 0;", "int64_t ks = 0;"),
+    ("block max drops NaN and ignores the zero sign", "if (total_cmp(x, m) > 0)\n                m = x;",
+     "if (x > m)\n                m = x;"),
+    ("shard end rounds down", "(gke - d + shards - 1) / shards", "(gke - d) / shards"),
+    ("global pin off by one", "pin = floor_div(gke - 1, global_block_size);",
+     "pin = floor_div(gke, global_block_size);"),
+    ("rows without context keep the pin", "if (gke <= 0)\n            for (b = 0; b < nbg; ++b)",
+     "if (gke < 0)\n            for (b = 0; b < nbg; ++b)"),
+    ("shard merge takes the min", "if (total_cmp(local_score[b], global_score[b]) > 0)",
+     "if (total_cmp(local_score[b], global_score[b]) < 0)"),
+    ("canonical NaN not written", "uint32_t bits = 0x7FC00000u;", "uint32_t bits = 0x7FC00001u;"),
+]
+
+
+def _battery() -> list:
+    """Run the pins against the currently bound oracle; return what failed."""
+    failed = []
+    for p in golden._cases():
+        case = p.values[0]
+        try:
+            golden.test_golden_case(case)
+        except AssertionError:
+            failed.append("golden:" + p.id)
+    for seed in range(25):
+        try:
+            pins.test_unsharded_matches_brute_force(seed)
+        except AssertionError:
+            failed.append(f"brute-unsharded:{seed}")
+        try:
+            pins.test_sharded_matches_brute_force(seed)
+        except AssertionError:
+            failed.append(f"brute-sharded:{seed}")
+    try:
+        pins.test_sharded_equals_unsharded_on_global_rows(4, 1, 9, 64, 2)
+    except AssertionError:
+        failed.append("interleave-identity")
+    return failed
+
+
+def test_unplanted_oracle_passes_battery():
+    assert _battery() == []
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(name, old, new, tmp_path):
+    with open(oracle._SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+    mutant_c = tmp_path / "dsa_oracle.c"
+    mutant_c.write_text(src.replace(old, new))
+    (tmp_path / "dsa_oracle.h").write_text(open(oracle._HDR).read())
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-o", str(so),
+                    str(mutant_c), "-lm"], check=True)
+    saved = oracle._lib
+    oracle._lib = oracle.bind(str(so))
+    try:
+        failed = _battery()
+    finally:
+        oracle._lib = saved
+    assert failed, f"planted mistake '{name}' passed every pin"

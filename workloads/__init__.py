@@ -1,0 +1,300 @@
+"""Seeded synthetic inputs for DSA candidate-block selection.
+
+This module only draws inputs. It holds none of the selection arithmetic
+(no windowing, block maxima, pins, shard ends or top-k): both the CPU oracle
+and the CUDA path receive exactly the arrays built here.
+
+Every workload follows the shapes, value distributions and structure of the
+indexer-logit rows that candidate selection consumes on the page
+"launcher/dcp2/diffs/02-model_executor_kernels_attention_dsa_candidate_blocks.py.diff"
+(``select_candidate_blocks`` / ``_select_candidate_blocks_impl``): fp32 logits
+in packed column space, int32 per-group ``row_ks`` / ``row_ke`` bounds shared by
+``row_repeat`` rows, and for the DCP form an interleave-1 shard layout
+(global token t lives on shard t % D at local column t // D, as in the
+SGLang ``dcp/kernels.py`` page, ``create_triton_kv_indices_for_dcp_triton``).
+
+Generators use ``numpy.random.Generator(PCG64(seed))``. Nothing here needs a
+GPU; arrays are C-contiguous numpy arrays.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+__all__ = [
+    "Workload",
+    "ShardedWorkload",
+    "CONFIG_NAMES",
+    "make",
+    "make_tiny",
+    "make_decode",
+    "make_prefill",
+    "make_long",
+    "make_dcp",
+    "round_to_bf16_grid",
+    "random_nan_bits",
+    "small_unsharded",
+    "small_sharded",
+]
+
+
+@dataclasses.dataclass
+class Workload:
+    """One unsharded selection problem.
+
+    ``logits`` is ``[rows, width]`` fp32. ``row_ks`` (or None) and ``row_ke`` are
+    int32 of length ``ceil(rows / row_repeat)``.
+    """
+
+    name: str
+    logits: np.ndarray
+    row_ks: Optional[np.ndarray]
+    row_ke: np.ndarray
+    block_size: int
+    topk_blocks: int
+    row_repeat: int
+    pin_newest: bool
+    seed: int
+    notes: dict = dataclasses.field(default_factory=dict)
+    logical_width: Optional[int] = None
+
+    @property
+    def rows(self) -> int:
+        return int(self.logits.shape[0])
+
+    @property
+    def width(self) -> int:
+        """Logical row length; rows may be padded up to ``logits.shape[1]``."""
+        if self.logical_width is not None:
+            return int(self.logical_width)
+        return int(self.logits.shape[1])
+
+
+@dataclasses.dataclass
+class ShardedWorkload:
+    """One selection problem held as D interleave-1 shards on one device.
+
+    ``logits`` is ``[D, rows, local_width]`` fp32; ``global_row_ke`` is int32 of
+    length ``ceil(rows / row_repeat)``.
+    """
+
+    name: str
+    logits: np.ndarray
+    global_row_ke: np.ndarray
+    global_block_size: int
+    max_global_blocks: int
+    topk_blocks: int
+    row_repeat: int
+    seed: int
+    notes: dict = dataclasses.field(default_factory=dict)
+
+    @property
+    def shards(self) -> int:
+        return int(self.logits.shape[0])
+
+    @property
+    def rows(self) -> int:
+        return int(self.logits.shape[1])
+
+    @property
+    def local_width(self) -> int:
+        return int(self.logits.shape[2])
+
+
+def _rng(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def round_to_bf16_grid(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to the nearest bf16-representable value (ties to even).
+
+    Works on the bit pattern: add 0x7FFF plus the lowest kept bit, then clear
+    the low 16 bits. Inputs must be finite (normal draws are).
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = (u + np.uint32(0x7FFF) + lsb) & np.uint32(0xFFFF0000)
+    return r.view(np.float32)
+
+
+def random_nan_bits(rng: np.random.Generator, n: int) -> np.ndarray:
+    """``n`` quiet NaNs with random sign and random payload, as fp32."""
+    sign = rng.integers(0, 2, size=n, dtype=np.uint32) << np.uint32(31)
+    payload = rng.integers(0, 1 << 22, size=n, dtype=np.uint32)
+    bits = sign | np.uint32(0x7FC00000) | payload
+    return bits.view(np.float32)
+
+
+# --------------------------------------------------------------------------
+# The five workloads
+# --------------------------------------------------------------------------
+
+CONFIG_NAMES = ("tiny", "decode", "prefill", "long", "long_pin", "dcp")
+
+
+def make_tiny(seed: int = 0) -> Workload:
+    """[64, 4096] N(0,1); no starts; ends uniform in [0, 4096] with one 0 and
+    one 4096 forced; block 64, top-16, pinned."""
+    rng = _rng(seed)
+    rows, width = 64, 4096
+    logits = rng.standard_normal((rows, width), dtype=np.float32)
+    ke = rng.integers(0, width, size=rows, endpoint=True).astype(np.int32)
+    ke[0] = 0
+    ke[1] = width
+    return Workload("tiny", logits, None, ke, 64, 16, 1, True, seed)
+
+
+def make_decode(seed: int = 1) -> Workload:
+    """64 sequences x 8 heads = 512 rows of [65536] N(0,1) on the bf16 grid
+    (forces ties); per-sequence ends uniform in [1, 65536]; no starts;
+    block 64, top-32, pinned, row_repeat 8."""
+    rng = _rng(seed)
+    seqs, heads, width = 64, 8, 65536
+    rows = seqs * heads
+    logits = round_to_bf16_grid(rng.standard_normal((rows, width), dtype=np.float32))
+    ke = rng.integers(1, width, size=seqs, endpoint=True).astype(np.int32)
+    return Workload("decode", logits, None, ke, 64, 32, heads, True, seed)
+
+
+def make_prefill(seed: int = 2, *, requests: int = 4, tokens: int = 2048,
+                 max_prefix: int = 6144, width: int = 16384,
+                 nan_fraction: float = 1e-6, sigma: float = 2.0) -> Workload:
+    """A packed multi-request prefill chunk.
+
+    ``requests`` requests of ``tokens`` query tokens each; request q has a
+    cached prefix p_q uniform in [0, max_prefix] and occupies packed columns
+    [off_q, off_q + p_q + tokens), requests back to back. Row (q, i) has
+    ks = off_q and ke = off_q + p_q + i + 1 (causal). Logits ~ N(0, sigma)
+    (sigma is the standard deviation) with round(nan_fraction * rows * width)
+    NaNs of random sign and payload at distinct uniform positions.
+
+    The four prefixes can need more than ``width`` columns; all four are
+    redrawn until they fit.
+    """
+    rng = _rng(seed)
+    rows = requests * tokens
+    draws = 0
+    while True:
+        draws += 1
+        prefix = rng.integers(0, max_prefix, size=requests, endpoint=True)
+        if int(np.sum(prefix + tokens)) <= width:
+            break
+    offsets = np.concatenate([[0], np.cumsum(prefix + tokens)[:-1]])
+    ks = np.repeat(offsets, tokens).astype(np.int32)
+    tok = np.tile(np.arange(tokens), requests)
+    ke = (np.repeat(offsets + prefix, tokens) + tok + 1).astype(np.int32)
+    logits = rng.standard_normal((rows, width), dtype=np.float32)
+    logits *= np.float32(sigma)
+    n_nan = int(round(nan_fraction * rows * width))
+    pos = rng.choice(rows * width, size=n_nan, replace=False)
+    logits.reshape(-1)[pos] = random_nan_bits(rng, n_nan)
+    notes = {"prefixes": [int(p) for p in prefix], "offsets": [int(o) for o in offsets],
+             "prefix_draws": draws, "nan_count": n_nan}
+    return Workload("prefill", logits, ks, ke, 64, 32, 1, True, seed, notes)
+
+
+def make_long(seed: int = 3, *, pin_newest: bool = False, rows: int = 1024,
+              width: int = 131072, spikes: int = 64) -> Workload:
+    """[1024, 131072] N(0,1) plus, per row, ``spikes`` distinct in-window
+    columns raised by U(3, 6); ends uniform in [65536, 131072], starts uniform
+    in [0, 4096]; block 128, top-16."""
+    rng = _rng(seed)
+    logits = rng.standard_normal((rows, width), dtype=np.float32)
+    ke = rng.integers(width // 2, width, size=rows, endpoint=True).astype(np.int32)
+    ks = rng.integers(0, 4096, size=rows, endpoint=True).astype(np.int32)
+    for r in range(rows):
+        span = int(ke[r]) - int(ks[r])
+        cols = int(ks[r]) + rng.choice(span, size=min(spikes, span), replace=False)
+        logits[r, cols] += rng.uniform(3.0, 6.0, size=cols.size).astype(np.float32)
+    name = "long_pin" if pin_newest else "long"
+    return Workload(name, logits, ks, ke, 128, 16, 1, pin_newest, seed)
+
+
+def make_dcp(seed: int = 4, *, shards: int = 8, rows: int = 4096,
+             global_width: int = 65536, global_block_size: int = 64,
+             max_global_blocks: int = 1024, topk_blocks: int = 32) -> ShardedWorkload:
+    """Simulated DCP layout: a global [rows, global_width] N(0,1) matrix G is
+    dealt over ``shards`` interleave-1 shards, L[d, r, c] = G[r, shards*c + d];
+    global ends uniform in [1, global_width]."""
+    rng = _rng(seed)
+    g = rng.standard_normal((rows, global_width), dtype=np.float32)
+    lw = global_width // shards
+    local = np.ascontiguousarray(g.reshape(rows, lw, shards).transpose(2, 0, 1))
+    del g
+    gke = rng.integers(1, global_width, size=rows, endpoint=True).astype(np.int32)
+    return ShardedWorkload("dcp", local, gke, global_block_size, max_global_blocks,
+                           topk_blocks, 1, seed)
+
+
+def make(name: str):
+    """Build one named workload at full size."""
+    if name == "tiny":
+        return make_tiny()
+    if name == "decode":
+        return make_decode()
+    if name == "prefill":
+        return make_prefill()
+    if name == "long":
+        return make_long(pin_newest=False)
+    if name == "long_pin":
+        return make_long(pin_newest=True)
+    if name == "dcp":
+        return make_dcp()
+    raise KeyError(name)
+
+
+# --------------------------------------------------------------------------
+# Small randomized problems for parity sweeps and edge cases
+# --------------------------------------------------------------------------
+
+def small_unsharded(seed: int, *, rows: int, width: int, block_size: int,
+                    topk_blocks: int, row_repeat: int = 1, starts: bool = True,
+                    pin_newest: bool = True, nan_count: int = 0,
+                    bf16_grid: bool = False, wild_bounds: bool = False,
+                    ld: Optional[int] = None) -> Workload:
+    """A random unsharded problem. ``wild_bounds`` draws bounds outside
+    [0, width] and starts above ends too. ``ld`` > width pads each row (the
+    pad holds large values that must never be read)."""
+    rng = _rng(seed)
+    groups = -(-rows // row_repeat) if rows else 0
+    ld = width if ld is None else ld
+    buf = rng.standard_normal((rows, ld), dtype=np.float32)
+    if bf16_grid:
+        buf = round_to_bf16_grid(buf)
+    if ld > width:
+        buf[:, width:] = np.float32(1e30)
+    if nan_count and rows and width:
+        pos = rng.choice(rows * width, size=min(nan_count, rows * width), replace=False)
+        buf[pos // width, pos % width] = random_nan_bits(rng, pos.size)
+    if wild_bounds:
+        ke = rng.integers(-3, width + 8, size=groups, endpoint=True).astype(np.int32)
+        ks = rng.integers(-5, width + 4, size=groups, endpoint=True).astype(np.int32)
+    else:
+        ke = rng.integers(0, width, size=groups, endpoint=True).astype(np.int32)
+        ks = np.minimum(rng.integers(0, max(width, 1), size=groups, endpoint=True),
+                        ke).astype(np.int32)
+    return Workload("small", buf, ks if starts else None, ke, block_size,
+                    topk_blocks, row_repeat, pin_newest, seed, {"ld": ld}, width)
+
+
+def small_sharded(seed: int, *, shards: int, rows: int, global_width: int,
+                  global_block_size: int, max_global_blocks: int,
+                  topk_blocks: int, row_repeat: int = 1,
+                  wild_bounds: bool = False) -> tuple[ShardedWorkload, np.ndarray]:
+    """A random sharded problem plus its global matrix G (so that tests can
+    compare against the unsharded form). ``global_width`` must be a multiple
+    of ``shards``."""
+    rng = _rng(seed)
+    assert global_width % shards == 0
+    g = rng.standard_normal((rows, global_width), dtype=np.float32)
+    lw = global_width // shards
+    local = np.ascontiguousarray(g.reshape(rows, lw, shards).transpose(2, 0, 1))
+    groups = -(-rows // row_repeat) if rows else 0
+    lo, hi = (-4, global_width + 40) if wild_bounds else (0, global_width)
+    gke = rng.integers(lo, hi, size=groups, endpoint=True).astype(np.int32)
+    wl = ShardedWorkload("small_sharded", local, gke, global_block_size,
+                         max_global_blocks, topk_blocks, row_repeat, seed)
+    return wl, g
