@@ -1,0 +1,523 @@
+#!/usr/bin/env python3
+"""Throughput of DSA candidate-block selection on GB300.
+
+One step = one call of the selection over one batch of synthetic rows with
+the inputs resident in HBM. The default workload is the simulated DCP layout
+(8 interleave-1 shards of a [4096, 65536] fp32 indexer-logit matrix, global
+block 64, 1024 global blocks, top-32): the largest configuration, and the
+one whose call covers every step of the path (window, block max, shard
+merge, pin, top-k, -1 store).
+
+Metric: algorithmic logits GB/s = (in-window logit bytes + bound bytes read +
+id bytes written) / time, with rows/s beside it. Window bytes only: the
+columns outside each row's window are never read and are not counted.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference]
+
+Prints one JSON line on rank 0. For N > 1 launch one process per GPU with
+torch.distributed.run; every rank runs the same workload on its own GPU
+(weak scaling, no data-path collective) and the slowest rank's time counts.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "candidate-select logits GB/s (% of GB300 HBM peak) and rows/s"
+UNIT = "GB/s"
+L2_BYTES = 129 * 1000 * 1000
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("deepseek_sparse_attention_row_gb300/csrc/dsa_cb.cu",
+                  "deepseek_sparse_attention_row_gb300/csrc/stream.cuh",
+                  "deepseek_sparse_attention_row_gb300/csrc/topk.cuh",
+                  "deepseek_sparse_attention_row_gb300/csrc/keys.cuh")
+
+
+# ---------------------------------------------------------------------------
+# Workload bookkeeping (host only)
+# ---------------------------------------------------------------------------
+
+def window_elements(wl) -> int:
+    """Number of in-window logits the selection must read."""
+    import numpy as np
+
+    if hasattr(wl, "global_row_ke"):
+        rows = wl.rows
+        g = np.repeat(wl.global_row_ke.astype(np.int64), wl.row_repeat)[:rows]
+        # shard d reads min(ceil((gke - d) / D), lw) columns
+        total = 0
+        for d in range(wl.shards):
+            lke = np.where(g > d, (g - d + wl.shards - 1) // wl.shards, 0)
+            total += int(np.minimum(lke, wl.local_width).sum())
+        return total
+    rows, width = wl.rows, wl.width
+    ke = np.repeat(wl.row_ke.astype(np.int64), wl.row_repeat)[:rows]
+    ks = (np.zeros(rows, np.int64) if wl.row_ks is None
+          else np.repeat(wl.row_ks.astype(np.int64), wl.row_repeat)[:rows])
+    e = np.minimum(ke, width)
+    s = np.minimum(np.maximum(ks, 0), e)
+    return int((e - s).sum())
+
+
+def algorithmic_bytes(wl) -> int:
+    """Bytes one call must move: in-window fp32 logits, the int32 bounds it
+    reads, the int32 ids it writes."""
+    bounds = wl.global_row_ke.size if hasattr(wl, "global_row_ke") else (
+        wl.row_ke.size + (0 if wl.row_ks is None else wl.row_ks.size))
+    return 4 * window_elements(wl) + 4 * bounds + 4 * wl.rows * wl.topk_blocks
+
+
+def workload_config(wl, name: str) -> dict:
+    if hasattr(wl, "global_row_ke"):
+        cfg = {"workload": f"dcp-sim D={wl.shards} [{wl.shards},{wl.rows},{wl.local_width}] fp32",
+               "shards": wl.shards, "rows": wl.rows, "local_width": wl.local_width,
+               "global_width": wl.shards * wl.local_width,
+               "global_block_size": wl.global_block_size,
+               "max_global_blocks": wl.max_global_blocks}
+    else:
+        cfg = {"workload": f"{name} [{wl.rows},{wl.width}] fp32", "rows": wl.rows,
+               "width": wl.width, "block_size": wl.block_size,
+               "pin_newest": bool(wl.pin_newest), "starts": wl.row_ks is not None}
+    cfg.update({"topk_blocks": wl.topk_blocks, "row_repeat": wl.row_repeat, "seed": wl.seed,
+                "window_bytes": 4 * window_elements(wl)})
+    if wl.notes:
+        cfg["notes"] = wl.notes
+    return cfg
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """Per-launch DRAM bytes of the top kernel from the committed ncu summary,
+    if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel_sources") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# Multi-rank plumbing (also exercised on CPU with gloo by the tests)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def dist_max(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Every rank processes the same units; the slowest rank's time counts."""
+    return units_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_QUERY = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (read only)."""
+
+    def __init__(self, uuid: str, period_ms: int = 100):
+        self.cmd = ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
+                    f"-lms={period_ms}"]
+        self.uuid = uuid.lower().replace("gpu-", "")
+        self.proc = None
+        self.text = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.text = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.text, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.text, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = [[c.strip() for c in r] for r in csv.reader(io.StringIO(self.text)) if len(r) >= 10]
+        mine = [r for r in rows if self.uuid and self.uuid in r[1].lower()]
+        if not mine and len({r[0] for r in rows}) == 1:
+            mine = rows
+        sm, mx, reasons = [], [], set()
+        for r in mine:
+            try:
+                sm.append(float(r[2]))
+                mx.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(REASONS, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def make_runner(wl, dsa, torch, device):
+    """Device-resident inputs and one-call step function."""
+    if hasattr(wl, "global_row_ke"):
+        logits = torch.from_numpy(wl.logits).to(device)
+        gke = torch.from_numpy(wl.global_row_ke).to(device)
+        out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)
+
+        def step():
+            dsa.dsa_select_candidate_blocks_sharded(logits, gke, wl.global_block_size,
+                                                    wl.max_global_blocks, wl.topk_blocks, out,
+                                                    wl.row_repeat)
+        return step, out
+    logits = torch.from_numpy(wl.logits).to(device)
+    ks = None if wl.row_ks is None else torch.from_numpy(wl.row_ks).to(device)
+    ke = torch.from_numpy(wl.row_ke).to(device)
+    out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)
+
+    def step():
+        dsa.dsa_select_candidate_blocks(logits, ks, ke, wl.topk_blocks, wl.block_size, out,
+                                        wl.row_repeat, wl.pin_newest)
+    return step, out
+
+
+def e2e_measure(wl, dsa, torch, device, steps: int):
+    """Same metric through the host-buffer API: pinned host inputs copied in
+    and ids copied out inside every timed step."""
+    sharded = hasattr(wl, "global_row_ke")
+    h_logits = torch.from_numpy(wl.logits).pin_memory()
+    h_out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32).pin_memory()
+    bufs = {"logits": torch.empty(h_logits.shape, dtype=torch.float32, device=device),
+            "out": torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)}
+    if sharded:
+        h_b = [torch.from_numpy(wl.global_row_ke).pin_memory()]
+        bufs["global_row_ke"] = torch.empty(h_b[0].shape, dtype=torch.int32, device=device)
+
+        def call():
+            dsa.select_candidate_blocks_sharded_host(h_logits, h_b[0], wl.global_block_size,
+                                                     wl.max_global_blocks, wl.topk_blocks,
+                                                     wl.row_repeat, out=h_out,
+                                                     device_buffers=bufs)
+    else:
+        h_b = [None if wl.row_ks is None else torch.from_numpy(wl.row_ks).pin_memory(),
+               torch.from_numpy(wl.row_ke).pin_memory()]
+        if h_b[0] is not None:
+            bufs["row_ks"] = torch.empty(h_b[0].shape, dtype=torch.int32, device=device)
+        bufs["row_ke"] = torch.empty(h_b[1].shape, dtype=torch.int32, device=device)
+
+        def call():
+            dsa.select_candidate_blocks_host(h_logits, h_b[0], h_b[1], wl.topk_blocks,
+                                             wl.block_size, wl.row_repeat, wl.pin_newest,
+                                             out=h_out, device_buffers=bufs)
+    h2d = h_logits.numel() * 4 + sum(b.numel() * 4 for b in h_b if b is not None)
+    d2h = h_out.numel() * 4
+    call()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        call()
+    torch.cuda.synchronize()
+    sec = (time.perf_counter() - t0) / steps
+    return sec, h2d, d2h
+
+
+def oracle_cpu_baseline(wl, budget_s: float = 10.0):
+    """The oracle as it stands, single-threaded on a host core, repeated over
+    the whole workload until about budget_s seconds have passed."""
+    import oracle
+
+    oracle.build()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.run_workload(wl, want_scores=False)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return el / reps, reps
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import workloads
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    __graft_entry__.build()
+    import deepseek_sparse_attention_row_gb300 as dsa
+
+    wl = workloads.make(args.workload)
+    step, out = make_runner(wl, dsa, torch, device)
+    nbytes = algorithmic_bytes(wl)
+    window_bytes = 4 * window_elements(wl)
+    flush = window_bytes < 2 * L2_BYTES
+    scratch = torch.empty(256 * 1000 * 1000 // 4, dtype=torch.float32, device=device) if flush \
+        else None
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    props = torch.cuda.get_device_properties(device)
+    uuid = str(getattr(props, "uuid", "") or "")
+
+    with ClockSampler(uuid) as sampler:
+        dist_barrier(world)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        if flush:
+            # L2 flushed before every step; each step timed on its own.
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for a, b in evs:
+                scratch.fill_(1.0)
+                a.record(stream)
+                step()
+                b.record(stream)
+            torch.cuda.synchronize()
+            gpu_ms = sum(a.elapsed_time(b) for a, b in evs)
+        else:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                step()
+            b.record(stream)
+            torch.cuda.synchronize()
+            gpu_ms = a.elapsed_time(b)
+        dist_barrier(world)
+        wall_s = time.perf_counter() - t_wall
+    clocks = sampler.summary()
+
+    max_ms = dist_max(gpu_ms, world, device)
+    ms_per_step = max_ms / args.steps
+    value = whole_job_rate(nbytes * args.steps, world, max_ms / 1e3) / 1e9
+    rows_per_s = whole_job_rate(wl.rows * args.steps, world, max_ms / 1e3)
+    launch_s = (gpu_ms / args.steps) / 1e3
+    achieved = nbytes / launch_s / 1e9
+    peak, peak_src = measured_peak()
+
+    e2e = None
+    cpu = None
+    if rank == 0 and not args.no_e2e:
+        sec, h2d, d2h = e2e_measure(wl, dsa, torch, device, args.e2e_steps)
+        e2e = {"value": round(nbytes / sec / 1e9 * world, 3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(sec * 1e3, 4), "steps": args.e2e_steps}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sec, reps = oracle_cpu_baseline(wl, args.cpu_budget)
+        cpu = {"value": round(nbytes / sec / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"the whole {args.workload} workload, {reps} pass(es), single-threaded "
+                         f"C oracle, {sec:.3f} s per pass"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded numpy PCG64; shapes and distributions of the workload)",
+            "config": {**workload_config(wl, args.workload),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": ("flushed before every step (256 MB write)" if flush else
+                              "inputs larger than L2 (window bytes per step > 2 x 129 MB)")},
+            "rows_per_s": round(rows_per_s, 1),
+            "algorithmic_bytes_per_step": nbytes,
+            "full_tensor_equivalent_gbs": round(
+                whole_job_rate(wl.logits.nbytes * args.steps, world, max_ms / 1e3) / 1e9, 3),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 3), "peak": peak,
+                         "unit": UNIT, "frac": round(achieved / peak, 4),
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_src == "measured" else "fallback 6.8 TB/s",
+                         "traffic": profiled_traffic(args.workload),
+                         "kernel": "select_kernel (one launch per step)"},
+            "clocks": clocks,
+            "gpu_launches": args.steps,
+            "wall_s_timed_region": round(wall_s, 3),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    oracle.build()
+    wl = workloads.make(args.workload)
+    full_bytes = algorithmic_bytes(wl)
+    # Calibrate on a slice of rows, then size each step's sample so that the
+    # whole run stays within about args.ref_budget seconds.
+    rows = wl.rows
+    probe = max(1, rows // 64)
+    sub = _row_slice(wl, 0, probe)
+    t0 = time.perf_counter()
+    oracle.run_workload(sub, want_scores=False)
+    per_row = max((time.perf_counter() - t0) / probe, 1e-7)
+    total_steps = args.steps + args.warmup
+    sample_rows = int(max(1, min(rows, args.ref_budget / total_steps / per_row)))
+    sample = _row_slice(wl, 0, sample_rows)
+    sample_bytes = algorithmic_bytes(sample)
+    for _ in range(args.warmup):
+        oracle.run_workload(sample, want_scores=False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run_workload(sample, want_scores=False)
+    sec = (time.perf_counter() - t0) / args.steps
+    value = sample_bytes / sec / 1e9
+    desc = (f"first {sample_rows} of {rows} rows of the {args.workload} workload per step "
+            f"({sample_bytes} algorithmic bytes; full step {full_bytes})")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy PCG64; shapes and distributions of the workload)",
+        "config": {**workload_config(wl, args.workload), "parallelism": "host, 1 thread"},
+        "rows_per_s": round(sample_rows / sec, 1),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _row_slice(wl, r0: int, r1: int):
+    """The same workload restricted to rows [r0, r1) (r0 a multiple of
+    row_repeat)."""
+    import copy
+
+    import numpy as np
+
+    assert r0 % wl.row_repeat == 0
+    g0, g1 = r0 // wl.row_repeat, -(-r1 // wl.row_repeat)
+    s = copy.copy(wl)
+    if hasattr(wl, "global_row_ke"):
+        s.logits = np.ascontiguousarray(wl.logits[:, r0:r1])
+        s.global_row_ke = wl.global_row_ke[g0:g1].copy()
+    else:
+        s.logits = wl.logits[r0:r1]
+        s.row_ke = wl.row_ke[g0:g1].copy()
+        s.row_ks = None if wl.row_ks is None else wl.row_ks[g0:g1].copy()
+    return s
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="dcp",
+                   choices=("dcp", "decode", "prefill", "long", "long_pin", "tiny"))
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget", type=float, default=10.0)
+    p.add_argument("--ref-budget", type=float, default=90.0)
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    _, world, _ = dist_env()
+    if args.gpus > 1 and world == 1 and args.impl == "ours":
+        p.error("--gpus N > 1 needs torch.distributed.run with N processes")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

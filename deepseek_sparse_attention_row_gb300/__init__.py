@@ -1,0 +1,252 @@
+"""GB300 (sm_103a) DSA candidate-block selection.
+
+A thin binding over ``libdsa_cb.so`` (C ABI declared in ``include/dsa_cb.h``):
+argument marshalling only. Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback, and every call
+raises if the library is missing or a call fails.
+
+Functions carry the C ABI's names:
+
+* ``dsa_block_scores`` -- per-block windowed maxima (candidate_blocks.py diff,
+  ``_block_scores``).
+* ``dsa_select_candidate_blocks`` -- ranked top-k block ids, -1 padded
+  (``select_candidate_blocks`` without a DCP group).
+* ``dsa_select_candidate_blocks_sharded`` -- the DCP form with the ranks'
+  local logits held as a leading ``[D, rows, local_width]`` axis.
+
+Tensors are PyTorch CUDA tensors (PyTorch supplies device memory and the
+current stream). ``select_candidate_blocks_host`` accepts host tensors and
+moves them through the device around one call.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = [
+    "DsaError",
+    "library",
+    "library_path",
+    "dsa_block_scores",
+    "dsa_select_candidate_blocks",
+    "dsa_select_candidate_blocks_sharded",
+    "select_candidate_blocks_host",
+    "select_candidate_blocks_sharded_host",
+    "max_select_blocks",
+    "EXPORTED_SYMBOLS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "_build", "libdsa_cb.so")
+
+EXPORTED_SYMBOLS = (
+    "dsa_status_string",
+    "dsa_select_max_blocks",
+    "dsa_select_max_shards",
+    "dsa_block_scores",
+    "dsa_select_candidate_blocks",
+    "dsa_select_candidate_blocks_sharded",
+)
+
+_lib = None
+
+
+class DsaError(RuntimeError):
+    """A library call returned a status other than DSA_OK."""
+
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: {text} (status {status})")
+        self.status = status
+
+
+def library():
+    """Load libdsa_cb.so (build it with ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise RuntimeError(f"libdsa_cb.so is not built ({library_path}); "
+                           "run __graft_entry__.build() first")
+    lib = ctypes.CDLL(library_path)
+    i64, i32, p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    lib.dsa_status_string.argtypes = [ctypes.c_int]
+    lib.dsa_status_string.restype = ctypes.c_char_p
+    lib.dsa_select_max_blocks.argtypes = []
+    lib.dsa_select_max_blocks.restype = i32
+    lib.dsa_select_max_shards.argtypes = []
+    lib.dsa_select_max_shards.restype = i32
+    lib.dsa_block_scores.argtypes = [p, i64, i64, i64, p, p, i32, i32, i32, p, i64, p]
+    lib.dsa_select_candidate_blocks.argtypes = [p, i64, i64, i64, p, p, i32, i32, i32, i32,
+                                                p, i64, p, i64, p]
+    lib.dsa_select_candidate_blocks_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32,
+                                                        i32, i32, p, i64, p, i64, p]
+    for f in (lib.dsa_block_scores, lib.dsa_select_candidate_blocks,
+              lib.dsa_select_candidate_blocks_sharded):
+        f.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise DsaError(fn, status, library().dsa_status_string(status).decode())
+
+
+def max_select_blocks() -> int:
+    return int(library().dsa_select_max_blocks())
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream) -> Optional[int]:
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream or None
+
+
+def _dev_ptr(t, dtype, name, *, allow_none=False):
+    torch = _torch()
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr() or None
+
+
+def _row_major(t, name):
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name} must have unit stride in its last dimension")
+    return t.stride(-2) if t.dim() >= 2 else t.shape[-1]
+
+
+def dsa_block_scores(logits, row_ks, row_ke, block_size: int, row_repeat: int = 1,
+                     pin_newest: bool = True, scores_out=None, stream=None):
+    """Block scores ``[rows, ceil(width / block_size)]`` fp32 (returned)."""
+    torch = _torch()
+    rows, width = logits.shape
+    nb = -(-width // block_size) if block_size > 0 else 0
+    if scores_out is None:
+        scores_out = torch.empty((rows, nb), dtype=torch.float32, device=logits.device)
+    st = library().dsa_block_scores(
+        _dev_ptr(logits, torch.float32, "logits"), rows, width, _row_major(logits, "logits"),
+        _dev_ptr(row_ks, torch.int32, "row_ks", allow_none=True),
+        _dev_ptr(row_ke, torch.int32, "row_ke"), block_size, row_repeat, int(bool(pin_newest)),
+        _dev_ptr(scores_out, torch.float32, "scores_out"),
+        _row_major(scores_out, "scores_out") if scores_out.numel() else nb,
+        _stream_handle(stream))
+    _check("dsa_block_scores", st)
+    return scores_out
+
+
+def dsa_select_candidate_blocks(logits, row_ks, row_ke, topk_blocks: int, block_size: int,
+                                out, row_repeat: int = 1, pin_newest: bool = True,
+                                scores_out=None, stream=None):
+    """Write ranked candidate block ids (-1 padded) into ``out`` [rows, >=topk]
+    int32; optionally the ranked block scores into ``scores_out``."""
+    torch = _torch()
+    rows, width = logits.shape
+    st = library().dsa_select_candidate_blocks(
+        _dev_ptr(logits, torch.float32, "logits"), rows, width, _row_major(logits, "logits"),
+        _dev_ptr(row_ks, torch.int32, "row_ks", allow_none=True),
+        _dev_ptr(row_ke, torch.int32, "row_ke"), topk_blocks, block_size, row_repeat,
+        int(bool(pin_newest)), _dev_ptr(out, torch.int32, "out"),
+        _row_major(out, "out") if out.dim() == 2 else topk_blocks,
+        _dev_ptr(scores_out, torch.float32, "scores_out", allow_none=True),
+        _row_major(scores_out, "scores_out") if scores_out is not None else 0,
+        _stream_handle(stream))
+    _check("dsa_select_candidate_blocks", st)
+    return out
+
+
+def dsa_select_candidate_blocks_sharded(logits, global_row_ke, global_block_size: int,
+                                        max_global_blocks: int, topk_blocks: int, out,
+                                        row_repeat: int = 1, scores_out=None, stream=None):
+    """DCP form: ``logits`` is ``[D, rows, local_width]`` (unit stride in the last
+    dimension); writes ranked global block ids into ``out``."""
+    torch = _torch()
+    shards, rows, lw = logits.shape
+    if logits.stride(2) != 1:
+        raise ValueError("logits must have unit stride in its last dimension")
+    st = library().dsa_select_candidate_blocks_sharded(
+        _dev_ptr(logits, torch.float32, "logits"), shards, rows, lw, logits.stride(1),
+        logits.stride(0), _dev_ptr(global_row_ke, torch.int32, "global_row_ke"),
+        global_block_size, max_global_blocks, row_repeat, topk_blocks,
+        _dev_ptr(out, torch.int32, "out"), _row_major(out, "out") if out.dim() == 2 else topk_blocks,
+        _dev_ptr(scores_out, torch.float32, "scores_out", allow_none=True),
+        _row_major(scores_out, "scores_out") if scores_out is not None else 0,
+        _stream_handle(stream))
+    _check("dsa_select_candidate_blocks_sharded", st)
+    return out
+
+
+def _to_device(host, dev_buf, stream):
+    torch = _torch()
+    if host is None:
+        return None
+    if dev_buf is None:
+        dev_buf = torch.empty(host.shape, dtype=host.dtype, device="cuda")
+    with torch.cuda.stream(stream):
+        dev_buf.copy_(host, non_blocking=True)
+    return dev_buf
+
+
+def select_candidate_blocks_host(logits, row_ks, row_ke, topk_blocks: int, block_size: int,
+                                 row_repeat: int = 1, pin_newest: bool = True, *,
+                                 out=None, device_buffers: Optional[dict] = None, stream=None):
+    """Host-memory form of ``dsa_select_candidate_blocks``: copies the host
+    (ideally pinned) inputs to the device, selects, and copies the ids back
+    into host tensor ``out`` (allocated when None). ``device_buffers`` may hold
+    preallocated device tensors under 'logits', 'row_ks', 'row_ke', 'out' so
+    that repeated calls allocate nothing. Waits for the result."""
+    torch = _torch()
+    stream = torch.cuda.current_stream() if stream is None else stream
+    db = device_buffers if device_buffers is not None else {}
+    d_logits = _to_device(logits, db.get("logits"), stream)
+    d_ks = _to_device(row_ks, db.get("row_ks"), stream)
+    d_ke = _to_device(row_ke, db.get("row_ke"), stream)
+    rows = logits.shape[0]
+    d_out = db.get("out")
+    if d_out is None:
+        d_out = torch.empty((rows, topk_blocks), dtype=torch.int32, device="cuda")
+    dsa_select_candidate_blocks(d_logits, d_ks, d_ke, topk_blocks, block_size, d_out,
+                                row_repeat, pin_newest, stream=stream)
+    if out is None:
+        out = torch.empty((rows, topk_blocks), dtype=torch.int32, pin_memory=True)
+    with torch.cuda.stream(stream):
+        out.copy_(d_out, non_blocking=True)
+    stream.synchronize()
+    return out
+
+
+def select_candidate_blocks_sharded_host(logits, global_row_ke, global_block_size: int,
+                                         max_global_blocks: int, topk_blocks: int,
+                                         row_repeat: int = 1, *, out=None,
+                                         device_buffers: Optional[dict] = None, stream=None):
+    """Host-memory form of ``dsa_select_candidate_blocks_sharded`` (see
+    ``select_candidate_blocks_host``)."""
+    torch = _torch()
+    stream = torch.cuda.current_stream() if stream is None else stream
+    db = device_buffers if device_buffers is not None else {}
+    d_logits = _to_device(logits, db.get("logits"), stream)
+    d_gke = _to_device(global_row_ke, db.get("global_row_ke"), stream)
+    rows = logits.shape[1]
+    d_out = db.get("out")
+    if d_out is None:
+        d_out = torch.empty((rows, topk_blocks), dtype=torch.int32, device="cuda")
+    dsa_select_candidate_blocks_sharded(d_logits, d_gke, global_block_size, max_global_blocks,
+                                        topk_blocks, d_out, row_repeat, stream=stream)
+    if out is None:
+        out = torch.empty((rows, topk_blocks), dtype=torch.int32, pin_memory=True)
+    with torch.cuda.stream(stream):
+        out.copy_(d_out, non_blocking=True)
+    stream.synchronize()
+    return out

@@ -1,0 +1,171 @@
+/*
+ * dsa_cb.h -- C ABI of the GB300 (sm_103a) DSA candidate-block selection
+ * library (libdsa_cb.so).
+ *
+ * The operation: every indexer-logit row is masked to its window
+ * [row_ks, row_ke) in packed column space, max-reduced per block of
+ * block_size columns counted from the window start, optionally has its newest
+ * block pinned to +inf, and yields the ids of its top topk_blocks blocks,
+ * -1 padded. Source: the page "launcher/dcp2/diffs/02-model_executor_
+ * kernels_attention_dsa_candidate_blocks.py.diff" (vLLM-fork
+ * candidate_blocks.py): _max_with_nan, _block_scores_kernel, _block_scores,
+ * select_candidate_blocks / _select_candidate_blocks_impl and the
+ * _store_candidates_kernel launch. The DCP form takes the interleave-1 token
+ * placement of the page "sgl-project--sglang/python/sglang/srt/layers/dcp/
+ * kernels.py" (create_triton_kv_indices_for_dcp_triton).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named logits, row_ks, row_ke, global_row_ke, out and
+ *    scores_out are DEVICE pointers owned by the caller. The library
+ *    allocates no memory and keeps no pointer after a call returns.
+ *  - Matrices are row-major with an explicit row stride in elements (ld_*).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL means the legacy
+ *    default stream) and the call returns without synchronising. Results are
+ *    ready when the stream reaches that point.
+ *  - Bounds are int32 and shared by groups of row_repeat consecutive rows:
+ *    row r reads entry r / row_repeat, so row_ks and row_ke hold
+ *    ceil(rows / row_repeat) entries.
+ *  - Out-of-range bounds are clamped, never trapped: e = min(ke, width),
+ *    s = min(max(ks, 0), e); a window with s >= e is empty.
+ *  - Block scores are fp32. Any NaN in a block makes its score the canonical
+ *    quiet NaN 0x7FC00000. Scores are ranked in the total order
+ *    -inf < ... < -0 < +0 < ... < +inf < NaN; equal scores rank the lower
+ *    block id first. A slot whose block scores -inf, or which lies past
+ *    k = min(topk_blocks, number of blocks), holds -1.
+ *  - Return values: DSA_OK, or an error code. Argument errors are detected
+ *    on the host before anything is enqueued. No entry point traps or spins
+ *    on the device.
+ */
+#ifndef DSA_CB_H
+#define DSA_CB_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_EINVAL = -1,       /* invalid argument; nothing was enqueued         */
+    DSA_ECUDA = -2,        /* a CUDA runtime call or kernel launch failed    */
+    DSA_EUNSUPPORTED = -3  /* valid, but beyond this build's limits (below)  */
+} dsa_status;
+
+/* Static text for a status code (never NULL). */
+const char *dsa_status_string(int status);
+
+/* Largest number of blocks per row that the selecting entry points accept
+ * (all block scores of a row are kept in on-chip shared memory while its
+ * top-k is taken). Larger rows return DSA_EUNSUPPORTED. */
+int32_t dsa_select_max_blocks(void);
+
+/* Largest shard count accepted by dsa_select_candidate_blocks_sharded. */
+int32_t dsa_select_max_shards(void);
+
+/*
+ * dsa_block_scores -- per-block scores of every row (candidate_blocks.py:
+ * _block_scores and _block_scores_kernel, with the PIN_NEWEST switch).
+ *
+ *   logits      [rows, ld_logits] fp32; columns [0, width) are read.
+ *   row_ks      nullable; NULL means every window starts at 0.
+ *   row_ke      window ends, ceil(rows / row_repeat) entries.
+ *   block_size  >= 1; nb = ceil(width / block_size) blocks per row.
+ *   pin_newest  nonzero: when e > s, block (e - s - 1) / block_size of the
+ *               row becomes +inf after the reduction.
+ *   scores_out  [rows, ld_scores] fp32, ld_scores >= nb; entry (r, b) is
+ *               the max over the in-window columns
+ *               [s + b*block_size, s + (b+1)*block_size) and [s, e), or
+ *               -inf when that set is empty.
+ *
+ * rows == 0 or width == 0: DSA_OK, nothing written. DSA_EINVAL for
+ * rows < 0, width < 0, block_size < 1, row_repeat < 1, ld_logits < width,
+ * ld_scores < nb, or a NULL logits / row_ke / scores_out. DSA_EUNSUPPORTED
+ * for width >= 2^31.
+ */
+dsa_status dsa_block_scores(const float *logits, int64_t rows, int64_t width,
+                            int64_t ld_logits, const int32_t *row_ks,
+                            const int32_t *row_ke, int32_t block_size,
+                            int32_t row_repeat, int32_t pin_newest,
+                            float *scores_out, int64_t ld_scores,
+                            void *stream);
+
+/*
+ * dsa_select_candidate_blocks -- ranked candidate block ids per row
+ * (candidate_blocks.py: select_candidate_blocks / _select_candidate_blocks_impl
+ * without a DCP group: block scores, then top-k, then the -1-padded store).
+ * The pages always pin the newest block here; pin_newest exposes the switch.
+ *
+ *   out         [rows, ld_out] int32, ld_out >= topk_blocks; slot j < topk
+ *               holds the block id of rank j (rank by score, then lower id)
+ *               or -1 (see the conventions above). Slots >= topk_blocks of
+ *               each row are left untouched.
+ *   scores_out  nullable; when given, [rows, ld_scores] fp32 with
+ *               ld_scores >= nb receives the block scores that were ranked
+ *               (pin applied), as dsa_block_scores would write them.
+ *
+ * rows == 0: DSA_OK, nothing written. width == 0: every slot of out is -1.
+ * topk_blocks == 0 and no scores_out: DSA_OK, nothing written.
+ * DSA_EINVAL for negative rows / width / topk_blocks, block_size < 1,
+ * row_repeat < 1, ld_logits < width, ld_out < topk_blocks, ld_scores < nb
+ * (with scores_out), or a NULL logits / row_ke / out (out only when
+ * topk_blocks > 0). DSA_EUNSUPPORTED when nb > dsa_select_max_blocks() or
+ * width >= 2^31.
+ */
+dsa_status dsa_select_candidate_blocks(const float *logits, int64_t rows,
+                                       int64_t width, int64_t ld_logits,
+                                       const int32_t *row_ks,
+                                       const int32_t *row_ke,
+                                       int32_t topk_blocks, int32_t block_size,
+                                       int32_t row_repeat, int32_t pin_newest,
+                                       int32_t *out, int64_t ld_out,
+                                       float *scores_out, int64_t ld_scores,
+                                       void *stream);
+
+/*
+ * dsa_select_candidate_blocks_sharded -- the DCP form on one device
+ * (candidate_blocks.py: _select_candidate_blocks_impl with a DCP group), the
+ * D ranks' local logits held as a leading axis instead of on D GPUs.
+ *
+ *   logits         shard d, row r, local column c at
+ *                  logits[d * shard_stride + r * ld_logits + c], c <
+ *                  local_width; local column c of shard d is global token
+ *                  shards * c + d (interleave 1).
+ *   global_row_ke  global window end of each row group (no starts: every
+ *                  global window begins at token 0).
+ *   global_block_size  multiple of shards; the local block is
+ *                  global_block_size / shards columns, so local block b of
+ *                  every shard is its share of global block b.
+ *   max_global_blocks  number of global blocks nbg = max(value, 1); ids are
+ *                  in [0, nbg).
+ *   out, scores_out  as for dsa_select_candidate_blocks with nb = nbg.
+ *
+ * Per row: shard d's window is its first ceil((gke - d) / shards) local
+ * columns when gke > d (else empty), clamped to local_width; local block
+ * scores are taken without a pin; the global score of block b is the max
+ * over shards for b < min(ceil(local_width / local block), nbg) and -inf
+ * beyond; block clamp((gke - 1) // global_block_size, 0, nbg - 1) becomes
+ * +inf; a row with gke <= 0 scores -inf everywhere; then top-k and -1 as
+ * above.
+ *
+ * rows == 0: DSA_OK. DSA_EINVAL for shards < 1, negative rows / local_width
+ * / topk_blocks, global_block_size < 1 or not a multiple of shards,
+ * row_repeat < 1, ld_logits < local_width, shard_stride < 0, ld_out <
+ * topk_blocks, ld_scores < nbg (with scores_out), or a NULL
+ * global_row_ke / out (out only when topk_blocks > 0) / logits (when
+ * local_width > 0). DSA_EUNSUPPORTED when nbg > dsa_select_max_blocks(),
+ * shards > dsa_select_max_shards() or local_width >= 2^31.
+ */
+dsa_status dsa_select_candidate_blocks_sharded(
+    const float *logits, int32_t shards, int64_t rows, int64_t local_width,
+    int64_t ld_logits, int64_t shard_stride, const int32_t *global_row_ke,
+    int32_t global_block_size, int32_t max_global_blocks, int32_t row_repeat,
+    int32_t topk_blocks, int32_t *out, int64_t ld_out, float *scores_out,
+    int64_t ld_scores, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_CB_H */

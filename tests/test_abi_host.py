@@ -1,0 +1,144 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every function that ``include/dsa_cb.h`` declares, and rejects invalid
+arguments on the host before touching the device (no call below reaches a
+CUDA API)."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa_cb.h")
+
+DSA_OK, DSA_EINVAL, DSA_ECUDA, DSA_EUNSUPPORTED = 0, -1, -2, -3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from deepseek_sparse_attention_row_gb300 import _build_lib
+
+    _build_lib.build()
+    import deepseek_sparse_attention_row_gb300 as dsa
+
+    return dsa.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_operations():
+    names = declared_functions()
+    for n in ("dsa_block_scores", "dsa_select_candidate_blocks",
+              "dsa_select_candidate_blocks_sharded"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import deepseek_sparse_attention_row_gb300 as dsa
+
+    names = declared_functions()
+    assert sorted(dsa.EXPORTED_SYMBOLS) == names
+    nm = subprocess.run(["nm", "-D", "--defined-only", dsa.library_path], capture_output=True,
+                        text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (\w+)", nm))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for st in (DSA_OK, DSA_EINVAL, DSA_ECUDA, DSA_EUNSUPPORTED, 12345):
+        assert lib.dsa_status_string(st)
+
+
+def test_limits(lib):
+    assert lib.dsa_select_max_blocks() >= 1024
+    assert lib.dsa_select_max_shards() >= 8
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(rows=-1), DSA_EINVAL),
+    (dict(width=-1), DSA_EINVAL),
+    (dict(block_size=0), DSA_EINVAL),
+    (dict(row_repeat=0), DSA_EINVAL),
+    (dict(ld=5), DSA_EINVAL),
+    (dict(scores=None), DSA_EINVAL),
+    (dict(ld_scores=1), DSA_EINVAL),
+    (dict(rows=0), DSA_OK),
+    (dict(width=0), DSA_OK),
+    (dict(width=1 << 31, ld=1 << 31, ld_scores=1 << 31), DSA_EUNSUPPORTED),
+])
+def test_block_scores_validation(lib, kw, want):
+    a = dict(logits=FAKE, rows=4, width=10, ld=10, ks=None, ke=FAKE, block_size=4,
+             row_repeat=1, pin=1, scores=FAKE, ld_scores=3)
+    a.update(kw)
+    st = lib.dsa_block_scores(a["logits"], a["rows"], a["width"], a["ld"], a["ks"], a["ke"],
+                              a["block_size"], a["row_repeat"], a["pin"], a["scores"],
+                              a["ld_scores"], None)
+    assert st == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(rows=-2), DSA_EINVAL),
+    (dict(topk=-1), DSA_EINVAL),
+    (dict(block_size=-3), DSA_EINVAL),
+    (dict(row_repeat=0), DSA_EINVAL),
+    (dict(out=None), DSA_EINVAL),
+    (dict(ld_out=3), DSA_EINVAL),
+    (dict(logits=None), DSA_EINVAL),
+    (dict(ke=None), DSA_EINVAL),
+    (dict(ld=99), DSA_EINVAL),
+    (dict(scores=FAKE, ld_scores=2), DSA_EINVAL),
+    (dict(rows=0), DSA_OK),
+    (dict(topk=0, out=None), DSA_OK),
+    (dict(block_size=1, width=20000, ld=20000), DSA_EUNSUPPORTED),
+])
+def test_select_validation(lib, kw, want):
+    a = dict(logits=FAKE, rows=4, width=100, ld=100, ks=None, ke=FAKE, topk=4, block_size=8,
+             row_repeat=1, pin=1, out=FAKE, ld_out=4, scores=None, ld_scores=0)
+    a.update(kw)
+    st = lib.dsa_select_candidate_blocks(a["logits"], a["rows"], a["width"], a["ld"], a["ks"],
+                                         a["ke"], a["topk"], a["block_size"], a["row_repeat"],
+                                         a["pin"], a["out"], a["ld_out"], a["scores"],
+                                         a["ld_scores"], None)
+    assert st == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(shards=0), DSA_EINVAL),
+    (dict(gbs=60), DSA_EINVAL),          # not a multiple of 8 shards
+    (dict(gbs=0), DSA_EINVAL),
+    (dict(rows=-1), DSA_EINVAL),
+    (dict(lw=-1), DSA_EINVAL),
+    (dict(topk=-1), DSA_EINVAL),
+    (dict(row_repeat=0), DSA_EINVAL),
+    (dict(ld=10), DSA_EINVAL),
+    (dict(shard_stride=-1), DSA_EINVAL),
+    (dict(gke=None), DSA_EINVAL),
+    (dict(out=None), DSA_EINVAL),
+    (dict(ld_out=1), DSA_EINVAL),
+    (dict(logits=None), DSA_EINVAL),
+    (dict(scores=FAKE, ld_scores=7), DSA_EINVAL),
+    (dict(rows=0), DSA_OK),
+    (dict(topk=0, out=None), DSA_OK),
+    (dict(max_gb=20000, scores=None), DSA_EUNSUPPORTED),
+    (dict(shards=2048, gbs=2048), DSA_EUNSUPPORTED),
+])
+def test_sharded_validation(lib, kw, want):
+    a = dict(logits=FAKE, shards=8, rows=4, lw=64, ld=64, shard_stride=256, gke=FAKE, gbs=64,
+             max_gb=8, row_repeat=1, topk=4, out=FAKE, ld_out=4, scores=None, ld_scores=0)
+    a.update(kw)
+    st = lib.dsa_select_candidate_blocks_sharded(
+        a["logits"], a["shards"], a["rows"], a["lw"], a["ld"], a["shard_stride"], a["gke"],
+        a["gbs"], a["max_gb"], a["row_repeat"], a["topk"], a["out"], a["ld_out"], a["scores"],
+        a["ld_scores"], None)
+    assert st == want

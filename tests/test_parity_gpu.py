@@ -1,0 +1,321 @@
+"""GPU parity: the sm_103a library against the CPU oracle, bit for bit.
+
+Every case compares the ordered id array exactly and the block-score array
+bit for bit (integer and index outputs, and fp32 values that are copies of
+input elements, so the tolerance is zero). Outputs are written into views
+of larger buffers whose guard columns must come back untouched, and rows of
+logits can be padded (ld > width) with values that must never win.
+
+Sizes span several 32-block split units, every cluster size the launcher
+picks (1 to 8 CTAs per row), both top-k sort networks (K <= 32 in one warp,
+larger K in shared memory), every streaming path (vector widths 4 / 2 / 1
+and the generic path for non-power-of-two blocks), ragged window ends and
+unaligned window starts.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from helpers import assert_bits_equal, deal_shards
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 3
+SENTINEL_ID = -7
+SENTINEL_SCORE = np.float32(-12345.5)
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import deepseek_sparse_attention_row_gb300 as dsa
+
+    assert torch.cuda.is_available(), "GPU parity tests need a CUDA device"
+    return torch, dsa
+
+
+def _dev(torch, a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _padded_logits(torch, logits, width, offset):
+    """Device copy of logits [rows, ld] placed `offset` elements into a larger
+    buffer, so the row starts get a chosen misalignment."""
+    rows, ld = logits.shape
+    buf = torch.full((rows * ld + offset + 8,), 1e30, dtype=torch.float32, device="cuda")
+    flat = buf[offset:offset + rows * ld]
+    flat.copy_(torch.from_numpy(np.ascontiguousarray(logits).reshape(-1)))
+    return flat.view(rows, ld)[:, :width]
+
+
+def run_unsharded(env, wl, *, want_scores=True, offset=0):
+    torch, dsa = env
+    rows, width, topk = wl.rows, wl.width, wl.topk_blocks
+    nb = -(-width // wl.block_size) if width else 0
+    logits = _padded_logits(torch, wl.logits, width, offset)
+    out_buf = torch.full((rows, topk + GUARD), SENTINEL_ID, dtype=torch.int32, device="cuda")
+    sc_buf = torch.full((rows, nb + GUARD), float(SENTINEL_SCORE), dtype=torch.float32,
+                        device="cuda")
+    dsa.dsa_select_candidate_blocks(logits, _dev(torch, wl.row_ks), _dev(torch, wl.row_ke), topk,
+                                    wl.block_size, out_buf[:, :topk], wl.row_repeat,
+                                    wl.pin_newest,
+                                    scores_out=sc_buf[:, :nb] if want_scores else None)
+    torch.cuda.synchronize()
+    out_all, sc_all = out_buf.cpu().numpy(), sc_buf.cpu().numpy()
+    assert (out_all[:, topk:] == SENTINEL_ID).all(), "guard ids overwritten"
+    assert (sc_all[:, nb:] == SENTINEL_SCORE).all(), "guard scores overwritten"
+    if not want_scores:
+        assert (sc_all == SENTINEL_SCORE).all()
+    return out_all[:, :topk], sc_all[:, :nb]
+
+
+def check_unsharded(env, wl, *, offset=0, with_scores=True):
+    ref_ids, ref_scores = oracle.run_workload(wl)
+    got_ids, got_scores = run_unsharded(env, wl, want_scores=with_scores, offset=offset)
+    np.testing.assert_array_equal(got_ids, ref_ids)
+    if with_scores and ref_scores is not None and wl.width:
+        assert_bits_equal(got_scores, ref_scores)
+
+
+def run_sharded(env, wl, *, offset=0, want_scores=True):
+    torch, dsa = env
+    D, rows, lw = wl.logits.shape
+    topk = wl.topk_blocks
+    nbg = max(wl.max_global_blocks, 1)
+    buf = torch.full((D * rows * lw + offset + 8,), 1e30, dtype=torch.float32, device="cuda")
+    local = buf[offset:offset + D * rows * lw].view(D, rows, lw)
+    local.copy_(torch.from_numpy(wl.logits))
+    out_buf = torch.full((rows, topk + GUARD), SENTINEL_ID, dtype=torch.int32, device="cuda")
+    sc_buf = torch.full((rows, nbg + GUARD), float(SENTINEL_SCORE), dtype=torch.float32,
+                        device="cuda")
+    dsa.dsa_select_candidate_blocks_sharded(local, _dev(torch, wl.global_row_ke),
+                                            wl.global_block_size, wl.max_global_blocks, topk,
+                                            out_buf[:, :topk], wl.row_repeat,
+                                            scores_out=sc_buf[:, :nbg] if want_scores else None)
+    torch.cuda.synchronize()
+    out_all, sc_all = out_buf.cpu().numpy(), sc_buf.cpu().numpy()
+    assert (out_all[:, topk:] == SENTINEL_ID).all(), "guard ids overwritten"
+    assert (sc_all[:, nbg:] == SENTINEL_SCORE).all(), "guard scores overwritten"
+    return out_all[:, :topk], sc_all[:, :nbg]
+
+
+def check_sharded(env, wl, *, offset=0, with_scores=True):
+    ref_ids, ref_scores = oracle.run_workload(wl)
+    got_ids, got_scores = run_sharded(env, wl, offset=offset, want_scores=with_scores)
+    np.testing.assert_array_equal(got_ids, ref_ids)
+    if with_scores:
+        assert_bits_equal(got_scores, ref_scores)
+
+
+# ---------------------------------------------------------------------------
+# Randomised sweeps at oracle-friendly sizes
+# ---------------------------------------------------------------------------
+
+BLOCK_SIZES = [1, 2, 3, 4, 5, 8, 12, 16, 24, 32, 48, 64, 100, 128, 256, 512]
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_unsharded_sweep(env, seed):
+    rng = np.random.default_rng(seed)
+    bs = int(BLOCK_SIZES[seed % len(BLOCK_SIZES)])
+    width = int(rng.choice([1, 7, 31, 64, 333, 1000, 4096, 5003, 13000, 30001, 70000]))
+    width = min(width, bs * 4000)  # keep nb within the shared-memory limit
+    rows = int(rng.integers(1, 40))
+    rr = int(rng.choice([1, 1, 2, 3, 8]))
+    nb = -(-width // bs)
+    topk = int(rng.choice([1, 5, 16, 32, 33, 100, nb, nb + 5]))
+    wl = workloads.small_unsharded(
+        seed, rows=rows, width=width, block_size=bs, topk_blocks=topk, row_repeat=rr,
+        starts=bool(rng.integers(0, 2)), pin_newest=bool(rng.integers(0, 2)),
+        nan_count=int(rng.choice([0, 0, 3, 50])), bf16_grid=bool(rng.integers(0, 2)),
+        wild_bounds=bool(rng.integers(0, 2)),
+        ld=width + int(rng.choice([0, 0, 1, 3, 4])))
+    check_unsharded(env, wl, offset=int(rng.choice([0, 0, 1, 2, 3])))
+
+
+@pytest.mark.parametrize("seed", range(36))
+def test_sharded_sweep(env, seed):
+    rng = np.random.default_rng(500 + seed)
+    shards = int(rng.choice([1, 2, 3, 4, 8, 8, 16]))
+    lbs = int(rng.choice([1, 2, 3, 4, 8, 8, 16, 32]))
+    gbs = lbs * shards
+    lw = int(rng.choice([1, 5, 64, 100, 1024, 2047, 8192]))
+    nlb = -(-lw // lbs)
+    max_gb = int(rng.choice([0, 1, max(nlb // 2, 1), nlb, nlb + 7]))
+    max_gb = min(max_gb, 16384)
+    rows = int(rng.integers(1, 40))
+    rr = int(rng.choice([1, 1, 2, 5]))
+    nbg = max(max_gb, 1)
+    topk = int(rng.choice([1, 8, 32, 40, nbg, nbg + 3]))
+    wl, _ = workloads.small_sharded(500 + seed, shards=shards, rows=rows,
+                                    global_width=lw * shards, global_block_size=gbs,
+                                    max_global_blocks=max_gb, topk_blocks=topk, row_repeat=rr,
+                                    wild_bounds=bool(rng.integers(0, 2)))
+    check_sharded(env, wl, offset=int(rng.choice([0, 0, 1, 2])))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_block_scores_sweep(env, seed):
+    torch, dsa = env
+    rng = np.random.default_rng(900 + seed)
+    bs = int(rng.choice(BLOCK_SIZES))
+    width = int(rng.choice([1, 100, 4096, 20000, 131072]))
+    rows = int(rng.integers(1, 24))
+    wl = workloads.small_unsharded(900 + seed, rows=rows, width=width, block_size=bs,
+                                   topk_blocks=1, row_repeat=int(rng.choice([1, 4])),
+                                   pin_newest=bool(rng.integers(0, 2)), nan_count=4,
+                                   wild_bounds=bool(rng.integers(0, 2)))
+    want = oracle.block_scores(wl.logits, wl.row_ks, wl.row_ke, bs, wl.row_repeat, wl.pin_newest)
+    nb = want.shape[1]
+    buf = torch.full((rows, nb + GUARD), float(SENTINEL_SCORE), dtype=torch.float32,
+                     device="cuda")
+    dsa.dsa_block_scores(_dev(torch, wl.logits), _dev(torch, wl.row_ks), _dev(torch, wl.row_ke),
+                         bs, wl.row_repeat, wl.pin_newest, scores_out=buf[:, :nb])
+    got = buf.cpu().numpy()
+    assert (got[:, nb:] == SENTINEL_SCORE).all()
+    assert_bits_equal(got[:, :nb], want)
+
+
+def test_sharded_equals_unsharded_on_device(env):
+    torch, dsa = env
+    wl, g = workloads.small_sharded(4242, shards=8, rows=64, global_width=65536,
+                                    global_block_size=64, max_global_blocks=1024, topk_blocks=32)
+    ids_s, sc_s = run_sharded(env, wl)
+    ids_u, sc_u = run_unsharded(env, workloads.Workload(
+        "g", g, None, wl.global_row_ke, 64, 32, 1, True, 0))
+    np.testing.assert_array_equal(ids_s, ids_u)
+    assert_bits_equal(sc_s, sc_u)
+
+
+# ---------------------------------------------------------------------------
+# Edge cases
+# ---------------------------------------------------------------------------
+
+def test_empty_rows_is_noop(env):
+    torch, dsa = env
+    out = torch.full((0, 4), 5, dtype=torch.int32, device="cuda")
+    dsa.dsa_select_candidate_blocks(torch.zeros((0, 16), device="cuda"), None,
+                                    torch.zeros(0, dtype=torch.int32, device="cuda"), 4, 4, out)
+    torch.cuda.synchronize()
+
+
+def test_zero_width_gives_minus_one(env):
+    torch, dsa = env
+    out = torch.full((5, 4), 5, dtype=torch.int32, device="cuda")
+    dsa.dsa_select_candidate_blocks(torch.zeros((5, 0), device="cuda"), None,
+                                    torch.zeros(5, dtype=torch.int32, device="cuda"), 4, 4, out)
+    assert (out.cpu() == -1).all()
+
+
+def test_topk_zero_with_scores(env):
+    wl = workloads.small_unsharded(7, rows=9, width=1000, block_size=16, topk_blocks=0)
+    want = oracle.block_scores(wl.logits, wl.row_ks, wl.row_ke, 16, 1, True)
+    _, got = run_unsharded(env, wl)
+    assert_bits_equal(got, want)
+
+
+def test_largest_supported_rows(env):
+    """nb at the shared-memory limit, K above 32 (shared-memory sort)."""
+    torch, dsa = env
+    nmax = dsa.max_select_blocks()
+    wl = workloads.small_unsharded(8, rows=6, width=nmax, block_size=1, topk_blocks=nmax,
+                                   starts=False, nan_count=3, bf16_grid=True)
+    check_unsharded(env, wl)
+    wl = workloads.small_unsharded(9, rows=5, width=nmax * 4, block_size=4, topk_blocks=600)
+    check_unsharded(env, wl)
+
+
+def test_beyond_limits_raise(env):
+    torch, dsa = env
+    nmax = dsa.max_select_blocks()
+    out = torch.empty((2, 4), dtype=torch.int32, device="cuda")
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_select_candidate_blocks(torch.zeros((2, nmax + 1), device="cuda"), None,
+                                        torch.ones(2, dtype=torch.int32, device="cuda"), 4, 1, out)
+    assert e.value.status == -3
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_select_candidate_blocks_sharded(torch.zeros((8, 2, 64), device="cuda"),
+                                                torch.ones(2, dtype=torch.int32, device="cuda"),
+                                                60, 8, 4, out)
+    assert e.value.status == -1
+
+
+def test_all_nan_and_all_inf_rows(env):
+    x = np.full((4, 256), np.nan, dtype=np.float32)
+    x[1] = np.inf
+    x[2] = -np.inf
+    x[3, ::2] = -0.0
+    x[3, 1::2] = 0.0
+    wl = workloads.Workload("edge", x, None, np.full(4, 256, np.int32), 16, 20, 1, False, 0)
+    check_unsharded(env, wl)
+    wl.pin_newest = True
+    check_unsharded(env, wl)
+
+
+def test_non_default_stream(env):
+    torch, dsa = env
+    wl = workloads.small_unsharded(10, rows=33, width=9000, block_size=64, topk_blocks=32)
+    want_ids, _ = oracle.run_workload(wl)
+    s = torch.cuda.Stream()
+    out = torch.empty((33, 32), dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(s):
+        logits = _dev(torch, wl.logits)
+        ks, ke = _dev(torch, wl.row_ks), _dev(torch, wl.row_ke)
+        dsa.dsa_select_candidate_blocks(logits, ks, ke, 32, 64, out)
+    s.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), want_ids)
+
+
+def test_repeated_calls_identical(env):
+    wl = workloads.small_unsharded(11, rows=64, width=65536, block_size=64, topk_blocks=32,
+                                   bf16_grid=True, starts=False)
+    a = run_unsharded(env, wl)
+    b = run_unsharded(env, wl)
+    np.testing.assert_array_equal(a[0], b[0])
+    assert_bits_equal(a[1], b[1])
+
+
+def test_host_buffer_entry_points(env):
+    torch, dsa = env
+    wl = workloads.small_unsharded(12, rows=16, width=5000, block_size=64, topk_blocks=16)
+    want_ids, _ = oracle.run_workload(wl)
+    got = dsa.select_candidate_blocks_host(torch.from_numpy(wl.logits),
+                                           torch.from_numpy(wl.row_ks),
+                                           torch.from_numpy(wl.row_ke), 16, 64)
+    np.testing.assert_array_equal(got.numpy(), want_ids)
+    swl, _ = workloads.small_sharded(13, shards=8, rows=16, global_width=4096,
+                                     global_block_size=64, max_global_blocks=64, topk_blocks=8)
+    want_ids, _ = oracle.run_workload(swl)
+    got = dsa.select_candidate_blocks_sharded_host(torch.from_numpy(swl.logits),
+                                                   torch.from_numpy(swl.global_row_ke), 64, 64, 8)
+    np.testing.assert_array_equal(got.numpy(), want_ids)
+
+
+# ---------------------------------------------------------------------------
+# The workloads at full size (bench launch configuration), every output
+# ---------------------------------------------------------------------------
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "long", "long_pin"])
+def test_full_size_unsharded(env, name):
+    wl = workloads.make(name)
+    check_unsharded(env, wl)
+    # the bench calls without scores_out
+    want_ids, _ = oracle.run_workload(wl, want_scores=False)
+    got_ids, _ = run_unsharded(env, wl, want_scores=False)
+    np.testing.assert_array_equal(got_ids, want_ids)
+
+
+@pytest.mark.slow
+def test_full_size_dcp(env):
+    wl = workloads.make("dcp")
+    check_sharded(env, wl)
+    want_ids, _ = oracle.run_workload(wl, want_scores=False)
+    got_ids, _ = run_sharded(env, wl, want_scores=False)
+    np.testing.assert_array_equal(got_ids, want_ids)

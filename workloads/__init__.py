@@ -35,6 +35,8 @@ __all__ = [
     "make_long",
     "make_dcp",
     "round_to_bf16_grid",
+    "deal_to_shards",
+    "gather_from_shards",
     "random_nan_bits",
     "small_unsharded",
     "small_sharded",
@@ -108,16 +110,48 @@ def _rng(seed: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(seed))
 
 
-def round_to_bf16_grid(x: np.ndarray) -> np.ndarray:
+def round_to_bf16_grid(x: np.ndarray, *, inplace: bool = False) -> np.ndarray:
     """Round fp32 values to the nearest bf16-representable value (ties to even).
 
     Works on the bit pattern: add 0x7FFF plus the lowest kept bit, then clear
-    the low 16 bits. Inputs must be finite (normal draws are).
+    the low 16 bits. Inputs must be finite (normal draws are). Processes the
+    array in chunks so that large inputs need no large temporaries.
     """
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    lsb = (u >> np.uint32(16)) & np.uint32(1)
-    r = (u + np.uint32(0x7FFF) + lsb) & np.uint32(0xFFFF0000)
-    return r.view(np.float32)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if not inplace:
+        x = x.copy()
+    u = x.reshape(-1).view(np.uint32)
+    step = 1 << 20
+    lsb = np.empty(min(step, u.size), dtype=np.uint32)
+    for i in range(0, u.size, step):
+        c = u[i:i + step]
+        t = lsb[:c.size]
+        np.right_shift(c, np.uint32(16), out=t)
+        np.bitwise_and(t, np.uint32(1), out=t)
+        t += np.uint32(0x7FFF)
+        c += t
+        c &= np.uint32(0xFFFF0000)
+    return x
+
+
+def _normal(rng: np.random.Generator, shape) -> np.ndarray:
+    """fp32 N(0, 1) draws written straight into one new array."""
+    out = np.empty(shape, dtype=np.float32)
+    rng.standard_normal(out=out, dtype=np.float32)
+    return out
+
+
+def deal_to_shards(g: np.ndarray, shards: int) -> np.ndarray:
+    """Interleave-1 layout: global token t of each row goes to shard t % D at
+    local column t // D. ``g`` is [rows, D * local_width]."""
+    rows, gw = g.shape
+    return np.ascontiguousarray(g.reshape(rows, gw // shards, shards).transpose(2, 0, 1))
+
+
+def gather_from_shards(local: np.ndarray) -> np.ndarray:
+    """Inverse of ``deal_to_shards``: [D, rows, lw] back to [rows, D * lw]."""
+    shards, rows, lw = local.shape
+    return np.ascontiguousarray(local.transpose(1, 2, 0)).reshape(rows, lw * shards)
 
 
 def random_nan_bits(rng: np.random.Generator, n: int) -> np.ndarray:
@@ -140,7 +174,7 @@ def make_tiny(seed: int = 0) -> Workload:
     one 4096 forced; block 64, top-16, pinned."""
     rng = _rng(seed)
     rows, width = 64, 4096
-    logits = rng.standard_normal((rows, width), dtype=np.float32)
+    logits = _normal(rng, (rows, width))
     ke = rng.integers(0, width, size=rows, endpoint=True).astype(np.int32)
     ke[0] = 0
     ke[1] = width
@@ -154,7 +188,7 @@ def make_decode(seed: int = 1) -> Workload:
     rng = _rng(seed)
     seqs, heads, width = 64, 8, 65536
     rows = seqs * heads
-    logits = round_to_bf16_grid(rng.standard_normal((rows, width), dtype=np.float32))
+    logits = round_to_bf16_grid(_normal(rng, (rows, width)), inplace=True)
     ke = rng.integers(1, width, size=seqs, endpoint=True).astype(np.int32)
     return Workload("decode", logits, None, ke, 64, 32, heads, True, seed)
 
@@ -186,7 +220,7 @@ def make_prefill(seed: int = 2, *, requests: int = 4, tokens: int = 2048,
     ks = np.repeat(offsets, tokens).astype(np.int32)
     tok = np.tile(np.arange(tokens), requests)
     ke = (np.repeat(offsets + prefix, tokens) + tok + 1).astype(np.int32)
-    logits = rng.standard_normal((rows, width), dtype=np.float32)
+    logits = _normal(rng, (rows, width))
     logits *= np.float32(sigma)
     n_nan = int(round(nan_fraction * rows * width))
     pos = rng.choice(rows * width, size=n_nan, replace=False)
@@ -202,7 +236,7 @@ def make_long(seed: int = 3, *, pin_newest: bool = False, rows: int = 1024,
     columns raised by U(3, 6); ends uniform in [65536, 131072], starts uniform
     in [0, 4096]; block 128, top-16."""
     rng = _rng(seed)
-    logits = rng.standard_normal((rows, width), dtype=np.float32)
+    logits = _normal(rng, (rows, width))
     ke = rng.integers(width // 2, width, size=rows, endpoint=True).astype(np.int32)
     ks = rng.integers(0, 4096, size=rows, endpoint=True).astype(np.int32)
     for r in range(rows):
@@ -216,14 +250,16 @@ def make_long(seed: int = 3, *, pin_newest: bool = False, rows: int = 1024,
 def make_dcp(seed: int = 4, *, shards: int = 8, rows: int = 4096,
              global_width: int = 65536, global_block_size: int = 64,
              max_global_blocks: int = 1024, topk_blocks: int = 32) -> ShardedWorkload:
-    """Simulated DCP layout: a global [rows, global_width] N(0,1) matrix G is
+    """Simulated DCP layout: a global [rows, global_width] N(0,1) matrix G
     dealt over ``shards`` interleave-1 shards, L[d, r, c] = G[r, shards*c + d];
-    global ends uniform in [1, global_width]."""
+    global ends uniform in [1, global_width].
+
+    Dealing an i.i.d. N(0,1) matrix gives an i.i.d. N(0,1) array, so L is
+    drawn directly in the shard layout and G is defined as its inverse deal
+    (``gather_from_shards``); this avoids a 1 GiB strided copy."""
     rng = _rng(seed)
-    g = rng.standard_normal((rows, global_width), dtype=np.float32)
     lw = global_width // shards
-    local = np.ascontiguousarray(g.reshape(rows, lw, shards).transpose(2, 0, 1))
-    del g
+    local = _normal(rng, (shards, rows, lw))
     gke = rng.integers(1, global_width, size=rows, endpoint=True).astype(np.int32)
     return ShardedWorkload("dcp", local, gke, global_block_size, max_global_blocks,
                            topk_blocks, 1, seed)
@@ -261,9 +297,9 @@ def small_unsharded(seed: int, *, rows: int, width: int, block_size: int,
     rng = _rng(seed)
     groups = -(-rows // row_repeat) if rows else 0
     ld = width if ld is None else ld
-    buf = rng.standard_normal((rows, ld), dtype=np.float32)
+    buf = _normal(rng, (rows, ld))
     if bf16_grid:
-        buf = round_to_bf16_grid(buf)
+        buf = round_to_bf16_grid(buf, inplace=True)
     if ld > width:
         buf[:, width:] = np.float32(1e30)
     if nan_count and rows and width:
@@ -289,9 +325,8 @@ def small_sharded(seed: int, *, shards: int, rows: int, global_width: int,
     of ``shards``."""
     rng = _rng(seed)
     assert global_width % shards == 0
-    g = rng.standard_normal((rows, global_width), dtype=np.float32)
-    lw = global_width // shards
-    local = np.ascontiguousarray(g.reshape(rows, lw, shards).transpose(2, 0, 1))
+    g = _normal(rng, (rows, global_width))
+    local = deal_to_shards(g, shards)
     groups = -(-rows // row_repeat) if rows else 0
     lo, hi = (-4, global_width + 40) if wild_bounds else (0, global_width)
     gke = rng.integers(lo, hi, size=groups, endpoint=True).astype(np.int32)
