@@ -66,7 +66,6 @@ struct RowPlan {
   int32_t len_max;
   int32_t nblk;       // blocks holding in-window data
   int32_t pin_block;  // -1: none
-  int32_t dead;       // sharded row with gke <= 0: everything -inf
   int vec, lpb_log2;
 };
 
@@ -87,45 +86,36 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Plans row `row` for the unsharded form (thread 0 only).
-__device__ void plan_unsharded(const SelectArgs& a, int64_t row, RowPlan& p, int32_t* len) {
-  const int64_t g = row / a.row_repeat;
-  const int64_t ks = a.row_ks ? static_cast<int64_t>(a.row_ks[g]) : 0;
-  const int64_t ke = static_cast<int64_t>(a.row_ke[g]);
-  const int64_t e = min(ke, static_cast<int64_t>(a.width));
-  const int64_t s = min(max(ks, int64_t(0)), e);
-  const int64_t n = e > s ? e - s : 0;
-  p.origin = a.logits + row * a.ld + s;
+// Window of an unsharded row: e = min(ke, width), s = min(max(ks, 0), e).
+// Every thread computes the same plan from the row's bounds.
+__device__ __forceinline__ RowPlan plan_unsharded(const float* logits, int64_t ld, int32_t width,
+                                                  const int32_t* row_ks, const int32_t* row_ke,
+                                                  int32_t row_repeat, int32_t block_size,
+                                                  int32_t pin_newest, int64_t row) {
+  const int64_t g = row / row_repeat;
+  const int32_t ks = row_ks ? __ldg(row_ks + g) : 0;
+  const int32_t ke = __ldg(row_ke + g);
+  const int32_t e = min(ke, width);
+  const int32_t s = min(max(ks, 0), e);
+  const uint32_t n = e > s ? static_cast<uint32_t>(e - s) : 0u;
+  RowPlan p;
+  p.origin = logits + row * ld + s;
   p.len_max = static_cast<int32_t>(n);
-  len[0] = static_cast<int32_t>(n);
-  p.nblk = static_cast<int32_t>((n + a.block_size - 1) / a.block_size);
-  p.pin_block = (a.pin_newest && n > 0) ? static_cast<int32_t>((n - 1) / a.block_size) : -1;
-  p.dead = 0;
-  p.vec = choose_vec(p.origin, a.block_size, &p.lpb_log2);
+  p.nblk = static_cast<int32_t>((n + static_cast<uint32_t>(block_size) - 1u) /
+                                static_cast<uint32_t>(block_size));
+  p.pin_block = (pin_newest && n > 0) ? static_cast<int32_t>((n - 1u) / block_size) : -1;
+  p.vec = choose_vec(p.origin, block_size, &p.lpb_log2);
+  return p;
 }
 
-// Plans row `row` for the sharded form. Thread 0 fills p; all threads fill len.
-__device__ void plan_sharded(const SelectArgs& a, int64_t row, RowPlan& p, int32_t* len,
-                             int64_t gke) {
-  const int D = a.shards;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    // Shard d holds the global tokens t = D*c + d; those below gke are its
-    // first ceil((gke - d) / D) local columns.
-    const int64_t lke = gke > d ? (gke - d + D - 1) / D : 0;
-    len[d] = static_cast<int32_t>(min(lke, static_cast<int64_t>(a.width)));
-  }
-  if (threadIdx.x == 0) {
-    const int64_t lke0 = gke > 0 ? (gke + D - 1) / D : 0;
-    const int64_t n0 = min(lke0, static_cast<int64_t>(a.width));
-    p.origin = a.logits + row * a.ld;
-    p.len_max = static_cast<int32_t>(n0);
-    p.nblk = static_cast<int32_t>(min((n0 + a.block_size - 1) / a.block_size,
-                                      static_cast<int64_t>(a.nb_data)));
-    p.dead = gke <= 0;
-    int64_t pin = gke >= 1 ? (gke - 1) / a.global_block_size : 0;
-    pin = min(pin, static_cast<int64_t>(a.nb - 1));
-    p.pin_block = p.dead ? -1 : static_cast<int32_t>(pin);
-  }
+// Local end of shard d for global end gke: shard d holds the global tokens
+// t = shards*c + d, so those below gke are its first ceil((gke - d) / shards)
+// local columns; clamped to the local width.
+__device__ __forceinline__ int32_t shard_len(int32_t gke, int32_t d, int32_t shards, int32_t lw) {
+  if (gke <= d) return 0;
+  const uint32_t lke = (static_cast<uint32_t>(gke - d) + static_cast<uint32_t>(shards - 1)) /
+                       static_cast<uint32_t>(shards);
+  return static_cast<int32_t>(min(lke, static_cast<uint32_t>(lw)));
 }
 
 template <int SVEC>
@@ -138,34 +128,47 @@ __device__ __forceinline__ void stream_sharded(const Window& w, int lpb_log2, in
   else if constexpr (SVEC == 1)
     stream_pow2<1, 4, 8>(w, lpb_log2, b0, b1, keys, 0);
   else
-    stream_generic<2, 8>(w, block_size, b0, b1, keys, 0);
+    stream_generic<4, 8>(w, block_size, b0, b1, keys, 0);
 }
 
-// SHARDED = false: unsharded rows (vector width chosen per row).
+// One row per cluster of csize CTAs (csize is 1 unless overridden).
+// SHARDED = false: unsharded rows, vector width chosen per row.
 // SHARDED = true: DCP rows; SVEC is the vector width fixed by the host
 // (0 = generic path).
 template <bool SHARDED, int SVEC>
-__global__ void __launch_bounds__(kThreads, 3) select_kernel(const SelectArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) select_kernel(const SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);                // [kpad]
   uint32_t* keys = reinterpret_cast<uint32_t*>(cand + a.kpad);           // [nb]
   int32_t* len = reinterpret_cast<int32_t*>(keys + a.nb);                // [shards]
-  __shared__ RowPlan plan;
   __shared__ TopkShared tsh;
-  __shared__ int64_t s_gke;
 
   const uint32_t csize = cluster_size();
   const uint32_t crank = cluster_rank();
   const int64_t row = blockIdx.x / csize;
 
+  RowPlan plan;
   if constexpr (SHARDED) {
-    if (threadIdx.x == 0) s_gke = a.row_ke[row / a.row_repeat];
-    __syncthreads();
-    plan_sharded(a, row, plan, len, s_gke);
+    const int32_t gke = __ldg(a.row_ke + row / a.row_repeat);
+    const int32_t n0 = shard_len(gke, 0, a.shards, a.width);
+    plan.origin = a.logits + row * a.ld;
+    plan.len_max = n0;
+    plan.nblk = min(static_cast<int32_t>((static_cast<uint32_t>(n0) + a.block_size - 1u) /
+                                         static_cast<uint32_t>(a.block_size)),
+                    a.nb_data);
+    plan.pin_block = gke >= 1 ? static_cast<int32_t>(min(
+                                    static_cast<uint32_t>(gke - 1) / a.global_block_size,
+                                    static_cast<uint32_t>(a.nb - 1)))
+                              : -1;
+    plan.vec = SVEC;
+    plan.lpb_log2 = SVEC ? __ffs(a.block_size / (SVEC ? SVEC : 1)) - 1 : 0;
+    for (int d = threadIdx.x; d < a.shards; d += blockDim.x)
+      len[d] = shard_len(gke, d, a.shards, a.width);
   } else {
-    if (threadIdx.x == 0) plan_unsharded(a, row, plan, len);
+    plan = plan_unsharded(a.logits, a.ld, a.width, a.row_ks, a.row_ke, a.row_repeat,
+                          a.block_size, a.pin_newest, row);
+    if (threadIdx.x == 0) len[0] = plan.len_max;
   }
-  __syncthreads();
 
   const int32_t nblk = plan.nblk;
   const int32_t units = (nblk + kSplitUnit - 1) / kSplitUnit;
@@ -178,18 +181,25 @@ __global__ void __launch_bounds__(kThreads, 3) select_kernel(const SelectArgs a)
   __syncthreads();
   if (csize > 1) cluster_arrive();  // phase 0: this CTA has started
 
+  Window w;
+  w.origin = plan.origin;
+  w.shard_stride = a.shard_stride;
+  w.shards = a.shards;
+  w.len = len;
+  w.len_max = plan.len_max;
   if (b0 < b1) {
-    Window w;
-    w.origin = plan.origin;
-    w.shard_stride = a.shard_stride;
-    w.shards = a.shards;
-    w.len = len;
-    w.len_max = plan.len_max;
     if constexpr (SHARDED)
-      stream_sharded<SVEC>(w, SVEC ? __ffs(a.block_size / (SVEC ? SVEC : 1)) - 1 : 0,
-                           a.block_size, b0, b1, keys);
+      stream_sharded<SVEC>(w, plan.lpb_log2, a.block_size, b0, b1, keys);
     else
       stream_row(w, plan.vec, plan.lpb_log2, a.block_size, b0, b1, keys, 0);
+  }
+  __syncthreads();
+  if (b0 < b1) {
+    if constexpr (SHARDED) {
+      if constexpr (SVEC > 1) finish_partial<SVEC>(w, a.block_size, b0, b1, keys, 0);
+    } else {
+      finish_row(w, plan.vec, a.block_size, b0, b1, keys, 0);
+    }
   }
   __syncthreads();
 
@@ -232,39 +242,29 @@ struct ScoresArgs {
   int64_t ld_scores;
 };
 
-__global__ void __launch_bounds__(kThreads, 3) block_scores_kernel(const ScoresArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) block_scores_kernel(const ScoresArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw);  // [chunk]
-  __shared__ RowPlan plan;
   __shared__ int32_t len[1];
   const int64_t row = blockIdx.x / a.chunks;
   const int32_t c0 = static_cast<int32_t>(blockIdx.x % a.chunks) * a.chunk;
   const int32_t c1 = min(c0 + a.chunk, a.nb);
 
-  if (threadIdx.x == 0) {
-    SelectArgs sa{};
-    sa.logits = a.logits;
-    sa.ld = a.ld;
-    sa.width = a.width;
-    sa.row_ks = a.row_ks;
-    sa.row_ke = a.row_ke;
-    sa.row_repeat = a.row_repeat;
-    sa.block_size = a.block_size;
-    sa.pin_newest = a.pin_newest;
-    plan_unsharded(sa, row, plan, len);
-  }
+  const RowPlan plan = plan_unsharded(a.logits, a.ld, a.width, a.row_ks, a.row_ke, a.row_repeat,
+                                      a.block_size, a.pin_newest, row);
+  if (threadIdx.x == 0) len[0] = plan.len_max;
   for (int32_t b = threadIdx.x; b < c1 - c0; b += blockDim.x) keys[b] = kKeyNegInf;
   __syncthreads();
   const int32_t b0 = min(c0, plan.nblk), b1 = min(c1, plan.nblk);
-  if (b0 < b1) {
-    Window w;
-    w.origin = plan.origin;
-    w.shard_stride = 0;
-    w.shards = 1;
-    w.len = len;
-    w.len_max = plan.len_max;
-    stream_row(w, plan.vec, plan.lpb_log2, a.block_size, b0, b1, keys, c0);
-  }
+  Window w;
+  w.origin = plan.origin;
+  w.shard_stride = 0;
+  w.shards = 1;
+  w.len = len;
+  w.len_max = plan.len_max;
+  if (b0 < b1) stream_row(w, plan.vec, plan.lpb_log2, a.block_size, b0, b1, keys, c0);
+  __syncthreads();
+  if (b0 < b1) finish_row(w, plan.vec, a.block_size, b0, b1, keys, c0);
   __syncthreads();
   if (threadIdx.x == 0 && plan.pin_block >= c0 && plan.pin_block < c1)
     keys[plan.pin_block - c0] = kKeyPosInf;
@@ -302,21 +302,48 @@ int32_t next_pow2(int32_t x) {
   return p;
 }
 
-// Cluster size from the largest possible per-row read: aim for at most
-// ~48 KiB of logits per CTA, a power of two up to 8.
-int choose_cluster(int64_t max_row_bytes) {
+// CTAs per row. One by default: splitting rows over thread-block clusters
+// measured slower on every workload (a cluster needs all its CTA slots free
+// in one GPC at once). DSA_CB_CLUSTER=2..8 forces a split for experiments.
+int choose_cluster(int64_t /*max_row_bytes*/) {
   const int forced = cluster_override();
-  if (forced > 0) return forced;
-  int c = 1;
-  while (c < kMaxCluster && max_row_bytes > static_cast<int64_t>(c) * 48 * 1024) c <<= 1;
-  return c;
+  return forced > 0 ? forced : 1;
 }
+
+// Opts a kernel in to `smem` bytes of dynamic shared memory on the current
+// device (static plus dynamic shared memory above 48 KiB needs the opt-in).
+// Remembers the largest size set per (kernel, device) so repeated launches
+// make no runtime call.
+struct SmemOptIn {
+  const void* fn;
+  int device;
+  size_t bytes;
+};
+std::mutex g_smem_mu;
+SmemOptIn g_smem_table[64];
+int g_smem_used = 0;
 
 template <typename K>
 cudaError_t set_smem_attr(K kernel, size_t smem) {
-  if (smem <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(smem));
+  if (smem == 0) return cudaSuccess;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const void* fn = reinterpret_cast<const void*>(kernel);
+  std::lock_guard<std::mutex> lock(g_smem_mu);
+  for (int i = 0; i < g_smem_used; ++i) {
+    if (g_smem_table[i].fn == fn && g_smem_table[i].device == dev) {
+      if (g_smem_table[i].bytes >= smem) return cudaSuccess;
+      err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+      if (err == cudaSuccess) g_smem_table[i].bytes = smem;
+      return err;
+    }
+  }
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+  if (err == cudaSuccess && g_smem_used < 64) g_smem_table[g_smem_used++] = {fn, dev, smem};
+  return err;
 }
 
 template <typename K>

@@ -7,26 +7,29 @@
 // its first len[d] local columns, local block b of every shard belongs to
 // global block b, and the global score is the max over shards.
 //
-// Both forms are the same loop here. Each CTA owns block range [b0, b1) of
-// one row and accumulates order keys (keys.cuh) into keys[b - kbase] in shared
-// memory, which the caller initialised to key(-inf). A warp streams a slab of
-// 32 x NV vectors of VEC floats per shard, lane l taking vectors l, l + 32, ...
-// so every load instruction is a contiguous, fully coalesced warp access; all
-// NV x SB loads of a slab are issued before any is used. Vector v of a shard
-// covers local elements [v*VEC, v*VEC + VEC) and lies in block
-// v / (block_size / VEC).
+// Both forms are the same loop. A CTA owns block range [b0, b1) of one row
+// and accumulates order keys (keys.cuh) into keys[b - kbase] in shared
+// memory, initialised by the caller to key(-inf). A warp streams a slab of
+// 32 x NV vectors of VEC floats per shard, lane l taking vectors l, l + 32,
+// ..., so every load instruction is one contiguous, fully coalesced warp
+// access; all NV x SB loads of a slab are issued before any is used, and a
+// lane folds everything it loaded for one vector slot (over shards and
+// vector elements) with max.NaN before anything crosses lanes. Vector v of a
+// shard covers local elements [v*VEC, v*VEC + VEC) and lies in block
+// v / LPB, LPB = block_size / VEC.
 //
-// Fast path (stream_pow2): VEC divides block_size, LPB = block_size / VEC is
-// a power of two, and every shard's origin is VEC*4-byte aligned. With
-// LPB <= 32 a load instruction covers 32 / LPB whole blocks, reduced by
-// log2(LPB) xor-shuffles and stored by the group's first lane; with LPB > 32
-// it covers part of one block, reduced with redux.sync and merged by a shared
-// atomicMax. Generic path (stream_generic): scalar loads, block id per lane,
-// a segmented shuffle reduction and an atomicMax per block segment.
+// Fast path (stream_pow2): VEC divides block_size, LPB is a power of two and
+// every shard origin is VEC*4-byte aligned. With LPB <= 32 a load
+// instruction covers 32 / LPB whole blocks: log2(LPB) xor-shuffles reduce a
+// block and its first lane stores the key. With LPB > 32 the instructions of
+// one block are folded in registers first, then one redux.sync and one
+// shared atomicMax per block and slab. Generic path (stream_generic): scalar
+// loads, a block id per lane, a segmented shuffle reduction and an atomicMax
+// per block segment.
 //
-// No element outside a window is read: full vectors are loaded only when
-// they lie inside the window, and the one partial vector per shard at the
-// window end is read element by element.
+// No element outside a window is read. The hot loop loads only whole vectors
+// inside the window; the one vector per shard that straddles the window end
+// is folded afterwards by finish_partial().
 #pragma once
 
 #include <cstdint>
@@ -40,25 +43,11 @@ constexpr int kWarps = kThreads / 32;
 
 struct Window {
   const float* origin;   // element 0 of shard 0's window
-  int64_t shard_stride;  // elements between shards (0 when shards == 1)
+  int64_t shard_stride;  // elements between shards
   int32_t shards;
   const int32_t* len;    // shared memory: in-window length of each shard
   int32_t len_max;       // max over shards of len[d]
 };
-
-template <int VEC>
-__device__ __forceinline__ void fill_neg(float (&x)[VEC]) {
-#pragma unroll
-  for (int i = 0; i < VEC; ++i) x[i] = __uint_as_float(0xFF800000u);  // -inf
-}
-
-template <int VEC>
-__device__ __forceinline__ uint32_t vec_key(const float (&x)[VEC]) {
-  uint32_t k = order_key(x[0]);
-#pragma unroll
-  for (int i = 1; i < VEC; ++i) k = max(k, order_key(x[i]));
-  return k;
-}
 
 // Fast path. lpb_log2 = log2(block_size / VEC).
 template <int VEC, int NV, int SB>
@@ -67,73 +56,100 @@ __device__ __forceinline__ void stream_pow2(const Window& w, int lpb_log2, int32
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int lpb = 1 << lpb_log2;
-  const int64_t nvec = (static_cast<int64_t>(w.len_max) + VEC - 1) / VEC;
-  const int64_t v_begin = static_cast<int64_t>(b0) << lpb_log2;
-  const int64_t v_end = min(static_cast<int64_t>(b1) << lpb_log2, nvec);
-  constexpr int64_t kSlab = 32 * NV;
+  const int32_t nvec = w.len_max / VEC;  // whole vectors of the longest shard
+  const int32_t v_begin = static_cast<int32_t>(static_cast<int64_t>(b0) << lpb_log2);
+  const int32_t v_end = static_cast<int32_t>(min(static_cast<int64_t>(b1) << lpb_log2,
+                                                 static_cast<int64_t>(nvec)));
+  // Several shard batches commit to the same blocks: merge with atomics.
+  const bool merge = w.shards > SB;
+  constexpr int32_t kSlab = 32 * NV;
 
-  for (int64_t slab = v_begin + warp * kSlab; slab < v_end; slab += kWarps * kSlab) {
-    uint32_t key[NV];
+  for (int d0 = 0; d0 < w.shards; d0 += SB) {
+    int32_t lim[SB];
 #pragma unroll
-    for (int m = 0; m < NV; ++m) key[m] = kKeyNegInf;
+    for (int j = 0; j < SB; ++j)
+      lim[j] = (d0 + j < w.shards) ? min(w.len[d0 + j] / VEC, v_end) : 0;
+    const float* base = w.origin + static_cast<int64_t>(d0) * w.shard_stride;
 
-    for (int d0 = 0; d0 < w.shards; d0 += SB) {
+    for (int32_t slab = v_begin + warp * kSlab; slab < v_end; slab += kWarps * kSlab) {
+      float acc[NV];
+#pragma unroll
+      for (int m = 0; m < NV; ++m) acc[m] = neg_inf();
       float x[SB][NV][VEC];
-      int32_t len[SB];
-#pragma unroll
-      for (int j = 0; j < SB; ++j) len[j] = (d0 + j < w.shards) ? w.len[d0 + j] : 0;
-      // Issue every full-vector load of the slab first.
 #pragma unroll
       for (int j = 0; j < SB; ++j) {
-        const float* src = w.origin + static_cast<int64_t>(d0 + j) * w.shard_stride;
+        const float* src = base + static_cast<int64_t>(j) * w.shard_stride;
 #pragma unroll
         for (int m = 0; m < NV; ++m) {
-          const int64_t v = slab + m * 32 + lane;
-          if (v < v_end && (v + 1) * VEC <= len[j])
-            ld_stream(src + v * VEC, x[j][m]);
-          else
-            fill_neg<VEC>(x[j][m]);
-        }
-      }
-      // The vector that straddles a shard's window end (at most one per
-      // shard) is read element by element.
-      if (VEC > 1) {
+          const int32_t v = slab + m * 32 + lane;
+          if (v < lim[j]) {
+            ld_stream(src + static_cast<int64_t>(v) * VEC, x[j][m]);
+          } else {
 #pragma unroll
-        for (int j = 0; j < SB; ++j) {
-          const float* src = w.origin + static_cast<int64_t>(d0 + j) * w.shard_stride;
-#pragma unroll
-          for (int m = 0; m < NV; ++m) {
-            const int64_t v = slab + m * 32 + lane;
-            if (v < v_end && v * VEC < len[j] && (v + 1) * VEC > len[j]) {
-#pragma unroll
-              for (int i = 0; i < VEC; ++i)
-                if (v * VEC + i < len[j]) x[j][m][i] = ld_stream1(src + v * VEC + i);
-            }
+            for (int i = 0; i < VEC; ++i) x[j][m][i] = neg_inf();
           }
         }
       }
 #pragma unroll
       for (int j = 0; j < SB; ++j)
 #pragma unroll
-        for (int m = 0; m < NV; ++m) key[m] = max(key[m], vec_key<VEC>(x[j][m]));
-    }
+        for (int m = 0; m < NV; ++m) acc[m] = fold(acc[m], x[j][m]);
 
-    // Reduce each load instruction's 32 vectors to block keys and commit.
-#pragma unroll
-    for (int m = 0; m < NV; ++m) {
-      const int64_t vfirst = slab + m * 32;
-      if (vfirst >= v_end) break;
-      uint32_t k = key[m];
       if (lpb_log2 >= 5) {
-        k = __reduce_max_sync(0xffffffffu, k);
-        if (lane == 0) atomicMax(&keys[static_cast<int32_t>(vfirst >> lpb_log2) - kbase], k);
+        // Instructions m of one block are consecutive; fold them, then one
+        // warp reduction per block.
+        float carry = neg_inf();
+#pragma unroll
+        for (int m = 0; m < NV; ++m) {
+          carry = max_nan(carry, acc[m]);
+          const int32_t blk = (slab + m * 32) >> lpb_log2;
+          const bool last = (m == NV - 1) || (((slab + (m + 1) * 32) >> lpb_log2) != blk);
+          if (last) {
+            if (blk < b1) {
+              const uint32_t k = __reduce_max_sync(0xffffffffu, order_key(carry));
+              if (lane == 0) atomicMax(&keys[blk - kbase], k);
+            }
+            carry = neg_inf();
+          }
+        }
       } else {
-        for (int o = 1; o < lpb; o <<= 1) k = max(k, __shfl_xor_sync(0xffffffffu, k, o));
-        const int64_t v = vfirst + lane;
-        if ((lane & (lpb - 1)) == 0 && v < v_end)
-          keys[static_cast<int32_t>(v >> lpb_log2) - kbase] = k;
+#pragma unroll
+        for (int m = 0; m < NV; ++m) {
+          const int32_t vfirst = slab + m * 32;
+          if (vfirst >= v_end) break;
+          uint32_t k = order_key(acc[m]);
+          for (int o = 1; o < lpb; o <<= 1) k = max(k, __shfl_xor_sync(0xffffffffu, k, o));
+          const int32_t v = vfirst + lane;
+          if ((lane & (lpb - 1)) == 0 && v < v_end) {
+            if (merge)
+              atomicMax(&keys[(v >> lpb_log2) - kbase], k);
+            else
+              keys[(v >> lpb_log2) - kbase] = k;
+          }
+        }
       }
     }
+  }
+}
+
+// Folds the elements past the last whole vector of each shard's window (at
+// most VEC - 1 per shard) into their block. Call after the streaming loop and
+// a __syncthreads(); one thread per shard.
+template <int VEC>
+__device__ __forceinline__ void finish_partial(const Window& w, int32_t block_size, int32_t b0,
+                                               int32_t b1, uint32_t* __restrict__ keys,
+                                               int32_t kbase) {
+  if (VEC == 1) return;
+  for (int d = threadIdx.x; d < w.shards; d += blockDim.x) {
+    const int32_t len = w.len[d];
+    const int32_t first = (len / VEC) * VEC;
+    if (first == len) continue;
+    const int32_t blk = first / block_size;
+    if (blk < b0 || blk >= b1) continue;
+    const float* src = w.origin + static_cast<int64_t>(d) * w.shard_stride;
+    float acc = neg_inf();
+    for (int32_t i = first; i < len; ++i) acc = max_nan(acc, ld_stream1(src + i));
+    atomicMax(&keys[blk - kbase], order_key(acc));
   }
 }
 
@@ -149,9 +165,9 @@ __device__ __forceinline__ void stream_generic(const Window& w, int32_t block_si
   constexpr int64_t kSlab = 32 * NV;
 
   for (int64_t slab = e_begin + warp * kSlab; slab < e_end; slab += kWarps * kSlab) {
-    uint32_t key[NV];
+    float acc[NV];
 #pragma unroll
-    for (int m = 0; m < NV; ++m) key[m] = kKeyNegInf;
+    for (int m = 0; m < NV; ++m) acc[m] = neg_inf();
     for (int d0 = 0; d0 < w.shards; d0 += SB) {
       float x[SB][NV];
 #pragma unroll
@@ -161,13 +177,13 @@ __device__ __forceinline__ void stream_generic(const Window& w, int32_t block_si
 #pragma unroll
         for (int m = 0; m < NV; ++m) {
           const int64_t i = slab + m * 32 + lane;
-          x[j][m] = (i < e_end && i < len) ? ld_stream1(src + i) : __uint_as_float(0xFF800000u);
+          x[j][m] = (i < e_end && i < len) ? ld_stream1(src + i) : neg_inf();
         }
       }
 #pragma unroll
       for (int j = 0; j < SB; ++j)
 #pragma unroll
-        for (int m = 0; m < NV; ++m) key[m] = max(key[m], order_key(x[j][m]));
+        for (int m = 0; m < NV; ++m) acc[m] = max_nan(acc[m], x[j][m]);
     }
 #pragma unroll
     for (int m = 0; m < NV; ++m) {
@@ -175,7 +191,7 @@ __device__ __forceinline__ void stream_generic(const Window& w, int32_t block_si
       if (first >= e_end) break;
       const int64_t i = first + lane;
       const int32_t blk = (i < e_end) ? static_cast<int32_t>(i / block_size) : -1;
-      uint32_t k = key[m];
+      uint32_t k = order_key(acc[m]);
       // Segmented max over runs of equal blk (runs are contiguous in lanes):
       // afterwards the first lane of each run holds the run's max.
 #pragma unroll
@@ -202,20 +218,28 @@ __device__ __forceinline__ int choose_vec(const float* origin, int32_t block_siz
     vec = 2;
   else if (pow2(block_size))
     vec = 1;
-  if (vec) *lpb_log2 = __ffs(block_size / vec) - 1;
+  *lpb_log2 = vec ? __ffs(block_size / vec) - 1 : 0;
   return vec;
 }
 
-// Unsharded dispatch: vector width chosen per row at run time.
+// Unsharded dispatch: vector width chosen per row at run time. Every path
+// keeps 32 floats per lane in flight per slab.
 __device__ __forceinline__ void stream_row(const Window& w, int vec, int lpb_log2,
                                            int32_t block_size, int32_t b0, int32_t b1,
                                            uint32_t* keys, int32_t kbase) {
   switch (vec) {
-    case 4: stream_pow2<4, 4, 1>(w, lpb_log2, b0, b1, keys, kbase); break;
-    case 2: stream_pow2<2, 8, 1>(w, lpb_log2, b0, b1, keys, kbase); break;
-    case 1: stream_pow2<1, 16, 1>(w, lpb_log2, b0, b1, keys, kbase); break;
-    default: stream_generic<8, 1>(w, block_size, b0, b1, keys, kbase); break;
+    case 4: stream_pow2<4, 8, 1>(w, lpb_log2, b0, b1, keys, kbase); break;
+    case 2: stream_pow2<2, 16, 1>(w, lpb_log2, b0, b1, keys, kbase); break;
+    case 1: stream_pow2<1, 32, 1>(w, lpb_log2, b0, b1, keys, kbase); break;
+    default: stream_generic<16, 1>(w, block_size, b0, b1, keys, kbase); break;
   }
+}
+
+__device__ __forceinline__ void finish_row(const Window& w, int vec, int32_t block_size,
+                                           int32_t b0, int32_t b1, uint32_t* keys,
+                                           int32_t kbase) {
+  if (vec == 4) finish_partial<4>(w, block_size, b0, b1, keys, kbase);
+  if (vec == 2) finish_partial<2>(w, block_size, b0, b1, keys, kbase);
 }
 
 }  // namespace dsa
