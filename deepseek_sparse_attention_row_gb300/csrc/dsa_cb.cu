@@ -138,8 +138,8 @@ __device__ __forceinline__ void stream_sharded(const Window& w, int lpb_log2, in
 template <bool SHARDED, int SVEC>
 __global__ void __launch_bounds__(kThreads, 4) select_kernel(const SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);                // [kpad]
-  uint32_t* keys = reinterpret_cast<uint32_t*>(cand + a.kpad);           // [nb]
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);  // [max(kpad, kRankMax)]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(cand + max(a.kpad, kRankMax));  // [nb]
   int32_t* len = reinterpret_cast<int32_t*>(keys + a.nb);                // [shards]
   __shared__ TopkShared tsh;
 
@@ -148,8 +148,9 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const SelectArgs a)
   const int64_t row = blockIdx.x / csize;
 
   RowPlan plan;
+  int32_t gke = 0;
   if constexpr (SHARDED) {
-    const int32_t gke = __ldg(a.row_ke + row / a.row_repeat);
+    gke = __ldg(a.row_ke + row / a.row_repeat);
     const int32_t n0 = shard_len(gke, 0, a.shards, a.width);
     plan.origin = a.logits + row * a.ld;
     plan.len_max = n0;
@@ -194,12 +195,15 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const SelectArgs a)
       stream_row(w, plan.vec, plan.lpb_log2, a.block_size, b0, b1, keys, 0);
   }
   __syncthreads();
-  if (b0 < b1) {
-    if constexpr (SHARDED) {
-      if constexpr (SVEC > 1) finish_partial<SVEC>(w, a.block_size, b0, b1, keys, 0);
-    } else {
-      finish_row(w, plan.vec, a.block_size, b0, b1, keys, 0);
-    }
+  if constexpr (SHARDED) {
+    if constexpr (SVEC > 1)
+      for (int d = threadIdx.x; d < a.shards; d += blockDim.x)
+        commit_partial(load_partial<SVEC>(plan.origin + d * a.shard_stride, len[d], a.block_size,
+                                          b0, b1),
+                       keys, 0);
+  } else {
+    if (threadIdx.x == 0)
+      commit_partial(load_partial_row(w, plan.vec, a.block_size, b0, b1), keys, 0);
   }
   __syncthreads();
 
@@ -216,14 +220,9 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const SelectArgs a)
   }
 
   // Leader: pin, scores, selection.
-  if (threadIdx.x == 0 && plan.pin_block >= 0) keys[plan.pin_block] = kKeyPosInf;
-  __syncthreads();
-  if (a.scores) {
-    float* srow = a.scores + row * a.ld_scores;
-    for (int32_t b = threadIdx.x; b < a.nb; b += blockDim.x) srow[b] = key_score(keys[b]);
-  }
-  if (a.topk > 0) topk_store(keys, a.nb, min(a.topk, a.nb), cand, a.kpad, a.out + row * a.ld_out,
-                             a.topk, tsh);
+  topk_store(keys, a.nb, min(a.topk, a.nb), plan.pin_block, cand, a.kpad,
+             a.topk > 0 ? a.out + row * a.ld_out : nullptr, a.topk,
+             a.scores ? a.scores + row * a.ld_scores : nullptr, tsh);
 }
 
 struct ScoresArgs {
@@ -264,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 4) block_scores_kernel(const ScoresA
   w.len_max = plan.len_max;
   if (b0 < b1) stream_row(w, plan.vec, plan.lpb_log2, a.block_size, b0, b1, keys, c0);
   __syncthreads();
-  if (b0 < b1) finish_row(w, plan.vec, a.block_size, b0, b1, keys, c0);
+  if (threadIdx.x == 0)
+    commit_partial(load_partial_row(w, plan.vec, a.block_size, b0, b1), keys, c0);
   __syncthreads();
   if (threadIdx.x == 0 && plan.pin_block >= c0 && plan.pin_block < c1)
     keys[plan.pin_block - c0] = kKeyPosInf;
@@ -374,7 +374,7 @@ dsa_status fill_minus_one(int32_t* out, int64_t rows, int32_t cols, int64_t ld, 
 }
 
 size_t select_smem(int32_t kpad, int32_t nb, int32_t shards) {
-  return static_cast<size_t>(kpad) * 8 + static_cast<size_t>(nb) * 4 +
+  return static_cast<size_t>(std::max(kpad, kRankMax)) * 8 + static_cast<size_t>(nb) * 4 +
          static_cast<size_t>(shards) * 4;
 }
 

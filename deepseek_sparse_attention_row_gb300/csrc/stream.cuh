@@ -29,7 +29,7 @@
 //
 // No element outside a window is read. The hot loop loads only whole vectors
 // inside the window; the one vector per shard that straddles the window end
-// is folded afterwards by finish_partial().
+// is read element by element by load_partial().
 #pragma once
 
 #include <cstdint>
@@ -132,25 +132,32 @@ __device__ __forceinline__ void stream_pow2(const Window& w, int lpb_log2, int32
   }
 }
 
-// Folds the elements past the last whole vector of each shard's window (at
-// most VEC - 1 per shard) into their block. Call after the streaming loop and
-// a __syncthreads(); one thread per shard.
+// The elements past the last whole vector of a shard's window (at most
+// VEC - 1) are read after the streaming loop: load_partial() folds them into
+// a register and commit_partial() merges that into their block, after a
+// __syncthreads() (the loop stores keys without atomics). Loading them before
+// the loop instead measured slower (the live registers cost the loop).
+struct Partial {
+  float v;
+  int32_t blk;  // -1: nothing to merge
+};
+
 template <int VEC>
-__device__ __forceinline__ void finish_partial(const Window& w, int32_t block_size, int32_t b0,
-                                               int32_t b1, uint32_t* __restrict__ keys,
-                                               int32_t kbase) {
-  if (VEC == 1) return;
-  for (int d = threadIdx.x; d < w.shards; d += blockDim.x) {
-    const int32_t len = w.len[d];
-    const int32_t first = (len / VEC) * VEC;
-    if (first == len) continue;
-    const int32_t blk = first / block_size;
-    if (blk < b0 || blk >= b1) continue;
-    const float* src = w.origin + static_cast<int64_t>(d) * w.shard_stride;
-    float acc = neg_inf();
-    for (int32_t i = first; i < len; ++i) acc = max_nan(acc, ld_stream1(src + i));
-    atomicMax(&keys[blk - kbase], order_key(acc));
-  }
+__device__ __forceinline__ Partial load_partial(const float* shard_origin, int32_t len,
+                                                    int32_t block_size, int32_t b0, int32_t b1) {
+  Partial p{neg_inf(), -1};
+  if (VEC == 1) return p;
+  const int32_t first = (len / VEC) * VEC;
+  if (first == len) return p;
+  const int32_t blk = first / block_size;
+  if (blk < b0 || blk >= b1) return p;
+  for (int32_t i = first; i < len; ++i) p.v = max_nan(p.v, ld_stream1(shard_origin + i));
+  p.blk = blk;
+  return p;
+}
+
+__device__ __forceinline__ void commit_partial(const Partial& p, uint32_t* keys, int32_t kbase) {
+  if (p.blk >= 0) atomicMax(&keys[p.blk - kbase], order_key(p.v));
 }
 
 // Generic path: any block size, any alignment. Elements, not vectors.
@@ -235,11 +242,11 @@ __device__ __forceinline__ void stream_row(const Window& w, int vec, int lpb_log
   }
 }
 
-__device__ __forceinline__ void finish_row(const Window& w, int vec, int32_t block_size,
-                                           int32_t b0, int32_t b1, uint32_t* keys,
-                                           int32_t kbase) {
-  if (vec == 4) finish_partial<4>(w, block_size, b0, b1, keys, kbase);
-  if (vec == 2) finish_partial<2>(w, block_size, b0, b1, keys, kbase);
+__device__ __forceinline__ Partial load_partial_row(const Window& w, int vec, int32_t block_size,
+                                                   int32_t b0, int32_t b1) {
+  if (vec == 4) return load_partial<4>(w.origin, w.len_max, block_size, b0, b1);
+  if (vec == 2) return load_partial<2>(w.origin, w.len_max, block_size, b0, b1);
+  return Partial{neg_inf(), -1};
 }
 
 }  // namespace dsa

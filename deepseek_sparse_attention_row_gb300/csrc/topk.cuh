@@ -3,26 +3,24 @@
 // candidate_blocks.py diff: after the block scores, _select_candidate_blocks_impl
 // takes scores.topk(min(topk_blocks, nblocks)) and _store_candidates_kernel
 // writes the ids, -1 padded. Here the whole step runs in one CTA on keys that
-// never leave shared memory:
+// never leave shared memory. Every candidate is the 64-bit composite
+// (key << 32) | ~id, so composites are distinct and their descending order is
+// exactly "score descending, then lower id first". Only keys above key(-inf)
+// can be selected (a -inf block yields -1); K = min(k, their count).
 //
-//  1. Count the keys above key(-inf) (a -inf block can only yield -1) and
-//     take their min m and max M. K = min(k, count) survivors are needed. If
-//     every such key survives there is nothing to select.
-//  2. Radix select for the K-th largest key. All keys in [m, M] share the
-//     bits above the highest bit where m and M differ, so the digits start
-//     right below that common prefix: the first histogram already spreads
-//     the keys (block maxima of similar rows share their top byte, which
-//     would put every key in one bin). Each pass histograms up to 8 bits of
-//     the keys that still match the prefix found so far and takes the digit
-//     where the running count from the top reaches the number still needed;
-//     when that digit's bin holds exactly what is still needed, every key
-//     with the new prefix is in and the search stops.
-//  3. Gather keys above the threshold; when the threshold key itself is
-//     tied, the lowest ids among the tied keys (ties rank the lower id
-//     first) are added by an ordered two-phase warp scan.
-//  4. Sort the K survivors descending by (key, -id) packed in 64 bits: one
-//     warp's shuffle bitonic network when K <= 32, otherwise a bitonic
-//     network in shared memory. Store ids, then -1 up to topk.
+// Fast path (k <= 8 * warps): thread t owns keys t, t + T, t + 2T, ... Each
+// warp finds the R-th largest key of its own keys, R = ceil(k / warps), with
+// R rounds of redux.sync at most. At least R keys of every warp are >= that
+// warp's value, so at least k keys are >= L, the smallest of the warps'
+// values. The candidates are the keys >= L (a few more than k on typical
+// rows); each is ranked by counting the candidates above it and rank r < K
+// is stored in slot r. Two barriers, no sort network, no tie handling.
+//
+// Exact path (larger k, or more candidates than kRankMax): radix select for
+// the K-th largest key with 8-bit digits starting right below the common
+// prefix of the row's min and max key; the lowest tied ids at the threshold
+// are taken by an ordered warp scan; the K survivors are then ranked by
+// counting (K <= kRankMax) or sorted by a bitonic network in shared memory.
 #pragma once
 
 #include <cstdint>
@@ -31,11 +29,13 @@
 
 namespace dsa {
 
+constexpr int kRankMax = 256;  // candidates ranked by counting
+
 struct TopkShared {
-  uint32_t hist[2][256];
-  uint32_t warp_count[32], warp_max[32], warp_min[32];
+  uint32_t hist[256];
+  uint32_t warp_count[32], warp_kth[32], warp_max[32], warp_min[32];
   uint32_t digit, above, eq;
-  uint32_t count_gt;
+  uint32_t count;
 };
 
 __device__ __forceinline__ uint64_t pack_candidate(uint32_t key, int32_t id) {
@@ -46,83 +46,65 @@ __device__ __forceinline__ int32_t candidate_id(uint64_t c) {
   return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(c));
 }
 
-// keys: [nb] in shared memory (final). cand: [kpad] in shared memory, kpad a
-// power of two >= min(k, nb). out: this row's output slots (global). Every
-// thread of the CTA calls this.
-__device__ void topk_store(const uint32_t* __restrict__ keys, int32_t nb, int32_t k,
-                           uint64_t* __restrict__ cand, int32_t kpad, int32_t* __restrict__ out,
-                           int32_t topk, TopkShared& sh) {
+// Stores ranks of cand[0 .. n) (distinct composites): rank r < K goes to
+// out[r]; out[K .. topk) becomes -1. No barrier inside.
+__device__ __forceinline__ void rank_store(const uint64_t* __restrict__ cand, int32_t n, int32_t K,
+                                           int32_t* __restrict__ out, int32_t topk) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint64_t ci = cand[i];
+    int32_t r = 0;
+    for (int j = 0; j < n; ++j) r += cand[j] > ci;
+    if (r < K) out[r] = candidate_id(ci);
+  }
+  for (int j = K + threadIdx.x; j < topk; j += blockDim.x) out[j] = -1;
+}
+
+// Exact path. Preconditions: keys final; total = number of keys above -inf,
+// m / M their min / max, 0 < K <= total. Ends with the row stored.
+__device__ void topk_exact(const uint32_t* __restrict__ keys, int32_t nb, int32_t K, uint32_t total,
+                           uint32_t m, uint32_t M, uint64_t* __restrict__ cand, int32_t kpad,
+                           int32_t* __restrict__ out, int32_t topk, TopkShared& sh) {
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int nthreads = blockDim.x;
   const int nwarps = nthreads >> 5;
 
-  // 1. Count, min and max of the keys above -inf.
-  {
-    uint32_t cnt = 0, mx = 0, mn = 0xFFFFFFFFu;
-    for (int b = tid; b < nb; b += nthreads) {
-      const uint32_t key = keys[b];
-      if (key > kKeyNegInf) {
-        ++cnt;
-        mx = max(mx, key);
-        mn = min(mn, key);
-      }
-    }
-    cnt = __reduce_add_sync(0xffffffffu, cnt);
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    mn = __reduce_min_sync(0xffffffffu, mn);
-    if (lane == 0) {
-      sh.warp_count[warp] = cnt;
-      sh.warp_max[warp] = mx;
-      sh.warp_min[warp] = mn;
-    }
-    for (int i = tid; i < 256; i += nthreads) sh.hist[0][i] = 0;
-    if (tid == 0) sh.count_gt = 0;
-  }
+  if (tid == 0) sh.count = 0;
+  for (int i = tid; i < 256; i += nthreads) sh.hist[i] = 0;
   __syncthreads();
-  uint32_t total = 0, M = 0, m = 0xFFFFFFFFu;
-  for (int i = 0; i < nwarps; ++i) {
-    total += sh.warp_count[i];
-    M = max(M, sh.warp_max[i]);
-    m = min(m, sh.warp_min[i]);
-  }
-  const int32_t K = static_cast<int32_t>(min(static_cast<uint32_t>(k), total));
 
-  // 2. Threshold: selected = keys >= prefix (take_all) or keys > prefix plus
-  // `need` tied keys equal to prefix.
-  uint32_t prefix = kKeyNegInf + 1u;
-  bool take_all = true;
+  uint32_t prefix = kKeyNegInf + 1u;  // selected: keys >= prefix (take_all) or
+  bool take_all = true;               // keys > prefix plus `need` tied keys
   int32_t need = 0;
-  if (K > 0 && static_cast<uint32_t>(K) < total) {
-    const uint32_t diff = m ^ M;
+  if (static_cast<uint32_t>(K) < total) {
     take_all = false;
     need = K;
-    if (diff == 0) {
-      prefix = M;  // every candidate key is equal: all ties
+    if (m == M) {
+      prefix = M;  // every key above -inf is equal: pure ties
     } else {
-      const int hb = 31 - __clz(diff);
+      const int hb = 31 - __clz(m ^ M);
       uint32_t mask = (hb == 31) ? 0u : ~((2u << hb) - 1u);
       prefix = M & mask;
       int hi = hb;
-      int pass = 0;
-      while (hi >= 0) {
+      for (int pass = 0; hi >= 0; ++pass) {
         const int lo = max(hi - 7, 0);
-        const uint32_t width_mask = (2u << (hi - lo)) - 1u;
-        uint32_t* hcur = sh.hist[pass & 1];
-        uint32_t* hnext = sh.hist[(pass + 1) & 1];
+        const uint32_t wmask = (2u << (hi - lo)) - 1u;
+        if (pass > 0) {
+          for (int i = tid; i < 256; i += nthreads) sh.hist[i] = 0;
+          __syncthreads();
+        }
         for (int b = tid; b < nb; b += nthreads) {
           const uint32_t key = keys[b];
-          if (key > kKeyNegInf && (key & mask) == prefix) atomicAdd(&hcur[(key >> lo) & width_mask], 1u);
+          if (key > kKeyNegInf && (key & mask) == prefix) atomicAdd(&sh.hist[(key >> lo) & wmask], 1u);
         }
-        for (int i = tid; i < 256; i += nthreads) hnext[i] = 0;
         __syncthreads();
         if (warp == 0) {
           // Lane l owns digits 255 - 8l down to 248 - 8l (highest first).
           uint32_t c[8], sum = 0;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            c[i] = hcur[255 - 8 * lane - i];
+            c[i] = sh.hist[255 - 8 * lane - i];
             sum += c[i];
           }
           uint32_t incl = sum;
@@ -148,7 +130,7 @@ __device__ void topk_store(const uint32_t* __restrict__ keys, int32_t nb, int32_
         }
         __syncthreads();
         prefix |= sh.digit << lo;
-        mask |= width_mask << lo;
+        mask |= wmask << lo;
         need -= static_cast<int32_t>(sh.above);
         if (static_cast<uint32_t>(need) == sh.eq) {
           take_all = true;
@@ -156,21 +138,19 @@ __device__ void topk_store(const uint32_t* __restrict__ keys, int32_t nb, int32_
           break;
         }
         hi = lo - 1;
-        ++pass;
       }
     }
   }
 
-  // 3. Gather.
-  if (K > 0) {
-    for (int b = tid; b < nb; b += nthreads) {
-      const uint32_t key = keys[b];
-      const bool sel = take_all ? (key >= prefix && key > kKeyNegInf) : (key > prefix);
-      if (sel) cand[atomicAdd(&sh.count_gt, 1u)] = pack_candidate(key, b);
-    }
+  // Gather exactly K survivors.
+  for (int b = tid; b < nb; b += nthreads) {
+    const uint32_t key = keys[b];
+    const bool sel = take_all ? (key >= prefix && key > kKeyNegInf) : (key > prefix);
+    if (sel) cand[atomicAdd(&sh.count, 1u)] = pack_candidate(key, b);
   }
   if (need > 0) {
-    // Ordered tie pass: warp w scans ids [w*span, (w+1)*span) in order.
+    // Ordered tie pass: warp w scans ids [w*span, (w+1)*span) in order and
+    // the lowest `need` tied ids overall are taken.
     const int32_t span = ((nb + nwarps - 1) / nwarps + 31) & ~31;
     const int32_t lo_id = warp * span, hi_id = min(lo_id + span, nb);
     uint32_t mine = 0;
@@ -182,7 +162,7 @@ __device__ void topk_store(const uint32_t* __restrict__ keys, int32_t nb, int32_
     __syncthreads();
     int32_t rank0 = 0;
     for (int i = 0; i < warp; ++i) rank0 += static_cast<int32_t>(sh.warp_count[i]);
-    const int32_t count_gt = static_cast<int32_t>(sh.count_gt);
+    const int32_t count_gt = static_cast<int32_t>(sh.count);
     for (int32_t base = lo_id; base < hi_id && rank0 < need; base += 32) {
       const int32_t b = base + lane;
       const bool tie = b < hi_id && keys[b] == prefix;
@@ -194,23 +174,8 @@ __device__ void topk_store(const uint32_t* __restrict__ keys, int32_t nb, int32_
   }
   __syncthreads();
 
-  // 4. Sort survivors descending and store.
-  if (kpad <= 32) {
-    if (warp == 0) {
-      uint64_t v = (lane < K) ? cand[lane] : 0ull;
-#pragma unroll
-      for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          const uint64_t o = __shfl_xor_sync(0xffffffffu, v, stride);
-          const bool desc = (lane & size) == 0;
-          const bool lower = (lane & stride) == 0;
-          v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
-        }
-      }
-      if (lane < topk) out[lane] = (lane < K) ? candidate_id(v) : -1;
-    }
-    for (int j = 32 + tid; j < topk; j += nthreads) out[j] = -1;
+  if (K <= kRankMax) {
+    rank_store(cand, K, K, out, topk);
     return;
   }
   for (int i = K + tid; i < kpad; i += nthreads) cand[i] = 0ull;
@@ -231,6 +196,105 @@ __device__ void topk_store(const uint32_t* __restrict__ keys, int32_t nb, int32_
     }
   }
   for (int j = tid; j < topk; j += nthreads) out[j] = (j < K) ? candidate_id(cand[j]) : -1;
+}
+
+// keys: [nb] in shared memory; block pin_block (if >= 0) becomes +inf here.
+// cand: [max(kpad, kRankMax)] in shared memory, kpad a power of two
+// >= min(k, nb). out: this row's output slots (global; unused when k == 0).
+// scores: optional fp32 row (nb entries) written with the final scores.
+// Every thread of the CTA calls this.
+__device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t k, int32_t pin_block,
+                           uint64_t* __restrict__ cand, int32_t kpad, int32_t* __restrict__ out,
+                           int32_t topk, float* __restrict__ scores, TopkShared& sh) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nthreads = blockDim.x;
+  const int nwarps = nthreads >> 5;
+  const bool fast = k > 0 && k <= 8 * nwarps;
+  const int R = fast ? (k + nwarps - 1) / nwarps : 0;
+
+  // 1. Each thread touches only its own keys: pin, scores, count, min, max,
+  // then its warp's R-th largest key (with multiplicity).
+  uint32_t cnt = 0, mx = 0, mn = 0xFFFFFFFFu;
+  for (int b = tid; b < nb; b += nthreads) {
+    uint32_t key = keys[b];
+    if (b == pin_block) {
+      key = kKeyPosInf;
+      keys[b] = key;
+    }
+    if (scores) scores[b] = key_score(key);
+    if (key > kKeyNegInf) {
+      ++cnt;
+      mx = max(mx, key);
+      mn = min(mn, key);
+    }
+  }
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  const uint32_t wmax = __reduce_max_sync(0xffffffffu, mx);
+  const uint32_t wmin = __reduce_min_sync(0xffffffffu, mn);
+  uint32_t kth = kKeyNegInf;
+  if (fast) {
+    uint32_t bound = wmax;  // candidate value of this round
+    int have = 0;
+    for (int r = 0; r < R && bound > kKeyNegInf; ++r) {
+      uint32_t c = 0, below = 0;
+      for (int b = tid; b < nb; b += nthreads) {
+        const uint32_t key = keys[b];
+        c += key == bound;
+        if (key < bound && key > kKeyNegInf) below = max(below, key);
+      }
+      have += static_cast<int>(__reduce_add_sync(0xffffffffu, c));
+      kth = bound;
+      if (have >= R) break;
+      bound = __reduce_max_sync(0xffffffffu, below);
+    }
+    if (have < R) kth = kKeyNegInf;  // fewer than R keys above -inf here
+  }
+  if (lane == 0) {
+    sh.warp_count[warp] = cnt;
+    sh.warp_max[warp] = wmax;
+    sh.warp_min[warp] = wmin;
+    sh.warp_kth[warp] = kth;
+  }
+  if (tid == 0) sh.count = 0;
+  __syncthreads();
+  if (k <= 0) return;
+
+  uint32_t total = 0, M = 0, m = 0xFFFFFFFFu, L = 0xFFFFFFFFu;
+  for (int i = 0; i < nwarps; ++i) {
+    total += sh.warp_count[i];
+    M = max(M, sh.warp_max[i]);
+    m = min(m, sh.warp_min[i]);
+    L = min(L, sh.warp_kth[i]);
+  }
+  const int32_t K = static_cast<int32_t>(min(static_cast<uint32_t>(k), total));
+  if (K == 0) {
+    for (int j = tid; j < topk; j += nthreads) out[j] = -1;
+    return;
+  }
+
+  if (fast) {
+    // 2. Candidates: keys >= L (every key above -inf when K == total).
+    const uint32_t thr = (static_cast<uint32_t>(K) == total) ? kKeyNegInf + 1u : max(L, kKeyNegInf + 1u);
+    const uint32_t cap = static_cast<uint32_t>(max(kpad, kRankMax));
+    for (int b = tid; b < nb; b += nthreads) {
+      const uint32_t key = keys[b];
+      if (key >= thr) {
+        const uint32_t pos = atomicAdd(&sh.count, 1u);
+        if (pos < cap) cand[pos] = pack_candidate(key, b);
+      }
+    }
+    __syncthreads();
+    const uint32_t n = sh.count;
+    if (n <= static_cast<uint32_t>(kRankMax)) {
+      // 3. Rank by counting.
+      rank_store(cand, static_cast<int32_t>(n), K, out, topk);
+      return;
+    }
+    __syncthreads();  // every thread has read sh.count before it is reset
+  }
+  topk_exact(keys, nb, K, total, m, M, cand, kpad, out, topk, sh);
 }
 
 }  // namespace dsa
