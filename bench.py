@@ -229,26 +229,46 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def make_runner(wl, dsa, torch, device):
-    """Device-resident inputs and one-call step function."""
+    """Device-resident inputs, an explicit workspace (so that graph capture
+    allocates nothing) and a one-call step function."""
     if hasattr(wl, "global_row_ke"):
         logits = torch.from_numpy(wl.logits).to(device)
         gke = torch.from_numpy(wl.global_row_ke).to(device)
         out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)
+        ws = torch.zeros(dsa.workspace_bytes(wl.rows, max(wl.max_global_blocks, 1)),
+                         dtype=torch.uint8, device=device)
 
         def step():
             dsa.dsa_select_candidate_blocks_sharded(logits, gke, wl.global_block_size,
                                                     wl.max_global_blocks, wl.topk_blocks, out,
-                                                    wl.row_repeat)
+                                                    wl.row_repeat, workspace=ws)
         return step, out
     logits = torch.from_numpy(wl.logits).to(device)
     ks = None if wl.row_ks is None else torch.from_numpy(wl.row_ks).to(device)
     ke = torch.from_numpy(wl.row_ke).to(device)
     out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)
+    ws = torch.zeros(dsa.workspace_bytes(wl.rows, -(-wl.width // wl.block_size)),
+                     dtype=torch.uint8, device=device)
 
     def step():
         dsa.dsa_select_candidate_blocks(logits, ks, ke, wl.topk_blocks, wl.block_size, out,
-                                        wl.row_repeat, wl.pin_newest)
+                                        wl.row_repeat, wl.pin_newest, workspace=ws)
     return step, out
+
+
+def graph_of(step, n: int, torch):
+    """A CUDA graph of n consecutive steps (launch cost paid once per replay,
+    not per step). The step must have run once before, outside capture."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(n):
+            step()
+    return g
+
+
+def steps_per_graph(k: int) -> int:
+    """Largest divisor of k up to 64: k steps are k / g replays of g steps."""
+    return max(d for d in range(1, min(k, 64) + 1) if k % d == 0)
 
 
 def e2e_measure(wl, dsa, torch, device, steps: int):
@@ -336,6 +356,15 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    # Steps are replayed from CUDA graphs so that host launch cost never
+    # starves the GPU between short steps.
+    one = graph_of(step, 1, torch)
+    per = steps_per_graph(args.steps)
+    many = graph_of(step, per, torch)
+    for _ in range(2):
+        one.replay()
+        many.replay()
+    torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     props = torch.cuda.get_device_properties(device)
     uuid = str(getattr(props, "uuid", "") or "")
@@ -351,15 +380,15 @@ def run_ours(args):
             for a, b in evs:
                 scratch.fill_(1.0)
                 a.record(stream)
-                step()
+                one.replay()
                 b.record(stream)
             torch.cuda.synchronize()
             gpu_ms = sum(a.elapsed_time(b) for a, b in evs)
         else:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for _ in range(args.steps):
-                step()
+            for _ in range(args.steps // per):
+                many.replay()
             b.record(stream)
             torch.cuda.synchronize()
             gpu_ms = a.elapsed_time(b)

@@ -45,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "dsa_status_string",
     "dsa_select_max_blocks",
     "dsa_select_max_shards",
+    "dsa_select_workspace_bytes",
     "dsa_block_scores",
     "dsa_select_candidate_blocks",
     "dsa_select_candidate_blocks_sharded",
@@ -77,11 +78,14 @@ def library():
     lib.dsa_select_max_blocks.restype = i32
     lib.dsa_select_max_shards.argtypes = []
     lib.dsa_select_max_shards.restype = i32
+    lib.dsa_select_workspace_bytes.argtypes = [i64, i64]
+    lib.dsa_select_workspace_bytes.restype = ctypes.c_size_t
     lib.dsa_block_scores.argtypes = [p, i64, i64, i64, p, p, i32, i32, i32, p, i64, p]
+    sz = ctypes.c_size_t
     lib.dsa_select_candidate_blocks.argtypes = [p, i64, i64, i64, p, p, i32, i32, i32, i32,
-                                                p, i64, p, i64, p]
+                                                p, i64, p, i64, p, sz, p]
     lib.dsa_select_candidate_blocks_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32,
-                                                        i32, i32, p, i64, p, i64, p]
+                                                        i32, i32, p, i64, p, i64, p, sz, p]
     for f in (lib.dsa_block_scores, lib.dsa_select_candidate_blocks,
               lib.dsa_select_candidate_blocks_sharded):
         f.restype = ctypes.c_int
@@ -101,6 +105,39 @@ def max_select_blocks() -> int:
 def _torch():
     import torch
     return torch
+
+
+def workspace_bytes(rows: int, nblocks: int) -> int:
+    """Bytes of workspace that let a selecting call split rows over CTAs."""
+    return int(library().dsa_select_workspace_bytes(rows, nblocks))
+
+
+_ws_cache = {}
+
+
+def _workspace(workspace, rows: int, nblocks: int, device, stream_handle):
+    """(pointer, bytes) of the workspace for one call.
+
+    ``workspace`` may be a CUDA tensor (zero-filled before its first use,
+    written by nothing but these calls, and not shared by calls that can
+    overlap), ``False`` (no workspace: one CTA per row) or ``None``: a
+    zero-filled workspace cached per (device, stream) and grown when a call
+    needs more."""
+    torch = _torch()
+    if workspace is False:
+        return None, 0
+    if workspace is not None:
+        if not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA tensor")
+        return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    need = workspace_bytes(rows, nblocks)
+    key = (device.index if device.index is not None else torch.cuda.current_device(),
+           stream_handle)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < need:
+        buf = torch.zeros(need, dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf.data_ptr(), buf.numel()
 
 
 def _stream_handle(stream) -> Optional[int]:
@@ -149,11 +186,15 @@ def dsa_block_scores(logits, row_ks, row_ke, block_size: int, row_repeat: int = 
 
 def dsa_select_candidate_blocks(logits, row_ks, row_ke, topk_blocks: int, block_size: int,
                                 out, row_repeat: int = 1, pin_newest: bool = True,
-                                scores_out=None, stream=None):
+                                scores_out=None, stream=None, workspace=None):
     """Write ranked candidate block ids (-1 padded) into ``out`` [rows, >=topk]
-    int32; optionally the ranked block scores into ``scores_out``."""
+    int32; optionally the ranked block scores into ``scores_out``.
+    ``workspace``: see ``_workspace``."""
     torch = _torch()
     rows, width = logits.shape
+    nb = -(-width // block_size) if block_size > 0 else 0
+    handle = _stream_handle(stream)
+    ws_ptr, ws_bytes = _workspace(workspace, rows, nb, logits.device, handle)
     st = library().dsa_select_candidate_blocks(
         _dev_ptr(logits, torch.float32, "logits"), rows, width, _row_major(logits, "logits"),
         _dev_ptr(row_ks, torch.int32, "row_ks", allow_none=True),
@@ -162,18 +203,23 @@ def dsa_select_candidate_blocks(logits, row_ks, row_ke, topk_blocks: int, block_
         _row_major(out, "out") if out.dim() == 2 else topk_blocks,
         _dev_ptr(scores_out, torch.float32, "scores_out", allow_none=True),
         _row_major(scores_out, "scores_out") if scores_out is not None else 0,
-        _stream_handle(stream))
+        ws_ptr, ws_bytes, handle)
     _check("dsa_select_candidate_blocks", st)
     return out
 
 
 def dsa_select_candidate_blocks_sharded(logits, global_row_ke, global_block_size: int,
                                         max_global_blocks: int, topk_blocks: int, out,
-                                        row_repeat: int = 1, scores_out=None, stream=None):
+                                        row_repeat: int = 1, scores_out=None, stream=None,
+                                        workspace=None):
     """DCP form: ``logits`` is ``[D, rows, local_width]`` (unit stride in the last
-    dimension); writes ranked global block ids into ``out``."""
+    dimension); writes ranked global block ids into ``out``.
+    ``workspace``: see ``_workspace``."""
     torch = _torch()
     shards, rows, lw = logits.shape
+    handle = _stream_handle(stream)
+    ws_ptr, ws_bytes = _workspace(workspace, rows, max(int(max_global_blocks), 1),
+                                  logits.device, handle)
     if logits.stride(2) != 1:
         raise ValueError("logits must have unit stride in its last dimension")
     st = library().dsa_select_candidate_blocks_sharded(
@@ -183,7 +229,7 @@ def dsa_select_candidate_blocks_sharded(logits, global_row_ke, global_block_size
         _dev_ptr(out, torch.int32, "out"), _row_major(out, "out") if out.dim() == 2 else topk_blocks,
         _dev_ptr(scores_out, torch.float32, "scores_out", allow_none=True),
         _row_major(scores_out, "scores_out") if scores_out is not None else 0,
-        _stream_handle(stream))
+        ws_ptr, ws_bytes, handle)
     _check("dsa_select_candidate_blocks_sharded", st)
     return out
 

@@ -4,23 +4,23 @@
 // stay in shared memory, the top-k runs on them in place, and only ids (and,
 // on request, block scores) are written back.
 //
-// Selecting kernel (select_kernel): one thread-block cluster of `csize` CTAs
-// per row. The row's blocks that hold in-window data are split among the
-// cluster's CTAs in units of 32 blocks; each CTA streams its share
-// (stream.cuh) into its own shared-memory key array, then copies it into the
-// leader CTA's array through distributed shared memory. After a cluster
-// barrier the leader applies the pin, writes scores if asked, and runs the
-// top-k (topk.cuh). Splitting long rows over a cluster keeps the largest unit
-// of work small, so uneven row lengths do not leave SMs idle at the end.
-// The DCP form is the same kernel reading `shards` slices per row and taking
-// the max over them before the reduction, i.e. the all-reduce MAX of
-// candidate_blocks.py's DCP branch happens in registers.
+// Selecting kernel (select_kernel): `split` CTAs per row (1 without a
+// workspace). The row's blocks that hold in-window data are divided among
+// them in units of 32 blocks; each CTA streams its share (stream.cuh) into a
+// shared-memory key array. With split = 1 the CTA then pins, writes scores if
+// asked, and runs the top-k (topk.cuh) on its own keys. With split > 1 every
+// CTA publishes its keys to the row's slice of the workspace and counts
+// itself in on the row's counter (arrive_last); the last CTA to arrive reads
+// the other shares back (they are in L2) and runs the pin and the top-k.
+// The others exit as soon as they have published, so their slots go back to
+// streaming. The DCP form is the same kernel reading `shards` slices per row
+// and taking the max over them before the reduction, i.e. the all-reduce MAX
+// of candidate_blocks.py's DCP branch happens in registers.
 //
 // Scores-only kernel (block_scores_kernel): one CTA per (row, chunk of
-// blocks), no cluster, no top-k.
+// blocks), no top-k.
 #include "../../include/dsa_cb.h"
 
-#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -36,8 +36,9 @@ namespace {
 
 constexpr int32_t kMaxSelectBlocks = 16384;
 constexpr int32_t kMaxShards = 1024;
-constexpr int32_t kSplitUnit = 32;  // blocks per unit of the in-cluster split
-constexpr int kMaxCluster = 8;
+constexpr int32_t kSplitUnit = 32;  // blocks per unit of a row split
+constexpr int kMaxSplit = 8;        // CTAs per row at most
+constexpr int kThreads = 256;       // scores-only kernel
 
 struct SelectArgs {
   const float* logits;
@@ -59,6 +60,9 @@ struct SelectArgs {
   int64_t ld_out;
   float* scores;
   int64_t ld_scores;
+  int32_t split;        // CTAs per row
+  uint32_t* ws_keys;    // split > 1: [rows, nb] block keys
+  uint32_t* ws_count;   // split > 1: [rows] arrival counters (zero between calls)
 };
 
 struct RowPlan {
@@ -69,21 +73,21 @@ struct RowPlan {
   int vec, lpb_log2;
 };
 
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t n;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
-  return n;
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+// Counts one arrival on a row's counter and returns true for the last of
+// `split`. The last arrival writes 0 back, so a completed call leaves its
+// counters at zero. A counter word can also hold block-key data left by an
+// earlier call of another shape; every block key is >= key(-inf) while a
+// count is <= kMaxSplit, so such a word is read as zero. Each failed CAS means
+// another CTA of the row succeeded, so at most `split` + 1 attempts are made.
+__device__ __forceinline__ bool arrive_last(uint32_t* counter, uint32_t split) {
+  uint32_t seen = 0u;
+  for (int i = 0; i < kMaxSplit + 2; ++i) {
+    const uint32_t count = (seen >= kKeyNegInf ? 0u : seen) + 1u;
+    const uint32_t prev = atomicCAS(counter, seen, count == split ? 0u : count);
+    if (prev == seen) return count == split;
+    seen = prev;
+  }
+  return false;
 }
 
 // Window of an unsharded row: e = min(ke, width), s = min(max(ks, 0), e).
@@ -131,26 +135,26 @@ __device__ __forceinline__ void stream_sharded(const Window& w, int lpb_log2, in
     stream_generic<4, 8>(w, block_size, b0, b1, keys, 0);
 }
 
-// One row per cluster of csize CTAs (csize is 1 unless overridden).
+// `a.split` CTAs per row.
 // SHARDED = false: unsharded rows, vector width chosen per row.
 // SHARDED = true: DCP rows; SVEC is the vector width fixed by the host
-// (0 = generic path).
-template <bool SHARDED, int SVEC>
-__global__ void __launch_bounds__(kThreads, 4) select_kernel(const SelectArgs a) {
+// (0 = generic path). T: threads per CTA.
+template <bool SHARDED, int SVEC, int T>
+__global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);  // [max(kpad, kRankMax)]
   uint32_t* keys = reinterpret_cast<uint32_t*>(cand + max(a.kpad, kRankMax));  // [nb]
   int32_t* len = reinterpret_cast<int32_t*>(keys + a.nb);                // [shards]
   __shared__ TopkShared tsh;
+  __shared__ int s_last;
 
-  const uint32_t csize = cluster_size();
-  const uint32_t crank = cluster_rank();
-  const int64_t row = blockIdx.x / csize;
+  const int32_t split = a.split;
+  const int64_t row = blockIdx.x / split;
+  const int32_t part = static_cast<int32_t>(blockIdx.x % split);
 
   RowPlan plan;
-  int32_t gke = 0;
   if constexpr (SHARDED) {
-    gke = __ldg(a.row_ke + row / a.row_repeat);
+    const int32_t gke = __ldg(a.row_ke + row / a.row_repeat);
     const int32_t n0 = shard_len(gke, 0, a.shards, a.width);
     plan.origin = a.logits + row * a.ld;
     plan.len_max = n0;
@@ -173,14 +177,11 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const SelectArgs a)
 
   const int32_t nblk = plan.nblk;
   const int32_t units = (nblk + kSplitUnit - 1) / kSplitUnit;
-  const int32_t b0 = min(static_cast<int32_t>(crank * units / csize) * kSplitUnit, nblk);
-  const int32_t b1 = min(static_cast<int32_t>((crank + 1) * units / csize) * kSplitUnit, nblk);
+  const int32_t b0 = min(part * units / split * kSplitUnit, nblk);
+  const int32_t b1 = min((part + 1) * units / split * kSplitUnit, nblk);
 
   for (int32_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) keys[b] = kKeyNegInf;
-  if (crank == 0)
-    for (int32_t b = nblk + threadIdx.x; b < a.nb; b += blockDim.x) keys[b] = kKeyNegInf;
   __syncthreads();
-  if (csize > 1) cluster_arrive();  // phase 0: this CTA has started
 
   Window w;
   w.origin = plan.origin;
@@ -207,19 +208,22 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const SelectArgs a)
   }
   __syncthreads();
 
-  if (csize > 1) {
-    cluster_wait();  // every CTA of the cluster has started
-    if (crank != 0 && b0 < b1) {
-      namespace cg = cooperative_groups;
-      uint32_t* leader = cg::this_cluster().map_shared_rank(keys, 0);
-      for (int32_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) leader[b] = keys[b];
-    }
-    cluster_arrive();  // phase 1: shares delivered
-    cluster_wait();
-    if (crank != 0) return;
+  if (split > 1) {
+    // Publish this share, count in; only the last CTA of the row goes on.
+    uint32_t* wrow = a.ws_keys + row * a.nb;
+    for (int32_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) __stcg(wrow + b, keys[b]);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = arrive_last(a.ws_count + row, static_cast<uint32_t>(split));
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int32_t b = threadIdx.x; b < nblk; b += blockDim.x)
+      if (b < b0 || b >= b1) keys[b] = __ldcg(wrow + b);
   }
+  for (int32_t b = nblk + threadIdx.x; b < a.nb; b += blockDim.x) keys[b] = kKeyNegInf;
+  __syncthreads();
 
-  // Leader: pin, scores, selection.
   topk_store(keys, a.nb, min(a.topk, a.nb), plan.pin_block, cand, a.kpad,
              a.topk > 0 ? a.out + row * a.ld_out : nullptr, a.topk,
              a.scores ? a.scores + row * a.ld_scores : nullptr, tsh);
@@ -284,16 +288,20 @@ __global__ void fill_minus_one_kernel(int32_t* out, int64_t rows, int32_t cols, 
 // Host side
 // ---------------------------------------------------------------------------
 
-int g_cluster_override = -1;  // DSA_CB_CLUSTER: 0 = automatic, 1..8 forced
+// Tuning overrides, read once: DSA_CB_SPLIT (CTAs per row, 1..8, used only
+// with a workspace) and DSA_CB_THREADS (128 or 256 threads per CTA).
+int g_split_override = 0, g_threads_override = 0;
 std::once_flag g_env_once;
 
-int cluster_override() {
+void read_overrides() {
   std::call_once(g_env_once, [] {
-    const char* s = std::getenv("DSA_CB_CLUSTER");
-    g_cluster_override = s ? std::atoi(s) : 0;
-    if (g_cluster_override < 0 || g_cluster_override > kMaxCluster) g_cluster_override = 0;
+    const char* s = std::getenv("DSA_CB_SPLIT");
+    const int v = s ? std::atoi(s) : 0;
+    g_split_override = (v >= 1 && v <= kMaxSplit) ? v : 0;
+    const char* t = std::getenv("DSA_CB_THREADS");
+    const int u = t ? std::atoi(t) : 0;
+    g_threads_override = (u == 128 || u == 256) ? u : 0;
   });
-  return g_cluster_override;
 }
 
 int32_t next_pow2(int32_t x) {
@@ -302,12 +310,56 @@ int32_t next_pow2(int32_t x) {
   return p;
 }
 
-// CTAs per row. One by default: splitting rows over thread-block clusters
-// measured slower on every workload (a cluster needs all its CTA slots free
-// in one GPC at once). DSA_CB_CLUSTER=2..8 forces a split for experiments.
-int choose_cluster(int64_t /*max_row_bytes*/) {
-  const int forced = cluster_override();
-  return forced > 0 ? forced : 1;
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace layout: rows arrival counters (uint32), then rows * nb block keys
+// (uint32), each part 256-byte aligned.
+size_t workspace_bytes(int64_t rows, int64_t nb) {
+  return align256(static_cast<size_t>(rows) * 4) +
+         align256(static_cast<size_t>(rows) * static_cast<size_t>(nb) * 4);
+}
+
+// Streaming multiprocessors of the current device, cached per device.
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Launch shape (measured on GB300 over the five workloads):
+//  - 128 threads per CTA (8 CTAs per SM at 64 registers) unless rows can be
+//    512 KiB long, then 256: a CTA's top-k leaves fewer threads idle and more
+//    rows are in flight; very long rows need the larger CTA's loads in flight.
+//  - Rows are split over S CTAs (with a workspace) only while there are fewer
+//    than ~3 waves of CTAs, and never below 64 KiB per CTA: small CTA shares
+//    are latency-bound, and a full machine gains nothing from splitting.
+struct Shape {
+  int split;
+  int threads;
+};
+
+Shape choose_shape(int64_t max_row_bytes, int64_t rows, bool have_workspace) {
+  read_overrides();
+  Shape sh{1, max_row_bytes >= 512 * 1024 ? 256 : 128};
+  if (g_threads_override) sh.threads = g_threads_override;
+  if (have_workspace) {
+    const int64_t slots = static_cast<int64_t>(sm_count()) * (1024 / sh.threads);
+    int split = 1;
+    while (split < kMaxSplit && rows * split < 3 * slots &&
+           max_row_bytes / (2 * split) >= 64 * 1024)
+      split <<= 1;
+    sh.split = g_split_override ? g_split_override : split;
+  }
+  return sh;
 }
 
 // Opts a kernel in to `smem` bytes of dynamic shared memory on the current
@@ -347,22 +399,29 @@ cudaError_t set_smem_attr(K kernel, size_t smem) {
 }
 
 template <typename K>
-dsa_status launch_select(K kernel, const SelectArgs& a, int64_t rows, int csize, size_t smem,
+dsa_status launch_select(K kernel, const SelectArgs& a, int64_t rows, int threads, size_t smem,
                          cudaStream_t stream) {
   if (set_smem_attr(kernel, smem) != cudaSuccess) return DSA_ECUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(rows * csize));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = csize;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a) == cudaSuccess ? DSA_OK : DSA_ECUDA;
+  kernel<<<static_cast<unsigned>(rows * a.split), threads, smem, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
+}
+
+// Instantiates the kernel for the chosen thread count.
+template <bool SHARDED, int SVEC>
+dsa_status launch_shape(const SelectArgs& a, int64_t rows, const Shape& sh, size_t smem,
+                        cudaStream_t stream) {
+  if (sh.threads == 128)
+    return launch_select(select_kernel<SHARDED, SVEC, 128>, a, rows, 128, smem, stream);
+  return launch_select(select_kernel<SHARDED, SVEC, 256>, a, rows, 256, smem, stream);
+}
+
+// Fills the workspace fields of `a` for the chosen shape.
+void attach_workspace(SelectArgs& a, int64_t rows, void* workspace, const Shape& sh) {
+  a.split = sh.split;
+  if (sh.split == 1) return;
+  a.ws_count = static_cast<uint32_t*>(workspace);
+  a.ws_keys = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
+                                          align256(static_cast<size_t>(rows) * 4));
 }
 
 dsa_status fill_minus_one(int32_t* out, int64_t rows, int32_t cols, int64_t ld, cudaStream_t s) {
@@ -397,6 +456,11 @@ const char* dsa_status_string(int status) {
 
 int32_t dsa_select_max_blocks(void) { return kMaxSelectBlocks; }
 int32_t dsa_select_max_shards(void) { return kMaxShards; }
+
+size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks) {
+  if (rows < 0 || nblocks < 0) return 0;
+  return workspace_bytes(rows, nblocks);
+}
 
 dsa_status dsa_block_scores(const float* logits, int64_t rows, int64_t width, int64_t ld_logits,
                             const int32_t* row_ks, const int32_t* row_ke, int32_t block_size,
@@ -441,7 +505,8 @@ dsa_status dsa_select_candidate_blocks(const float* logits, int64_t rows, int64_
                                        const int32_t* row_ke, int32_t topk_blocks,
                                        int32_t block_size, int32_t row_repeat,
                                        int32_t pin_newest, int32_t* out, int64_t ld_out,
-                                       float* scores_out, int64_t ld_scores, void* stream) {
+                                       float* scores_out, int64_t ld_scores, void* workspace,
+                                       size_t workspace_size, void* stream) {
   if (rows < 0 || width < 0 || topk_blocks < 0 || block_size < 1 || row_repeat < 1)
     return DSA_EINVAL;
   if (rows == 0) return DSA_OK;
@@ -453,7 +518,7 @@ dsa_status dsa_select_candidate_blocks(const float* logits, int64_t rows, int64_
   if (scores_out && ld_scores < nb) return DSA_EINVAL;
   if (topk_blocks == 0 && !scores_out) return DSA_OK;
   if (nb > kMaxSelectBlocks || width > INT32_MAX - 64) return DSA_EUNSUPPORTED;
-  if (rows * kMaxCluster > INT32_MAX) return DSA_EUNSUPPORTED;
+  if (rows * kMaxSplit > INT32_MAX) return DSA_EUNSUPPORTED;
 
   SelectArgs a{};
   a.logits = logits;
@@ -474,8 +539,10 @@ dsa_status dsa_select_candidate_blocks(const float* logits, int64_t rows, int64_
   a.ld_out = ld_out;
   a.scores = scores_out;
   a.ld_scores = ld_scores;
-  const int csize = choose_cluster(width * 4);
-  return launch_select(select_kernel<false, 0>, a, rows, csize, select_smem(a.kpad, a.nb, 1), s);
+  const bool ws = workspace && workspace_size >= workspace_bytes(rows, a.nb);
+  const Shape sh = choose_shape(width * 4, rows, ws);
+  attach_workspace(a, rows, workspace, sh);
+  return launch_shape<false, 0>(a, rows, sh, select_smem(a.kpad, a.nb, 1), s);
 }
 
 dsa_status dsa_select_candidate_blocks_sharded(const float* logits, int32_t shards, int64_t rows,
@@ -486,6 +553,7 @@ dsa_status dsa_select_candidate_blocks_sharded(const float* logits, int32_t shar
                                                int32_t max_global_blocks, int32_t row_repeat,
                                                int32_t topk_blocks, int32_t* out, int64_t ld_out,
                                                float* scores_out, int64_t ld_scores,
+                                               void* workspace, size_t workspace_size,
                                                void* stream) {
   if (shards < 1 || rows < 0 || local_width < 0 || topk_blocks < 0 || global_block_size < 1 ||
       global_block_size % shards != 0 || row_repeat < 1 || ld_logits < local_width ||
@@ -499,7 +567,7 @@ dsa_status dsa_select_candidate_blocks_sharded(const float* logits, int32_t shar
   if (topk_blocks == 0 && !scores_out) return DSA_OK;
   if (nbg > kMaxSelectBlocks || shards > kMaxShards || local_width > INT32_MAX - 64)
     return DSA_EUNSUPPORTED;
-  if (rows * kMaxCluster > INT32_MAX) return DSA_EUNSUPPORTED;
+  if (rows * kMaxSplit > INT32_MAX) return DSA_EUNSUPPORTED;
 
   const int32_t lbs = global_block_size / shards;
   SelectArgs a{};
@@ -532,12 +600,14 @@ dsa_status dsa_select_candidate_blocks_sharded(const float* logits, int32_t shar
            shard_stride % vec == 0;
   };
   const size_t smem = select_smem(a.kpad, a.nb, shards);
-  const int csize = choose_cluster(local_width * 4 * shards);
+  const bool ws = workspace && workspace_size >= workspace_bytes(rows, a.nb);
+  const Shape sh = choose_shape(local_width * 4 * shards, rows, ws);
+  attach_workspace(a, rows, workspace, sh);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (aligned(4)) return launch_select(select_kernel<true, 4>, a, rows, csize, smem, s);
-  if (aligned(2)) return launch_select(select_kernel<true, 2>, a, rows, csize, smem, s);
-  if (pow2(lbs)) return launch_select(select_kernel<true, 1>, a, rows, csize, smem, s);
-  return launch_select(select_kernel<true, 0>, a, rows, csize, smem, s);
+  if (aligned(4)) return launch_shape<true, 4>(a, rows, sh, smem, s);
+  if (aligned(2)) return launch_shape<true, 2>(a, rows, sh, smem, s);
+  if (pow2(lbs)) return launch_shape<true, 1>(a, rows, sh, smem, s);
+  return launch_shape<true, 0>(a, rows, sh, smem, s);
 }
 
 }  // extern "C"

@@ -38,9 +38,6 @@
 
 namespace dsa {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-
 struct Window {
   const float* origin;   // element 0 of shard 0's window
   int64_t shard_stride;  // elements between shards
@@ -71,7 +68,8 @@ __device__ __forceinline__ void stream_pow2(const Window& w, int lpb_log2, int32
       lim[j] = (d0 + j < w.shards) ? min(w.len[d0 + j] / VEC, v_end) : 0;
     const float* base = w.origin + static_cast<int64_t>(d0) * w.shard_stride;
 
-    for (int32_t slab = v_begin + warp * kSlab; slab < v_end; slab += kWarps * kSlab) {
+    const int32_t step = static_cast<int32_t>(blockDim.x >> 5) * kSlab;
+    for (int32_t slab = v_begin + warp * kSlab; slab < v_end; slab += step) {
       float acc[NV];
 #pragma unroll
       for (int m = 0; m < NV; ++m) acc[m] = neg_inf();
@@ -171,7 +169,8 @@ __device__ __forceinline__ void stream_generic(const Window& w, int32_t block_si
   const int64_t e_end = min(static_cast<int64_t>(b1) * block_size, static_cast<int64_t>(w.len_max));
   constexpr int64_t kSlab = 32 * NV;
 
-  for (int64_t slab = e_begin + warp * kSlab; slab < e_end; slab += kWarps * kSlab) {
+  const int64_t step = static_cast<int64_t>(blockDim.x >> 5) * kSlab;
+  for (int64_t slab = e_begin + warp * kSlab; slab < e_end; slab += step) {
     float acc[NV];
 #pragma unroll
     for (int m = 0; m < NV; ++m) acc[m] = neg_inf();

@@ -16,8 +16,8 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Pointers named logits, row_ks, row_ke, global_row_ke, out and
- *    scores_out are DEVICE pointers owned by the caller. The library
+ *  - Pointers named logits, row_ks, row_ke, global_row_ke, out, scores_out
+ *    and workspace are DEVICE pointers owned by the caller. The library
  *    allocates no memory and keeps no pointer after a call returns.
  *  - Matrices are row-major with an explicit row stride in elements (ld_*).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL means the legacy
@@ -40,6 +40,7 @@
 #ifndef DSA_CB_H
 #define DSA_CB_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -63,6 +64,24 @@ int32_t dsa_select_max_blocks(void);
 
 /* Largest shard count accepted by dsa_select_candidate_blocks_sharded. */
 int32_t dsa_select_max_shards(void);
+
+/*
+ * Bytes of optional device workspace that lets the selecting entry points
+ * split each row over several CTAs: one arrival counter per row, then
+ * rows * nblocks block keys, each part 256-byte aligned. nblocks is
+ * ceil(width / block_size) for dsa_select_candidate_blocks and
+ * max(max_global_blocks, 1) for the sharded form. Returns 0 for negative
+ * arguments.
+ *
+ * Workspace contract: caller-owned device memory of at least this many bytes,
+ * all zero bytes before its first use (e.g. one cudaMemset), and written by
+ * nothing but these calls afterwards. Every completed call leaves its
+ * counters at zero; block keys that a call of another shape left where this
+ * call's counters are can never be mistaken for a count, so one workspace
+ * serves calls of any shape in turn. Two calls that may run at the same
+ * time (different streams) must not share a workspace.
+ */
+size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks);
 
 /*
  * dsa_block_scores -- per-block scores of every row (candidate_blocks.py:
@@ -104,9 +123,15 @@ dsa_status dsa_block_scores(const float *logits, int64_t rows, int64_t width,
  *   scores_out  nullable; when given, [rows, ld_scores] fp32 with
  *               ld_scores >= nb receives the block scores that were ranked
  *               (pin applied), as dsa_block_scores would write them.
+ *   workspace   nullable; see dsa_select_workspace_bytes. With a workspace
+ *               of sufficient size long rows are split over several CTAs
+ *               (their block keys meet in the workspace and the last CTA of
+ *               the row to finish ranks them); without one, one CTA handles
+ *               each row. Results are identical either way.
  *
  * rows == 0: DSA_OK, nothing written. width == 0: every slot of out is -1.
- * topk_blocks == 0 and no scores_out: DSA_OK, nothing written.
+ * topk_blocks == 0 and no scores_out: DSA_OK, nothing written. A workspace
+ * smaller than dsa_select_workspace_bytes is not used (one CTA per row).
  * DSA_EINVAL for negative rows / width / topk_blocks, block_size < 1,
  * row_repeat < 1, ld_logits < width, ld_out < topk_blocks, ld_scores < nb
  * (with scores_out), or a NULL logits / row_ke / out (out only when
@@ -121,6 +146,7 @@ dsa_status dsa_select_candidate_blocks(const float *logits, int64_t rows,
                                        int32_t row_repeat, int32_t pin_newest,
                                        int32_t *out, int64_t ld_out,
                                        float *scores_out, int64_t ld_scores,
+                                       void *workspace, size_t workspace_bytes,
                                        void *stream);
 
 /*
@@ -139,7 +165,8 @@ dsa_status dsa_select_candidate_blocks(const float *logits, int64_t rows,
  *                  every shard is its share of global block b.
  *   max_global_blocks  number of global blocks nbg = max(value, 1); ids are
  *                  in [0, nbg).
- *   out, scores_out  as for dsa_select_candidate_blocks with nb = nbg.
+ *   out, scores_out, workspace  as for dsa_select_candidate_blocks with
+ *                  nb = nbg.
  *
  * Per row: shard d's window is its first ceil((gke - d) / shards) local
  * columns when gke > d (else empty), clamped to local_width; local block
@@ -162,7 +189,7 @@ dsa_status dsa_select_candidate_blocks_sharded(
     int64_t ld_logits, int64_t shard_stride, const int32_t *global_row_ke,
     int32_t global_block_size, int32_t max_global_blocks, int32_t row_repeat,
     int32_t topk_blocks, int32_t *out, int64_t ld_out, float *scores_out,
-    int64_t ld_scores, void *stream);
+    int64_t ld_scores, void *workspace, size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

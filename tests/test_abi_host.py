@@ -57,6 +57,14 @@ def test_status_strings(lib):
         assert lib.dsa_status_string(st)
 
 
+def test_workspace_bytes(lib):
+    # one counter per row and rows * nblocks keys, each part 256-byte aligned
+    assert lib.dsa_select_workspace_bytes(4096, 1024) == 16384 + 4096 * 1024 * 4
+    assert lib.dsa_select_workspace_bytes(3, 5) == 256 + 256
+    assert lib.dsa_select_workspace_bytes(0, 7) == 0
+    assert lib.dsa_select_workspace_bytes(-1, 7) == 0
+
+
 def test_limits(lib):
     assert lib.dsa_select_max_blocks() >= 1024
     assert lib.dsa_select_max_shards() >= 8
@@ -104,12 +112,13 @@ def test_block_scores_validation(lib, kw, want):
 ])
 def test_select_validation(lib, kw, want):
     a = dict(logits=FAKE, rows=4, width=100, ld=100, ks=None, ke=FAKE, topk=4, block_size=8,
-             row_repeat=1, pin=1, out=FAKE, ld_out=4, scores=None, ld_scores=0)
+             row_repeat=1, pin=1, out=FAKE, ld_out=4, scores=None, ld_scores=0, ws=FAKE,
+             ws_bytes=1 << 20)
     a.update(kw)
     st = lib.dsa_select_candidate_blocks(a["logits"], a["rows"], a["width"], a["ld"], a["ks"],
                                          a["ke"], a["topk"], a["block_size"], a["row_repeat"],
                                          a["pin"], a["out"], a["ld_out"], a["scores"],
-                                         a["ld_scores"], None)
+                                         a["ld_scores"], a["ws"], a["ws_bytes"], None)
     assert st == want
 
 
@@ -135,10 +144,11 @@ def test_select_validation(lib, kw, want):
 ])
 def test_sharded_validation(lib, kw, want):
     a = dict(logits=FAKE, shards=8, rows=4, lw=64, ld=64, shard_stride=256, gke=FAKE, gbs=64,
-             max_gb=8, row_repeat=1, topk=4, out=FAKE, ld_out=4, scores=None, ld_scores=0)
+             max_gb=8, row_repeat=1, topk=4, out=FAKE, ld_out=4, scores=None, ld_scores=0,
+             ws=None, ws_bytes=0)
     a.update(kw)
     st = lib.dsa_select_candidate_blocks_sharded(
         a["logits"], a["shards"], a["rows"], a["lw"], a["ld"], a["shard_stride"], a["gke"],
         a["gbs"], a["max_gb"], a["row_repeat"], a["topk"], a["out"], a["ld_out"], a["scores"],
-        a["ld_scores"], None)
+        a["ld_scores"], a["ws"], a["ws_bytes"], None)
     assert st == want

@@ -6,11 +6,12 @@ input elements, so the tolerance is zero). Outputs are written into views
 of larger buffers whose guard columns must come back untouched, and rows of
 logits can be padded (ld > width) with values that must never win.
 
-Sizes span several 32-block split units, every cluster size the launcher
-picks (1 to 8 CTAs per row), both top-k sort networks (K <= 32 in one warp,
-larger K in shared memory), every streaming path (vector widths 4 / 2 / 1
-and the generic path for non-power-of-two blocks), ragged window ends and
-unaligned window starts.
+Every case runs twice: with a workspace, where rows are split over the 1 to 8
+CTAs the launcher picks for the width, and without one (one CTA per row).
+Sizes span several 32-block split units, both CTA sizes, both top-k paths
+(bound-and-rank, and the exact radix path with its bitonic sort for large
+K), every streaming path (vector widths 4 / 2 / 1 and the generic path for
+non-power-of-two blocks), ragged window ends and unaligned window starts.
 """
 
 import numpy as np
@@ -54,7 +55,7 @@ def _padded_logits(torch, logits, width, offset):
     return flat.view(rows, ld)[:, :width]
 
 
-def run_unsharded(env, wl, *, want_scores=True, offset=0):
+def run_unsharded(env, wl, *, want_scores=True, offset=0, workspace=None):
     torch, dsa = env
     rows, width, topk = wl.rows, wl.width, wl.topk_blocks
     nb = -(-width // wl.block_size) if width else 0
@@ -65,7 +66,8 @@ def run_unsharded(env, wl, *, want_scores=True, offset=0):
     dsa.dsa_select_candidate_blocks(logits, _dev(torch, wl.row_ks), _dev(torch, wl.row_ke), topk,
                                     wl.block_size, out_buf[:, :topk], wl.row_repeat,
                                     wl.pin_newest,
-                                    scores_out=sc_buf[:, :nb] if want_scores else None)
+                                    scores_out=sc_buf[:, :nb] if want_scores else None,
+                                    workspace=workspace)
     torch.cuda.synchronize()
     out_all, sc_all = out_buf.cpu().numpy(), sc_buf.cpu().numpy()
     assert (out_all[:, topk:] == SENTINEL_ID).all(), "guard ids overwritten"
@@ -77,13 +79,15 @@ def run_unsharded(env, wl, *, want_scores=True, offset=0):
 
 def check_unsharded(env, wl, *, offset=0, with_scores=True):
     ref_ids, ref_scores = oracle.run_workload(wl)
-    got_ids, got_scores = run_unsharded(env, wl, want_scores=with_scores, offset=offset)
-    np.testing.assert_array_equal(got_ids, ref_ids)
-    if with_scores and ref_scores is not None and wl.width:
-        assert_bits_equal(got_scores, ref_scores)
+    for ws in (None, False):
+        got_ids, got_scores = run_unsharded(env, wl, want_scores=with_scores, offset=offset,
+                                            workspace=ws)
+        np.testing.assert_array_equal(got_ids, ref_ids)
+        if with_scores and ref_scores is not None and wl.width:
+            assert_bits_equal(got_scores, ref_scores)
 
 
-def run_sharded(env, wl, *, offset=0, want_scores=True):
+def run_sharded(env, wl, *, offset=0, want_scores=True, workspace=None):
     torch, dsa = env
     D, rows, lw = wl.logits.shape
     topk = wl.topk_blocks
@@ -97,7 +101,8 @@ def run_sharded(env, wl, *, offset=0, want_scores=True):
     dsa.dsa_select_candidate_blocks_sharded(local, _dev(torch, wl.global_row_ke),
                                             wl.global_block_size, wl.max_global_blocks, topk,
                                             out_buf[:, :topk], wl.row_repeat,
-                                            scores_out=sc_buf[:, :nbg] if want_scores else None)
+                                            scores_out=sc_buf[:, :nbg] if want_scores else None,
+                                            workspace=workspace)
     torch.cuda.synchronize()
     out_all, sc_all = out_buf.cpu().numpy(), sc_buf.cpu().numpy()
     assert (out_all[:, topk:] == SENTINEL_ID).all(), "guard ids overwritten"
@@ -107,10 +112,12 @@ def run_sharded(env, wl, *, offset=0, want_scores=True):
 
 def check_sharded(env, wl, *, offset=0, with_scores=True):
     ref_ids, ref_scores = oracle.run_workload(wl)
-    got_ids, got_scores = run_sharded(env, wl, offset=offset, want_scores=with_scores)
-    np.testing.assert_array_equal(got_ids, ref_ids)
-    if with_scores:
-        assert_bits_equal(got_scores, ref_scores)
+    for ws in (None, False):
+        got_ids, got_scores = run_sharded(env, wl, offset=offset, want_scores=with_scores,
+                                          workspace=ws)
+        np.testing.assert_array_equal(got_ids, ref_ids)
+        if with_scores:
+            assert_bits_equal(got_scores, ref_scores)
 
 
 # ---------------------------------------------------------------------------
@@ -256,6 +263,58 @@ def test_all_nan_and_all_inf_rows(env):
     check_unsharded(env, wl)
     wl.pin_newest = True
     check_unsharded(env, wl)
+
+
+def test_workspace_reuse_across_shapes(env):
+    """A caller-owned, zero-filled workspace serves calls of different shapes
+    in turn: key data one call leaves where a later call keeps its arrival
+    counters is never taken for a count."""
+    torch, dsa = env
+    ws = torch.zeros(dsa.workspace_bytes(600, 2048), dtype=torch.uint8, device="cuda")
+    cases = [workloads.small_unsharded(40, rows=300, width=131072, block_size=64,
+                                       topk_blocks=32, starts=False),
+             workloads.small_unsharded(41, rows=17, width=70000, block_size=128, topk_blocks=7),
+             workloads.small_unsharded(42, rows=200, width=40000, block_size=32,
+                                       topk_blocks=40, bf16_grid=True)]
+    for wl in cases:
+        ref_ids, _ = oracle.run_workload(wl)
+        for _ in range(2):
+            got, _ = run_unsharded(env, wl, want_scores=False, workspace=ws)
+            np.testing.assert_array_equal(got, ref_ids)
+    # the calls above left block keys all over the workspace; a larger call
+    # now finds them where its counters are
+    wl = workloads.small_unsharded(43, rows=600, width=131072, block_size=128,
+                                   topk_blocks=16, starts=False)
+    ref_ids, _ = oracle.run_workload(wl)
+    for _ in range(2):
+        got, _ = run_unsharded(env, wl, want_scores=False, workspace=ws)
+        np.testing.assert_array_equal(got, ref_ids)
+
+
+@pytest.mark.parametrize("sharded", [False, True])
+def test_graph_replay_matches_oracle(env, sharded):
+    """The bench replays selection from CUDA graphs: replays must give the
+    oracle's ids, including the workspace split path."""
+    torch, dsa = env
+    import bench
+
+    if sharded:
+        wl, _ = workloads.small_sharded(60, shards=8, rows=96, global_width=65536,
+                                        global_block_size=64, max_global_blocks=1024,
+                                        topk_blocks=32)
+    else:
+        wl = workloads.small_unsharded(61, rows=96, width=65536, block_size=64, topk_blocks=32,
+                                       row_repeat=8, starts=False, bf16_grid=True)
+    ref_ids, _ = oracle.run_workload(wl)
+    step, out = bench.make_runner(wl, dsa, torch, torch.device("cuda"))
+    step()
+    torch.cuda.synchronize()
+    g = bench.graph_of(step, 3, torch)
+    out.fill_(-9)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), ref_ids)
 
 
 def test_non_default_stream(env):
