@@ -49,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "dsa_block_scores",
     "dsa_select_candidate_blocks",
     "dsa_select_candidate_blocks_sharded",
+    "dsa_select_candidate_blocks_sharded_static",
 )
 
 _lib = None

@@ -611,3 +611,75 @@ dsa_status dsa_select_candidate_blocks_sharded(const float* logits, int32_t shar
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point
+// ---------------------------------------------------------------------------
+//
+// dsa_select_candidate_blocks_sharded_static: the sharded selection with its
+// workspace taken from a fixed array in device memory that this library
+// declares at file scope, for callers that must not allocate device memory at
+// call time. Examples: serving engines whose memory planner reserves nearly
+// all of HBM (KV cache pools) at start-up, so that a cudaMalloc in the middle
+// of a step can fail or block on the allocator; and plugin hosts whose
+// operators may not allocate behind the host framework's back.
+//
+// The array (kStaticScratchBytes) is created when the library's device code
+// is loaded on a GPU and stays there until the process exits; every call on
+// that GPU shares it. In host code the array's name is only a host-side
+// stand-in, so its device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current.
+
+namespace dsa {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void* g_static_addr[64] = {};
+
+// Device address of g_static_scratch on the current device (looked up on
+// the first call per device).
+cudaError_t static_scratch_address(void** addr) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (err != cudaSuccess) return err;
+    g_static_addr[dev] = p;
+  }
+  *addr = g_static_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" dsa_status dsa_select_candidate_blocks_sharded_static(
+    const float* logits, int32_t shards, int64_t rows, int64_t local_width, int64_t ld_logits,
+    int64_t shard_stride, const int32_t* global_row_ke, int32_t global_block_size,
+    int32_t max_global_blocks, int32_t row_repeat, int32_t topk_blocks, int32_t* out,
+    int64_t ld_out, float* scores_out, int64_t ld_scores, void* stream) {
+  if (rows <= 0)
+    return dsa_select_candidate_blocks_sharded(
+        logits, shards, rows, local_width, ld_logits, shard_stride, global_row_ke,
+        global_block_size, max_global_blocks, row_repeat, topk_blocks, out, ld_out, scores_out,
+        ld_scores, nullptr, 0, stream);
+  const int64_t nbg = max_global_blocks > 1 ? max_global_blocks : 1;
+  if (dsa::workspace_bytes(rows, nbg) > dsa::kStaticScratchBytes) return DSA_EUNSUPPORTED;
+  void* scratch = nullptr;
+  if (dsa::static_scratch_address(&scratch) != cudaSuccess) return DSA_ECUDA;
+  // The array keeps the previous call's contents: clear the arrival counters.
+  if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(rows) * 4,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DSA_ECUDA;
+  return dsa_select_candidate_blocks_sharded(
+      logits, shards, rows, local_width, ld_logits, shard_stride, global_row_ke,
+      global_block_size, max_global_blocks, row_repeat, topk_blocks, out, ld_out, scores_out,
+      ld_scores, scratch, dsa::kStaticScratchBytes, stream);
+}

@@ -191,6 +191,38 @@ dsa_status dsa_select_candidate_blocks_sharded(
     int32_t topk_blocks, int32_t *out, int64_t ld_out, float *scores_out,
     int64_t ld_scores, void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * dsa_select_candidate_blocks_sharded_static -- dsa_select_candidate_blocks_
+ * sharded without a caller-supplied workspace. The pages have no counterpart:
+ * this entry point exists for callers that must not allocate device memory
+ * when they call, such as serving engines whose memory planner reserves
+ * nearly all of HBM at start-up (a cudaMalloc in the middle of a step could
+ * fail or stall on the allocator) and plugin hosts whose operators may not
+ * allocate on their own.
+ *
+ * It allocates nothing. Its workspace is a fixed 8 MiB array that the library
+ * declares in device memory; every GPU that loads the library holds that
+ * array until the process exits, and all calls on a GPU share it.
+ *
+ *   Arguments, results and errors are those of
+ *   dsa_select_candidate_blocks_sharded (without workspace and
+ *   workspace_bytes), plus DSA_EUNSUPPORTED when
+ *   dsa_select_workspace_bytes(rows, max(max_global_blocks, 1)) exceeds
+ *   8 MiB (8388608 bytes).
+ *
+ * The first call on each device looks up the array's device address with that
+ * device current; make that first call before any stream capture. Each call
+ * clears the array's arrival counters with cudaMemsetAsync on `stream`.
+ * Calls that overlap on the GPU (different streams, or different host
+ * threads) race on the shared array and must not be issued.
+ */
+dsa_status dsa_select_candidate_blocks_sharded_static(
+    const float *logits, int32_t shards, int64_t rows, int64_t local_width,
+    int64_t ld_logits, int64_t shard_stride, const int32_t *global_row_ke,
+    int32_t global_block_size, int32_t max_global_blocks, int32_t row_repeat,
+    int32_t topk_blocks, int32_t *out, int64_t ld_out, float *scores_out,
+    int64_t ld_scores, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
