@@ -221,10 +221,13 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
     for (int32_t b = threadIdx.x; b < nblk; b += blockDim.x)
       if (b < b0 || b >= b1) keys[b] = __ldcg(wrow + b);
   }
-  for (int32_t b = nblk + threadIdx.x; b < a.nb; b += blockDim.x) keys[b] = kKeyNegInf;
+  // Blocks past the data blocks up to the pin are -inf (the pin can lie past
+  // the data in the DCP form); topk_store never reads further.
+  for (int32_t b = nblk + threadIdx.x; b <= plan.pin_block; b += blockDim.x) keys[b] = kKeyNegInf;
   __syncthreads();
 
-  topk_store(keys, a.nb, min(a.topk, a.nb), plan.pin_block, cand, a.kpad,
+  topk_store(keys, a.nb, max(nblk, plan.pin_block + 1), min(a.topk, a.nb), plan.pin_block,
+             cand, a.kpad,
              a.topk > 0 ? a.out + row * a.ld_out : nullptr, a.topk,
              a.scores ? a.scores + row * a.ld_scores : nullptr, tsh);
 }

@@ -8,13 +8,17 @@
 // exactly "score descending, then lower id first". Only keys above key(-inf)
 // can be selected (a -inf block yields -1); K = min(k, their count).
 //
-// Fast path (k <= 8 * warps): thread t owns keys t, t + T, t + 2T, ... Each
-// warp finds the R-th largest key of its own keys, R = ceil(k / warps), with
-// R rounds of redux.sync at most. At least R keys of every warp are >= that
-// warp's value, so at least k keys are >= L, the smallest of the warps'
-// values. The candidates are the keys >= L (a few more than k on typical
-// rows); each is ranked by counting the candidates above it and rank r < K
-// is stored in slot r. Two barriers, no sort network, no tie handling.
+// Only the row's live blocks are touched: blocks past the last one holding
+// in-window data (or the pin) are -inf by construction.
+//
+// Fast path (k <= 32 * warps, up to 8 live keys per thread): thread t holds
+// keys t, t + T, ... in registers. Each warp ranks its 32 lane maxima with
+// shuffles and takes the R-th largest, R = ceil(k / warps): R lanes each hold
+// a key at or above it, so every warp has at least R keys >= its value and
+// at least k keys are >= L, the smallest of the warps' values. The
+// candidates are the keys >= L (a few more than k on typical rows); each is
+// ranked by counting the candidates above it and rank r < K is stored in
+// slot r. Two barriers, no sort network, no tie handling.
 //
 // Exact path (larger k, or more candidates than kRankMax): radix select for
 // the K-th largest key with 8-bit digits starting right below the common
@@ -198,59 +202,81 @@ __device__ void topk_exact(const uint32_t* __restrict__ keys, int32_t nb, int32_
   for (int j = tid; j < topk; j += nthreads) out[j] = (j < K) ? candidate_id(cand[j]) : -1;
 }
 
-// keys: [nb] in shared memory; block pin_block (if >= 0) becomes +inf here.
-// cand: [max(kpad, kRankMax)] in shared memory, kpad a power of two
-// >= min(k, nb). out: this row's output slots (global; unused when k == 0).
-// scores: optional fp32 row (nb entries) written with the final scores.
-// Every thread of the CTA calls this.
-__device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t k, int32_t pin_block,
-                           uint64_t* __restrict__ cand, int32_t kpad, int32_t* __restrict__ out,
-                           int32_t topk, float* __restrict__ scores, TopkShared& sh) {
+// keys: [nb] in shared memory, every block at or past n_live equal to
+// key(-inf) (n_live covers the pinned block); block pin_block (if >= 0)
+// becomes +inf here. cand: [max(kpad, kRankMax)] in shared memory, kpad a
+// power of two >= min(k, nb). out: this row's output slots (global; unused
+// when k == 0). scores: optional fp32 row (nb entries) written with the final
+// scores. Every thread of the CTA calls this.
+__device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t n_live, int32_t k,
+                           int32_t pin_block, uint64_t* __restrict__ cand, int32_t kpad,
+                           int32_t* __restrict__ out, int32_t topk, float* __restrict__ scores,
+                           TopkShared& sh) {
+  constexpr int KR = 8;  // live keys per thread held in registers
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int nthreads = blockDim.x;
   const int nwarps = nthreads >> 5;
-  const bool fast = k > 0 && k <= 8 * nwarps;
+  const bool in_regs = n_live <= KR * nthreads;
+  const bool fast = k > 0 && k <= 32 * nwarps && in_regs;
   const int R = fast ? (k + nwarps - 1) / nwarps : 0;
 
-  // 1. Each thread touches only its own keys: pin, scores, count, min, max,
-  // then its warp's R-th largest key (with multiplicity).
+  if (scores)
+    for (int b = tid; b < nb; b += nthreads)
+      scores[b] = key_score(b == pin_block ? kKeyPosInf : (b < n_live ? keys[b] : kKeyNegInf));
+
+  // 1. Each thread takes its own keys b = tid + i*T: pin, count, min, max and
+  // its largest key (lane max).
+  uint32_t kr[KR];
   uint32_t cnt = 0, mx = 0, mn = 0xFFFFFFFFu;
-  for (int b = tid; b < nb; b += nthreads) {
-    uint32_t key = keys[b];
-    if (b == pin_block) {
-      key = kKeyPosInf;
-      keys[b] = key;
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < KR; ++i) {
+      const int b = tid + i * nthreads;
+      uint32_t key = b < n_live ? keys[b] : kKeyNegInf;
+      if (b == pin_block) {
+        key = kKeyPosInf;
+        keys[b] = key;
+      }
+      kr[i] = key;
+      if (key > kKeyNegInf) {
+        ++cnt;
+        mx = max(mx, key);
+        mn = min(mn, key);
+      }
     }
-    if (scores) scores[b] = key_score(key);
-    if (key > kKeyNegInf) {
-      ++cnt;
-      mx = max(mx, key);
-      mn = min(mn, key);
+  } else {
+    for (int b = tid; b < n_live; b += nthreads) {
+      uint32_t key = keys[b];
+      if (b == pin_block) {
+        key = kKeyPosInf;
+        keys[b] = key;
+      }
+      if (key > kKeyNegInf) {
+        ++cnt;
+        mx = max(mx, key);
+        mn = min(mn, key);
+      }
     }
+  }
+  // Warp bound: the R-th largest lane max. R lanes each hold a key at or
+  // above it, so at least R of the warp's keys are >= it.
+  uint32_t kth = kKeyNegInf;
+  if (fast) {
+    int rank = 0;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t o = __shfl_sync(0xffffffffu, mx, j);
+      rank += (o > mx) || (o == mx && j < lane);
+    }
+    const uint32_t who = __ballot_sync(0xffffffffu, rank == R - 1);
+    kth = __shfl_sync(0xffffffffu, mx, __ffs(who) - 1);
+    if (kth <= kKeyNegInf) kth = kKeyNegInf;  // fewer than R lanes hold keys
   }
   cnt = __reduce_add_sync(0xffffffffu, cnt);
   const uint32_t wmax = __reduce_max_sync(0xffffffffu, mx);
   const uint32_t wmin = __reduce_min_sync(0xffffffffu, mn);
-  uint32_t kth = kKeyNegInf;
-  if (fast) {
-    uint32_t bound = wmax;  // candidate value of this round
-    int have = 0;
-    for (int r = 0; r < R && bound > kKeyNegInf; ++r) {
-      uint32_t c = 0, below = 0;
-      for (int b = tid; b < nb; b += nthreads) {
-        const uint32_t key = keys[b];
-        c += key == bound;
-        if (key < bound && key > kKeyNegInf) below = max(below, key);
-      }
-      have += static_cast<int>(__reduce_add_sync(0xffffffffu, c));
-      kth = bound;
-      if (have >= R) break;
-      bound = __reduce_max_sync(0xffffffffu, below);
-    }
-    if (have < R) kth = kKeyNegInf;  // fewer than R keys above -inf here
-  }
   if (lane == 0) {
     sh.warp_count[warp] = cnt;
     sh.warp_max[warp] = wmax;
@@ -278,11 +304,11 @@ __device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t k, i
     // 2. Candidates: keys >= L (every key above -inf when K == total).
     const uint32_t thr = (static_cast<uint32_t>(K) == total) ? kKeyNegInf + 1u : max(L, kKeyNegInf + 1u);
     const uint32_t cap = static_cast<uint32_t>(max(kpad, kRankMax));
-    for (int b = tid; b < nb; b += nthreads) {
-      const uint32_t key = keys[b];
-      if (key >= thr) {
+#pragma unroll
+    for (int i = 0; i < KR; ++i) {
+      if (kr[i] >= thr) {
         const uint32_t pos = atomicAdd(&sh.count, 1u);
-        if (pos < cap) cand[pos] = pack_candidate(key, b);
+        if (pos < cap) cand[pos] = pack_candidate(kr[i], tid + i * nthreads);
       }
     }
     __syncthreads();
@@ -294,7 +320,7 @@ __device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t k, i
     }
     __syncthreads();  // every thread has read sh.count before it is reset
   }
-  topk_exact(keys, nb, K, total, m, M, cand, kpad, out, topk, sh);
+  topk_exact(keys, n_live, K, total, m, M, cand, kpad, out, topk, sh);
 }
 
 }  // namespace dsa
