@@ -30,6 +30,7 @@
 #include "keys.cuh"
 #include "stream.cuh"
 #include "topk.cuh"
+#include "topk_warp.cuh"
 
 namespace dsa {
 namespace {
@@ -63,6 +64,7 @@ struct SelectArgs {
   int32_t split;        // CTAs per row
   uint32_t* ws_keys;    // split > 1: [rows, nb] block keys
   uint32_t* ws_count;   // split > 1: [rows] arrival counters (zero between calls)
+  int64_t rows;         // select_warp_kernel: rows to handle
 };
 
 struct RowPlan {
@@ -125,14 +127,15 @@ __device__ __forceinline__ int32_t shard_len(int32_t gke, int32_t d, int32_t sha
 template <int SVEC>
 __device__ __forceinline__ void stream_sharded(const Window& w, int lpb_log2, int32_t block_size,
                                                int32_t b0, int32_t b1, uint32_t* keys) {
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   if constexpr (SVEC == 4)
-    stream_pow2<4, 1, 8>(w, lpb_log2, b0, b1, keys, 0);
+    stream_pow2<4, 1, 8>(w, lpb_log2, b0, b1, keys, 0, warp, nwarps);
   else if constexpr (SVEC == 2)
-    stream_pow2<2, 2, 8>(w, lpb_log2, b0, b1, keys, 0);
+    stream_pow2<2, 2, 8>(w, lpb_log2, b0, b1, keys, 0, warp, nwarps);
   else if constexpr (SVEC == 1)
-    stream_pow2<1, 4, 8>(w, lpb_log2, b0, b1, keys, 0);
+    stream_pow2<1, 4, 8>(w, lpb_log2, b0, b1, keys, 0, warp, nwarps);
   else
-    stream_generic<4, 8>(w, block_size, b0, b1, keys, 0);
+    stream_generic<4, 8>(w, block_size, b0, b1, keys, 0, warp, nwarps);
 }
 
 // `a.split` CTAs per row.
@@ -193,7 +196,8 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
     if constexpr (SHARDED)
       stream_sharded<SVEC>(w, plan.lpb_log2, a.block_size, b0, b1, keys);
     else
-      stream_row(w, plan.vec, plan.lpb_log2, a.block_size, b0, b1, keys, 0);
+      stream_row(w, plan.vec, plan.lpb_log2, a.block_size, b0, b1, keys, 0, threadIdx.x >> 5,
+                 blockDim.x >> 5);
   }
   __syncthreads();
   if constexpr (SHARDED) {
@@ -232,6 +236,47 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
              a.scores ? a.scores + row * a.ld_scores : nullptr, tsh);
 }
 
+// Shared memory per warp in select_warp_kernel: candidates, keys, length.
+__host__ __device__ __forceinline__ size_t warp_slice_bytes(int32_t nb) {
+  return static_cast<size_t>(kWarpCand) * 8 + static_cast<size_t>((nb + 3) & ~3) * 4 + 16;
+}
+
+// One row per warp, W warps per CTA, for short unsharded rows: each warp
+// streams its row alone (stream_row with one warp) into its own key array
+// and ranks it with topk_warp; no CTA barrier anywhere, so W rows of a CTA
+// proceed independently and up to 32 rows are in flight per SM.
+template <int W>
+__global__ void __launch_bounds__(W * 32, 1024 / (W * 32)) select_warp_kernel(const SelectArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * W + warp;
+  if (row >= a.rows) return;
+  unsigned char* slice = smem_raw + warp * warp_slice_bytes(a.nb);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(slice);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(cand + kWarpCand);
+  int32_t* len = reinterpret_cast<int32_t*>(keys + ((a.nb + 3) & ~3));
+
+  const RowPlan plan = plan_unsharded(a.logits, a.ld, a.width, a.row_ks, a.row_ke, a.row_repeat,
+                                      a.block_size, a.pin_newest, row);
+  if (lane == 0) len[0] = plan.len_max;
+  const int32_t nblk = plan.nblk;
+  for (int32_t b = lane; b < nblk; b += 32) keys[b] = kKeyNegInf;
+  __syncwarp();
+  Window w;
+  w.origin = plan.origin;
+  w.shard_stride = 0;
+  w.shards = 1;
+  w.len = len;
+  w.len_max = plan.len_max;
+  if (nblk > 0) stream_row(w, plan.vec, plan.lpb_log2, a.block_size, 0, nblk, keys, 0, 0, 1);
+  __syncwarp();
+  if (lane == 0) commit_partial(load_partial_row(w, plan.vec, a.block_size, 0, nblk), keys, 0);
+  __syncwarp();
+  topk_warp(keys, a.nb, nblk, min(a.topk, a.nb), plan.pin_block, cand,
+            a.topk > 0 ? a.out + row * a.ld_out : nullptr, a.topk,
+            a.scores ? a.scores + row * a.ld_scores : nullptr);
+}
+
 struct ScoresArgs {
   const float* logits;
   int64_t ld;
@@ -268,7 +313,9 @@ __global__ void __launch_bounds__(kThreads, 4) block_scores_kernel(const ScoresA
   w.shards = 1;
   w.len = len;
   w.len_max = plan.len_max;
-  if (b0 < b1) stream_row(w, plan.vec, plan.lpb_log2, a.block_size, b0, b1, keys, c0);
+  if (b0 < b1)
+    stream_row(w, plan.vec, plan.lpb_log2, a.block_size, b0, b1, keys, c0, threadIdx.x >> 5,
+               blockDim.x >> 5);
   __syncthreads();
   if (threadIdx.x == 0)
     commit_partial(load_partial_row(w, plan.vec, a.block_size, b0, b1), keys, c0);
@@ -292,8 +339,9 @@ __global__ void fill_minus_one_kernel(int32_t* out, int64_t rows, int32_t cols, 
 // ---------------------------------------------------------------------------
 
 // Tuning overrides, read once: DSA_CB_SPLIT (CTAs per row, 1..8, used only
-// with a workspace) and DSA_CB_THREADS (128 or 256 threads per CTA).
-int g_split_override = 0, g_threads_override = 0;
+// with a workspace), DSA_CB_THREADS (128 or 256 threads per CTA) and
+// DSA_CB_WARP=0 (never one row per warp).
+int g_split_override = 0, g_threads_override = 0, g_warp_off = 0;
 std::once_flag g_env_once;
 
 void read_overrides() {
@@ -304,6 +352,8 @@ void read_overrides() {
     const char* t = std::getenv("DSA_CB_THREADS");
     const int u = t ? std::atoi(t) : 0;
     g_threads_override = (u == 128 || u == 256) ? u : 0;
+    const char* wv = std::getenv("DSA_CB_WARP");
+    g_warp_off = wv && std::atoi(wv) == 0;
   });
 }
 
@@ -542,6 +592,19 @@ dsa_status dsa_select_candidate_blocks(const float* logits, int64_t rows, int64_
   a.ld_out = ld_out;
   a.scores = scores_out;
   a.ld_scores = ld_scores;
+  // Many short rows: one row per warp (32 rows in flight per SM instead of
+  // 8). With few rows a CTA per row keeps more of the GPU busy.
+  read_overrides();
+  if (!g_warp_off && width * 4 <= 64 * 1024 && topk_blocks <= 32 && a.nb <= 2048 &&
+      rows >= 8 * static_cast<int64_t>(sm_count())) {
+    constexpr int W = 4;
+    a.split = 1;
+    a.rows = rows;
+    const size_t smem = W * warp_slice_bytes(a.nb);
+    if (set_smem_attr(select_warp_kernel<W>, smem) != cudaSuccess) return DSA_ECUDA;
+    select_warp_kernel<W><<<static_cast<unsigned>((rows + W - 1) / W), W * 32, smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
+  }
   const bool ws = workspace && workspace_size >= workspace_bytes(rows, a.nb);
   const Shape sh = choose_shape(width * 4, rows, ws);
   attach_workspace(a, rows, workspace, sh);

@@ -47,11 +47,13 @@ struct Window {
 };
 
 // Fast path. lpb_log2 = log2(block_size / VEC).
+// Warp `warp` of `nwarps` warps working on the range (a whole CTA: the CTA's
+// warp index and count; one warp alone: 0 and 1).
 template <int VEC, int NV, int SB>
 __device__ __forceinline__ void stream_pow2(const Window& w, int lpb_log2, int32_t b0, int32_t b1,
-                                            uint32_t* __restrict__ keys, int32_t kbase) {
+                                            uint32_t* __restrict__ keys, int32_t kbase, int warp,
+                                            int nwarps) {
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
   const int lpb = 1 << lpb_log2;
   const int32_t nvec = w.len_max / VEC;  // whole vectors of the longest shard
   const int32_t v_begin = static_cast<int32_t>(static_cast<int64_t>(b0) << lpb_log2);
@@ -68,7 +70,7 @@ __device__ __forceinline__ void stream_pow2(const Window& w, int lpb_log2, int32
       lim[j] = (d0 + j < w.shards) ? min(w.len[d0 + j] / VEC, v_end) : 0;
     const float* base = w.origin + static_cast<int64_t>(d0) * w.shard_stride;
 
-    const int32_t step = static_cast<int32_t>(blockDim.x >> 5) * kSlab;
+    const int32_t step = nwarps * kSlab;
     for (int32_t slab = v_begin + warp * kSlab; slab < v_end; slab += step) {
       float acc[NV];
 #pragma unroll
@@ -162,14 +164,13 @@ __device__ __forceinline__ void commit_partial(const Partial& p, uint32_t* keys,
 template <int NV, int SB>
 __device__ __forceinline__ void stream_generic(const Window& w, int32_t block_size, int32_t b0,
                                                int32_t b1, uint32_t* __restrict__ keys,
-                                               int32_t kbase) {
+                                               int32_t kbase, int warp, int nwarps) {
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
   const int64_t e_begin = static_cast<int64_t>(b0) * block_size;
   const int64_t e_end = min(static_cast<int64_t>(b1) * block_size, static_cast<int64_t>(w.len_max));
   constexpr int64_t kSlab = 32 * NV;
 
-  const int64_t step = static_cast<int64_t>(blockDim.x >> 5) * kSlab;
+  const int64_t step = static_cast<int64_t>(nwarps) * kSlab;
   for (int64_t slab = e_begin + warp * kSlab; slab < e_end; slab += step) {
     float acc[NV];
 #pragma unroll
@@ -232,12 +233,12 @@ __device__ __forceinline__ int choose_vec(const float* origin, int32_t block_siz
 // keeps 32 floats per lane in flight per slab.
 __device__ __forceinline__ void stream_row(const Window& w, int vec, int lpb_log2,
                                            int32_t block_size, int32_t b0, int32_t b1,
-                                           uint32_t* keys, int32_t kbase) {
+                                           uint32_t* keys, int32_t kbase, int warp, int nwarps) {
   switch (vec) {
-    case 4: stream_pow2<4, 8, 1>(w, lpb_log2, b0, b1, keys, kbase); break;
-    case 2: stream_pow2<2, 16, 1>(w, lpb_log2, b0, b1, keys, kbase); break;
-    case 1: stream_pow2<1, 32, 1>(w, lpb_log2, b0, b1, keys, kbase); break;
-    default: stream_generic<16, 1>(w, block_size, b0, b1, keys, kbase); break;
+    case 4: stream_pow2<4, 8, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps); break;
+    case 2: stream_pow2<2, 16, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps); break;
+    case 1: stream_pow2<1, 32, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps); break;
+    default: stream_generic<16, 1>(w, block_size, b0, b1, keys, kbase, warp, nwarps); break;
   }
 }
 
