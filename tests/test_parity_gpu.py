@@ -189,6 +189,39 @@ def test_block_scores_sweep(env, seed):
     assert_bits_equal(got[:, :nb], want)
 
 
+WARP_CASES = [  # (block_size, width, topk, row_repeat, starts, bf16 grid, nan_count, wild)
+    (64, 16384, 32, 1, True, False, 40, False),
+    (64, 16000, 16, 4, False, True, 0, True),
+    (128, 16383, 32, 1, True, False, 0, False),
+    (8, 16384, 32, 1, True, False, 5, False),     # 2048 blocks: keys beyond registers
+    (3, 4000, 20, 2, True, False, 9, True),       # generic streaming path
+    (1, 1500, 32, 1, False, True, 0, False),
+    (100, 9000, 7, 8, True, False, 3, False),
+]
+
+
+@pytest.mark.parametrize("case", WARP_CASES, ids=[f"bs{c[0]}-w{c[1]}-k{c[2]}" for c in WARP_CASES])
+def test_warp_per_row_sweep(env, case):
+    """Many short rows take the one-row-per-warp kernel."""
+    bs, width, topk, rr, starts, bf16, nans, wild = case
+    wl = workloads.small_unsharded(3000 + bs, rows=1300 + 97 * rr, width=width, block_size=bs,
+                                   topk_blocks=topk, row_repeat=rr, starts=starts,
+                                   bf16_grid=bf16, nan_count=nans, wild_bounds=wild)
+    check_unsharded(env, wl, offset=1 if bs % 4 else 0)
+
+
+def test_warp_per_row_ties_fallback(env):
+    """Rows whose blocks all tie leave more candidates than a warp ranks by
+    counting; the warp falls back to repeated maxima."""
+    rows, width = 1400, 8192
+    x = np.zeros((rows, width), dtype=np.float32)
+    x[::2] = 1.5  # even rows: every block ties
+    x[1::2] = workloads.round_to_bf16_grid(
+        np.random.default_rng(5).standard_normal((rows // 2, width), dtype=np.float32)).round(0)
+    wl = workloads.Workload("ties", x, None, np.full(rows, width, np.int32), 32, 32, 1, True, 0)
+    check_unsharded(env, wl)
+
+
 def test_sharded_equals_unsharded_on_device(env):
     torch, dsa = env
     wl, g = workloads.small_sharded(4242, shards=8, rows=64, global_width=65536,
