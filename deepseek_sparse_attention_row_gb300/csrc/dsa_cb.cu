@@ -73,6 +73,7 @@ struct RowPlan {
   int32_t nblk;       // blocks holding in-window data
   int32_t pin_block;  // -1: none
   int vec, lpb_log2;
+  int shift;          // vec == kVecShift: floats past the 16-byte boundary
 };
 
 // Counts one arrival on a row's counter and returns true for the last of
@@ -110,7 +111,17 @@ __device__ __forceinline__ RowPlan plan_unsharded(const float* logits, int64_t l
   p.nblk = static_cast<int32_t>((n + static_cast<uint32_t>(block_size) - 1u) /
                                 static_cast<uint32_t>(block_size));
   p.pin_block = (pin_newest && n > 0) ? static_cast<int32_t>((n - 1u) / block_size) : -1;
-  p.vec = choose_vec(p.origin, block_size, &p.lpb_log2);
+  // A window off the 16-byte grid still reads 16-byte vectors when the block
+  // splits into a power of two of them and the aligned base stays inside the
+  // row (s >= shift).
+  p.shift = static_cast<int>((reinterpret_cast<uintptr_t>(p.origin) >> 2) & 3);
+  const int32_t lpb4 = block_size / 4;
+  if (p.shift != 0 && s >= p.shift && block_size % 4 == 0 && (lpb4 & (lpb4 - 1)) == 0) {
+    p.vec = kVecShift;
+    p.lpb_log2 = __ffs(lpb4) - 1;
+  } else {
+    p.vec = choose_vec(p.origin, block_size, &p.lpb_log2);
+  }
   return p;
 }
 
@@ -196,8 +207,8 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
     if constexpr (SHARDED)
       stream_sharded<SVEC>(w, plan.lpb_log2, a.block_size, b0, b1, keys);
     else
-      stream_row(w, plan.vec, plan.lpb_log2, a.block_size, b0, b1, keys, 0, threadIdx.x >> 5,
-                 blockDim.x >> 5);
+      stream_row(w, plan.vec, plan.shift, plan.lpb_log2, a.block_size, b0, b1, keys, 0,
+                 threadIdx.x >> 5, blockDim.x >> 5);
   }
   __syncthreads();
   if constexpr (SHARDED) {
@@ -207,8 +218,7 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
                                           b0, b1),
                        keys, 0);
   } else {
-    if (threadIdx.x == 0)
-      commit_partial(load_partial_row(w, plan.vec, a.block_size, b0, b1), keys, 0);
+    if (threadIdx.x == 0) finish_row(w, plan.vec, plan.shift, a.block_size, b0, b1, keys, 0);
   }
   __syncthreads();
 
@@ -268,9 +278,10 @@ __global__ void __launch_bounds__(W * 32, 1024 / (W * 32)) select_warp_kernel(co
   w.shards = 1;
   w.len = len;
   w.len_max = plan.len_max;
-  if (nblk > 0) stream_row(w, plan.vec, plan.lpb_log2, a.block_size, 0, nblk, keys, 0, 0, 1);
+  if (nblk > 0)
+    stream_row(w, plan.vec, plan.shift, plan.lpb_log2, a.block_size, 0, nblk, keys, 0, 0, 1);
   __syncwarp();
-  if (lane == 0) commit_partial(load_partial_row(w, plan.vec, a.block_size, 0, nblk), keys, 0);
+  if (lane == 0) finish_row(w, plan.vec, plan.shift, a.block_size, 0, nblk, keys, 0);
   __syncwarp();
   topk_warp(keys, a.nb, nblk, min(a.topk, a.nb), plan.pin_block, cand,
             a.topk > 0 ? a.out + row * a.ld_out : nullptr, a.topk,
@@ -314,11 +325,10 @@ __global__ void __launch_bounds__(kThreads, 4) block_scores_kernel(const ScoresA
   w.len = len;
   w.len_max = plan.len_max;
   if (b0 < b1)
-    stream_row(w, plan.vec, plan.lpb_log2, a.block_size, b0, b1, keys, c0, threadIdx.x >> 5,
-               blockDim.x >> 5);
+    stream_row(w, plan.vec, plan.shift, plan.lpb_log2, a.block_size, b0, b1, keys, c0,
+               threadIdx.x >> 5, blockDim.x >> 5);
   __syncthreads();
-  if (threadIdx.x == 0)
-    commit_partial(load_partial_row(w, plan.vec, a.block_size, b0, b1), keys, c0);
+  if (threadIdx.x == 0) finish_row(w, plan.vec, plan.shift, a.block_size, b0, b1, keys, c0);
   __syncthreads();
   if (threadIdx.x == 0 && plan.pin_block >= c0 && plan.pin_block < c1)
     keys[plan.pin_block - c0] = kKeyPosInf;

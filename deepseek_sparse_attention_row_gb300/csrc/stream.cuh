@@ -132,6 +132,110 @@ __device__ __forceinline__ void stream_pow2(const Window& w, int lpb_log2, int32
   }
 }
 
+// Unsharded window whose start lies r = 1..3 floats past a 16-byte boundary,
+// block size a power-of-two multiple of 4 (LPB = block_size / 4 a power of
+// two). Loads aligned float4s from base = origin - r. Vector v of base covers
+// window elements [4v - r, 4v - r + 4); all of them belong to block
+// v / LPB except, in the block's first vector (v % LPB == 0), the r elements
+// below the block boundary, which belong to block v / LPB - 1 (and, for
+// v = 0, precede the window and are dropped). Each lane folds its vectors
+// into a "hi" value for block v / LPB and, in a block's first vector, a "lo"
+// value for the block before; both are merged into shared memory with
+// atomicMax. Vector b1 * LPB is read only for its lo part (it completes block
+// b1 - 1). Elements past the last whole vector are left to load_partial_shifted.
+template <int NV>
+__device__ __forceinline__ void stream_shift4(const float* origin, int32_t r, int32_t len,
+                                              int lpb_log2, int32_t b0, int32_t b1,
+                                              uint32_t* __restrict__ keys, int32_t kbase,
+                                              int warp, int nwarps) {
+  const int lane = threadIdx.x & 31;
+  const int lpb = 1 << lpb_log2;
+  const float* base = origin - r;
+  const int32_t nvec = (len + r) / 4;  // whole vectors of base inside [base, origin + len)
+  const int32_t v_begin = static_cast<int32_t>(static_cast<int64_t>(b0) << lpb_log2);
+  const int32_t v_end = static_cast<int32_t>(min((static_cast<int64_t>(b1) << lpb_log2) + 1,
+                                                 static_cast<int64_t>(nvec)));
+  constexpr int32_t kSlab = 32 * NV;
+  const int32_t step = nwarps * kSlab;
+  for (int32_t slab = v_begin + warp * kSlab; slab < v_end; slab += step) {
+    float x[NV][4];
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      const int32_t v = slab + m * 32 + lane;
+      if (v < v_end) {
+        ld_stream(base + static_cast<int64_t>(v) * 4, x[m]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[m][i] = neg_inf();
+      }
+    }
+    float hi[NV], lo[NV];
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      const int32_t v = slab + m * 32 + lane;
+      const bool lead = (v & (lpb - 1)) == 0;
+      hi[m] = neg_inf();
+      lo[m] = neg_inf();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool below = lead && i < r;
+        hi[m] = max_nan(hi[m], below ? neg_inf() : x[m][i]);
+        lo[m] = max_nan(lo[m], below ? x[m][i] : neg_inf());
+      }
+    }
+    // lo parts: the lead lane of each block sends them to the block before.
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      const int32_t v = slab + m * 32 + lane;
+      const int32_t blk = (v >> lpb_log2) - 1;
+      if ((v & (lpb - 1)) == 0 && v < v_end && blk >= b0 && blk < b1)
+        atomicMax(&keys[blk - kbase], order_key(lo[m]));
+    }
+    // hi parts, reduced per block as in the aligned path.
+    if (lpb_log2 >= 5) {
+      float carry = neg_inf();
+#pragma unroll
+      for (int m = 0; m < NV; ++m) {
+        carry = max_nan(carry, hi[m]);
+        const int32_t blk = (slab + m * 32) >> lpb_log2;
+        const bool last = (m == NV - 1) || (((slab + (m + 1) * 32) >> lpb_log2) != blk);
+        if (last) {
+          if (blk < b1) {
+            const uint32_t k = __reduce_max_sync(0xffffffffu, order_key(carry));
+            if (lane == 0) atomicMax(&keys[blk - kbase], k);
+          }
+          carry = neg_inf();
+        }
+      }
+    } else {
+#pragma unroll
+      for (int m = 0; m < NV; ++m) {
+        const int32_t vfirst = slab + m * 32;
+        if (vfirst >= v_end) break;
+        uint32_t k = order_key(hi[m]);
+        for (int o = 1; o < lpb; o <<= 1) k = max(k, __shfl_xor_sync(0xffffffffu, k, o));
+        const int32_t v = vfirst + lane;
+        const int32_t blk = v >> lpb_log2;
+        if ((lane & (lpb - 1)) == 0 && v < v_end && blk < b1) atomicMax(&keys[blk - kbase], k);
+      }
+    }
+  }
+}
+
+// Elements of a shifted window (stream_shift4) past its last whole vector:
+// window elements [4 * nvec - r, len), each to its own block (the run can
+// cross one block boundary). One thread; call after the loop and a barrier.
+__device__ __forceinline__ void commit_partial_shifted(const float* origin, int32_t r, int32_t len,
+                                                       int32_t block_size, int32_t b0,
+                                                       int32_t b1, uint32_t* keys,
+                                                       int32_t kbase) {
+  const int32_t first = max(((len + r) / 4) * 4 - r, 0);
+  for (int32_t i = first; i < len; ++i) {
+    const int32_t blk = i / block_size;
+    if (blk >= b0 && blk < b1) atomicMax(&keys[blk - kbase], order_key(ld_stream1(origin + i)));
+  }
+}
+
 // The elements past the last whole vector of a shard's window (at most
 // VEC - 1) are read after the streaming loop: load_partial() folds them into
 // a register and commit_partial() merges that into their block, after a
@@ -231,10 +335,17 @@ __device__ __forceinline__ int choose_vec(const float* origin, int32_t block_siz
 
 // Unsharded dispatch: vector width chosen per row at run time. Every path
 // keeps 32 floats per lane in flight per slab.
-__device__ __forceinline__ void stream_row(const Window& w, int vec, int lpb_log2,
+// vec 8: shifted 16-byte loads (stream_shift4) for a window starting
+// `shift` floats past a 16-byte boundary.
+constexpr int kVecShift = 8;
+
+__device__ __forceinline__ void stream_row(const Window& w, int vec, int shift, int lpb_log2,
                                            int32_t block_size, int32_t b0, int32_t b1,
                                            uint32_t* keys, int32_t kbase, int warp, int nwarps) {
   switch (vec) {
+    case kVecShift:
+      stream_shift4<8>(w.origin, shift, w.len_max, lpb_log2, b0, b1, keys, kbase, warp, nwarps);
+      break;
     case 4: stream_pow2<4, 8, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps); break;
     case 2: stream_pow2<2, 16, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps); break;
     case 1: stream_pow2<1, 32, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps); break;
@@ -242,11 +353,15 @@ __device__ __forceinline__ void stream_row(const Window& w, int vec, int lpb_log
   }
 }
 
-__device__ __forceinline__ Partial load_partial_row(const Window& w, int vec, int32_t block_size,
-                                                   int32_t b0, int32_t b1) {
-  if (vec == 4) return load_partial<4>(w.origin, w.len_max, block_size, b0, b1);
-  if (vec == 2) return load_partial<2>(w.origin, w.len_max, block_size, b0, b1);
-  return Partial{neg_inf(), -1};
+// Tail of an unsharded row past its last whole vector; one thread, after the
+// loop and a barrier.
+__device__ __forceinline__ void finish_row(const Window& w, int vec, int shift, int32_t block_size,
+                                           int32_t b0, int32_t b1, uint32_t* keys,
+                                           int32_t kbase) {
+  if (vec == 4) commit_partial(load_partial<4>(w.origin, w.len_max, block_size, b0, b1), keys, kbase);
+  if (vec == 2) commit_partial(load_partial<2>(w.origin, w.len_max, block_size, b0, b1), keys, kbase);
+  if (vec == kVecShift)
+    commit_partial_shifted(w.origin, shift, w.len_max, block_size, b0, b1, keys, kbase);
 }
 
 }  // namespace dsa
