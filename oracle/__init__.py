@@ -55,8 +55,10 @@ def bind(path: str):
     lib.dsa_oracle_select.argtypes = [p, i64, i64, i64, p, p, i32, i32, i32, i32, p, i64, p, i64]
     lib.dsa_oracle_select_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32, i32, i32,
                                               p, i64, p, i64]
+    lib.dsa_oracle_mask.argtypes = [p, i64, i64, i64, p, p, p, i64, i64, i32, i32]
+    lib.dsa_oracle_mask_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32, p, i64, i64]
     for f in (lib.dsa_oracle_block_scores, lib.dsa_oracle_select,
-              lib.dsa_oracle_select_sharded):
+              lib.dsa_oracle_select_sharded, lib.dsa_oracle_mask, lib.dsa_oracle_mask_sharded):
         f.restype = ctypes.c_int
     return lib
 
@@ -158,3 +160,35 @@ def run_workload(wl, want_scores: bool = True):
     return select(wl.logits, wl.row_ks, wl.row_ke, wl.topk_blocks, wl.block_size,
                   wl.row_repeat, wl.pin_newest, width=wl.width,
                   want_scores=want_scores)
+
+
+def mask(logits: np.ndarray, row_ks, row_ke, candidates: np.ndarray, block_size: int,
+         row_repeat: int = 1, width: Optional[int] = None) -> np.ndarray:
+    """Masked copy of ``logits`` [rows, ld]: -inf outside each row's window
+    and outside its candidate blocks (``candidates`` [rows, topk], -1 = empty)."""
+    out = np.array(_f32(logits), copy=True)
+    rows, ld = out.shape
+    width = ld if width is None else width
+    cand = np.ascontiguousarray(candidates, dtype=np.int32)
+    ks, ke = _i32(row_ks), _i32(row_ke)
+    topk = cand.shape[1] if cand.ndim == 2 else 0
+    rc = _load().dsa_oracle_mask(_ptr(out), rows, width, ld, _ptr(ks), _ptr(ke), _ptr(cand),
+                                 topk, max(topk, 1), block_size, row_repeat)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return out
+
+
+def mask_sharded(logits: np.ndarray, global_row_ke, global_block_size: int,
+                 candidates: np.ndarray, row_repeat: int = 1) -> np.ndarray:
+    """Masked copy of a ``[shards, rows, local_width]`` DCP layout."""
+    out = np.array(_f32(logits), copy=True)
+    shards, rows, lw = out.shape
+    cand = np.ascontiguousarray(candidates, dtype=np.int32)
+    topk = cand.shape[1] if cand.ndim == 2 else 0
+    rc = _load().dsa_oracle_mask_sharded(_ptr(out), shards, rows, lw, lw, rows * lw,
+                                         _ptr(_i32(global_row_ke)), global_block_size,
+                                         row_repeat, _ptr(cand), topk, max(topk, 1))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return out

@@ -35,6 +35,8 @@
  *   R7 DCP local ends: shard d holds the global tokens t < gke with
  *      t % D == d, so its local end is ceil((gke - d) / D) when gke > d,
  *      else 0 ([SG] interleave-1 placement).
+ *   R8 masking (below): a logit outside its window or outside the row's
+ *      candidate blocks becomes -inf; the rest are untouched.
  *
  * Floating-point values are widened to double for every comparison; no
  * arithmetic is done on them, so the results are exact.
@@ -324,5 +326,81 @@ int dsa_oracle_select_sharded(const float *logits, int32_t shards,
     free(global_score);
     free(local_score);
     free(tmp);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Masking to candidates ([CB] masking function after selection)        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * R8 (reading of the masking function, whose body is not on the page): in
+ * place, logits[r][c] for c in [0, width) becomes -inf when c lies outside the
+ * row's window [s, e) (R3) or when its request-local block (c - s) / bs is
+ * not one of the row's candidate ids cand[r][0 .. topk) (ids < 0 are empty
+ * slots). Kept logits are left bit for bit as they were.
+ */
+static int is_candidate(const int32_t *cand, int64_t topk, int64_t b)
+{
+    int64_t j;
+    for (j = 0; j < topk; ++j)
+        if (cand[j] >= 0 && (int64_t)cand[j] == b)
+            return 1;
+    return 0;
+}
+
+int dsa_oracle_mask(float *logits, int64_t rows, int64_t width, int64_t ld_logits,
+                    const int32_t *row_ks, const int32_t *row_ke,
+                    const int32_t *cand, int64_t topk, int64_t ld_cand,
+                    int32_t block_size, int32_t row_repeat)
+{
+    int64_t r, c;
+    if (rows < 0 || width < 0 || block_size < 1 || row_repeat < 1 || topk < 0)
+        return -1;
+    for (r = 0; r < rows; ++r) {
+        int64_t s, e;
+        float *row = logits + r * ld_logits;
+        row_window(r, width, row_ks, row_ke, row_repeat, &s, &e);
+        for (c = 0; c < width; ++c) {
+            int keep = c >= s && c < e &&
+                       is_candidate(cand + r * ld_cand, topk, (c - s) / block_size);
+            if (!keep)
+                row[c] = -INFINITY;
+        }
+    }
+    return 0;
+}
+
+/*
+ * The DCP form: shard d of row r keeps its local columns [0, lke_d) (R7)
+ * whose local block c / (gbs / shards) is a candidate of the row; the
+ * candidate ids are global block ids, which name the same local blocks on
+ * every shard ([CB] masking function: under DCP the local block size is
+ * passed and the ids apply unchanged).
+ */
+int dsa_oracle_mask_sharded(float *logits, int32_t shards, int64_t rows, int64_t local_width,
+                            int64_t ld_logits, int64_t shard_stride,
+                            const int32_t *global_row_ke, int32_t global_block_size,
+                            int32_t row_repeat, const int32_t *cand, int64_t topk,
+                            int64_t ld_cand)
+{
+    int64_t r, d, c, lbs;
+    if (shards < 1 || rows < 0 || local_width < 0 || global_block_size < 1 ||
+        global_block_size % shards != 0 || row_repeat < 1 || topk < 0)
+        return -1;
+    lbs = global_block_size / shards;
+    for (r = 0; r < rows; ++r) {
+        int64_t gke = (int64_t)global_row_ke[r / row_repeat];
+        for (d = 0; d < shards; ++d) {
+            float *row = logits + d * shard_stride + r * ld_logits;
+            int64_t lke = gke > d ? (gke - d + shards - 1) / shards : 0;
+            int64_t e = imin64(lke, local_width);
+            for (c = 0; c < local_width; ++c) {
+                int keep = c < e && is_candidate(cand + r * ld_cand, topk, c / lbs);
+                if (!keep)
+                    row[c] = -INFINITY;
+            }
+        }
+    }
     return 0;
 }

@@ -34,6 +34,17 @@ int dsa_oracle_select_sharded(const float *logits, int32_t shards,
                               int32_t topk_blocks, int32_t *out,
                               int64_t ld_out, float *scores, int64_t ld_scores);
 
+int dsa_oracle_mask(float *logits, int64_t rows, int64_t width, int64_t ld_logits,
+                    const int32_t *row_ks, const int32_t *row_ke,
+                    const int32_t *cand, int64_t topk, int64_t ld_cand,
+                    int32_t block_size, int32_t row_repeat);
+
+int dsa_oracle_mask_sharded(float *logits, int32_t shards, int64_t rows, int64_t local_width,
+                            int64_t ld_logits, int64_t shard_stride,
+                            const int32_t *global_row_ke, int32_t global_block_size,
+                            int32_t row_repeat, const int32_t *cand, int64_t topk,
+                            int64_t ld_cand);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,8 @@ def _cases():
         fx = load_golden(name)
         assert fx.get("cite") and fx.get("why"), name
         for i, case in enumerate(fx["cases"]):
-            yield pytest.param(case, id=f"{name[:-5]}-{i}")
+            if case["op"] in ("select", "block_scores", "sharded"):  # masking: test_oracle_mask
+                yield pytest.param(case, id=f"{name[:-5]}-{i}")
 
 
 def run_oracle_case(case):

@@ -32,7 +32,9 @@ MUTATIONS = [
     ("starts ignored", "int64_t ks = row_ks ? (int64_t)row_ks[g] : 0;", "int64_t ks = 0;"),
     ("block max drops NaN and ignores the zero sign", "if (total_cmp(x, m) > 0)\n                m = x;",
      "if (x > m)\n                m = x;"),
-    ("shard end rounds down", "(gke - d + shards - 1) / shards", "(gke - d) / shards"),
+    ("shard end rounds down",
+     "(gke - d + shards - 1) / shards : 0;\n            int64_t e = imin64(lke, local_width);\n            if (nlb == 0)",
+     "(gke - d) / shards : 0;\n            int64_t e = imin64(lke, local_width);\n            if (nlb == 0)"),
     ("global pin off by one", "pin = floor_div(gke - 1, global_block_size);",
      "pin = floor_div(gke, global_block_size);"),
     ("rows without context keep the pin", "if (gke <= 0)\n            for (b = 0; b < nbg; ++b)",
@@ -40,6 +42,12 @@ MUTATIONS = [
     ("shard merge takes the min", "if (total_cmp(local_score[b], global_score[b]) > 0)",
      "if (total_cmp(local_score[b], global_score[b]) < 0)"),
     ("canonical NaN not written", "uint32_t bits = 0x7FC00000u;", "uint32_t bits = 0x7FC00001u;"),
+    ("mask uses absolute blocks", "is_candidate(cand + r * ld_cand, topk, (c - s) / block_size)",
+     "is_candidate(cand + r * ld_cand, topk, c / block_size)"),
+    ("mask keeps columns before the window", "int keep = c >= s && c < e &&",
+     "int keep = c < e &&"),
+    ("mask treats -1 as block 0", "if (cand[j] >= 0 && (int64_t)cand[j] == b)",
+     "if ((int64_t)(cand[j] < 0 ? 0 : cand[j]) == b)"),
 ]
 
 
@@ -65,6 +73,18 @@ def _battery() -> list:
         pins.test_sharded_equals_unsharded_on_global_rows(4, 1, 9, 64, 2)
     except AssertionError:
         failed.append("interleave-identity")
+    import test_oracle_mask as mask_pins
+    for name, fn in (("mask-golden", mask_pins.test_golden_mask),
+                     ("mask-after-select", mask_pins.test_mask_after_select_keeps_exactly_the_selected_blocks)):
+        try:
+            fn()
+        except AssertionError:
+            failed.append(name)
+    for seed in range(15):
+        try:
+            mask_pins.test_mask_matches_brute_force(seed)
+        except AssertionError:
+            failed.append(f"mask-brute:{seed}")
     return failed
 
 
