@@ -32,6 +32,8 @@ __all__ = [
     "dsa_block_scores",
     "dsa_select_candidate_blocks",
     "dsa_select_candidate_blocks_sharded",
+    "dsa_mask_candidate_logits",
+    "dsa_mask_candidate_logits_sharded",
     "select_candidate_blocks_host",
     "select_candidate_blocks_sharded_host",
     "max_select_blocks",
@@ -49,6 +51,8 @@ EXPORTED_SYMBOLS = (
     "dsa_block_scores",
     "dsa_select_candidate_blocks",
     "dsa_select_candidate_blocks_sharded",
+    "dsa_mask_candidate_logits",
+    "dsa_mask_candidate_logits_sharded",
     "dsa_select_candidate_blocks_sharded_static",
 )
 
@@ -87,8 +91,12 @@ def library():
                                                 p, i64, p, i64, p, sz, p]
     lib.dsa_select_candidate_blocks_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32,
                                                         i32, i32, p, i64, p, i64, p, sz, p]
+    lib.dsa_mask_candidate_logits.argtypes = [p, i64, i64, i64, p, p, p, i32, i64, i32, i32, p]
+    lib.dsa_mask_candidate_logits_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32, p,
+                                                      i32, i64, p]
     for f in (lib.dsa_block_scores, lib.dsa_select_candidate_blocks,
-              lib.dsa_select_candidate_blocks_sharded):
+              lib.dsa_select_candidate_blocks_sharded, lib.dsa_mask_candidate_logits,
+              lib.dsa_mask_candidate_logits_sharded):
         f.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -233,6 +241,43 @@ def dsa_select_candidate_blocks_sharded(logits, global_row_ke, global_block_size
         ws_ptr, ws_bytes, handle)
     _check("dsa_select_candidate_blocks_sharded", st)
     return out
+
+
+def dsa_mask_candidate_logits(logits, row_ks, row_ke, candidates, block_size: int,
+                              row_repeat: int = 1, stream=None):
+    """In place: -inf for every logit outside its row's window or outside the
+    row's candidate blocks (``candidates`` [rows, topk] int32, -1 = empty)."""
+    torch = _torch()
+    rows, width = logits.shape
+    topk = candidates.shape[1] if candidates is not None else 0
+    st = library().dsa_mask_candidate_logits(
+        _dev_ptr(logits, torch.float32, "logits"), rows, width, _row_major(logits, "logits"),
+        _dev_ptr(row_ks, torch.int32, "row_ks", allow_none=True),
+        _dev_ptr(row_ke, torch.int32, "row_ke"),
+        _dev_ptr(candidates, torch.int32, "candidates", allow_none=True), topk,
+        _row_major(candidates, "candidates") if candidates is not None else 0, block_size,
+        row_repeat, _stream_handle(stream))
+    _check("dsa_mask_candidate_logits", st)
+    return logits
+
+
+def dsa_mask_candidate_logits_sharded(logits, global_row_ke, global_block_size: int, candidates,
+                                      row_repeat: int = 1, stream=None):
+    """DCP form of ``dsa_mask_candidate_logits`` on ``[D, rows, local_width]``."""
+    torch = _torch()
+    shards, rows, lw = logits.shape
+    if logits.stride(2) != 1:
+        raise ValueError("logits must have unit stride in its last dimension")
+    topk = candidates.shape[1] if candidates is not None else 0
+    st = library().dsa_mask_candidate_logits_sharded(
+        _dev_ptr(logits, torch.float32, "logits"), shards, rows, lw, logits.stride(1),
+        logits.stride(0), _dev_ptr(global_row_ke, torch.int32, "global_row_ke"),
+        global_block_size, row_repeat,
+        _dev_ptr(candidates, torch.int32, "candidates", allow_none=True), topk,
+        _row_major(candidates, "candidates") if candidates is not None else 0,
+        _stream_handle(stream))
+    _check("dsa_mask_candidate_logits_sharded", st)
+    return logits
 
 
 def _to_device(host, dev_buf, stream):

@@ -192,6 +192,51 @@ dsa_status dsa_select_candidate_blocks_sharded(
     int64_t ld_scores, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * dsa_mask_candidate_logits -- mask packed logits to the selected candidate
+ * blocks, in place (candidate_blocks.py: the masking function after
+ * selection, "mask packed logits outside causal bounds and request-local
+ * candidates"; its body is not on the page).
+ *
+ *   logits       [rows, ld_logits] fp32, modified in place over columns
+ *                [0, width): column c becomes -inf when it lies outside the
+ *                row's window [s, e) (clamped as for selection) or when its
+ *                request-local block (c - s) / block_size is not among
+ *                candidates[r, 0 .. topk_blocks); entries < 0 are empty
+ *                slots. Kept columns are not read or written.
+ *   candidates   [rows, ld_candidates] int32, e.g. the `out` of
+ *                dsa_select_candidate_blocks; nullable when topk_blocks == 0
+ *                (then every column is masked).
+ *   row_ks, row_ke, block_size, row_repeat  as for the selection.
+ *
+ * rows == 0 or width == 0: DSA_OK, nothing written. DSA_EINVAL for negative
+ * rows / width / topk_blocks, block_size < 1, row_repeat < 1, ld_logits <
+ * width, ld_candidates < topk_blocks, or a NULL logits / row_ke / candidates
+ * (candidates only when topk_blocks > 0). DSA_EUNSUPPORTED for widths near
+ * 2^31.
+ */
+dsa_status dsa_mask_candidate_logits(float *logits, int64_t rows, int64_t width,
+                                     int64_t ld_logits, const int32_t *row_ks,
+                                     const int32_t *row_ke,
+                                     const int32_t *candidates,
+                                     int32_t topk_blocks, int64_t ld_candidates,
+                                     int32_t block_size, int32_t row_repeat,
+                                     void *stream);
+
+/*
+ * dsa_mask_candidate_logits_sharded -- the DCP form of the masking: shard d of
+ * row r keeps its local columns below ceil((gke - d) / shards) (none when
+ * gke <= d) whose local block c / (global_block_size / shards) is a
+ * candidate; the candidate ids are global block ids, which name the same
+ * local blocks on every shard. Layout, strides and errors as for
+ * dsa_select_candidate_blocks_sharded and dsa_mask_candidate_logits.
+ */
+dsa_status dsa_mask_candidate_logits_sharded(
+    float *logits, int32_t shards, int64_t rows, int64_t local_width,
+    int64_t ld_logits, int64_t shard_stride, const int32_t *global_row_ke,
+    int32_t global_block_size, int32_t row_repeat, const int32_t *candidates,
+    int32_t topk_blocks, int64_t ld_candidates, void *stream);
+
+/*
  * dsa_select_candidate_blocks_sharded_static -- dsa_select_candidate_blocks_
  * sharded without a caller-supplied workspace. The pages have no counterpart:
  * this entry point exists for callers that must not allocate device memory

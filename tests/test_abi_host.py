@@ -152,3 +152,48 @@ def test_sharded_validation(lib, kw, want):
         a["gbs"], a["max_gb"], a["row_repeat"], a["topk"], a["out"], a["ld_out"], a["scores"],
         a["ld_scores"], a["ws"], a["ws_bytes"], None)
     assert st == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(rows=-1), DSA_EINVAL),
+    (dict(width=-1), DSA_EINVAL),
+    (dict(block_size=0), DSA_EINVAL),
+    (dict(row_repeat=0), DSA_EINVAL),
+    (dict(topk=-1), DSA_EINVAL),
+    (dict(ld=5), DSA_EINVAL),
+    (dict(logits=None), DSA_EINVAL),
+    (dict(ke=None), DSA_EINVAL),
+    (dict(cand=None), DSA_EINVAL),
+    (dict(ld_cand=1), DSA_EINVAL),
+    (dict(rows=0), DSA_OK),
+    (dict(width=0), DSA_OK),
+])
+def test_mask_validation(lib, kw, want):
+    a = dict(logits=FAKE, rows=4, width=100, ld=100, ks=None, ke=FAKE, cand=FAKE, topk=4,
+             ld_cand=4, block_size=8, row_repeat=1)
+    a.update(kw)
+    st = lib.dsa_mask_candidate_logits(a["logits"], a["rows"], a["width"], a["ld"], a["ks"],
+                                       a["ke"], a["cand"], a["topk"], a["ld_cand"],
+                                       a["block_size"], a["row_repeat"], None)
+    assert st == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(shards=0), DSA_EINVAL),
+    (dict(gbs=60), DSA_EINVAL),
+    (dict(row_repeat=0), DSA_EINVAL),
+    (dict(ld=10), DSA_EINVAL),
+    (dict(gke=None), DSA_EINVAL),
+    (dict(cand=None), DSA_EINVAL),
+    (dict(rows=0), DSA_OK),
+    (dict(lw=0, ld=0), DSA_OK),
+])
+def test_mask_sharded_validation(lib, kw, want):
+    a = dict(logits=FAKE, shards=8, rows=4, lw=64, ld=64, shard_stride=256, gke=FAKE, gbs=64,
+             row_repeat=1, cand=FAKE, topk=4, ld_cand=4)
+    a.update(kw)
+    st = lib.dsa_mask_candidate_logits_sharded(a["logits"], a["shards"], a["rows"], a["lw"],
+                                               a["ld"], a["shard_stride"], a["gke"], a["gbs"],
+                                               a["row_repeat"], a["cand"], a["topk"],
+                                               a["ld_cand"], None)
+    assert st == want

@@ -222,6 +222,91 @@ def test_warp_per_row_ties_fallback(env):
     check_unsharded(env, wl)
 
 
+# ---------------------------------------------------------------------------
+# Masking to the selected candidate blocks
+# ---------------------------------------------------------------------------
+
+def _random_candidates(rng, rows, topk, nb):
+    """Ids in [-1, nb + 2): empty slots, duplicates and ids past the row's
+    blocks all occur."""
+    return rng.integers(-1, nb + 2, size=(rows, topk)).astype(np.int32)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_mask_sweep(env, seed):
+    torch, dsa = env
+    rng = np.random.default_rng(8000 + seed)
+    bs = int(BLOCK_SIZES[seed % len(BLOCK_SIZES)])
+    width = int(rng.choice([1, 5, 100, 4096, 8191, 8192, 8193, 30001]))
+    rows = int(rng.integers(1, 30))
+    rr = int(rng.choice([1, 2, 3]))
+    topk = int(rng.choice([0, 1, 7, 32, 100]))
+    wl = workloads.small_unsharded(8000 + seed, rows=rows, width=width, block_size=bs,
+                                   topk_blocks=max(topk, 1), row_repeat=rr,
+                                   starts=bool(rng.integers(0, 2)), nan_count=7,
+                                   wild_bounds=bool(rng.integers(0, 2)),
+                                   ld=width + int(rng.choice([0, 1, 3])))
+    nb = -(-width // bs)
+    cand = _random_candidates(rng, rows, topk, nb)
+    want = oracle.mask(wl.logits, wl.row_ks, wl.row_ke, cand, bs, rr, width=width)
+    logits = _padded_logits(torch, wl.logits, width, int(rng.choice([0, 1, 2, 3])))
+    dsa.dsa_mask_candidate_logits(logits, _dev(torch, wl.row_ks), _dev(torch, wl.row_ke),
+                                  _dev(torch, cand) if topk else None, bs, rr)
+    torch.cuda.synchronize()
+    got = logits.cpu().numpy()
+    assert_bits_equal(got, want[:, :width])
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_mask_sharded_sweep(env, seed):
+    torch, dsa = env
+    rng = np.random.default_rng(8500 + seed)
+    shards = int(rng.choice([1, 2, 3, 8]))
+    lbs = int(rng.choice([1, 3, 8, 16]))
+    lw = int(rng.choice([1, 100, 2047, 8192, 9000]))
+    rows, topk = int(rng.integers(1, 20)), int(rng.choice([0, 5, 32]))
+    wl, _ = workloads.small_sharded(8500 + seed, shards=shards, rows=rows,
+                                    global_width=lw * shards, global_block_size=lbs * shards,
+                                    max_global_blocks=-(-lw // lbs), topk_blocks=max(topk, 1),
+                                    wild_bounds=True)
+    cand = _random_candidates(rng, rows, topk, -(-lw // lbs))
+    want = oracle.mask_sharded(wl.logits, wl.global_row_ke, lbs * shards, cand)
+    local = torch.from_numpy(wl.logits).cuda()
+    dsa.dsa_mask_candidate_logits_sharded(local, _dev(torch, wl.global_row_ke), lbs * shards,
+                                          _dev(torch, cand) if topk else None)
+    torch.cuda.synchronize()
+    assert_bits_equal(local.cpu().numpy(), want)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["decode", "prefill", "dcp"])
+def test_select_then_mask_full_size(env, name):
+    """The pipeline as used: select on the GPU, then mask on the GPU with the
+    selected ids, against the oracle doing both."""
+    torch, dsa = env
+    wl = workloads.make(name)
+    ids, _ = oracle.run_workload(wl, want_scores=False)
+    if hasattr(wl, "global_row_ke"):
+        want = oracle.mask_sharded(wl.logits, wl.global_row_ke, wl.global_block_size, ids)
+        local = torch.from_numpy(wl.logits).cuda()
+        gke = _dev(torch, wl.global_row_ke)
+        out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device="cuda")
+        dsa.dsa_select_candidate_blocks_sharded(local, gke, wl.global_block_size,
+                                                wl.max_global_blocks, wl.topk_blocks, out)
+        dsa.dsa_mask_candidate_logits_sharded(local, gke, wl.global_block_size, out)
+    else:
+        want = oracle.mask(wl.logits, wl.row_ks, wl.row_ke, ids, wl.block_size, wl.row_repeat)
+        local = torch.from_numpy(wl.logits).cuda()
+        ks, ke = _dev(torch, wl.row_ks), _dev(torch, wl.row_ke)
+        out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device="cuda")
+        dsa.dsa_select_candidate_blocks(local, ks, ke, wl.topk_blocks, wl.block_size, out,
+                                        wl.row_repeat, wl.pin_newest)
+        dsa.dsa_mask_candidate_logits(local, ks, ke, out, wl.block_size, wl.row_repeat)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), ids)
+    assert_bits_equal(local.cpu().numpy(), want)
+
+
 def test_sharded_equals_unsharded_on_device(env):
     torch, dsa = env
     wl, g = workloads.small_sharded(4242, shards=8, rows=64, global_width=65536,
