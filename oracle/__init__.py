@@ -9,7 +9,12 @@ shares no code with it.
 readings taken where the pages are silent. Every function here is pinned by
 ``tests/test_oracle_pins.py`` and ``tests/test_oracle_golden.py``.
 
-``build()`` compiles ``dsa_oracle.c`` with gcc into ``oracle/_build``.
+``dcp_lse_oracle.c`` does the same for the DCP partial-attention LSE
+correction (``correct_attn_out``, ``merge_attn_out``); its pins are in
+``tests/test_oracle_lse.py``.
+
+``build()`` compiles both C files with gcc into one library in
+``oracle/_build``.
 """
 
 from __future__ import annotations
@@ -24,6 +29,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "dsa_oracle.c")
 _HDR = os.path.join(_HERE, "dsa_oracle.h")
+_LSE_SRC = os.path.join(_HERE, "dcp_lse_oracle.c")
+_LSE_HDR = os.path.join(_HERE, "dcp_lse_oracle.h")
+SOURCES = (_SRC, _LSE_SRC)
+HEADERS = (_HDR, _LSE_HDR)
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libdsa_oracle.so")
 
@@ -34,21 +43,28 @@ def build(force: bool = False) -> str:
     """Compile the oracle (portable C, no target-specific flags)."""
     os.makedirs(_BUILD, exist_ok=True)
     fresh = (os.path.exists(_LIB_PATH)
-             and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
-                                                    os.path.getmtime(_HDR)))
+             and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(f)
+                                                    for f in SOURCES + HEADERS))
     if fresh and not force:
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-Wall", "-Wextra",
-           "-o", tmp, _SRC, "-lm"]
-    subprocess.run(cmd, check=True)
+    compile_sources(SOURCES, tmp, warnings=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
 
+def compile_sources(sources, path: str, warnings: bool = False) -> None:
+    """gcc the given C sources (with the headers beside them) into a shared
+    library at ``path``."""
+    cmd = ["gcc", "-std=c99", "-O2", "-fPIC", "-shared"]
+    if warnings:
+        cmd += ["-Wall", "-Wextra"]
+    subprocess.run(cmd + ["-o", path, *sources, "-lm"], check=True)
+
+
 def bind(path: str):
-    """Load an oracle library built from ``dsa_oracle.c`` and declare its
-    entry points."""
+    """Load an oracle library built from the C sources and declare its entry
+    points."""
     lib = ctypes.CDLL(path)
     i64, i32, p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
     lib.dsa_oracle_block_scores.argtypes = [p, i64, i64, i64, p, p, i32, i32, i32, p, i64]
@@ -57,8 +73,11 @@ def bind(path: str):
                                               p, i64, p, i64]
     lib.dsa_oracle_mask.argtypes = [p, i64, i64, i64, p, p, p, i64, i64, i32, i32]
     lib.dsa_oracle_mask_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32, p, i64, i64]
+    lib.dcp_oracle_correct_attn_out.argtypes = [p, p, i32, i64, i64, i64, i32, p, p]
+    lib.dcp_oracle_merge_attn_out.argtypes = [p, p, i32, i64, i64, i64, p, p]
     for f in (lib.dsa_oracle_block_scores, lib.dsa_oracle_select,
-              lib.dsa_oracle_select_sharded, lib.dsa_oracle_mask, lib.dsa_oracle_mask_sharded):
+              lib.dsa_oracle_select_sharded, lib.dsa_oracle_mask, lib.dsa_oracle_mask_sharded,
+              lib.dcp_oracle_correct_attn_out, lib.dcp_oracle_merge_attn_out):
         f.restype = ctypes.c_int
     return lib
 
@@ -192,3 +211,41 @@ def mask_sharded(logits: np.ndarray, global_row_ke, global_block_size: int,
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (status {rc})")
     return out
+
+
+def correct_attn_out(out: np.ndarray, lses: np.ndarray, rank: int):
+    """DCP LSE correction of one shard's partial attention output.
+
+    ``out`` [B, H, Dh] and ``lses`` [N, B, H] (base-2 LSEs of all N shards)
+    are read as fp32 (bf16 inputs widen exactly). Returns ``new_out``
+    [H, B, Dh] and the combined LSE [B, H], both float64."""
+    out = np.ascontiguousarray(out, dtype=np.float32)
+    lses = np.ascontiguousarray(lses, dtype=np.float32)
+    B, H, Dh = out.shape
+    N = lses.shape[0]
+    assert lses.shape == (N, B, H)
+    new_out = np.zeros((H, B, Dh), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    rc = _load().dcp_oracle_correct_attn_out(_ptr(out), _ptr(lses), N, B, H, Dh, rank,
+                                             _ptr(new_out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return new_out, lse
+
+
+def merge_attn_out(outs: np.ndarray, lses: np.ndarray):
+    """Sum over shards of the corrected partial outputs.
+
+    ``outs`` [N, B, H, Dh], ``lses`` [N, B, H]. Returns the merged output
+    [H, B, Dh] and the combined LSE [B, H], both float64."""
+    outs = np.ascontiguousarray(outs, dtype=np.float32)
+    lses = np.ascontiguousarray(lses, dtype=np.float32)
+    N, B, H, Dh = outs.shape
+    assert lses.shape == (N, B, H)
+    merged = np.zeros((H, B, Dh), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    rc = _load().dcp_oracle_merge_attn_out(_ptr(outs), _ptr(lses), N, B, H, Dh,
+                                           _ptr(merged), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return merged, lse

@@ -10,7 +10,6 @@ the test process.
 """
 
 import os
-import subprocess
 
 import numpy as np
 import pytest
@@ -100,9 +99,10 @@ def test_planted_mistake_is_caught(name, old, new, tmp_path):
     mutant_c = tmp_path / "dsa_oracle.c"
     mutant_c.write_text(src.replace(old, new))
     (tmp_path / "dsa_oracle.h").write_text(open(oracle._HDR).read())
+    (tmp_path / "dcp_lse_oracle.c").write_text(open(oracle._LSE_SRC).read())
+    (tmp_path / "dcp_lse_oracle.h").write_text(open(oracle._LSE_HDR).read())
     so = tmp_path / "libmutant.so"
-    subprocess.run(["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-o", str(so),
-                    str(mutant_c), "-lm"], check=True)
+    oracle.compile_sources([str(mutant_c), str(tmp_path / "dcp_lse_oracle.c")], str(so))
     saved = oracle._lib
     oracle._lib = oracle.bind(str(so))
     try:

@@ -13,6 +13,10 @@ in packed column space, int32 per-group ``row_ks`` / ``row_ke`` bounds shared by
 (global token t lives on shard t % D at local column t // D, as in the
 SGLang ``dcp/kernels.py`` page, ``create_triton_kv_indices_for_dcp_triton``).
 
+The DCP partial-attention LSE correction (SGLang ``dcp/kernels.py`` page,
+``correct_attn_out``) gets its own inputs at the end: partial outputs and
+base-2 LSEs of N context shards (``make_lse``).
+
 Generators use ``numpy.random.Generator(PCG64(seed))``. Nothing here needs a
 GPU; arrays are C-contiguous numpy arrays.
 """
@@ -40,6 +44,10 @@ __all__ = [
     "random_nan_bits",
     "small_unsharded",
     "small_sharded",
+    "LseWorkload",
+    "LSE_NAMES",
+    "make_lse",
+    "make_lse_named",
 ]
 
 
@@ -333,3 +341,89 @@ def small_sharded(seed: int, *, shards: int, rows: int, global_width: int,
     wl = ShardedWorkload("small_sharded", local, gke, global_block_size,
                          max_global_blocks, topk_blocks, row_repeat, seed)
     return wl, g
+
+
+# --------------------------------------------------------------------------
+# DCP partial-attention LSE correction inputs
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class LseWorkload:
+    """Partial attention results of ``shards`` context shards.
+
+    ``outs`` is ``[N, B, H, Dh]`` fp32 (values on the bf16 grid when
+    ``dtype == "bf16"``), ``lses`` ``[N, B, H]`` fp32 base-2 log-sum-exps.
+    A shard that holds no key for a (token, head) has LSE -inf and a zero
+    partial output.
+    """
+
+    name: str
+    outs: np.ndarray
+    lses: np.ndarray
+    dtype: str
+    seed: int
+    notes: dict = dataclasses.field(default_factory=dict)
+
+    @property
+    def shards(self) -> int:
+        return int(self.outs.shape[0])
+
+    @property
+    def batch(self) -> int:
+        return int(self.outs.shape[1])
+
+    @property
+    def heads(self) -> int:
+        return int(self.outs.shape[2])
+
+    @property
+    def head_dim(self) -> int:
+        return int(self.outs.shape[3])
+
+
+LSE_NAMES = ("lse_decode", "lse_decode_bf16", "lse_tiny")
+
+
+def make_lse(seed: int = 5, *, shards: int = 8, batch: int = 512, heads: int = 128,
+             head_dim: int = 512, dtype: str = "f32", empty_rate: float = 1 / 32,
+             specials: bool = False) -> LseWorkload:
+    """Random partial results of an MLA decode step split over ``shards``.
+
+    Per (token, head) a centre mu ~ U(4, 20); each shard's LSE is
+    mu + N(0, 1). With probability ``empty_rate`` a (shard, token) pair holds
+    no keys (every head's LSE -inf, output 0), as for short contexts.
+    Partial outputs are N(0, 1). ``specials`` also plants NaN and +inf LSEs
+    (1 in 64 entries each, random payload NaNs) and makes token 0 empty on
+    every shard.
+    """
+    assert dtype in ("f32", "bf16")
+    rng = _rng(seed)
+    outs = _normal(rng, (shards, batch, heads, head_dim))
+    if dtype == "bf16":
+        outs = round_to_bf16_grid(outs, inplace=True)
+    mu = rng.uniform(4.0, 20.0, size=(batch, heads)).astype(np.float32)
+    lses = mu[None] + _normal(rng, (shards, batch, heads))
+    empty = rng.random((shards, batch)) < empty_rate
+    if specials and batch:
+        empty[:, 0] = True
+    lses[empty] = -np.inf
+    outs[empty] = 0.0
+    if specials and lses.size:
+        flat = lses.reshape(-1)
+        k = max(1, flat.size // 64)
+        pos = rng.choice(flat.size, size=2 * k, replace=False)
+        flat[pos[:k]] = random_nan_bits(rng, k)
+        flat[pos[k:]] = np.inf
+    return LseWorkload("lse", outs, lses.astype(np.float32), dtype, seed,
+                       {"empty_rate": empty_rate, "specials": specials})
+
+
+def make_lse_named(name: str) -> LseWorkload:
+    """The named LSE-correction workloads (full size, plus a small one)."""
+    if name == "lse_decode":
+        return make_lse(5)
+    if name == "lse_decode_bf16":
+        return make_lse(6, dtype="bf16")
+    if name == "lse_tiny":
+        return make_lse(7, shards=4, batch=16, heads=8, head_dim=64, specials=True)
+    raise KeyError(name)
