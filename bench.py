@@ -13,7 +13,12 @@ id bytes written) / time, with rows/s beside it. Window bytes only: the
 columns outside each row's window are never read and are not counted.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl reference]
+                    [--impl reference] [--op select|mask]
+
+--op mask times the masking pass that follows selection instead: one step
+sets every logit outside the selected candidate blocks (or outside the
+window) to -inf, in place; its bytes are the -inf stores plus the bounds and
+ids read.
 
 Prints one JSON line on rank 0. For N > 1 launch one process per GPU with
 torch.distributed.run; every rank runs the same workload on its own GPU
@@ -38,13 +43,26 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "candidate-select logits GB/s (% of GB300 HBM peak) and rows/s"
+MASK_METRIC = "candidate-mask -inf write GB/s (% of GB300 HBM peak) and rows/s"
+LSE_METRICS = {
+    "correct": "DCP LSE-correction GB/s (% of GB300 HBM peak) and (token, head) rows/s",
+    "merge": "DCP LSE-merge GB/s (% of GB300 HBM peak) and (token, head) rows/s",
+}
+LSE_OPS = tuple(LSE_METRICS)
+LSE_NAMES = ("lse_decode", "lse_decode_bf16", "lse_tiny")
 UNIT = "GB/s"
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ("deepseek_sparse_attention_row_gb300/csrc/dsa_cb.cu",
-                  "deepseek_sparse_attention_row_gb300/csrc/stream.cuh",
-                  "deepseek_sparse_attention_row_gb300/csrc/topk.cuh",
-                  "deepseek_sparse_attention_row_gb300/csrc/keys.cuh")
+_CSRC = "deepseek_sparse_attention_row_gb300/csrc/"
+# The sources each timed kernel is built from; a committed traffic figure
+# counts only while their hash still matches.
+KERNEL_SOURCES = {
+    "select": tuple(_CSRC + f for f in ("dsa_cb.cu", "stream.cuh", "topk.cuh", "topk_warp.cuh",
+                                        "keys.cuh")),
+    "mask": tuple(_CSRC + f for f in ("mask.cu", "keys.cuh")),
+    "correct": (_CSRC + "dcp_lse.cu",),
+    "merge": (_CSRC + "dcp_lse.cu",),
+}
 
 
 # ---------------------------------------------------------------------------
@@ -109,24 +127,25 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(op: str = "select") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[op]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """Per-launch DRAM bytes of the top kernel from the committed ncu summary,
-    if it was taken on the current kernel sources; else None."""
+def profiled_traffic(op: str, workload: str):
+    """Per-launch DRAM bytes of the op's kernel on this workload from the
+    committed ncu summary, if it was taken on the current kernel sources;
+    else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f).get(workload)
+            rec = json.load(f).get(f"{op}/{workload}")
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("kernel_sources") != kernel_source_hash():
+    if not rec or rec.get("kernel_sources") != kernel_source_hash(op):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -256,6 +275,122 @@ def make_runner(wl, dsa, torch, device):
     return step, out
 
 
+def mask_written_elements(wl, ids) -> int:
+    """Logits the masking pass sets to -inf: every column of every (shard)
+    row minus the columns of selected blocks inside the window."""
+    import numpy as np
+
+    if hasattr(wl, "global_row_ke"):
+        D, rows, lw = wl.logits.shape
+        lbs = wl.global_block_size // D
+        g = np.repeat(wl.global_row_ke.astype(np.int64), wl.row_repeat)[:rows]
+        kept = 0
+        for d in range(D):
+            e = np.minimum(np.where(g > d, (g - d + D - 1) // D, 0), lw)
+            for j in range(ids.shape[1]):
+                b = ids[:, j].astype(np.int64)
+                lo = b * lbs
+                kept += int(np.where(b >= 0, np.clip(np.minimum(lo + lbs, e) - lo, 0, None),
+                                     0).sum())
+        return D * rows * lw - kept
+    rows, width, bs = wl.rows, wl.logits.shape[1], wl.block_size
+    ke = np.repeat(wl.row_ke.astype(np.int64), wl.row_repeat)[:rows]
+    ks = (np.zeros(rows, np.int64) if wl.row_ks is None
+          else np.repeat(wl.row_ks.astype(np.int64), wl.row_repeat)[:rows])
+    e = np.minimum(ke, width)
+    s = np.minimum(np.maximum(ks, 0), e)
+    kept = 0
+    for j in range(ids.shape[1]):
+        b = ids[:, j].astype(np.int64)
+        lo = s + b * bs
+        kept += int(np.where(b >= 0, np.clip(np.minimum(lo + bs, e) - lo, 0, None), 0).sum())
+    return rows * width - kept
+
+
+def make_mask_runner(wl, dsa, torch, device):
+    """Device-resident logits and the ids the selection picks for them, and a
+    one-call masking step (idempotent: it only writes -inf)."""
+    step_sel, ids_dev = make_runner(wl, dsa, torch, device)
+    step_sel()
+    torch.cuda.synchronize()
+    if hasattr(wl, "global_row_ke"):
+        logits = torch.from_numpy(wl.logits).to(device)
+        gke = torch.from_numpy(wl.global_row_ke).to(device)
+
+        def step():
+            dsa.dsa_mask_candidate_logits_sharded(logits, gke, wl.global_block_size, ids_dev,
+                                                  wl.row_repeat)
+    else:
+        logits = torch.from_numpy(wl.logits).to(device)
+        ks = None if wl.row_ks is None else torch.from_numpy(wl.row_ks).to(device)
+        ke = torch.from_numpy(wl.row_ke).to(device)
+
+        def step():
+            dsa.dsa_mask_candidate_logits(logits, ks, ke, ids_dev, wl.block_size, wl.row_repeat)
+    ids = ids_dev.cpu().numpy()
+    bounds = wl.global_row_ke.size if hasattr(wl, "global_row_ke") else (
+        wl.row_ke.size + (0 if wl.row_ks is None else wl.row_ks.size))
+    nbytes = 4 * mask_written_elements(wl, ids) + 4 * bounds + 4 * ids.size
+    return step, nbytes, ids
+
+
+def lse_algorithmic_bytes(wl, op: str) -> int:
+    """Bytes one LSE call must move: the partial output(s) read, the LSEs
+    read, the corrected / merged output and the combined LSE written."""
+    esize = 2 if wl.dtype == "bf16" else 4
+    N, B, H, D = wl.outs.shape
+    plane = B * H * D * esize
+    reads = (N if op == "merge" else 1) * plane + 4 * N * B * H
+    return reads + plane + 4 * B * H
+
+
+def lse_workload_config(wl, name: str) -> dict:
+    N, B, H, D = wl.outs.shape
+    return {"workload": f"{name} N={N} [B={B}, H={H}, Dh={D}] {wl.dtype}", "shards": N,
+            "batch": B, "heads": H, "head_dim": D, "dtype": wl.dtype, "seed": wl.seed,
+            "notes": wl.notes}
+
+
+def make_lse_runner(wl, op: str, dsa, torch, device):
+    """Device-resident partial outputs and LSEs, preallocated results, and a
+    one-call step."""
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    N, B, H, D = wl.outs.shape
+    lses = torch.from_numpy(wl.lses).to(device)
+    lse_out = torch.empty((B, H), dtype=torch.float32, device=device)
+    res = torch.empty((H, B, D), dtype=tdt, device=device)
+    if op == "merge":
+        outs = torch.from_numpy(wl.outs).to(device).to(tdt)
+
+        def step():
+            dsa.dsa_merge_attn_out(outs, lses, res, lse_out)
+    else:
+        out = torch.from_numpy(wl.outs[N // 2]).to(device).to(tdt)
+
+        def step():
+            dsa.dsa_correct_attn_out(out, lses, N // 2, res, lse_out)
+    return step
+
+
+def oracle_lse_baseline(wl, op: str, budget_s: float = 10.0):
+    """The LSE oracle as it stands, single-threaded, over the whole workload."""
+    import oracle
+
+    oracle.build()
+    N = wl.shards
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        if op == "merge":
+            oracle.merge_attn_out(wl.outs, wl.lses)
+        else:
+            oracle.correct_attn_out(wl.outs[N // 2], wl.lses, N // 2)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return el / reps, reps
+
+
 def graph_of(step, n: int, torch):
     """A CUDA graph of n consecutive steps (launch cost paid once per replay,
     not per step). The step must have run once before, outside capture."""
@@ -327,6 +462,27 @@ def oracle_cpu_baseline(wl, budget_s: float = 10.0):
     return el / reps, reps
 
 
+def oracle_mask_baseline(wl, ids, budget_s: float = 10.0):
+    """The masking oracle as it stands, single-threaded, repeated over the
+    whole workload until about budget_s seconds have passed."""
+    import oracle
+
+    oracle.build()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        if hasattr(wl, "global_row_ke"):
+            oracle.mask_sharded(wl.logits, wl.global_row_ke, wl.global_block_size, ids,
+                                wl.row_repeat)
+        else:
+            oracle.mask(wl.logits, wl.row_ks, wl.row_ke, ids, wl.block_size, wl.row_repeat,
+                        width=wl.width)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return el / reps, reps
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -345,11 +501,21 @@ def run_ours(args):
     __graft_entry__.build()
     import deepseek_sparse_attention_row_gb300 as dsa
 
-    wl = workloads.make(args.workload)
-    step, out = make_runner(wl, dsa, torch, device)
-    nbytes = algorithmic_bytes(wl)
-    window_bytes = 4 * window_elements(wl)
-    flush = window_bytes < 2 * L2_BYTES
+    if args.op in LSE_OPS:
+        wl = workloads.make_lse_named(args.workload)
+        step = make_lse_runner(wl, args.op, dsa, torch, device)
+        nbytes = lse_algorithmic_bytes(wl, args.op)
+        flush = nbytes < 2 * L2_BYTES
+    elif args.op == "mask":
+        wl = workloads.make(args.workload)
+        step, nbytes, mask_ids = make_mask_runner(wl, dsa, torch, device)
+        flush = nbytes < 2 * L2_BYTES
+    else:
+        wl = workloads.make(args.workload)
+        step, out = make_runner(wl, dsa, torch, device)
+        nbytes = algorithmic_bytes(wl)
+        window_bytes = 4 * window_elements(wl)
+        flush = window_bytes < 2 * L2_BYTES
     scratch = torch.empty(256 * 1000 * 1000 // 4, dtype=torch.float32, device=device) if flush \
         else None
 
@@ -399,44 +565,67 @@ def run_ours(args):
     max_ms = dist_max(gpu_ms, world, device)
     ms_per_step = max_ms / args.steps
     value = whole_job_rate(nbytes * args.steps, world, max_ms / 1e3) / 1e9
-    rows_per_s = whole_job_rate(wl.rows * args.steps, world, max_ms / 1e3)
+    nrows = wl.batch * wl.heads if args.op in LSE_OPS else wl.rows
+    rows_per_s = whole_job_rate(nrows * args.steps, world, max_ms / 1e3)
     launch_s = (gpu_ms / args.steps) / 1e3
     achieved = nbytes / launch_s / 1e9
     peak, peak_src = measured_peak()
 
     e2e = None
     cpu = None
-    if rank == 0 and not args.no_e2e:
+    if rank == 0 and not args.no_e2e and args.op == "select":
         sec, h2d, d2h = e2e_measure(wl, dsa, torch, device, args.e2e_steps)
         e2e = {"value": round(nbytes / sec / 1e9 * world, 3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(sec * 1e3, 4), "steps": args.e2e_steps}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.op in LSE_OPS:
+        sec, reps = oracle_lse_baseline(wl, args.op, args.cpu_budget)
+        cpu = {"value": round(nbytes / sec / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"the whole {args.workload} workload, {reps} pass(es), single-threaded "
+                         f"C oracle ({args.op}), {sec:.3f} s per pass"}
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline and args.op == "mask":
+        sec, reps = oracle_mask_baseline(wl, mask_ids, args.cpu_budget)
+        cpu = {"value": round(nbytes / sec / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"the whole {args.workload} workload, {reps} pass(es), single-threaded "
+                         f"C oracle masking, {sec:.3f} s per pass"}
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         sec, reps = oracle_cpu_baseline(wl, args.cpu_budget)
         cpu = {"value": round(nbytes / sec / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"the whole {args.workload} workload, {reps} pass(es), single-threaded "
                          f"C oracle, {sec:.3f} s per pass"}
 
     if rank == 0:
+        metric = {"select": METRIC, "mask": MASK_METRIC}.get(args.op) or LSE_METRICS[args.op]
+        if args.op in LSE_OPS:
+            config = lse_workload_config(wl, args.workload)
+            full_gbs = None
+            kernel = "lse_kernel (one launch per step)"
+            dtype = "f32" if wl.dtype == "f32" else "f32 arithmetic, bf16 data"
+        else:
+            config = workload_config(wl, args.workload)
+            full_gbs = round(whole_job_rate(wl.logits.nbytes * args.steps, world,
+                                            max_ms / 1e3) / 1e9, 3)
+            kernel = ("select_kernel (one launch per step)" if args.op == "select"
+                      else "mask_kernel (one launch per step)")
+            dtype = "f32"
         line = {
-            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "metric": metric, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
             "data": "synthetic (seeded numpy PCG64; shapes and distributions of the workload)",
-            "config": {**workload_config(wl, args.workload),
+            "config": {**config,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": ("flushed before every step (256 MB write)" if flush else
-                              "inputs larger than L2 (window bytes per step > 2 x 129 MB)")},
+                              "inputs larger than L2 (bytes per step > 2 x 129 MB)")},
             "rows_per_s": round(rows_per_s, 1),
             "algorithmic_bytes_per_step": nbytes,
-            "full_tensor_equivalent_gbs": round(
-                whole_job_rate(wl.logits.nbytes * args.steps, world, max_ms / 1e3) / 1e9, 3),
+            "full_tensor_equivalent_gbs": full_gbs,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 3), "peak": peak,
                          "unit": UNIT, "frac": round(achieved / peak, 4),
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_src == "measured" else "fallback 6.8 TB/s",
-                         "traffic": profiled_traffic(args.workload),
-                         "kernel": "select_kernel (one launch per step)"},
+                         "traffic": profiled_traffic(args.op, args.workload),
+                         "kernel": kernel},
             "clocks": clocks,
             "gpu_launches": args.steps,
             "wall_s_timed_region": round(wall_s, 3),
@@ -464,37 +653,112 @@ def run_reference(args):
     import workloads
 
     oracle.build()
+    if args.op in LSE_OPS:
+        return run_reference_lse(args, oracle, workloads, world)
     wl = workloads.make(args.workload)
-    full_bytes = algorithmic_bytes(wl)
+
+    def oracle_mask_step(w, ids):
+        if hasattr(w, "global_row_ke"):
+            oracle.mask_sharded(w.logits, w.global_row_ke, w.global_block_size, ids,
+                                w.row_repeat)
+        else:
+            oracle.mask(w.logits, w.row_ks, w.row_ke, ids, w.block_size, w.row_repeat,
+                        width=w.logits.shape[1])
+
+    def prepare(w):
+        """(step, algorithmic bytes) of one oracle pass over workload w."""
+        if args.op == "select":
+            return (lambda: oracle.run_workload(w, want_scores=False)), algorithmic_bytes(w)
+        ids, _ = oracle.run_workload(w, want_scores=False)
+        nb = (w.global_row_ke.size if hasattr(w, "global_row_ke")
+              else w.row_ke.size + (0 if w.row_ks is None else w.row_ks.size))
+        return ((lambda: oracle_mask_step(w, ids)),
+                4 * mask_written_elements(w, ids) + 4 * nb + 4 * ids.size)
+
     # Calibrate on a slice of rows, then size each step's sample so that the
     # whole run stays within about args.ref_budget seconds.
     rows = wl.rows
     probe = max(1, rows // 64)
-    sub = _row_slice(wl, 0, probe)
+    probe_step, _ = prepare(_row_slice(wl, 0, probe))
     t0 = time.perf_counter()
-    oracle.run_workload(sub, want_scores=False)
+    probe_step()
     per_row = max((time.perf_counter() - t0) / probe, 1e-7)
     total_steps = args.steps + args.warmup
     sample_rows = int(max(1, min(rows, args.ref_budget / total_steps / per_row)))
-    sample = _row_slice(wl, 0, sample_rows)
-    sample_bytes = algorithmic_bytes(sample)
+    ref_step, sample_bytes = prepare(_row_slice(wl, 0, sample_rows))
     for _ in range(args.warmup):
-        oracle.run_workload(sample, want_scores=False)
+        ref_step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.run_workload(sample, want_scores=False)
+        ref_step()
     sec = (time.perf_counter() - t0) / args.steps
     value = sample_bytes / sec / 1e9
     desc = (f"first {sample_rows} of {rows} rows of the {args.workload} workload per step "
-            f"({sample_bytes} algorithmic bytes; full step {full_bytes})")
+            f"({sample_bytes} algorithmic bytes)")
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "impl": "reference", "metric": METRIC if args.op == "select" else MASK_METRIC,
+        "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(sec * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded numpy PCG64; shapes and distributions of the workload)",
         "config": {**workload_config(wl, args.workload), "parallelism": "host, 1 thread"},
         "rows_per_s": round(sample_rows / sec, 1),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_lse(args, oracle, workloads, world):
+    """Reference arm for the LSE ops: the oracle on the first tokens of the
+    workload, sized so that the whole run takes about args.ref_budget s."""
+    import copy
+
+    wl = workloads.make_lse_named(args.workload)
+    N, B = wl.shards, wl.batch
+
+    def sliced(b):
+        w = copy.copy(wl)
+        w.outs = np.ascontiguousarray(wl.outs[:, :b])
+        w.lses = np.ascontiguousarray(wl.lses[:, :b])
+        return w
+
+    def run(w):
+        if args.op == "merge":
+            oracle.merge_attn_out(w.outs, w.lses)
+        else:
+            oracle.correct_attn_out(w.outs[N // 2], w.lses, N // 2)
+
+    import numpy as np
+
+    probe = sliced(max(1, B // 32))
+    t0 = time.perf_counter()
+    run(probe)
+    per_tok = max((time.perf_counter() - t0) / probe.batch, 1e-7)
+    total_steps = args.steps + args.warmup
+    b = int(max(1, min(B, args.ref_budget / total_steps / per_tok)))
+    sample = sliced(b)
+    sample_bytes = lse_algorithmic_bytes(sample, args.op)
+    for _ in range(args.warmup):
+        run(sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run(sample)
+    sec = (time.perf_counter() - t0) / args.steps
+    value = sample_bytes / sec / 1e9
+    desc = (f"first {b} of {B} tokens (all heads) of the {args.workload} workload per step "
+            f"({sample_bytes} algorithmic bytes)")
+    line = {
+        "impl": "reference", "metric": LSE_METRICS[args.op], "value": round(value, 4),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded numpy PCG64; shapes and distributions of the workload)",
+        "config": {**lse_workload_config(wl, args.workload), "parallelism": "host, 1 thread"},
+        "rows_per_s": round(b * wl.heads / sec, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -529,8 +793,14 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--workload", default="dcp",
-                   choices=("dcp", "decode", "prefill", "long", "long_pin", "tiny"))
+    p.add_argument("--op", choices=("select", "mask") + LSE_OPS, default="select",
+                   help="select: candidate selection (the bench line); mask: the masking "
+                        "pass that follows it; correct / merge: the DCP partial-attention "
+                        "LSE correction of one shard / merge of all shards")
+    p.add_argument("--workload", default=None,
+                   choices=("dcp", "decode", "prefill", "long", "long_pin", "tiny")
+                   + tuple(LSE_NAMES),
+                   help="default: dcp for select / mask, lse_decode for correct / merge")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -539,6 +809,10 @@ def main(argv=None):
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
+    if args.workload is None:
+        args.workload = "lse_decode" if args.op in LSE_OPS else "dcp"
+    if (args.op in LSE_OPS) != (args.workload in LSE_NAMES):
+        p.error(f"--op {args.op} does not run on --workload {args.workload}")
     _, world, _ = dist_env()
     if args.gpus > 1 and world == 1 and args.impl == "ours":
         p.error("--gpus N > 1 needs torch.distributed.run with N processes")

@@ -1,6 +1,7 @@
 """GB300 (sm_103a) DSA candidate-block selection.
 
-A thin binding over ``libdsa_cb.so`` (C ABI declared in ``include/dsa_cb.h``):
+A thin binding over ``libdsa_cb.so`` (C ABI declared in ``include/dsa_cb.h``
+and ``include/dsa_dcp_attn.h``):
 argument marshalling only. Every step of the computation runs in the
 library's CUDA kernels; there is no CPU or PyTorch fallback, and every call
 raises if the library is missing or a call fails.
@@ -13,6 +14,11 @@ Functions carry the C ABI's names:
   (``select_candidate_blocks`` without a DCP group).
 * ``dsa_select_candidate_blocks_sharded`` -- the DCP form with the ranks'
   local logits held as a leading ``[D, rows, local_width]`` axis.
+* ``dsa_mask_candidate_logits[_sharded]`` -- the masking pass after
+  selection: -inf outside each row's window and candidate blocks.
+* ``dsa_correct_attn_out`` / ``dsa_merge_attn_out`` -- the DCP partial-
+  attention LSE correction (sglang ``dcp/kernels.py``, ``correct_attn_out``;
+  C ABI in ``include/dsa_dcp_attn.h``) and the sum over shards after it.
 
 Tensors are PyTorch CUDA tensors (PyTorch supplies device memory and the
 current stream). ``select_candidate_blocks_host`` accepts host tensors and
@@ -34,6 +40,8 @@ __all__ = [
     "dsa_select_candidate_blocks_sharded",
     "dsa_mask_candidate_logits",
     "dsa_mask_candidate_logits_sharded",
+    "dsa_correct_attn_out",
+    "dsa_merge_attn_out",
     "select_candidate_blocks_host",
     "select_candidate_blocks_sharded_host",
     "max_select_blocks",
@@ -54,6 +62,9 @@ EXPORTED_SYMBOLS = (
     "dsa_mask_candidate_logits",
     "dsa_mask_candidate_logits_sharded",
     "dsa_select_candidate_blocks_sharded_static",
+    "dsa_attn_max_shards",
+    "dsa_correct_attn_out",
+    "dsa_merge_attn_out",
 )
 
 _lib = None
@@ -94,9 +105,16 @@ def library():
     lib.dsa_mask_candidate_logits.argtypes = [p, i64, i64, i64, p, p, p, i32, i64, i32, i32, p]
     lib.dsa_mask_candidate_logits_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32, p,
                                                       i32, i64, p]
+    lib.dsa_attn_max_shards.argtypes = []
+    lib.dsa_attn_max_shards.restype = i32
+    lib.dsa_correct_attn_out.argtypes = [p, i32, i64, i64, i64, i64, i64, i64, p, i32, i64, i64,
+                                         i64, i32, p, i64, i64, i64, p, i64, i64, p]
+    lib.dsa_merge_attn_out.argtypes = [p, i32, i32, i64, i64, i64, i64, i64, i64, i64, p, i64,
+                                       i64, i64, p, i64, i64, i64, p, i64, i64, p]
     for f in (lib.dsa_block_scores, lib.dsa_select_candidate_blocks,
               lib.dsa_select_candidate_blocks_sharded, lib.dsa_mask_candidate_logits,
-              lib.dsa_mask_candidate_logits_sharded):
+              lib.dsa_mask_candidate_logits_sharded, lib.dsa_correct_attn_out,
+              lib.dsa_merge_attn_out):
         f.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -278,6 +296,89 @@ def dsa_mask_candidate_logits_sharded(logits, global_row_ke, global_block_size: 
         _stream_handle(stream))
     _check("dsa_mask_candidate_logits_sharded", st)
     return logits
+
+
+DTYPE_F32, DTYPE_BF16 = 0, 1
+
+
+def _attn_dtype(t, name):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError(f"{name} must be float32 or bfloat16, got {t.dtype}")
+
+
+def _attn_ptr(t, name, dtype_code):
+    torch = _torch()
+    want = torch.float32 if dtype_code == DTYPE_F32 else torch.bfloat16
+    return _dev_ptr(t, want, name)
+
+
+def dsa_correct_attn_out(out, lses, rank: int, new_out=None, lse_out=None, stream=None):
+    """DCP LSE correction of shard ``rank``'s partial attention output.
+
+    ``out`` [B, H, Dh] (or [B, 1, H, Dh]) fp32 or bf16; ``lses`` [N, B, H]
+    fp32 base-2 LSEs of all shards (a trailing or second size-1 dimension is
+    squeezed, as on the page). Writes ``new_out`` [H, B, Dh] (allocated when
+    None, same dtype as ``out``) and the combined LSE ``lse_out`` [B, H]
+    fp32 (allocated when None); returns both."""
+    torch = _torch()
+    if out.dim() == 4 and out.shape[1] == 1:
+        out = out.squeeze(1)
+    if lses.dim() == 4 and lses.shape[-1] == 1:
+        lses = lses.squeeze(-1)
+    if lses.dim() == 4 and lses.shape[1] == 1:
+        lses = lses.squeeze(1)
+    if out.dim() != 3 or lses.dim() != 3:
+        raise ValueError("expected out [B, H, Dh] and lses [N, B, H]")
+    B, H, D = out.shape
+    N = lses.shape[0]
+    if tuple(lses.shape[1:]) != (B, H):
+        raise ValueError(f"lses {tuple(lses.shape)} does not match out {tuple(out.shape)}")
+    code = _attn_dtype(out, "out")
+    if new_out is None:
+        new_out = torch.empty((H, B, D), dtype=out.dtype, device=out.device)
+    if lse_out is None:
+        lse_out = torch.empty((B, H), dtype=torch.float32, device=out.device)
+    if tuple(new_out.shape) != (H, B, D) or tuple(lse_out.shape) != (B, H):
+        raise ValueError("new_out must be [H, B, Dh] and lse_out [B, H]")
+    st = library().dsa_correct_attn_out(
+        _attn_ptr(out, "out", code), code, B, H, D, *out.stride(),
+        _dev_ptr(lses, torch.float32, "lses"), N, *lses.stride(), rank,
+        _attn_ptr(new_out, "new_out", code), *new_out.stride(),
+        _dev_ptr(lse_out, torch.float32, "lse_out"), *lse_out.stride(), _stream_handle(stream))
+    _check("dsa_correct_attn_out", st)
+    return new_out, lse_out
+
+
+def dsa_merge_attn_out(outs, lses, merged=None, lse_out=None, stream=None):
+    """Sum over shards of the corrected partial outputs.
+
+    ``outs`` [N, B, H, Dh] fp32 or bf16, ``lses`` [N, B, H] fp32. Writes
+    ``merged`` [H, B, Dh] (same dtype as ``outs``) and ``lse_out`` [B, H]
+    fp32, allocating them when None; returns both."""
+    torch = _torch()
+    if outs.dim() != 4 or lses.dim() != 3:
+        raise ValueError("expected outs [N, B, H, Dh] and lses [N, B, H]")
+    N, B, H, D = outs.shape
+    if tuple(lses.shape) != (N, B, H):
+        raise ValueError(f"lses {tuple(lses.shape)} does not match outs {tuple(outs.shape)}")
+    code = _attn_dtype(outs, "outs")
+    if merged is None:
+        merged = torch.empty((H, B, D), dtype=outs.dtype, device=outs.device)
+    if lse_out is None:
+        lse_out = torch.empty((B, H), dtype=torch.float32, device=outs.device)
+    if tuple(merged.shape) != (H, B, D) or tuple(lse_out.shape) != (B, H):
+        raise ValueError("merged must be [H, B, Dh] and lse_out [B, H]")
+    st = library().dsa_merge_attn_out(
+        _attn_ptr(outs, "outs", code), code, N, B, H, D, *outs.stride(),
+        _dev_ptr(lses, torch.float32, "lses"), *lses.stride(),
+        _attn_ptr(merged, "merged", code), *merged.stride(),
+        _dev_ptr(lse_out, torch.float32, "lse_out"), *lse_out.stride(), _stream_handle(stream))
+    _check("dsa_merge_attn_out", st)
+    return merged, lse_out
 
 
 def _to_device(host, dev_buf, stream):

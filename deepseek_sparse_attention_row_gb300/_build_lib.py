@@ -1,8 +1,10 @@
 """Compile libdsa_cb.so (sm_103a) in tree, under ``_build/``.
 
-The library is one translation unit (``csrc/dsa_cb.cu``) compiled by nvcc for
-``-gencode arch=compute_103a,code=sm_103a`` with the CUDA runtime linked
-statically, so it loads next to any PyTorch build without a runtime search.
+Each ``csrc/*.cu`` is compiled by nvcc for
+``-gencode arch=compute_103a,code=sm_103a`` (in parallel, one object each)
+and the objects are linked into one shared library with the CUDA runtime
+linked statically, so it loads next to any PyTorch build without a runtime
+search.
 """
 
 from __future__ import annotations
@@ -16,13 +18,14 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libdsa_cb.so")
-HEADER = os.path.join(ROOT, "include", "dsa_cb.h")
+INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
 def sources() -> list:
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
-                  if f.endswith((".cu", ".cuh"))) + [HEADER]
+    return (sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                   if f.endswith((".cu", ".cuh")))
+            + sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")))
 
 
 def nvcc() -> str:
@@ -32,23 +35,47 @@ def nvcc() -> str:
     return "nvcc"
 
 
+def units() -> list:
+    """The translation units, one object each."""
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     if (not force and os.path.exists(LIB)
             and os.path.getmtime(LIB) >= max(os.path.getmtime(s) for s in sources())):
         return LIB
-    tmp = f"{LIB}.tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-           "-shared", "-o", tmp, os.path.join(CSRC, "dsa_cb.cu")]
+    tag = f"tmp{os.getpid()}"
+    flags = [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC"]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        sys.stderr.write(res.stdout + res.stderr)
-        raise RuntimeError("nvcc failed to build libdsa_cb.so")
-    if verbose:
-        sys.stderr.write(res.stderr)
-    os.replace(tmp, LIB)
+        flags.append("-Xptxas=-v")
+    procs, objs = [], []
+    for cu in units():
+        obj = os.path.join(BUILD, os.path.basename(cu)[:-3] + f".{tag}.o")
+        objs.append(obj)
+        procs.append((cu, subprocess.Popen([nvcc(), *flags, "-c", "-o", obj, cu],
+                                           stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                           text=True)))
+    failed = False
+    for cu, p in procs:
+        out, err = p.communicate()
+        if p.returncode != 0 or verbose:
+            sys.stderr.write(f"== {os.path.basename(cu)}\n" + out + err)
+        failed |= p.returncode != 0
+    try:
+        if failed:
+            raise RuntimeError("nvcc failed to build libdsa_cb.so")
+        tmp = f"{LIB}.{tag}"
+        res = subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs],
+                             capture_output=True, text=True)
+        if res.returncode != 0:
+            sys.stderr.write(res.stdout + res.stderr)
+            raise RuntimeError("nvcc failed to link libdsa_cb.so")
+        os.replace(tmp, LIB)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return LIB
 
 

@@ -28,7 +28,6 @@
 #include <mutex>
 
 #include "keys.cuh"
-#include "mask.cuh"
 #include "stream.cuh"
 #include "topk.cuh"
 #include "topk_warp.cuh"
@@ -688,83 +687,6 @@ dsa_status dsa_select_candidate_blocks_sharded(const float* logits, int32_t shar
 }
 
 }  // extern "C"
-
-// ---------------------------------------------------------------------------
-// Masking to candidates
-// ---------------------------------------------------------------------------
-
-namespace dsa {
-namespace {
-
-dsa_status launch_mask(MaskArgs& a, cudaStream_t stream) {
-  a.chunks = static_cast<int32_t>((static_cast<int64_t>(a.width) + kMaskChunk - 1) / kMaskChunk);
-  const int64_t grid = static_cast<int64_t>(a.shards) * a.rows * a.chunks;
-  if (grid > INT32_MAX) return DSA_EUNSUPPORTED;
-  mask_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
-}
-
-}  // namespace
-}  // namespace dsa
-
-extern "C" dsa_status dsa_mask_candidate_logits(float* logits, int64_t rows, int64_t width,
-                                                int64_t ld_logits, const int32_t* row_ks,
-                                                const int32_t* row_ke, const int32_t* candidates,
-                                                int32_t topk_blocks, int64_t ld_candidates,
-                                                int32_t block_size, int32_t row_repeat,
-                                                void* stream) {
-  if (rows < 0 || width < 0 || block_size < 1 || row_repeat < 1 || topk_blocks < 0)
-    return DSA_EINVAL;
-  if (rows == 0 || width == 0) return DSA_OK;
-  if (!logits || !row_ke || ld_logits < width) return DSA_EINVAL;
-  if (topk_blocks > 0 && (!candidates || ld_candidates < topk_blocks)) return DSA_EINVAL;
-  if (width > INT32_MAX - kMaskChunk) return DSA_EUNSUPPORTED;
-  dsa::MaskArgs a{};
-  a.logits = logits;
-  a.ld = ld_logits;
-  a.shard_stride = 0;
-  a.shards = 1;
-  a.rows = rows;
-  a.width = static_cast<int32_t>(width);
-  a.row_ks = row_ks;
-  a.row_ke = row_ke;
-  a.row_repeat = row_repeat;
-  a.block_size = block_size;
-  a.cand = candidates;
-  a.topk = topk_blocks;
-  a.ld_cand = ld_candidates;
-  return dsa::launch_mask(a, static_cast<cudaStream_t>(stream));
-}
-
-extern "C" dsa_status dsa_mask_candidate_logits_sharded(
-    float* logits, int32_t shards, int64_t rows, int64_t local_width, int64_t ld_logits,
-    int64_t shard_stride, const int32_t* global_row_ke, int32_t global_block_size,
-    int32_t row_repeat, const int32_t* candidates, int32_t topk_blocks, int64_t ld_candidates,
-    void* stream) {
-  if (shards < 1 || rows < 0 || local_width < 0 || global_block_size < 1 ||
-      global_block_size % shards != 0 || row_repeat < 1 || topk_blocks < 0 ||
-      ld_logits < local_width || shard_stride < 0)
-    return DSA_EINVAL;
-  if (rows == 0 || local_width == 0) return DSA_OK;
-  if (!logits || !global_row_ke) return DSA_EINVAL;
-  if (topk_blocks > 0 && (!candidates || ld_candidates < topk_blocks)) return DSA_EINVAL;
-  if (local_width > INT32_MAX - kMaskChunk) return DSA_EUNSUPPORTED;
-  dsa::MaskArgs a{};
-  a.logits = logits;
-  a.ld = ld_logits;
-  a.shard_stride = shard_stride;
-  a.shards = shards;
-  a.rows = rows;
-  a.width = static_cast<int32_t>(local_width);
-  a.row_ks = nullptr;
-  a.row_ke = global_row_ke;
-  a.row_repeat = row_repeat;
-  a.block_size = global_block_size / shards;
-  a.cand = candidates;
-  a.topk = topk_blocks;
-  a.ld_cand = ld_candidates;
-  return dsa::launch_mask(a, static_cast<cudaStream_t>(stream));
-}
 
 // ---------------------------------------------------------------------------
 // Allocation-free entry point

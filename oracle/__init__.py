@@ -13,7 +13,11 @@ readings taken where the pages are silent. Every function here is pinned by
 correction (``correct_attn_out``, ``merge_attn_out``); its pins are in
 ``tests/test_oracle_lse.py``.
 
-``build()`` compiles both C files with gcc into one library in
+``dsa_oracle_bf16.c`` gives the selection, block-score and masking entry
+points for bf16 logits (``*_bf16``: uint16 bit patterns in and out); its pins
+are in ``tests/test_oracle_bf16.py``.
+
+``build()`` compiles the C files with gcc into one library in
 ``oracle/_build``.
 """
 
@@ -31,7 +35,8 @@ _SRC = os.path.join(_HERE, "dsa_oracle.c")
 _HDR = os.path.join(_HERE, "dsa_oracle.h")
 _LSE_SRC = os.path.join(_HERE, "dcp_lse_oracle.c")
 _LSE_HDR = os.path.join(_HERE, "dcp_lse_oracle.h")
-SOURCES = (_SRC, _LSE_SRC)
+_BF16_SRC = os.path.join(_HERE, "dsa_oracle_bf16.c")
+SOURCES = (_SRC, _LSE_SRC, _BF16_SRC)
 HEADERS = (_HDR, _LSE_HDR)
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libdsa_oracle.so")
@@ -73,11 +78,19 @@ def bind(path: str):
                                               p, i64, p, i64]
     lib.dsa_oracle_mask.argtypes = [p, i64, i64, i64, p, p, p, i64, i64, i32, i32]
     lib.dsa_oracle_mask_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32, p, i64, i64]
+    lib.dsa_oracle_block_scores_bf16.argtypes = lib.dsa_oracle_block_scores.argtypes
+    lib.dsa_oracle_select_bf16.argtypes = lib.dsa_oracle_select.argtypes
+    lib.dsa_oracle_select_sharded_bf16.argtypes = lib.dsa_oracle_select_sharded.argtypes
+    lib.dsa_oracle_mask_bf16.argtypes = lib.dsa_oracle_mask.argtypes
+    lib.dsa_oracle_mask_sharded_bf16.argtypes = lib.dsa_oracle_mask_sharded.argtypes
     lib.dcp_oracle_correct_attn_out.argtypes = [p, p, i32, i64, i64, i64, i32, p, p]
     lib.dcp_oracle_merge_attn_out.argtypes = [p, p, i32, i64, i64, i64, p, p]
     for f in (lib.dsa_oracle_block_scores, lib.dsa_oracle_select,
               lib.dsa_oracle_select_sharded, lib.dsa_oracle_mask, lib.dsa_oracle_mask_sharded,
-              lib.dcp_oracle_correct_attn_out, lib.dcp_oracle_merge_attn_out):
+              lib.dcp_oracle_correct_attn_out, lib.dcp_oracle_merge_attn_out,
+              lib.dsa_oracle_block_scores_bf16, lib.dsa_oracle_select_bf16,
+              lib.dsa_oracle_select_sharded_bf16, lib.dsa_oracle_mask_bf16,
+              lib.dsa_oracle_mask_sharded_bf16):
         f.restype = ctypes.c_int
     return lib
 
@@ -97,6 +110,18 @@ def _f32(a):
     a = np.asarray(a, dtype=np.float32)
     assert a.flags.c_contiguous
     return a
+
+
+def _u16(a):
+    """bf16 logits as their uint16 bit patterns (a numpy uint16 array, or a
+    float32 array whose values are exactly bf16-representable)."""
+    a = np.asarray(a)
+    if a.dtype == np.float32:
+        bits = a.view(np.uint32)
+        assert not (bits & 0xFFFF).any(), "float32 values are not on the bf16 grid"
+        a = (bits >> 16).astype(np.uint16)
+    assert a.dtype == np.uint16
+    return np.ascontiguousarray(a)
 
 
 def _i32(a):
@@ -249,3 +274,99 @@ def merge_attn_out(outs: np.ndarray, lses: np.ndarray):
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (status {rc})")
     return merged, lse
+
+
+# --------------------------------------------------------------------------
+# bf16 logits (dsa_oracle_bf16.c): inputs and scores are uint16 bit patterns
+# --------------------------------------------------------------------------
+
+def block_scores_bf16(logits, row_ks, row_ke, block_size: int, row_repeat: int = 1,
+                      pin_newest: bool = True, width: Optional[int] = None) -> np.ndarray:
+    """bf16 block scores (uint16 bits) of bf16 logits ``[rows, ld]``."""
+    x = _u16(logits)
+    rows, ld = x.shape
+    width = ld if width is None else width
+    nb = nblocks(width, block_size)
+    scores = np.zeros((rows, nb), dtype=np.uint16)
+    rc = _load().dsa_oracle_block_scores_bf16(_ptr(x), rows, width, ld, _ptr(_i32(row_ks)),
+                                              _ptr(_i32(row_ke)), block_size, row_repeat,
+                                              int(pin_newest), _ptr(scores), nb)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return scores
+
+
+def select_bf16(logits, row_ks, row_ke, topk_blocks: int, block_size: int, row_repeat: int = 1,
+                pin_newest: bool = True, width: Optional[int] = None, want_scores: bool = True):
+    """``select`` on bf16 logits: ids and bf16 scores (uint16 bits)."""
+    x = _u16(logits)
+    rows, ld = x.shape
+    width = ld if width is None else width
+    nb = nblocks(width, block_size)
+    out = np.full((rows, topk_blocks), -7, dtype=np.int32)
+    scores = np.zeros((rows, nb), dtype=np.uint16) if want_scores and nb else None
+    rc = _load().dsa_oracle_select_bf16(_ptr(x), rows, width, ld, _ptr(_i32(row_ks)),
+                                        _ptr(_i32(row_ke)), topk_blocks, block_size, row_repeat,
+                                        int(pin_newest), _ptr(out), topk_blocks, _ptr(scores),
+                                        max(nb, 1))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return out, scores
+
+
+def select_sharded_bf16(logits, global_row_ke, global_block_size: int, max_global_blocks: int,
+                        topk_blocks: int, row_repeat: int = 1, want_scores: bool = True):
+    """``select_sharded`` on bf16 logits ``[shards, rows, local_width]``."""
+    x = _u16(logits)
+    shards, rows, lw = x.shape
+    nbg = max(int(max_global_blocks), 1)
+    out = np.full((rows, topk_blocks), -7, dtype=np.int32)
+    scores = np.zeros((rows, nbg), dtype=np.uint16) if want_scores else None
+    rc = _load().dsa_oracle_select_sharded_bf16(_ptr(x), shards, rows, lw, lw, rows * lw,
+                                                _ptr(_i32(global_row_ke)), global_block_size,
+                                                max_global_blocks, row_repeat, topk_blocks,
+                                                _ptr(out), topk_blocks, _ptr(scores), nbg)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return out, scores
+
+
+def mask_bf16(logits, row_ks, row_ke, candidates, block_size: int, row_repeat: int = 1,
+              width: Optional[int] = None) -> np.ndarray:
+    """Masked copy (uint16 bits) of bf16 logits ``[rows, ld]``."""
+    out = np.array(_u16(logits), copy=True)
+    rows, ld = out.shape
+    width = ld if width is None else width
+    cand = np.ascontiguousarray(candidates, dtype=np.int32)
+    topk = cand.shape[1] if cand.ndim == 2 else 0
+    rc = _load().dsa_oracle_mask_bf16(_ptr(out), rows, width, ld, _ptr(_i32(row_ks)),
+                                      _ptr(_i32(row_ke)), _ptr(cand), topk, max(topk, 1),
+                                      block_size, row_repeat)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return out
+
+
+def mask_sharded_bf16(logits, global_row_ke, global_block_size: int, candidates,
+                      row_repeat: int = 1) -> np.ndarray:
+    """Masked copy (uint16 bits) of bf16 logits ``[shards, rows, local_width]``."""
+    out = np.array(_u16(logits), copy=True)
+    shards, rows, lw = out.shape
+    cand = np.ascontiguousarray(candidates, dtype=np.int32)
+    topk = cand.shape[1] if cand.ndim == 2 else 0
+    rc = _load().dsa_oracle_mask_sharded_bf16(_ptr(out), shards, rows, lw, lw, rows * lw,
+                                              _ptr(_i32(global_row_ke)), global_block_size,
+                                              row_repeat, _ptr(cand), topk, max(topk, 1))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return out
+
+
+def run_workload_bf16(wl, want_scores: bool = True):
+    """Run the bf16 oracle on a workload whose logits are on the bf16 grid."""
+    if hasattr(wl, "global_row_ke"):
+        return select_sharded_bf16(wl.logits, wl.global_row_ke, wl.global_block_size,
+                                   wl.max_global_blocks, wl.topk_blocks, wl.row_repeat,
+                                   want_scores=want_scores)
+    return select_bf16(wl.logits, wl.row_ks, wl.row_ke, wl.topk_blocks, wl.block_size,
+                       wl.row_repeat, wl.pin_newest, width=wl.width, want_scores=want_scores)

@@ -1,5 +1,5 @@
 """The C ABI without a GPU: the library builds for sm_103a, loads, exports
-every function that ``include/dsa_cb.h`` declares, and rejects invalid
+every function that the headers in ``include/`` declare, and rejects invalid
 arguments on the host before touching the device (no call below reaches a
 CUDA API)."""
 
@@ -11,7 +11,8 @@ import subprocess
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "dsa_cb.h")
+INCLUDE = os.path.join(ROOT, "include")
+HEADERS = sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h"))
 
 DSA_OK, DSA_EINVAL, DSA_ECUDA, DSA_EUNSUPPORTED = 0, -1, -2, -3
 
@@ -27,15 +28,19 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
-def test_header_declares_the_three_operations():
+def test_headers_declare_the_operations():
     names = declared_functions()
     for n in ("dsa_block_scores", "dsa_select_candidate_blocks",
-              "dsa_select_candidate_blocks_sharded"):
+              "dsa_select_candidate_blocks_sharded", "dsa_mask_candidate_logits",
+              "dsa_mask_candidate_logits_sharded", "dsa_correct_attn_out",
+              "dsa_merge_attn_out"):
         assert n in names
 
 
@@ -197,3 +202,53 @@ def test_mask_sharded_validation(lib, kw, want):
                                                a["row_repeat"], a["cand"], a["topk"],
                                                a["ld_cand"], None)
     assert st == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(dtype=2), DSA_EINVAL),
+    (dict(shards=0), DSA_EINVAL),
+    (dict(rank=-1), DSA_EINVAL),
+    (dict(rank=8), DSA_EINVAL),
+    (dict(batch=-1), DSA_EINVAL),
+    (dict(head_dim=-1), DSA_EINVAL),
+    (dict(lses=None), DSA_EINVAL),
+    (dict(out=None), DSA_EINVAL),
+    (dict(new_out=None), DSA_EINVAL),
+    (dict(shards=33, rank=0), DSA_EUNSUPPORTED),
+    (dict(batch=0), DSA_OK),
+    (dict(heads=0), DSA_OK),
+])
+def test_correct_attn_out_validation(lib, kw, want):
+    a = dict(out=FAKE, dtype=0, batch=4, heads=8, head_dim=64, lses=FAKE, shards=8, rank=3,
+             new_out=FAKE)
+    a.update(kw)
+    B, H, D = a["batch"], a["heads"], a["head_dim"]
+    st = lib.dsa_correct_attn_out(a["out"], a["dtype"], B, H, D, H * D, D, 1, a["lses"],
+                                  a["shards"], B * H, H, 1, a["rank"], a["new_out"], B * D, D, 1,
+                                  None, H, 1, None)
+    assert st == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(dtype=-1), DSA_EINVAL),
+    (dict(shards=0), DSA_EINVAL),
+    (dict(heads=-1), DSA_EINVAL),
+    (dict(lses=None), DSA_EINVAL),
+    (dict(outs=None), DSA_EINVAL),
+    (dict(merged=None), DSA_EINVAL),
+    (dict(shards=64), DSA_EUNSUPPORTED),
+    (dict(batch=0), DSA_OK),
+])
+def test_merge_attn_out_validation(lib, kw, want):
+    a = dict(outs=FAKE, dtype=1, shards=4, batch=4, heads=8, head_dim=64, lses=FAKE,
+             merged=FAKE)
+    a.update(kw)
+    N, B, H, D = a["shards"], a["batch"], a["heads"], a["head_dim"]
+    st = lib.dsa_merge_attn_out(a["outs"], a["dtype"], N, B, H, D, B * H * D, H * D, D, 1,
+                                a["lses"], B * H, H, 1, a["merged"], B * D, D, 1, None, H, 1,
+                                None)
+    assert st == want
+
+
+def test_attn_limits(lib):
+    assert lib.dsa_attn_max_shards() == 32

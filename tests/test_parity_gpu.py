@@ -257,6 +257,28 @@ def test_mask_sweep(env, seed):
     assert_bits_equal(got, want[:, :width])
 
 
+@pytest.mark.parametrize("bs", [2, 1000, 4096, 8193, 20000])
+def test_mask_long_kept_runs(env, bs):
+    """Kept runs longer than a chunk, runs that start or end inside a 16-byte
+    slot, and adjacent candidate blocks whose runs meet inside a slot."""
+    torch, dsa = env
+    rng = np.random.default_rng(8800 + bs)
+    width, rows = 40001, 6
+    wl = workloads.small_unsharded(8800 + bs, rows=rows, width=width, block_size=bs,
+                                   topk_blocks=8, starts=True, ld=width + 1)
+    nb = -(-width // bs)
+    cand = np.stack([rng.permutation(nb)[:8] if nb >= 8 else
+                     np.concatenate([np.arange(nb), -np.ones(8 - nb, int)])
+                     for _ in range(rows)]).astype(np.int32)
+    cand[0, :2] = [0, 1]           # adjacent blocks
+    want = oracle.mask(wl.logits, wl.row_ks, wl.row_ke, cand, bs, 1, width=width)
+    logits = _padded_logits(torch, wl.logits, width, 1)
+    dsa.dsa_mask_candidate_logits(logits, _dev(torch, wl.row_ks), _dev(torch, wl.row_ke),
+                                  _dev(torch, cand), bs, 1)
+    torch.cuda.synchronize()
+    assert_bits_equal(logits.cpu().numpy(), want[:, :width])
+
+
 @pytest.mark.parametrize("seed", range(8))
 def test_mask_sharded_sweep(env, seed):
     torch, dsa = env
