@@ -58,6 +58,25 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def build_variant(directory: str, replacements: dict) -> str:
+    """Build a copy of the oracle library in ``directory`` with the given
+    ``{file name: new text}`` replacing those sources (used by the tests to
+    plant mistakes); returns the library's path."""
+    srcs = []
+    for f in SOURCES + HEADERS:
+        name = os.path.basename(f)
+        with open(f) as fh:
+            text = fh.read()
+        dst = os.path.join(directory, name)
+        with open(dst, "w") as fh:
+            fh.write(replacements.get(name, text))
+        if name.endswith(".c"):
+            srcs.append(dst)
+    path = os.path.join(directory, "libvariant.so")
+    compile_sources(srcs, path)
+    return path
+
+
 def compile_sources(sources, path: str, warnings: bool = False) -> None:
     """gcc the given C sources (with the headers beside them) into a shared
     library at ``path``."""

@@ -206,15 +206,9 @@ def test_planted_lse_mistake_is_caught(name, old, new, tmp_path):
     with open(oracle._LSE_SRC) as f:
         src = f.read()
     assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
-    (tmp_path / "dcp_lse_oracle.c").write_text(src.replace(old, new))
-    (tmp_path / "dcp_lse_oracle.h").write_text(open(oracle._LSE_HDR).read())
-    (tmp_path / "dsa_oracle.c").write_text(open(oracle._SRC).read())
-    (tmp_path / "dsa_oracle.h").write_text(open(oracle._HDR).read())
-    so = tmp_path / "libmutant.so"
-    oracle.compile_sources([str(tmp_path / "dsa_oracle.c"), str(tmp_path / "dcp_lse_oracle.c")],
-                           str(so))
+    so = oracle.build_variant(str(tmp_path), {"dcp_lse_oracle.c": src.replace(old, new)})
     saved = oracle._lib
-    oracle._lib = oracle.bind(str(so))
+    oracle._lib = oracle.bind(so)
     try:
         failed = _battery()
     finally:

@@ -96,15 +96,9 @@ def test_planted_mistake_is_caught(name, old, new, tmp_path):
     with open(oracle._SRC) as f:
         src = f.read()
     assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
-    mutant_c = tmp_path / "dsa_oracle.c"
-    mutant_c.write_text(src.replace(old, new))
-    (tmp_path / "dsa_oracle.h").write_text(open(oracle._HDR).read())
-    (tmp_path / "dcp_lse_oracle.c").write_text(open(oracle._LSE_SRC).read())
-    (tmp_path / "dcp_lse_oracle.h").write_text(open(oracle._LSE_HDR).read())
-    so = tmp_path / "libmutant.so"
-    oracle.compile_sources([str(mutant_c), str(tmp_path / "dcp_lse_oracle.c")], str(so))
+    so = oracle.build_variant(str(tmp_path), {"dsa_oracle.c": src.replace(old, new)})
     saved = oracle._lib
-    oracle._lib = oracle.bind(str(so))
+    oracle._lib = oracle.bind(so)
     try:
         failed = _battery()
     finally:
