@@ -91,27 +91,34 @@ def window_elements(wl) -> int:
     return int((e - s).sum())
 
 
+def esize(wl) -> int:
+    """Bytes per logit: 2 for the bf16 workloads, else 4."""
+    return 2 if getattr(wl, "dtype", "f32") == "bf16" else 4
+
+
 def algorithmic_bytes(wl) -> int:
-    """Bytes one call must move: in-window fp32 logits, the int32 bounds it
-    reads, the int32 ids it writes."""
+    """Bytes one call must move: in-window logits (fp32 or bf16), the int32
+    bounds it reads, the int32 ids it writes."""
     bounds = wl.global_row_ke.size if hasattr(wl, "global_row_ke") else (
         wl.row_ke.size + (0 if wl.row_ks is None else wl.row_ks.size))
-    return 4 * window_elements(wl) + 4 * bounds + 4 * wl.rows * wl.topk_blocks
+    return esize(wl) * window_elements(wl) + 4 * bounds + 4 * wl.rows * wl.topk_blocks
 
 
 def workload_config(wl, name: str) -> dict:
     if hasattr(wl, "global_row_ke"):
-        cfg = {"workload": f"dcp-sim D={wl.shards} [{wl.shards},{wl.rows},{wl.local_width}] fp32",
+        cfg = {"workload": f"dcp-sim D={wl.shards} [{wl.shards},{wl.rows},{wl.local_width}] "
+                           f"{'bf16' if esize(wl) == 2 else 'fp32'}",
                "shards": wl.shards, "rows": wl.rows, "local_width": wl.local_width,
                "global_width": wl.shards * wl.local_width,
                "global_block_size": wl.global_block_size,
                "max_global_blocks": wl.max_global_blocks}
     else:
-        cfg = {"workload": f"{name} [{wl.rows},{wl.width}] fp32", "rows": wl.rows,
+        cfg = {"workload": f"{name} [{wl.rows},{wl.width}] {'bf16' if esize(wl) == 2 else 'fp32'}",
+               "rows": wl.rows,
                "width": wl.width, "block_size": wl.block_size,
                "pin_newest": bool(wl.pin_newest), "starts": wl.row_ks is not None}
     cfg.update({"topk_blocks": wl.topk_blocks, "row_repeat": wl.row_repeat, "seed": wl.seed,
-                "window_bytes": 4 * window_elements(wl)})
+                "window_bytes": esize(wl) * window_elements(wl)})
     if wl.notes:
         cfg["notes"] = wl.notes
     return cfg
@@ -247,11 +254,18 @@ class ClockSampler:
 # Our arm
 # ---------------------------------------------------------------------------
 
+def device_logits(wl, torch, device):
+    """The workload's logits on the device, as fp32 or (for the bf16
+    workloads, whose values lie on the bf16 grid) bf16."""
+    t = torch.from_numpy(wl.logits).to(device)
+    return t.to(torch.bfloat16) if esize(wl) == 2 else t
+
+
 def make_runner(wl, dsa, torch, device):
     """Device-resident inputs, an explicit workspace (so that graph capture
     allocates nothing) and a one-call step function."""
     if hasattr(wl, "global_row_ke"):
-        logits = torch.from_numpy(wl.logits).to(device)
+        logits = device_logits(wl, torch, device)
         gke = torch.from_numpy(wl.global_row_ke).to(device)
         out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)
         ws = torch.zeros(dsa.workspace_bytes(wl.rows, max(wl.max_global_blocks, 1)),
@@ -262,7 +276,7 @@ def make_runner(wl, dsa, torch, device):
                                                     wl.max_global_blocks, wl.topk_blocks, out,
                                                     wl.row_repeat, workspace=ws)
         return step, out
-    logits = torch.from_numpy(wl.logits).to(device)
+    logits = device_logits(wl, torch, device)
     ks = None if wl.row_ks is None else torch.from_numpy(wl.row_ks).to(device)
     ke = torch.from_numpy(wl.row_ke).to(device)
     out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)
@@ -314,14 +328,14 @@ def make_mask_runner(wl, dsa, torch, device):
     step_sel()
     torch.cuda.synchronize()
     if hasattr(wl, "global_row_ke"):
-        logits = torch.from_numpy(wl.logits).to(device)
+        logits = device_logits(wl, torch, device)
         gke = torch.from_numpy(wl.global_row_ke).to(device)
 
         def step():
             dsa.dsa_mask_candidate_logits_sharded(logits, gke, wl.global_block_size, ids_dev,
                                                   wl.row_repeat)
     else:
-        logits = torch.from_numpy(wl.logits).to(device)
+        logits = device_logits(wl, torch, device)
         ks = None if wl.row_ks is None else torch.from_numpy(wl.row_ks).to(device)
         ke = torch.from_numpy(wl.row_ke).to(device)
 
@@ -330,7 +344,7 @@ def make_mask_runner(wl, dsa, torch, device):
     ids = ids_dev.cpu().numpy()
     bounds = wl.global_row_ke.size if hasattr(wl, "global_row_ke") else (
         wl.row_ke.size + (0 if wl.row_ks is None else wl.row_ks.size))
-    nbytes = 4 * mask_written_elements(wl, ids) + 4 * bounds + 4 * ids.size
+    nbytes = esize(wl) * mask_written_elements(wl, ids) + 4 * bounds + 4 * ids.size
     return step, nbytes, ids
 
 
@@ -410,9 +424,12 @@ def e2e_measure(wl, dsa, torch, device, steps: int):
     """Same metric through the host-buffer API: pinned host inputs copied in
     and ids copied out inside every timed step."""
     sharded = hasattr(wl, "global_row_ke")
-    h_logits = torch.from_numpy(wl.logits).pin_memory()
+    h_logits = torch.from_numpy(wl.logits)
+    if esize(wl) == 2:
+        h_logits = h_logits.to(torch.bfloat16)  # values on the bf16 grid: exact
+    h_logits = h_logits.pin_memory()
     h_out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32).pin_memory()
-    bufs = {"logits": torch.empty(h_logits.shape, dtype=torch.float32, device=device),
+    bufs = {"logits": torch.empty(h_logits.shape, dtype=h_logits.dtype, device=device),
             "out": torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)}
     if sharded:
         h_b = [torch.from_numpy(wl.global_row_ke).pin_memory()]
@@ -434,7 +451,7 @@ def e2e_measure(wl, dsa, torch, device, steps: int):
             dsa.select_candidate_blocks_host(h_logits, h_b[0], h_b[1], wl.topk_blocks,
                                              wl.block_size, wl.row_repeat, wl.pin_newest,
                                              out=h_out, device_buffers=bufs)
-    h2d = h_logits.numel() * 4 + sum(b.numel() * 4 for b in h_b if b is not None)
+    h2d = h_logits.numel() * esize(wl) + sum(b.numel() * 4 for b in h_b if b is not None)
     d2h = h_out.numel() * 4
     call()
     torch.cuda.synchronize()
@@ -452,9 +469,10 @@ def oracle_cpu_baseline(wl, budget_s: float = 10.0):
     import oracle
 
     oracle.build()
+    run = oracle.run_workload_bf16 if esize(wl) == 2 else oracle.run_workload
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.run_workload(wl, want_scores=False)
+        run(wl, want_scores=False)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= 50:
@@ -470,11 +488,13 @@ def oracle_mask_baseline(wl, ids, budget_s: float = 10.0):
     oracle.build()
     reps, t0 = 0, time.perf_counter()
     while True:
+        bf16 = esize(wl) == 2
         if hasattr(wl, "global_row_ke"):
-            oracle.mask_sharded(wl.logits, wl.global_row_ke, wl.global_block_size, ids,
-                                wl.row_repeat)
+            (oracle.mask_sharded_bf16 if bf16 else oracle.mask_sharded)(
+                wl.logits, wl.global_row_ke, wl.global_block_size, ids, wl.row_repeat)
         else:
-            oracle.mask(wl.logits, wl.row_ks, wl.row_ke, ids, wl.block_size, wl.row_repeat,
+            (oracle.mask_bf16 if bf16 else oracle.mask)(
+                wl.logits, wl.row_ks, wl.row_ke, ids, wl.block_size, wl.row_repeat,
                         width=wl.width)
         reps += 1
         el = time.perf_counter() - t0
@@ -514,7 +534,7 @@ def run_ours(args):
         wl = workloads.make(args.workload)
         step, out = make_runner(wl, dsa, torch, device)
         nbytes = algorithmic_bytes(wl)
-        window_bytes = 4 * window_elements(wl)
+        window_bytes = esize(wl) * window_elements(wl)
         flush = window_bytes < 2 * L2_BYTES
     scratch = torch.empty(256 * 1000 * 1000 // 4, dtype=torch.float32, device=device) if flush \
         else None
@@ -603,11 +623,11 @@ def run_ours(args):
             dtype = "f32" if wl.dtype == "f32" else "f32 arithmetic, bf16 data"
         else:
             config = workload_config(wl, args.workload)
-            full_gbs = round(whole_job_rate(wl.logits.nbytes * args.steps, world,
+            full_gbs = round(whole_job_rate(wl.logits.size * esize(wl) * args.steps, world,
                                             max_ms / 1e3) / 1e9, 3)
             kernel = ("select_kernel (one launch per step)" if args.op == "select"
                       else "mask_kernel (one launch per step)")
-            dtype = "f32"
+            dtype = "f32" if esize(wl) == 4 else "bf16 data, exact compares"
         line = {
             "metric": metric, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -657,23 +677,27 @@ def run_reference(args):
         return run_reference_lse(args, oracle, workloads, world)
     wl = workloads.make(args.workload)
 
+    bf16 = esize(wl) == 2
+    run_select = oracle.run_workload_bf16 if bf16 else oracle.run_workload
+
     def oracle_mask_step(w, ids):
         if hasattr(w, "global_row_ke"):
-            oracle.mask_sharded(w.logits, w.global_row_ke, w.global_block_size, ids,
-                                w.row_repeat)
+            (oracle.mask_sharded_bf16 if bf16 else oracle.mask_sharded)(
+                w.logits, w.global_row_ke, w.global_block_size, ids, w.row_repeat)
         else:
-            oracle.mask(w.logits, w.row_ks, w.row_ke, ids, w.block_size, w.row_repeat,
+            (oracle.mask_bf16 if bf16 else oracle.mask)(
+                w.logits, w.row_ks, w.row_ke, ids, w.block_size, w.row_repeat,
                         width=w.logits.shape[1])
 
     def prepare(w):
         """(step, algorithmic bytes) of one oracle pass over workload w."""
         if args.op == "select":
-            return (lambda: oracle.run_workload(w, want_scores=False)), algorithmic_bytes(w)
-        ids, _ = oracle.run_workload(w, want_scores=False)
+            return (lambda: run_select(w, want_scores=False)), algorithmic_bytes(w)
+        ids, _ = run_select(w, want_scores=False)
         nb = (w.global_row_ke.size if hasattr(w, "global_row_ke")
               else w.row_ke.size + (0 if w.row_ks is None else w.row_ks.size))
         return ((lambda: oracle_mask_step(w, ids)),
-                4 * mask_written_elements(w, ids) + 4 * nb + 4 * ids.size)
+                esize(w) * mask_written_elements(w, ids) + 4 * nb + 4 * ids.size)
 
     # Calibrate on a slice of rows, then size each step's sample so that the
     # whole run stays within about args.ref_budget seconds.
@@ -700,7 +724,7 @@ def run_reference(args):
         "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(sec * 1e3, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32",
+        "vs_baseline": None, "dtype": "f32" if esize(wl) == 4 else "bf16 data, exact compares",
         "data": "synthetic (seeded numpy PCG64; shapes and distributions of the workload)",
         "config": {**workload_config(wl, args.workload), "parallelism": "host, 1 thread"},
         "rows_per_s": round(sample_rows / sec, 1),
@@ -798,8 +822,8 @@ def main(argv=None):
                         "pass that follows it; correct / merge: the DCP partial-attention "
                         "LSE correction of one shard / merge of all shards")
     p.add_argument("--workload", default=None,
-                   choices=("dcp", "decode", "prefill", "long", "long_pin", "tiny")
-                   + tuple(LSE_NAMES),
+                   choices=("dcp", "decode", "prefill", "long", "long_pin", "tiny",
+                            "dcp_bf16", "decode_bf16") + tuple(LSE_NAMES),
                    help="default: dcp for select / mask, lse_decode for correct / merge")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")

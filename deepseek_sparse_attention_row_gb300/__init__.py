@@ -21,7 +21,8 @@ Functions carry the C ABI's names:
   C ABI in ``include/dsa_dcp_attn.h``) and the sum over shards after it.
 
 Tensors are PyTorch CUDA tensors (PyTorch supplies device memory and the
-current stream). ``select_candidate_blocks_host`` accepts host tensors and
+current stream). Logits may be float32 or bfloat16 (the ``*_bf16`` C entry
+points); scores follow the logits' dtype. ``select_candidate_blocks_host`` accepts host tensors and
 moves them through the device around one call.
 """
 
@@ -65,6 +66,11 @@ EXPORTED_SYMBOLS = (
     "dsa_attn_max_shards",
     "dsa_correct_attn_out",
     "dsa_merge_attn_out",
+    "dsa_block_scores_bf16",
+    "dsa_select_candidate_blocks_bf16",
+    "dsa_select_candidate_blocks_sharded_bf16",
+    "dsa_mask_candidate_logits_bf16",
+    "dsa_mask_candidate_logits_sharded_bf16",
 )
 
 _lib = None
@@ -111,10 +117,16 @@ def library():
                                          i64, i32, p, i64, i64, i64, p, i64, i64, p]
     lib.dsa_merge_attn_out.argtypes = [p, i32, i32, i64, i64, i64, i64, i64, i64, i64, p, i64,
                                        i64, i64, p, i64, i64, i64, p, i64, i64, p]
+    for name in ("dsa_block_scores", "dsa_select_candidate_blocks",
+                 "dsa_select_candidate_blocks_sharded", "dsa_mask_candidate_logits",
+                 "dsa_mask_candidate_logits_sharded"):
+        getattr(lib, name + "_bf16").argtypes = getattr(lib, name).argtypes
     for f in (lib.dsa_block_scores, lib.dsa_select_candidate_blocks,
               lib.dsa_select_candidate_blocks_sharded, lib.dsa_mask_candidate_logits,
               lib.dsa_mask_candidate_logits_sharded, lib.dsa_correct_attn_out,
-              lib.dsa_merge_attn_out):
+              lib.dsa_merge_attn_out, lib.dsa_block_scores_bf16,
+              lib.dsa_select_candidate_blocks_bf16, lib.dsa_select_candidate_blocks_sharded_bf16,
+              lib.dsa_mask_candidate_logits_bf16, lib.dsa_mask_candidate_logits_sharded_bf16):
         f.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -186,6 +198,16 @@ def _dev_ptr(t, dtype, name, *, allow_none=False):
     return t.data_ptr() or None
 
 
+def _logits_kind(t, name="logits"):
+    """(dtype, C-ABI name suffix) of a logits tensor: fp32 or bf16."""
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return torch.float32, ""
+    if t.dtype == torch.bfloat16:
+        return torch.bfloat16, "_bf16"
+    raise TypeError(f"{name} must be float32 or bfloat16, got {t.dtype}")
+
+
 def _row_major(t, name):
     if t.stride(-1) != 1:
         raise ValueError(f"{name} must have unit stride in its last dimension")
@@ -194,20 +216,22 @@ def _row_major(t, name):
 
 def dsa_block_scores(logits, row_ks, row_ke, block_size: int, row_repeat: int = 1,
                      pin_newest: bool = True, scores_out=None, stream=None):
-    """Block scores ``[rows, ceil(width / block_size)]`` fp32 (returned)."""
+    """Block scores ``[rows, ceil(width / block_size)]`` in the logits' dtype
+    (fp32 or bf16; returned)."""
     torch = _torch()
+    dt, sfx = _logits_kind(logits)
     rows, width = logits.shape
     nb = -(-width // block_size) if block_size > 0 else 0
     if scores_out is None:
-        scores_out = torch.empty((rows, nb), dtype=torch.float32, device=logits.device)
-    st = library().dsa_block_scores(
-        _dev_ptr(logits, torch.float32, "logits"), rows, width, _row_major(logits, "logits"),
+        scores_out = torch.empty((rows, nb), dtype=dt, device=logits.device)
+    st = getattr(library(), "dsa_block_scores" + sfx)(
+        _dev_ptr(logits, dt, "logits"), rows, width, _row_major(logits, "logits"),
         _dev_ptr(row_ks, torch.int32, "row_ks", allow_none=True),
         _dev_ptr(row_ke, torch.int32, "row_ke"), block_size, row_repeat, int(bool(pin_newest)),
-        _dev_ptr(scores_out, torch.float32, "scores_out"),
+        _dev_ptr(scores_out, dt, "scores_out"),
         _row_major(scores_out, "scores_out") if scores_out.numel() else nb,
         _stream_handle(stream))
-    _check("dsa_block_scores", st)
+    _check("dsa_block_scores" + sfx, st)
     return scores_out
 
 
@@ -215,23 +239,24 @@ def dsa_select_candidate_blocks(logits, row_ks, row_ke, topk_blocks: int, block_
                                 out, row_repeat: int = 1, pin_newest: bool = True,
                                 scores_out=None, stream=None, workspace=None):
     """Write ranked candidate block ids (-1 padded) into ``out`` [rows, >=topk]
-    int32; optionally the ranked block scores into ``scores_out``.
-    ``workspace``: see ``_workspace``."""
+    int32; optionally the block scores into ``scores_out`` (the logits'
+    dtype). Logits are fp32 or bf16. ``workspace``: see ``_workspace``."""
     torch = _torch()
+    dt, sfx = _logits_kind(logits)
     rows, width = logits.shape
     nb = -(-width // block_size) if block_size > 0 else 0
     handle = _stream_handle(stream)
     ws_ptr, ws_bytes = _workspace(workspace, rows, nb, logits.device, handle)
-    st = library().dsa_select_candidate_blocks(
-        _dev_ptr(logits, torch.float32, "logits"), rows, width, _row_major(logits, "logits"),
+    st = getattr(library(), "dsa_select_candidate_blocks" + sfx)(
+        _dev_ptr(logits, dt, "logits"), rows, width, _row_major(logits, "logits"),
         _dev_ptr(row_ks, torch.int32, "row_ks", allow_none=True),
         _dev_ptr(row_ke, torch.int32, "row_ke"), topk_blocks, block_size, row_repeat,
         int(bool(pin_newest)), _dev_ptr(out, torch.int32, "out"),
         _row_major(out, "out") if out.dim() == 2 else topk_blocks,
-        _dev_ptr(scores_out, torch.float32, "scores_out", allow_none=True),
+        _dev_ptr(scores_out, dt, "scores_out", allow_none=True),
         _row_major(scores_out, "scores_out") if scores_out is not None else 0,
         ws_ptr, ws_bytes, handle)
-    _check("dsa_select_candidate_blocks", st)
+    _check("dsa_select_candidate_blocks" + sfx, st)
     return out
 
 
@@ -243,21 +268,22 @@ def dsa_select_candidate_blocks_sharded(logits, global_row_ke, global_block_size
     dimension); writes ranked global block ids into ``out``.
     ``workspace``: see ``_workspace``."""
     torch = _torch()
+    dt, sfx = _logits_kind(logits)
     shards, rows, lw = logits.shape
     handle = _stream_handle(stream)
     ws_ptr, ws_bytes = _workspace(workspace, rows, max(int(max_global_blocks), 1),
                                   logits.device, handle)
     if logits.stride(2) != 1:
         raise ValueError("logits must have unit stride in its last dimension")
-    st = library().dsa_select_candidate_blocks_sharded(
-        _dev_ptr(logits, torch.float32, "logits"), shards, rows, lw, logits.stride(1),
+    st = getattr(library(), "dsa_select_candidate_blocks_sharded" + sfx)(
+        _dev_ptr(logits, dt, "logits"), shards, rows, lw, logits.stride(1),
         logits.stride(0), _dev_ptr(global_row_ke, torch.int32, "global_row_ke"),
         global_block_size, max_global_blocks, row_repeat, topk_blocks,
         _dev_ptr(out, torch.int32, "out"), _row_major(out, "out") if out.dim() == 2 else topk_blocks,
-        _dev_ptr(scores_out, torch.float32, "scores_out", allow_none=True),
+        _dev_ptr(scores_out, dt, "scores_out", allow_none=True),
         _row_major(scores_out, "scores_out") if scores_out is not None else 0,
         ws_ptr, ws_bytes, handle)
-    _check("dsa_select_candidate_blocks_sharded", st)
+    _check("dsa_select_candidate_blocks_sharded" + sfx, st)
     return out
 
 
@@ -266,16 +292,17 @@ def dsa_mask_candidate_logits(logits, row_ks, row_ke, candidates, block_size: in
     """In place: -inf for every logit outside its row's window or outside the
     row's candidate blocks (``candidates`` [rows, topk] int32, -1 = empty)."""
     torch = _torch()
+    dt, sfx = _logits_kind(logits)
     rows, width = logits.shape
     topk = candidates.shape[1] if candidates is not None else 0
-    st = library().dsa_mask_candidate_logits(
-        _dev_ptr(logits, torch.float32, "logits"), rows, width, _row_major(logits, "logits"),
+    st = getattr(library(), "dsa_mask_candidate_logits" + sfx)(
+        _dev_ptr(logits, dt, "logits"), rows, width, _row_major(logits, "logits"),
         _dev_ptr(row_ks, torch.int32, "row_ks", allow_none=True),
         _dev_ptr(row_ke, torch.int32, "row_ke"),
         _dev_ptr(candidates, torch.int32, "candidates", allow_none=True), topk,
         _row_major(candidates, "candidates") if candidates is not None else 0, block_size,
         row_repeat, _stream_handle(stream))
-    _check("dsa_mask_candidate_logits", st)
+    _check("dsa_mask_candidate_logits" + sfx, st)
     return logits
 
 
@@ -283,18 +310,19 @@ def dsa_mask_candidate_logits_sharded(logits, global_row_ke, global_block_size: 
                                       row_repeat: int = 1, stream=None):
     """DCP form of ``dsa_mask_candidate_logits`` on ``[D, rows, local_width]``."""
     torch = _torch()
+    dt, sfx = _logits_kind(logits)
     shards, rows, lw = logits.shape
     if logits.stride(2) != 1:
         raise ValueError("logits must have unit stride in its last dimension")
     topk = candidates.shape[1] if candidates is not None else 0
-    st = library().dsa_mask_candidate_logits_sharded(
-        _dev_ptr(logits, torch.float32, "logits"), shards, rows, lw, logits.stride(1),
+    st = getattr(library(), "dsa_mask_candidate_logits_sharded" + sfx)(
+        _dev_ptr(logits, dt, "logits"), shards, rows, lw, logits.stride(1),
         logits.stride(0), _dev_ptr(global_row_ke, torch.int32, "global_row_ke"),
         global_block_size, row_repeat,
         _dev_ptr(candidates, torch.int32, "candidates", allow_none=True), topk,
         _row_major(candidates, "candidates") if candidates is not None else 0,
         _stream_handle(stream))
-    _check("dsa_mask_candidate_logits_sharded", st)
+    _check("dsa_mask_candidate_logits_sharded" + sfx, st)
     return logits
 
 

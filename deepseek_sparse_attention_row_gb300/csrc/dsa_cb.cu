@@ -42,7 +42,7 @@ constexpr int kMaxSplit = 8;        // CTAs per row at most
 constexpr int kThreads = 256;       // scores-only kernel
 
 struct SelectArgs {
-  const float* logits;
+  const void* logits;    // E::T elements
   int64_t ld;            // row stride (elements)
   int64_t shard_stride;  // sharded: elements between shards
   int32_t shards;        // 1 for the unsharded form
@@ -59,7 +59,7 @@ struct SelectArgs {
   int32_t kpad;
   int32_t* out;
   int64_t ld_out;
-  float* scores;
+  void* scores;          // E::T elements, nullable
   int64_t ld_scores;
   int32_t split;        // CTAs per row
   uint32_t* ws_keys;    // split > 1: [rows, nb] block keys
@@ -67,13 +67,14 @@ struct SelectArgs {
   int64_t rows;         // select_warp_kernel: rows to handle
 };
 
+template <typename E>
 struct RowPlan {
-  const float* origin;
+  const typename E::T* origin;
   int32_t len_max;
   int32_t nblk;       // blocks holding in-window data
   int32_t pin_block;  // -1: none
   int vec, lpb_log2;
-  int shift;          // vec == kVecShift: floats past the 16-byte boundary
+  int shift;          // vec == kVecShift: elements past the 16-byte boundary
 };
 
 // Counts one arrival on a row's counter and returns true for the last of
@@ -95,17 +96,20 @@ __device__ __forceinline__ bool arrive_last(uint32_t* counter, uint32_t split) {
 
 // Window of an unsharded row: e = min(ke, width), s = min(max(ks, 0), e).
 // Every thread computes the same plan from the row's bounds.
-__device__ __forceinline__ RowPlan plan_unsharded(const float* logits, int64_t ld, int32_t width,
-                                                  const int32_t* row_ks, const int32_t* row_ke,
-                                                  int32_t row_repeat, int32_t block_size,
-                                                  int32_t pin_newest, int64_t row) {
+template <typename E>
+__device__ __forceinline__ RowPlan<E> plan_unsharded(const typename E::T* logits, int64_t ld,
+                                                     int32_t width, const int32_t* row_ks,
+                                                     const int32_t* row_ke, int32_t row_repeat,
+                                                     int32_t block_size, int32_t pin_newest,
+                                                     int64_t row) {
+  constexpr int V16 = 16 / E::kBytes;  // elements per 16-byte vector
   const int64_t g = row / row_repeat;
   const int32_t ks = row_ks ? __ldg(row_ks + g) : 0;
   const int32_t ke = __ldg(row_ke + g);
   const int32_t e = min(ke, width);
   const int32_t s = min(max(ks, 0), e);
   const uint32_t n = e > s ? static_cast<uint32_t>(e - s) : 0u;
-  RowPlan p;
+  RowPlan<E> p;
   p.origin = logits + row * ld + s;
   p.len_max = static_cast<int32_t>(n);
   p.nblk = static_cast<int32_t>((n + static_cast<uint32_t>(block_size) - 1u) /
@@ -114,13 +118,13 @@ __device__ __forceinline__ RowPlan plan_unsharded(const float* logits, int64_t l
   // A window off the 16-byte grid still reads 16-byte vectors when the block
   // splits into a power of two of them and the aligned base stays inside the
   // row (s >= shift).
-  p.shift = static_cast<int>((reinterpret_cast<uintptr_t>(p.origin) >> 2) & 3);
-  const int32_t lpb4 = block_size / 4;
-  if (p.shift != 0 && s >= p.shift && block_size % 4 == 0 && (lpb4 & (lpb4 - 1)) == 0) {
+  p.shift = static_cast<int>((reinterpret_cast<uintptr_t>(p.origin) / E::kBytes) & (V16 - 1));
+  const int32_t lpbv = block_size / V16;
+  if (p.shift != 0 && s >= p.shift && block_size % V16 == 0 && (lpbv & (lpbv - 1)) == 0) {
     p.vec = kVecShift;
-    p.lpb_log2 = __ffs(lpb4) - 1;
+    p.lpb_log2 = __ffs(lpbv) - 1;
   } else {
-    p.vec = choose_vec(p.origin, block_size, &p.lpb_log2);
+    p.vec = choose_vec<E>(p.origin, block_size, &p.lpb_log2);
   }
   return p;
 }
@@ -135,26 +139,30 @@ __device__ __forceinline__ int32_t shard_len(int32_t gke, int32_t d, int32_t sha
   return static_cast<int32_t>(min(lke, static_cast<uint32_t>(lw)));
 }
 
-template <int SVEC>
-__device__ __forceinline__ void stream_sharded(const Window& w, int lpb_log2, int32_t block_size,
-                                               int32_t b0, int32_t b1, uint32_t* keys) {
+// SVEC elements per vector (0: generic path); 8 shards per batch and NV
+// vectors per shard, so that each lane has 8 x 16 bytes in flight (8 x 8
+// bytes for single bf16 elements, whose loads fill one register each).
+template <typename E, int SVEC>
+__device__ __forceinline__ void stream_sharded(const Window<E>& w, int lpb_log2,
+                                               int32_t block_size, int32_t b0, int32_t b1,
+                                               uint32_t* keys) {
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  if constexpr (SVEC == 4)
-    stream_pow2<4, 1, 8>(w, lpb_log2, b0, b1, keys, 0, warp, nwarps);
-  else if constexpr (SVEC == 2)
-    stream_pow2<2, 2, 8>(w, lpb_log2, b0, b1, keys, 0, warp, nwarps);
-  else if constexpr (SVEC == 1)
-    stream_pow2<1, 4, 8>(w, lpb_log2, b0, b1, keys, 0, warp, nwarps);
-  else
-    stream_generic<4, 8>(w, block_size, b0, b1, keys, 0, warp, nwarps);
+  if constexpr (SVEC > 0) {
+    constexpr int NV = 16 / (SVEC * E::kBytes) < 4 ? 16 / (SVEC * E::kBytes) : 4;
+    stream_pow2<E, SVEC, NV, 8>(w, lpb_log2, b0, b1, keys, 0, warp, nwarps);
+  } else {
+    stream_generic<E, 4, 8>(w, block_size, b0, b1, keys, 0, warp, nwarps);
+  }
 }
 
 // `a.split` CTAs per row.
 // SHARDED = false: unsharded rows, vector width chosen per row.
 // SHARDED = true: DCP rows; SVEC is the vector width fixed by the host
 // (0 = generic path). T: threads per CTA.
-template <bool SHARDED, int SVEC, int T>
+template <typename E, bool SHARDED, int SVEC, int T>
 __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a) {
+  using TE = typename E::T;
+  const TE* logits = static_cast<const TE*>(a.logits);
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);  // [max(kpad, kRankMax)]
   uint32_t* keys = reinterpret_cast<uint32_t*>(cand + max(a.kpad, kRankMax));  // [nb]
@@ -166,11 +174,11 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   const int64_t row = blockIdx.x / split;
   const int32_t part = static_cast<int32_t>(blockIdx.x % split);
 
-  RowPlan plan;
+  RowPlan<E> plan;
   if constexpr (SHARDED) {
     const int32_t gke = __ldg(a.row_ke + row / a.row_repeat);
     const int32_t n0 = shard_len(gke, 0, a.shards, a.width);
-    plan.origin = a.logits + row * a.ld;
+    plan.origin = logits + row * a.ld;
     plan.len_max = n0;
     plan.nblk = min(static_cast<int32_t>((static_cast<uint32_t>(n0) + a.block_size - 1u) /
                                          static_cast<uint32_t>(a.block_size)),
@@ -184,8 +192,8 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
     for (int d = threadIdx.x; d < a.shards; d += blockDim.x)
       len[d] = shard_len(gke, d, a.shards, a.width);
   } else {
-    plan = plan_unsharded(a.logits, a.ld, a.width, a.row_ks, a.row_ke, a.row_repeat,
-                          a.block_size, a.pin_newest, row);
+    plan = plan_unsharded<E>(logits, a.ld, a.width, a.row_ks, a.row_ke, a.row_repeat,
+                             a.block_size, a.pin_newest, row);
     if (threadIdx.x == 0) len[0] = plan.len_max;
   }
 
@@ -197,7 +205,7 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   for (int32_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) keys[b] = kKeyNegInf;
   __syncthreads();
 
-  Window w;
+  Window<E> w;
   w.origin = plan.origin;
   w.shard_stride = a.shard_stride;
   w.shards = a.shards;
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   w.len_max = plan.len_max;
   if (b0 < b1) {
     if constexpr (SHARDED)
-      stream_sharded<SVEC>(w, plan.lpb_log2, a.block_size, b0, b1, keys);
+      stream_sharded<E, SVEC>(w, plan.lpb_log2, a.block_size, b0, b1, keys);
     else
       stream_row(w, plan.vec, plan.shift, plan.lpb_log2, a.block_size, b0, b1, keys, 0,
                  threadIdx.x >> 5, blockDim.x >> 5);
@@ -214,8 +222,8 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   if constexpr (SHARDED) {
     if constexpr (SVEC > 1)
       for (int d = threadIdx.x; d < a.shards; d += blockDim.x)
-        commit_partial(load_partial<SVEC>(plan.origin + d * a.shard_stride, len[d], a.block_size,
-                                          b0, b1),
+        commit_partial(load_partial<E, SVEC>(plan.origin + d * a.shard_stride, len[d],
+                                             a.block_size, b0, b1),
                        keys, 0);
   } else {
     if (threadIdx.x == 0) finish_row(w, plan.vec, plan.shift, a.block_size, b0, b1, keys, 0);
@@ -243,7 +251,7 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   topk_store(keys, a.nb, max(nblk, plan.pin_block + 1), min(a.topk, a.nb), plan.pin_block,
              cand, a.kpad,
              a.topk > 0 ? a.out + row * a.ld_out : nullptr, a.topk,
-             a.scores ? a.scores + row * a.ld_scores : nullptr, tsh);
+             a.scores ? static_cast<TE*>(a.scores) + row * a.ld_scores : nullptr, tsh);
 }
 
 // Shared memory per warp in select_warp_kernel: candidates, keys, length.
@@ -255,8 +263,9 @@ __host__ __device__ __forceinline__ size_t warp_slice_bytes(int32_t nb) {
 // streams its row alone (stream_row with one warp) into its own key array
 // and ranks it with topk_warp; no CTA barrier anywhere, so W rows of a CTA
 // proceed independently and up to 32 rows are in flight per SM.
-template <int W>
+template <typename E, int W>
 __global__ void __launch_bounds__(W * 32, 1024 / (W * 32)) select_warp_kernel(const SelectArgs a) {
+  using TE = typename E::T;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * W + warp;
@@ -266,13 +275,14 @@ __global__ void __launch_bounds__(W * 32, 1024 / (W * 32)) select_warp_kernel(co
   uint32_t* keys = reinterpret_cast<uint32_t*>(cand + kWarpCand);
   int32_t* len = reinterpret_cast<int32_t*>(keys + ((a.nb + 3) & ~3));
 
-  const RowPlan plan = plan_unsharded(a.logits, a.ld, a.width, a.row_ks, a.row_ke, a.row_repeat,
-                                      a.block_size, a.pin_newest, row);
+  const RowPlan<E> plan =
+      plan_unsharded<E>(static_cast<const TE*>(a.logits), a.ld, a.width, a.row_ks, a.row_ke,
+                        a.row_repeat, a.block_size, a.pin_newest, row);
   if (lane == 0) len[0] = plan.len_max;
   const int32_t nblk = plan.nblk;
   for (int32_t b = lane; b < nblk; b += 32) keys[b] = kKeyNegInf;
   __syncwarp();
-  Window w;
+  Window<E> w;
   w.origin = plan.origin;
   w.shard_stride = 0;
   w.shards = 1;
@@ -285,11 +295,11 @@ __global__ void __launch_bounds__(W * 32, 1024 / (W * 32)) select_warp_kernel(co
   __syncwarp();
   topk_warp(keys, a.nb, nblk, min(a.topk, a.nb), plan.pin_block, cand,
             a.topk > 0 ? a.out + row * a.ld_out : nullptr, a.topk,
-            a.scores ? a.scores + row * a.ld_scores : nullptr);
+            a.scores ? static_cast<TE*>(a.scores) + row * a.ld_scores : nullptr);
 }
 
 struct ScoresArgs {
-  const float* logits;
+  const void* logits;  // E::T elements
   int64_t ld;
   int32_t width;
   const int32_t* row_ks;
@@ -300,11 +310,13 @@ struct ScoresArgs {
   int32_t pin_newest;
   int32_t chunk;   // blocks per CTA
   int32_t chunks;  // CTAs per row
-  float* scores;
+  void* scores;        // E::T elements
   int64_t ld_scores;
 };
 
+template <typename E>
 __global__ void __launch_bounds__(kThreads, 4) block_scores_kernel(const ScoresArgs a) {
+  using TE = typename E::T;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw);  // [chunk]
   __shared__ int32_t len[1];
@@ -312,13 +324,14 @@ __global__ void __launch_bounds__(kThreads, 4) block_scores_kernel(const ScoresA
   const int32_t c0 = static_cast<int32_t>(blockIdx.x % a.chunks) * a.chunk;
   const int32_t c1 = min(c0 + a.chunk, a.nb);
 
-  const RowPlan plan = plan_unsharded(a.logits, a.ld, a.width, a.row_ks, a.row_ke, a.row_repeat,
-                                      a.block_size, a.pin_newest, row);
+  const RowPlan<E> plan =
+      plan_unsharded<E>(static_cast<const TE*>(a.logits), a.ld, a.width, a.row_ks, a.row_ke,
+                        a.row_repeat, a.block_size, a.pin_newest, row);
   if (threadIdx.x == 0) len[0] = plan.len_max;
   for (int32_t b = threadIdx.x; b < c1 - c0; b += blockDim.x) keys[b] = kKeyNegInf;
   __syncthreads();
   const int32_t b0 = min(c0, plan.nblk), b1 = min(c1, plan.nblk);
-  Window w;
+  Window<E> w;
   w.origin = plan.origin;
   w.shard_stride = 0;
   w.shards = 1;
@@ -333,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 4) block_scores_kernel(const ScoresA
   if (threadIdx.x == 0 && plan.pin_block >= c0 && plan.pin_block < c1)
     keys[plan.pin_block - c0] = kKeyPosInf;
   __syncthreads();
-  float* srow = a.scores + row * a.ld_scores;
-  for (int32_t b = c0 + threadIdx.x; b < c1; b += blockDim.x) srow[b] = key_score(keys[b - c0]);
+  TE* srow = static_cast<TE*>(a.scores) + row * a.ld_scores;
+  for (int32_t b = c0 + threadIdx.x; b < c1; b += blockDim.x) put_score(srow + b, keys[b - c0]);
 }
 
 __global__ void fill_minus_one_kernel(int32_t* out, int64_t rows, int32_t cols, int64_t ld) {
@@ -470,12 +483,12 @@ dsa_status launch_select(K kernel, const SelectArgs& a, int64_t rows, int thread
 }
 
 // Instantiates the kernel for the chosen thread count.
-template <bool SHARDED, int SVEC>
+template <typename E, bool SHARDED, int SVEC>
 dsa_status launch_shape(const SelectArgs& a, int64_t rows, const Shape& sh, size_t smem,
                         cudaStream_t stream) {
   if (sh.threads == 128)
-    return launch_select(select_kernel<SHARDED, SVEC, 128>, a, rows, 128, smem, stream);
-  return launch_select(select_kernel<SHARDED, SVEC, 256>, a, rows, 256, smem, stream);
+    return launch_select(select_kernel<E, SHARDED, SVEC, 128>, a, rows, 128, smem, stream);
+  return launch_select(select_kernel<E, SHARDED, SVEC, 256>, a, rows, 256, smem, stream);
 }
 
 // Fills the workspace fields of `a` for the chosen shape.
@@ -525,10 +538,16 @@ size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks) {
   return workspace_bytes(rows, nblocks);
 }
 
-dsa_status dsa_block_scores(const float* logits, int64_t rows, int64_t width, int64_t ld_logits,
-                            const int32_t* row_ks, const int32_t* row_ke, int32_t block_size,
-                            int32_t row_repeat, int32_t pin_newest, float* scores_out,
-                            int64_t ld_scores, void* stream) {
+}  // extern "C"
+
+namespace dsa {
+namespace {
+
+template <typename E>
+dsa_status block_scores_impl(const typename E::T* logits, int64_t rows, int64_t width,
+                             int64_t ld_logits, const int32_t* row_ks, const int32_t* row_ke,
+                             int32_t block_size, int32_t row_repeat, int32_t pin_newest,
+                             typename E::T* scores_out, int64_t ld_scores, void* stream) {
   if (rows < 0 || width < 0 || block_size < 1 || row_repeat < 1) return DSA_EINVAL;
   if (rows == 0 || width == 0) return DSA_OK;
   if (!logits || !row_ke || !scores_out || ld_logits < width) return DSA_EINVAL;
@@ -547,7 +566,7 @@ dsa_status dsa_block_scores(const float* logits, int64_t rows, int64_t width, in
   a.nb = static_cast<int32_t>(nb);
   a.pin_newest = pin_newest != 0;
   // About 64 KiB of logits per CTA, at least 32 blocks, at most 4096.
-  int64_t chunk = (64 * 1024 / 4) / block_size;
+  int64_t chunk = (64 * 1024 / E::kBytes) / block_size;
   chunk = std::max<int64_t>(32, std::min<int64_t>(4096, chunk));
   chunk = std::min<int64_t>(chunk, nb);
   a.chunk = static_cast<int32_t>(chunk);
@@ -555,21 +574,21 @@ dsa_status dsa_block_scores(const float* logits, int64_t rows, int64_t width, in
   a.scores = scores_out;
   a.ld_scores = ld_scores;
   const size_t smem = static_cast<size_t>(chunk) * 4;
-  if (set_smem_attr(block_scores_kernel, smem) != cudaSuccess) return DSA_ECUDA;
+  if (set_smem_attr(block_scores_kernel<E>, smem) != cudaSuccess) return DSA_ECUDA;
   const int64_t grid = rows * a.chunks;
   if (grid > INT32_MAX) return DSA_EUNSUPPORTED;
-  block_scores_kernel<<<static_cast<unsigned>(grid), kThreads, smem,
-                        static_cast<cudaStream_t>(stream)>>>(a);
+  block_scores_kernel<E><<<static_cast<unsigned>(grid), kThreads, smem,
+                           static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
 }
 
-dsa_status dsa_select_candidate_blocks(const float* logits, int64_t rows, int64_t width,
-                                       int64_t ld_logits, const int32_t* row_ks,
-                                       const int32_t* row_ke, int32_t topk_blocks,
-                                       int32_t block_size, int32_t row_repeat,
-                                       int32_t pin_newest, int32_t* out, int64_t ld_out,
-                                       float* scores_out, int64_t ld_scores, void* workspace,
-                                       size_t workspace_size, void* stream) {
+template <typename E>
+dsa_status select_impl(const typename E::T* logits, int64_t rows, int64_t width,
+                       int64_t ld_logits, const int32_t* row_ks, const int32_t* row_ke,
+                       int32_t topk_blocks, int32_t block_size, int32_t row_repeat,
+                       int32_t pin_newest, int32_t* out, int64_t ld_out,
+                       typename E::T* scores_out, int64_t ld_scores, void* workspace,
+                       size_t workspace_size, void* stream) {
   if (rows < 0 || width < 0 || topk_blocks < 0 || block_size < 1 || row_repeat < 1)
     return DSA_EINVAL;
   if (rows == 0) return DSA_OK;
@@ -602,35 +621,34 @@ dsa_status dsa_select_candidate_blocks(const float* logits, int64_t rows, int64_
   a.ld_out = ld_out;
   a.scores = scores_out;
   a.ld_scores = ld_scores;
+  const int64_t row_bytes = width * E::kBytes;
   // Many short rows: one row per warp (32 rows in flight per SM instead of
   // 8). With few rows a CTA per row keeps more of the GPU busy.
   read_overrides();
-  if (!g_warp_off && width * 4 <= 64 * 1024 && topk_blocks <= 32 && a.nb <= 2048 &&
+  if (!g_warp_off && row_bytes <= 64 * 1024 && topk_blocks <= 32 && a.nb <= 2048 &&
       rows >= 8 * static_cast<int64_t>(sm_count())) {
     constexpr int W = 4;
     a.split = 1;
     a.rows = rows;
     const size_t smem = W * warp_slice_bytes(a.nb);
-    if (set_smem_attr(select_warp_kernel<W>, smem) != cudaSuccess) return DSA_ECUDA;
-    select_warp_kernel<W><<<static_cast<unsigned>((rows + W - 1) / W), W * 32, smem, s>>>(a);
+    if (set_smem_attr(select_warp_kernel<E, W>, smem) != cudaSuccess) return DSA_ECUDA;
+    select_warp_kernel<E, W><<<static_cast<unsigned>((rows + W - 1) / W), W * 32, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
   }
   const bool ws = workspace && workspace_size >= workspace_bytes(rows, a.nb);
-  const Shape sh = choose_shape(width * 4, rows, ws);
+  const Shape sh = choose_shape(row_bytes, rows, ws);
   attach_workspace(a, rows, workspace, sh);
-  return launch_shape<false, 0>(a, rows, sh, select_smem(a.kpad, a.nb, 1), s);
+  return launch_shape<E, false, 0>(a, rows, sh, select_smem(a.kpad, a.nb, 1), s);
 }
 
-dsa_status dsa_select_candidate_blocks_sharded(const float* logits, int32_t shards, int64_t rows,
-                                               int64_t local_width, int64_t ld_logits,
-                                               int64_t shard_stride,
-                                               const int32_t* global_row_ke,
-                                               int32_t global_block_size,
-                                               int32_t max_global_blocks, int32_t row_repeat,
-                                               int32_t topk_blocks, int32_t* out, int64_t ld_out,
-                                               float* scores_out, int64_t ld_scores,
-                                               void* workspace, size_t workspace_size,
-                                               void* stream) {
+template <typename E>
+dsa_status select_sharded_impl(const typename E::T* logits, int32_t shards, int64_t rows,
+                               int64_t local_width, int64_t ld_logits, int64_t shard_stride,
+                               const int32_t* global_row_ke, int32_t global_block_size,
+                               int32_t max_global_blocks, int32_t row_repeat,
+                               int32_t topk_blocks, int32_t* out, int64_t ld_out,
+                               typename E::T* scores_out, int64_t ld_scores, void* workspace,
+                               size_t workspace_size, void* stream) {
   if (shards < 1 || rows < 0 || local_width < 0 || topk_blocks < 0 || global_block_size < 1 ||
       global_block_size % shards != 0 || row_repeat < 1 || ld_logits < local_width ||
       shard_stride < 0)
@@ -667,23 +685,102 @@ dsa_status dsa_select_candidate_blocks_sharded(const float* logits, int32_t shar
   a.scores = scores_out;
   a.ld_scores = ld_scores;
 
-  // One vector width for every shard row: all shard origins must share the
-  // alignment and the local block must split into a power of two of vectors.
+  // One vector width (in elements) for every shard row: all shard origins
+  // must share the alignment and the local block must split into a power of
+  // two of vectors.
   auto pow2 = [](int32_t x) { return x > 0 && (x & (x - 1)) == 0; };
   const uintptr_t base = reinterpret_cast<uintptr_t>(logits);
   auto aligned = [&](int vec) {
-    return lbs % vec == 0 && pow2(lbs / vec) && (base % (4 * vec)) == 0 && ld_logits % vec == 0 &&
-           shard_stride % vec == 0;
+    return lbs % vec == 0 && pow2(lbs / vec) && (base % (E::kBytes * vec)) == 0 &&
+           ld_logits % vec == 0 && shard_stride % vec == 0;
   };
   const size_t smem = select_smem(a.kpad, a.nb, shards);
   const bool ws = workspace && workspace_size >= workspace_bytes(rows, a.nb);
-  const Shape sh = choose_shape(local_width * 4 * shards, rows, ws);
+  const Shape sh = choose_shape(local_width * E::kBytes * shards, rows, ws);
   attach_workspace(a, rows, workspace, sh);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (aligned(4)) return launch_shape<true, 4>(a, rows, sh, smem, s);
-  if (aligned(2)) return launch_shape<true, 2>(a, rows, sh, smem, s);
-  if (pow2(lbs)) return launch_shape<true, 1>(a, rows, sh, smem, s);
-  return launch_shape<true, 0>(a, rows, sh, smem, s);
+  constexpr int V16 = 16 / E::kBytes, V8 = 8 / E::kBytes, V4 = 4 / E::kBytes;
+  if (aligned(V16)) return launch_shape<E, true, V16>(a, rows, sh, smem, s);
+  if (aligned(V8)) return launch_shape<E, true, V8>(a, rows, sh, smem, s);
+  if constexpr (V4 > 1) {
+    if (aligned(V4)) return launch_shape<E, true, V4>(a, rows, sh, smem, s);
+  }
+  if (pow2(lbs)) return launch_shape<E, true, 1>(a, rows, sh, smem, s);
+  return launch_shape<E, true, 0>(a, rows, sh, smem, s);
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" {
+
+dsa_status dsa_block_scores(const float* logits, int64_t rows, int64_t width, int64_t ld_logits,
+                            const int32_t* row_ks, const int32_t* row_ke, int32_t block_size,
+                            int32_t row_repeat, int32_t pin_newest, float* scores_out,
+                            int64_t ld_scores, void* stream) {
+  return block_scores_impl<F32>(logits, rows, width, ld_logits, row_ks, row_ke, block_size,
+                                row_repeat, pin_newest, scores_out, ld_scores, stream);
+}
+
+dsa_status dsa_block_scores_bf16(const uint16_t* logits, int64_t rows, int64_t width,
+                                 int64_t ld_logits, const int32_t* row_ks, const int32_t* row_ke,
+                                 int32_t block_size, int32_t row_repeat, int32_t pin_newest,
+                                 uint16_t* scores_out, int64_t ld_scores, void* stream) {
+  return block_scores_impl<BF16>(logits, rows, width, ld_logits, row_ks, row_ke, block_size,
+                                 row_repeat, pin_newest, scores_out, ld_scores, stream);
+}
+
+dsa_status dsa_select_candidate_blocks(const float* logits, int64_t rows, int64_t width,
+                                       int64_t ld_logits, const int32_t* row_ks,
+                                       const int32_t* row_ke, int32_t topk_blocks,
+                                       int32_t block_size, int32_t row_repeat,
+                                       int32_t pin_newest, int32_t* out, int64_t ld_out,
+                                       float* scores_out, int64_t ld_scores, void* workspace,
+                                       size_t workspace_size, void* stream) {
+  return select_impl<F32>(logits, rows, width, ld_logits, row_ks, row_ke, topk_blocks,
+                          block_size, row_repeat, pin_newest, out, ld_out, scores_out, ld_scores,
+                          workspace, workspace_size, stream);
+}
+
+dsa_status dsa_select_candidate_blocks_bf16(const uint16_t* logits, int64_t rows, int64_t width,
+                                            int64_t ld_logits, const int32_t* row_ks,
+                                            const int32_t* row_ke, int32_t topk_blocks,
+                                            int32_t block_size, int32_t row_repeat,
+                                            int32_t pin_newest, int32_t* out, int64_t ld_out,
+                                            uint16_t* scores_out, int64_t ld_scores,
+                                            void* workspace, size_t workspace_size,
+                                            void* stream) {
+  return select_impl<BF16>(logits, rows, width, ld_logits, row_ks, row_ke, topk_blocks,
+                           block_size, row_repeat, pin_newest, out, ld_out, scores_out,
+                           ld_scores, workspace, workspace_size, stream);
+}
+
+dsa_status dsa_select_candidate_blocks_sharded(const float* logits, int32_t shards, int64_t rows,
+                                               int64_t local_width, int64_t ld_logits,
+                                               int64_t shard_stride,
+                                               const int32_t* global_row_ke,
+                                               int32_t global_block_size,
+                                               int32_t max_global_blocks, int32_t row_repeat,
+                                               int32_t topk_blocks, int32_t* out, int64_t ld_out,
+                                               float* scores_out, int64_t ld_scores,
+                                               void* workspace, size_t workspace_size,
+                                               void* stream) {
+  return select_sharded_impl<F32>(logits, shards, rows, local_width, ld_logits, shard_stride,
+                                  global_row_ke, global_block_size, max_global_blocks,
+                                  row_repeat, topk_blocks, out, ld_out, scores_out, ld_scores,
+                                  workspace, workspace_size, stream);
+}
+
+dsa_status dsa_select_candidate_blocks_sharded_bf16(
+    const uint16_t* logits, int32_t shards, int64_t rows, int64_t local_width, int64_t ld_logits,
+    int64_t shard_stride, const int32_t* global_row_ke, int32_t global_block_size,
+    int32_t max_global_blocks, int32_t row_repeat, int32_t topk_blocks, int32_t* out,
+    int64_t ld_out, uint16_t* scores_out, int64_t ld_scores, void* workspace,
+    size_t workspace_size, void* stream) {
+  return select_sharded_impl<BF16>(logits, shards, rows, local_width, ld_logits, shard_stride,
+                                   global_row_ke, global_block_size, max_global_blocks,
+                                   row_repeat, topk_blocks, out, ld_out, scores_out, ld_scores,
+                                   workspace, workspace_size, stream);
 }
 
 }  // extern "C"

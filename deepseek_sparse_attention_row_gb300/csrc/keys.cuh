@@ -1,5 +1,5 @@
 // keys.cuh -- order-preserving uint32 keys for fp32 scores, the NaN-propagating
-// max, and streaming global loads.
+// max, streaming global loads, and the fp32 / bf16 element types.
 //
 // Block maxima and ranking both use one total order on fp32 values:
 //   -inf < negative finite < -0 < +0 < positive finite < +inf < NaN,
@@ -80,5 +80,101 @@ __device__ __forceinline__ float fold(float acc, const float (&x)[2]) {
   return max_nan(acc, x[0], x[1]);
 }
 __device__ __forceinline__ float fold(float acc, const float (&x)[1]) { return max_nan(acc, x[0]); }
+
+// ---------------------------------------------------------------------------
+// Element types of the logits
+// ---------------------------------------------------------------------------
+//
+// F32: fp32 logits and scores. BF16: bf16 logits held as their 16-bit
+// patterns; a bf16 value widens exactly to the fp32 value with those bits on
+// top, so the max and the keys above apply unchanged to the widened values,
+// and a bf16 score is the upper half of the fp32 score (exact: a block max
+// is one of the block's values, +-inf, or the canonical NaN 0x7FC00000,
+// whose upper half is the bf16 canonical NaN 0x7FC0).
+struct F32 {
+  using T = float;
+  static constexpr int kBytes = 4;
+  static constexpr uint32_t kNegInfWord = 0xFF800000u;  // one -inf
+};
+struct BF16 {
+  using T = uint16_t;
+  static constexpr int kBytes = 2;
+  static constexpr uint32_t kNegInfWord = 0xFF80FF80u;  // two -inf
+};
+
+// VEC elements as loaded: whole 32-bit words (a lone bf16 sits in the low
+// half of its word).
+template <typename E, int VEC>
+struct Raw {
+  static constexpr int kWords = (VEC * E::kBytes + 3) / 4;
+  uint32_t w[kWords];
+};
+
+template <typename E, int VEC>
+__device__ __forceinline__ void raw_neg_inf(Raw<E, VEC>& r) {
+#pragma unroll
+  for (int i = 0; i < Raw<E, VEC>::kWords; ++i)
+    r.w[i] = (E::kBytes * VEC >= 4) ? E::kNegInfWord : (E::kNegInfWord & 0xFFFFu);
+}
+
+// Streaming load of VEC elements (16, 8, 4 or 2 bytes, naturally aligned).
+template <typename E, int VEC>
+__device__ __forceinline__ void ld_raw(const typename E::T* p, Raw<E, VEC>& r) {
+  constexpr int kB = VEC * E::kBytes;
+  if constexpr (kB == 16) {
+    asm("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
+        : "l"(p));
+  } else if constexpr (kB == 8) {
+    asm("ld.global.nc.L1::no_allocate.v2.b32 {%0, %1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "l"(p));
+  } else if constexpr (kB == 4) {
+    asm("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(r.w[0]) : "l"(p));
+  } else {
+    static_assert(kB == 2, "vector of 2, 4, 8 or 16 bytes");
+    r.w[0] = __ldg(reinterpret_cast<const unsigned short*>(p));
+  }
+}
+
+// Element i of a loaded vector, widened to fp32.
+template <typename E, int VEC>
+__device__ __forceinline__ float raw_elem(const Raw<E, VEC>& r, int i) {
+  if constexpr (E::kBytes == 4) {
+    return __uint_as_float(r.w[i]);
+  } else {
+    const uint32_t w = r.w[i >> 1];
+    return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+}
+
+// Fold a loaded vector into an accumulator with the NaN-propagating max.
+template <typename E, int VEC>
+__device__ __forceinline__ float fold(float acc, const Raw<E, VEC>& r) {
+  if constexpr (E::kBytes == 4) {
+    float x[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) x[i] = __uint_as_float(r.w[i]);
+    return fold(acc, x);
+  } else if constexpr (VEC == 1) {
+    return max_nan(acc, __uint_as_float(r.w[0] << 16));
+  } else {
+#pragma unroll
+    for (int i = 0; i < Raw<E, VEC>::kWords; ++i)
+      acc = max_nan(acc, __uint_as_float(r.w[i] << 16), __uint_as_float(r.w[i] & 0xFFFF0000u));
+    return acc;
+  }
+}
+
+// One element, widened (streaming scalar load).
+__device__ __forceinline__ float ld_elem(const float* p) { return ld_stream1(p); }
+__device__ __forceinline__ float ld_elem(const uint16_t* p) {
+  return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p)))
+                         << 16);
+}
+
+// A score written from its key, in the logits' type.
+__device__ __forceinline__ void put_score(float* p, uint32_t key) { *p = key_score(key); }
+__device__ __forceinline__ void put_score(uint16_t* p, uint32_t key) {
+  *p = static_cast<uint16_t>(__float_as_uint(key_score(key)) >> 16);
+}
 
 }  // namespace dsa

@@ -1,5 +1,5 @@
 // mask.cu -- masking packed logits to the selected candidate blocks: the C
-// ABI dsa_mask_candidate_logits[_sharded] of include/dsa_cb.h.
+// ABI dsa_mask_candidate_logits[_sharded][_bf16] of include/dsa_cb.h.
 //
 // candidate_blocks.py diff, the masking function after selection ("mask
 // packed logits outside causal bounds and request-local candidates"; under
@@ -11,13 +11,14 @@
 // HBM write bandwidth.
 //
 // One CTA per (shard, row, chunk of kMaskChunk columns). The chunk is cut
-// into 16-byte-aligned slots of four columns. Before any store, the CTA turns
-// the row's candidate ids into two slot bitmaps in shared memory: `touch`
-// (the slot holds at least one kept column) and `whole` (all four columns
-// lie in one kept run). Then every slot costs one shared-memory bit test: an
-// untouched slot gets one 16-byte store of -inf, a whole slot is skipped, and
-// only the few slots at the edges of kept runs test their columns one by one
-// (against a third bitmap, of candidate blocks).
+// into 16-byte-aligned slots (four fp32 or eight bf16 columns). Before any
+// store, the CTA turns the row's candidate ids into two slot bitmaps in
+// shared memory: `touch` (the slot holds at least one kept column) and
+// `whole` (all the slot's columns lie in one kept run). Then every slot costs
+// one shared-memory bit test: an untouched slot gets one 16-byte store of
+// -inf (fp32 0xFF800000 or bf16 0xFF80 per column), a whole slot is skipped,
+// and only the few slots at the edges of kept runs test their columns one by
+// one (against a third bitmap, of candidate blocks).
 #include "../../include/dsa_cb.h"
 
 #include <cuda_runtime.h>
@@ -31,8 +32,9 @@ namespace {
 
 constexpr int32_t kMaskChunk = 8192;  // columns per CTA
 constexpr int kMaskThreads = 256;
-// A chunk's columns fall in at most kMaskChunk / 4 + 1 aligned slots (the
-// chunk may start up to three columns past a 16-byte boundary).
+// A chunk's columns fall in at most kMaskChunk / 4 + 1 aligned slots (fp32;
+// the chunk may start up to three columns past a 16-byte boundary; bf16
+// needs at most kMaskChunk / 8 + 1).
 constexpr int32_t kSlots = kMaskChunk / 4 + 1;
 constexpr int32_t kSlotWords = (kSlots + 31) / 32;
 // Blocks that overlap a chunk: at most kMaskChunk + 1 (block size 1).
@@ -40,7 +42,7 @@ constexpr int32_t kBlockBits = kMaskChunk + 1;
 constexpr int32_t kBlockWords = (kBlockBits + 31) / 32;
 
 struct MaskArgs {
-  float* logits;
+  void* logits;           // E::T elements
   int64_t ld;
   int64_t shard_stride;
   int32_t shards;         // 1: unsharded
@@ -56,10 +58,13 @@ struct MaskArgs {
   int32_t chunks;         // chunks per row
 };
 
-__device__ __forceinline__ void st_neg_inf4(float* p) {
-  const float n = neg_inf();
-  asm volatile("st.global.v4.f32 [%0], {%1, %1, %1, %1};" ::"l"(p), "f"(n) : "memory");
+template <typename E>
+__device__ __forceinline__ void st_neg_inf16(typename E::T* p) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %1, %1, %1};" ::"l"(p), "r"(E::kNegInfWord)
+               : "memory");
 }
+__device__ __forceinline__ void st_neg_inf1(float* p) { *p = neg_inf(); }
+__device__ __forceinline__ void st_neg_inf1(uint16_t* p) { *p = 0xFF80u; }
 
 // Sets bits [k0, k1) of a shared-memory bitmap (k0 < k1).
 __device__ __forceinline__ void set_bits(uint32_t* bits, int32_t k0, int32_t k1) {
@@ -76,7 +81,10 @@ __device__ __forceinline__ bool test_bit(const uint32_t* bits, int32_t k) {
   return (bits[k >> 5] >> (k & 31)) & 1u;
 }
 
+template <typename E>
 __global__ void __launch_bounds__(kMaskThreads) mask_kernel(const MaskArgs a) {
+  constexpr int P = 16 / E::kBytes;  // columns per slot
+  constexpr int kLogP = P == 4 ? 2 : 3;
   __shared__ uint32_t touch[kSlotWords];
   __shared__ uint32_t whole[kSlotWords];
   __shared__ uint32_t blocks[kBlockWords];
@@ -98,18 +106,21 @@ __global__ void __launch_bounds__(kMaskThreads) mask_kernel(const MaskArgs a) {
     s = 0;
     e = 0;
     if (gke > d) {
-      const uint32_t lke = (static_cast<uint32_t>(gke - d) + static_cast<uint32_t>(a.shards - 1)) /
-                           static_cast<uint32_t>(a.shards);
+      const uint32_t lke =
+          (static_cast<uint32_t>(gke - d) + static_cast<uint32_t>(a.shards - 1)) /
+          static_cast<uint32_t>(a.shards);
       e = static_cast<int32_t>(min(lke, static_cast<uint32_t>(a.width)));
     }
   }
   const int32_t c0 = chunk * kMaskChunk;
   const int32_t c1 = min(c0 + kMaskChunk, a.width);
-  float* rowp = a.logits + static_cast<int64_t>(d) * a.shard_stride + row * a.ld;
-  // 16-byte slots: slot k covers columns [a0 + 4k, a0 + 4k + 4).
-  const int32_t mis = static_cast<int32_t>((reinterpret_cast<uintptr_t>(rowp + c0) >> 2) & 3);
+  typename E::T* rowp = static_cast<typename E::T*>(a.logits) +
+                        static_cast<int64_t>(d) * a.shard_stride + row * a.ld;
+  // 16-byte slots: slot k covers columns [a0 + P k, a0 + P k + P).
+  const int32_t mis =
+      static_cast<int32_t>((reinterpret_cast<uintptr_t>(rowp + c0) / E::kBytes) & (P - 1));
   const int32_t a0 = c0 - mis;
-  const int32_t nslots = (c1 - a0 + 3) / 4;  // <= kSlots
+  const int32_t nslots = (c1 - a0 + P - 1) / P;  // <= kSlots
 
   for (int i = threadIdx.x; i < kSlotWords; i += kMaskThreads) {
     touch[i] = 0u;
@@ -132,61 +143,59 @@ __global__ void __launch_bounds__(kMaskThreads) mask_kernel(const MaskArgs a) {
       // [blo, bhi)).
       const int64_t bstart = static_cast<int64_t>(s) + static_cast<int64_t>(b) * a.block_size;
       const int32_t lo = static_cast<int32_t>(max(static_cast<int64_t>(lo_c), bstart));
-      const int32_t hi = static_cast<int32_t>(min(static_cast<int64_t>(hi_c), bstart + a.block_size));
-      set_bits(touch, (lo - a0) >> 2, ((hi - 1 - a0) >> 2) + 1);
-      const int32_t f0 = (lo - a0 + 3) >> 2, f1 = (hi - a0) >> 2;
+      const int32_t hi =
+          static_cast<int32_t>(min(static_cast<int64_t>(hi_c), bstart + a.block_size));
+      set_bits(touch, (lo - a0) >> kLogP, ((hi - 1 - a0) >> kLogP) + 1);
+      const int32_t f0 = (lo - a0 + P - 1) >> kLogP, f1 = (hi - a0) >> kLogP;
       if (f0 < f1) set_bits(whole, f0, f1);
     }
   }
   __syncthreads();
 
   for (int32_t k = threadIdx.x; k < nslots; k += kMaskThreads) {
-    const int32_t cb = a0 + 4 * k;
+    const int32_t cb = a0 + P * k;
     if (!test_bit(touch, k)) {
-      if (cb >= c0 && cb + 4 <= c1) {
-        st_neg_inf4(rowp + cb);
+      if (cb >= c0 && cb + P <= c1) {
+        st_neg_inf16<E>(rowp + cb);
       } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (cb + i >= c0 && cb + i < c1) rowp[cb + i] = neg_inf();
+        for (int i = 0; i < P; ++i)
+          if (cb + i >= c0 && cb + i < c1) st_neg_inf1(rowp + cb + i);
       }
       continue;
     }
     if (test_bit(whole, k)) continue;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < P; ++i) {
       const int32_t c = cb + i;
       if (c < c0 || c >= c1) continue;
       const bool kept = c >= s && c < e && test_bit(blocks, (c - s) / a.block_size - blo);
-      if (!kept) rowp[c] = neg_inf();
+      if (!kept) st_neg_inf1(rowp + c);
     }
   }
 }
 
+template <typename E>
 dsa_status launch_mask(MaskArgs& a, cudaStream_t stream) {
   a.chunks = static_cast<int32_t>((static_cast<int64_t>(a.width) + kMaskChunk - 1) / kMaskChunk);
   const int64_t grid = static_cast<int64_t>(a.shards) * a.rows * a.chunks;
   if (grid > INT32_MAX) return DSA_EUNSUPPORTED;
-  mask_kernel<<<static_cast<unsigned>(grid), kMaskThreads, 0, stream>>>(a);
+  mask_kernel<E><<<static_cast<unsigned>(grid), kMaskThreads, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
 }
 
-}  // namespace
-}  // namespace dsa
-
-extern "C" dsa_status dsa_mask_candidate_logits(float* logits, int64_t rows, int64_t width,
-                                                int64_t ld_logits, const int32_t* row_ks,
-                                                const int32_t* row_ke, const int32_t* candidates,
-                                                int32_t topk_blocks, int64_t ld_candidates,
-                                                int32_t block_size, int32_t row_repeat,
-                                                void* stream) {
+template <typename E>
+dsa_status mask_impl(typename E::T* logits, int64_t rows, int64_t width, int64_t ld_logits,
+                     const int32_t* row_ks, const int32_t* row_ke, const int32_t* candidates,
+                     int32_t topk_blocks, int64_t ld_candidates, int32_t block_size,
+                     int32_t row_repeat, void* stream) {
   if (rows < 0 || width < 0 || block_size < 1 || row_repeat < 1 || topk_blocks < 0)
     return DSA_EINVAL;
   if (rows == 0 || width == 0) return DSA_OK;
   if (!logits || !row_ke || ld_logits < width) return DSA_EINVAL;
   if (topk_blocks > 0 && (!candidates || ld_candidates < topk_blocks)) return DSA_EINVAL;
-  if (width > INT32_MAX - dsa::kMaskChunk) return DSA_EUNSUPPORTED;
-  dsa::MaskArgs a{};
+  if (width > INT32_MAX - kMaskChunk) return DSA_EUNSUPPORTED;
+  MaskArgs a{};
   a.logits = logits;
   a.ld = ld_logits;
   a.shard_stride = 0;
@@ -200,14 +209,15 @@ extern "C" dsa_status dsa_mask_candidate_logits(float* logits, int64_t rows, int
   a.cand = candidates;
   a.topk = topk_blocks;
   a.ld_cand = ld_candidates;
-  return dsa::launch_mask(a, static_cast<cudaStream_t>(stream));
+  return launch_mask<E>(a, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" dsa_status dsa_mask_candidate_logits_sharded(
-    float* logits, int32_t shards, int64_t rows, int64_t local_width, int64_t ld_logits,
-    int64_t shard_stride, const int32_t* global_row_ke, int32_t global_block_size,
-    int32_t row_repeat, const int32_t* candidates, int32_t topk_blocks, int64_t ld_candidates,
-    void* stream) {
+template <typename E>
+dsa_status mask_sharded_impl(typename E::T* logits, int32_t shards, int64_t rows,
+                             int64_t local_width, int64_t ld_logits, int64_t shard_stride,
+                             const int32_t* global_row_ke, int32_t global_block_size,
+                             int32_t row_repeat, const int32_t* candidates, int32_t topk_blocks,
+                             int64_t ld_candidates, void* stream) {
   if (shards < 1 || rows < 0 || local_width < 0 || global_block_size < 1 ||
       global_block_size % shards != 0 || row_repeat < 1 || topk_blocks < 0 ||
       ld_logits < local_width || shard_stride < 0)
@@ -215,8 +225,8 @@ extern "C" dsa_status dsa_mask_candidate_logits_sharded(
   if (rows == 0 || local_width == 0) return DSA_OK;
   if (!logits || !global_row_ke) return DSA_EINVAL;
   if (topk_blocks > 0 && (!candidates || ld_candidates < topk_blocks)) return DSA_EINVAL;
-  if (local_width > INT32_MAX - dsa::kMaskChunk) return DSA_EUNSUPPORTED;
-  dsa::MaskArgs a{};
+  if (local_width > INT32_MAX - kMaskChunk) return DSA_EUNSUPPORTED;
+  MaskArgs a{};
   a.logits = logits;
   a.ld = ld_logits;
   a.shard_stride = shard_stride;
@@ -230,5 +240,52 @@ extern "C" dsa_status dsa_mask_candidate_logits_sharded(
   a.cand = candidates;
   a.topk = topk_blocks;
   a.ld_cand = ld_candidates;
-  return dsa::launch_mask(a, static_cast<cudaStream_t>(stream));
+  return launch_mask<E>(a, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" dsa_status dsa_mask_candidate_logits(float* logits, int64_t rows, int64_t width,
+                                                int64_t ld_logits, const int32_t* row_ks,
+                                                const int32_t* row_ke, const int32_t* candidates,
+                                                int32_t topk_blocks, int64_t ld_candidates,
+                                                int32_t block_size, int32_t row_repeat,
+                                                void* stream) {
+  return dsa::mask_impl<dsa::F32>(logits, rows, width, ld_logits, row_ks, row_ke, candidates,
+                                  topk_blocks, ld_candidates, block_size, row_repeat, stream);
+}
+
+extern "C" dsa_status dsa_mask_candidate_logits_bf16(uint16_t* logits, int64_t rows,
+                                                     int64_t width, int64_t ld_logits,
+                                                     const int32_t* row_ks,
+                                                     const int32_t* row_ke,
+                                                     const int32_t* candidates,
+                                                     int32_t topk_blocks, int64_t ld_candidates,
+                                                     int32_t block_size, int32_t row_repeat,
+                                                     void* stream) {
+  return dsa::mask_impl<dsa::BF16>(logits, rows, width, ld_logits, row_ks, row_ke, candidates,
+                                   topk_blocks, ld_candidates, block_size, row_repeat, stream);
+}
+
+extern "C" dsa_status dsa_mask_candidate_logits_sharded(
+    float* logits, int32_t shards, int64_t rows, int64_t local_width, int64_t ld_logits,
+    int64_t shard_stride, const int32_t* global_row_ke, int32_t global_block_size,
+    int32_t row_repeat, const int32_t* candidates, int32_t topk_blocks, int64_t ld_candidates,
+    void* stream) {
+  return dsa::mask_sharded_impl<dsa::F32>(logits, shards, rows, local_width, ld_logits,
+                                          shard_stride, global_row_ke, global_block_size,
+                                          row_repeat, candidates, topk_blocks, ld_candidates,
+                                          stream);
+}
+
+extern "C" dsa_status dsa_mask_candidate_logits_sharded_bf16(
+    uint16_t* logits, int32_t shards, int64_t rows, int64_t local_width, int64_t ld_logits,
+    int64_t shard_stride, const int32_t* global_row_ke, int32_t global_block_size,
+    int32_t row_repeat, const int32_t* candidates, int32_t topk_blocks, int64_t ld_candidates,
+    void* stream) {
+  return dsa::mask_sharded_impl<dsa::BF16>(logits, shards, rows, local_width, ld_logits,
+                                           shard_stride, global_row_ke, global_block_size,
+                                           row_repeat, candidates, topk_blocks, ld_candidates,
+                                           stream);
 }

@@ -38,8 +38,9 @@
 
 namespace dsa {
 
+template <typename E>
 struct Window {
-  const float* origin;   // element 0 of shard 0's window
+  const typename E::T* origin;  // element 0 of shard 0's window
   int64_t shard_stride;  // elements between shards
   int32_t shards;
   const int32_t* len;    // shared memory: in-window length of each shard
@@ -49,8 +50,8 @@ struct Window {
 // Fast path. lpb_log2 = log2(block_size / VEC).
 // Warp `warp` of `nwarps` warps working on the range (a whole CTA: the CTA's
 // warp index and count; one warp alone: 0 and 1).
-template <int VEC, int NV, int SB>
-__device__ __forceinline__ void stream_pow2(const Window& w, int lpb_log2, int32_t b0, int32_t b1,
+template <typename E, int VEC, int NV, int SB>
+__device__ __forceinline__ void stream_pow2(const Window<E>& w, int lpb_log2, int32_t b0, int32_t b1,
                                             uint32_t* __restrict__ keys, int32_t kbase, int warp,
                                             int nwarps) {
   const int lane = threadIdx.x & 31;
@@ -68,26 +69,24 @@ __device__ __forceinline__ void stream_pow2(const Window& w, int lpb_log2, int32
 #pragma unroll
     for (int j = 0; j < SB; ++j)
       lim[j] = (d0 + j < w.shards) ? min(w.len[d0 + j] / VEC, v_end) : 0;
-    const float* base = w.origin + static_cast<int64_t>(d0) * w.shard_stride;
+    const typename E::T* base = w.origin + static_cast<int64_t>(d0) * w.shard_stride;
 
     const int32_t step = nwarps * kSlab;
     for (int32_t slab = v_begin + warp * kSlab; slab < v_end; slab += step) {
       float acc[NV];
 #pragma unroll
       for (int m = 0; m < NV; ++m) acc[m] = neg_inf();
-      float x[SB][NV][VEC];
+      Raw<E, VEC> x[SB][NV];
 #pragma unroll
       for (int j = 0; j < SB; ++j) {
-        const float* src = base + static_cast<int64_t>(j) * w.shard_stride;
+        const typename E::T* src = base + static_cast<int64_t>(j) * w.shard_stride;
 #pragma unroll
         for (int m = 0; m < NV; ++m) {
           const int32_t v = slab + m * 32 + lane;
-          if (v < lim[j]) {
-            ld_stream(src + static_cast<int64_t>(v) * VEC, x[j][m]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < VEC; ++i) x[j][m][i] = neg_inf();
-          }
+          if (v < lim[j])
+            ld_raw<E, VEC>(src + static_cast<int64_t>(v) * VEC, x[j][m]);
+          else
+            raw_neg_inf(x[j][m]);
         }
       }
 #pragma unroll
@@ -132,42 +131,43 @@ __device__ __forceinline__ void stream_pow2(const Window& w, int lpb_log2, int32
   }
 }
 
-// Unsharded window whose start lies r = 1..3 floats past a 16-byte boundary,
-// block size a power-of-two multiple of 4 (LPB = block_size / 4 a power of
-// two). Loads aligned float4s from base = origin - r. Vector v of base covers
-// window elements [4v - r, 4v - r + 4); all of them belong to block
-// v / LPB except, in the block's first vector (v % LPB == 0), the r elements
-// below the block boundary, which belong to block v / LPB - 1 (and, for
-// v = 0, precede the window and are dropped). Each lane folds its vectors
+// Unsharded window whose start lies r = 1..VEC-1 elements past a 16-byte
+// boundary (VEC = 16-byte vector in elements: 4 fp32 or 8 bf16), block size a
+// power-of-two multiple of VEC (LPB = block_size / VEC a power of two).
+// Loads aligned 16-byte vectors from base = origin - r. Vector v of base
+// covers window elements [VEC*v - r, VEC*v - r + VEC); all of them belong to
+// block v / LPB except, in the block's first vector (v % LPB == 0), the r
+// elements below the block boundary, which belong to block v / LPB - 1 (and,
+// for v = 0, precede the window and are dropped). Each lane folds its vectors
 // into a "hi" value for block v / LPB and, in a block's first vector, a "lo"
 // value for the block before; both are merged into shared memory with
 // atomicMax. Vector b1 * LPB is read only for its lo part (it completes block
-// b1 - 1). Elements past the last whole vector are left to load_partial_shifted.
-template <int NV>
-__device__ __forceinline__ void stream_shift4(const float* origin, int32_t r, int32_t len,
-                                              int lpb_log2, int32_t b0, int32_t b1,
-                                              uint32_t* __restrict__ keys, int32_t kbase,
-                                              int warp, int nwarps) {
+// b1 - 1). Elements past the last whole vector are left to
+// commit_partial_shifted.
+template <typename E, int NV>
+__device__ __forceinline__ void stream_shift(const typename E::T* origin, int32_t r, int32_t len,
+                                             int lpb_log2, int32_t b0, int32_t b1,
+                                             uint32_t* __restrict__ keys, int32_t kbase,
+                                             int warp, int nwarps) {
+  constexpr int VEC = 16 / E::kBytes;
   const int lane = threadIdx.x & 31;
   const int lpb = 1 << lpb_log2;
-  const float* base = origin - r;
-  const int32_t nvec = (len + r) / 4;  // whole vectors of base inside [base, origin + len)
+  const typename E::T* base = origin - r;
+  const int32_t nvec = (len + r) / VEC;  // whole vectors of base inside [base, origin + len)
   const int32_t v_begin = static_cast<int32_t>(static_cast<int64_t>(b0) << lpb_log2);
   const int32_t v_end = static_cast<int32_t>(min((static_cast<int64_t>(b1) << lpb_log2) + 1,
                                                  static_cast<int64_t>(nvec)));
   constexpr int32_t kSlab = 32 * NV;
   const int32_t step = nwarps * kSlab;
   for (int32_t slab = v_begin + warp * kSlab; slab < v_end; slab += step) {
-    float x[NV][4];
+    Raw<E, VEC> x[NV];
 #pragma unroll
     for (int m = 0; m < NV; ++m) {
       const int32_t v = slab + m * 32 + lane;
-      if (v < v_end) {
-        ld_stream(base + static_cast<int64_t>(v) * 4, x[m]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) x[m][i] = neg_inf();
-      }
+      if (v < v_end)
+        ld_raw<E, VEC>(base + static_cast<int64_t>(v) * VEC, x[m]);
+      else
+        raw_neg_inf(x[m]);
     }
     float hi[NV], lo[NV];
 #pragma unroll
@@ -177,10 +177,11 @@ __device__ __forceinline__ void stream_shift4(const float* origin, int32_t r, in
       hi[m] = neg_inf();
       lo[m] = neg_inf();
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < VEC; ++i) {
         const bool below = lead && i < r;
-        hi[m] = max_nan(hi[m], below ? neg_inf() : x[m][i]);
-        lo[m] = max_nan(lo[m], below ? x[m][i] : neg_inf());
+        const float xi = raw_elem(x[m], i);
+        hi[m] = max_nan(hi[m], below ? neg_inf() : xi);
+        lo[m] = max_nan(lo[m], below ? xi : neg_inf());
       }
     }
     // lo parts: the lead lane of each block sends them to the block before.
@@ -222,17 +223,19 @@ __device__ __forceinline__ void stream_shift4(const float* origin, int32_t r, in
   }
 }
 
-// Elements of a shifted window (stream_shift4) past its last whole vector:
-// window elements [4 * nvec - r, len), each to its own block (the run can
+// Elements of a shifted window (stream_shift) past its last whole vector:
+// window elements [VEC * nvec - r, len), each to its own block (the run can
 // cross one block boundary). One thread; call after the loop and a barrier.
-__device__ __forceinline__ void commit_partial_shifted(const float* origin, int32_t r, int32_t len,
-                                                       int32_t block_size, int32_t b0,
-                                                       int32_t b1, uint32_t* keys,
+template <typename E>
+__device__ __forceinline__ void commit_partial_shifted(const typename E::T* origin, int32_t r,
+                                                       int32_t len, int32_t block_size,
+                                                       int32_t b0, int32_t b1, uint32_t* keys,
                                                        int32_t kbase) {
-  const int32_t first = max(((len + r) / 4) * 4 - r, 0);
+  constexpr int VEC = 16 / E::kBytes;
+  const int32_t first = max(((len + r) / VEC) * VEC - r, 0);
   for (int32_t i = first; i < len; ++i) {
     const int32_t blk = i / block_size;
-    if (blk >= b0 && blk < b1) atomicMax(&keys[blk - kbase], order_key(ld_stream1(origin + i)));
+    if (blk >= b0 && blk < b1) atomicMax(&keys[blk - kbase], order_key(ld_elem(origin + i)));
   }
 }
 
@@ -246,16 +249,16 @@ struct Partial {
   int32_t blk;  // -1: nothing to merge
 };
 
-template <int VEC>
-__device__ __forceinline__ Partial load_partial(const float* shard_origin, int32_t len,
-                                                    int32_t block_size, int32_t b0, int32_t b1) {
+template <typename E, int VEC>
+__device__ __forceinline__ Partial load_partial(const typename E::T* shard_origin, int32_t len,
+                                                int32_t block_size, int32_t b0, int32_t b1) {
   Partial p{neg_inf(), -1};
   if (VEC == 1) return p;
   const int32_t first = (len / VEC) * VEC;
   if (first == len) return p;
   const int32_t blk = first / block_size;
   if (blk < b0 || blk >= b1) return p;
-  for (int32_t i = first; i < len; ++i) p.v = max_nan(p.v, ld_stream1(shard_origin + i));
+  for (int32_t i = first; i < len; ++i) p.v = max_nan(p.v, ld_elem(shard_origin + i));
   p.blk = blk;
   return p;
 }
@@ -265,8 +268,8 @@ __device__ __forceinline__ void commit_partial(const Partial& p, uint32_t* keys,
 }
 
 // Generic path: any block size, any alignment. Elements, not vectors.
-template <int NV, int SB>
-__device__ __forceinline__ void stream_generic(const Window& w, int32_t block_size, int32_t b0,
+template <typename E, int NV, int SB>
+__device__ __forceinline__ void stream_generic(const Window<E>& w, int32_t block_size, int32_t b0,
                                                int32_t b1, uint32_t* __restrict__ keys,
                                                int32_t kbase, int warp, int nwarps) {
   const int lane = threadIdx.x & 31;
@@ -284,11 +287,11 @@ __device__ __forceinline__ void stream_generic(const Window& w, int32_t block_si
 #pragma unroll
       for (int j = 0; j < SB; ++j) {
         const int32_t len = (d0 + j < w.shards) ? w.len[d0 + j] : 0;
-        const float* src = w.origin + static_cast<int64_t>(d0 + j) * w.shard_stride;
+        const typename E::T* src = w.origin + static_cast<int64_t>(d0 + j) * w.shard_stride;
 #pragma unroll
         for (int m = 0; m < NV; ++m) {
           const int64_t i = slab + m * 32 + lane;
-          x[j][m] = (i < e_end && i < len) ? ld_stream1(src + i) : neg_inf();
+          x[j][m] = (i < e_end && i < len) ? ld_elem(src + i) : neg_inf();
         }
       }
 #pragma unroll
@@ -317,51 +320,73 @@ __device__ __forceinline__ void stream_generic(const Window& w, int32_t block_si
   }
 }
 
-// Per-row choice of the vector width for a window origin (unsharded rows
-// start at arbitrary columns). Returns 0 for the generic path.
-__device__ __forceinline__ int choose_vec(const float* origin, int32_t block_size, int* lpb_log2) {
+// Per-row choice of the vector width (elements) for a window origin
+// (unsharded rows start at arbitrary columns): the widest of 16, 8, 4 (and,
+// for bf16, 2) bytes that the origin's alignment allows and that splits the
+// block into a power of two of vectors. Returns 0 for the generic path.
+template <typename E>
+__device__ __forceinline__ int choose_vec(const typename E::T* origin, int32_t block_size,
+                                          int* lpb_log2) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(origin);
   auto pow2 = [](int32_t x) { return x > 0 && (x & (x - 1)) == 0; };
   int vec = 0;
-  if (block_size % 4 == 0 && (a & 15) == 0 && pow2(block_size / 4))
-    vec = 4;
-  else if (block_size % 2 == 0 && (a & 7) == 0 && pow2(block_size / 2))
-    vec = 2;
-  else if (pow2(block_size))
-    vec = 1;
+  for (int bytes = 16; bytes >= 2 * E::kBytes; bytes >>= 1) {
+    const int v = bytes / E::kBytes;
+    if (block_size % v == 0 && (a & (bytes - 1)) == 0 && pow2(block_size / v)) {
+      vec = v;
+      break;
+    }
+  }
+  if (!vec && pow2(block_size)) vec = 1;
   *lpb_log2 = vec ? __ffs(block_size / vec) - 1 : 0;
   return vec;
 }
 
 // Unsharded dispatch: vector width chosen per row at run time. Every path
-// keeps 32 floats per lane in flight per slab.
-// vec 8: shifted 16-byte loads (stream_shift4) for a window starting
-// `shift` floats past a 16-byte boundary.
-constexpr int kVecShift = 8;
+// keeps 32 words per lane in flight per slab.
+// kVecShift: shifted 16-byte loads (stream_shift) for a window starting
+// `shift` elements past a 16-byte boundary (no element count is this large).
+constexpr int kVecShift = 64;
 
-__device__ __forceinline__ void stream_row(const Window& w, int vec, int shift, int lpb_log2,
+template <typename E>
+__device__ __forceinline__ void stream_row(const Window<E>& w, int vec, int shift, int lpb_log2,
                                            int32_t block_size, int32_t b0, int32_t b1,
                                            uint32_t* keys, int32_t kbase, int warp, int nwarps) {
-  switch (vec) {
-    case kVecShift:
-      stream_shift4<8>(w.origin, shift, w.len_max, lpb_log2, b0, b1, keys, kbase, warp, nwarps);
-      break;
-    case 4: stream_pow2<4, 8, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps); break;
-    case 2: stream_pow2<2, 16, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps); break;
-    case 1: stream_pow2<1, 32, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps); break;
-    default: stream_generic<16, 1>(w, block_size, b0, b1, keys, kbase, warp, nwarps); break;
-  }
+  constexpr int V16 = 16 / E::kBytes;  // elements per 16 / 8 / 4-byte vector
+  constexpr int V8 = 8 / E::kBytes;
+  constexpr int V4 = 4 / E::kBytes;
+  if (vec == kVecShift)
+    stream_shift<E, 8>(w.origin, shift, w.len_max, lpb_log2, b0, b1, keys, kbase, warp, nwarps);
+  else if (vec == V16)
+    stream_pow2<E, V16, 8, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps);
+  else if (vec == V8)
+    stream_pow2<E, V8, 16, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps);
+  else if (vec == V4 && V4 > 1)
+    stream_pow2<E, (V4 > 1 ? V4 : 2), 32, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps);
+  else if (vec == 1)
+    stream_pow2<E, 1, 32, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps);
+  else
+    stream_generic<E, 16, 1>(w, block_size, b0, b1, keys, kbase, warp, nwarps);
 }
 
 // Tail of an unsharded row past its last whole vector; one thread, after the
 // loop and a barrier.
-__device__ __forceinline__ void finish_row(const Window& w, int vec, int shift, int32_t block_size,
-                                           int32_t b0, int32_t b1, uint32_t* keys,
-                                           int32_t kbase) {
-  if (vec == 4) commit_partial(load_partial<4>(w.origin, w.len_max, block_size, b0, b1), keys, kbase);
-  if (vec == 2) commit_partial(load_partial<2>(w.origin, w.len_max, block_size, b0, b1), keys, kbase);
-  if (vec == kVecShift)
-    commit_partial_shifted(w.origin, shift, w.len_max, block_size, b0, b1, keys, kbase);
+template <typename E>
+__device__ __forceinline__ void finish_row(const Window<E>& w, int vec, int shift,
+                                           int32_t block_size, int32_t b0, int32_t b1,
+                                           uint32_t* keys, int32_t kbase) {
+  constexpr int V16 = 16 / E::kBytes;
+  constexpr int V8 = 8 / E::kBytes;
+  constexpr int V4 = 4 / E::kBytes;
+  if (vec == V16)
+    commit_partial(load_partial<E, V16>(w.origin, w.len_max, block_size, b0, b1), keys, kbase);
+  else if (vec == V8)
+    commit_partial(load_partial<E, V8>(w.origin, w.len_max, block_size, b0, b1), keys, kbase);
+  else if (vec == V4 && V4 > 1)
+    commit_partial(load_partial<E, (V4 > 1 ? V4 : 2)>(w.origin, w.len_max, block_size, b0, b1),
+                   keys, kbase);
+  else if (vec == kVecShift)
+    commit_partial_shifted<E>(w.origin, shift, w.len_max, block_size, b0, b1, keys, kbase);
 }
 
 }  // namespace dsa

@@ -206,11 +206,12 @@ __device__ void topk_exact(const uint32_t* __restrict__ keys, int32_t nb, int32_
 // key(-inf) (n_live covers the pinned block); block pin_block (if >= 0)
 // becomes +inf here. cand: [max(kpad, kRankMax)] in shared memory, kpad a
 // power of two >= min(k, nb). out: this row's output slots (global; unused
-// when k == 0). scores: optional fp32 row (nb entries) written with the final
-// scores. Every thread of the CTA calls this.
+// when k == 0). scores: optional row (nb entries, fp32 or bf16 bits like the
+// logits) written with the final scores. Every thread of the CTA calls this.
+template <typename S>
 __device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t n_live, int32_t k,
                            int32_t pin_block, uint64_t* __restrict__ cand, int32_t kpad,
-                           int32_t* __restrict__ out, int32_t topk, float* __restrict__ scores,
+                           int32_t* __restrict__ out, int32_t topk, S* __restrict__ scores,
                            TopkShared& sh) {
   constexpr int KR = 8;  // live keys per thread held in registers
   const int tid = threadIdx.x;
@@ -224,7 +225,7 @@ __device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t n_li
 
   if (scores)
     for (int b = tid; b < nb; b += nthreads)
-      scores[b] = key_score(b == pin_block ? kKeyPosInf : (b < n_live ? keys[b] : kKeyNegInf));
+      put_score(scores + b, b == pin_block ? kKeyPosInf : (b < n_live ? keys[b] : kKeyNegInf));
 
   // 1. Each thread takes its own keys b = tid + i*T: pin, count, min, max and
   // its largest key (lane max).

@@ -26,10 +26,12 @@ constexpr int kWarpCand = 128;  // candidates ranked by counting, per warp
 // keys: this warp's [n_live] block keys in shared memory (the pinned block,
 // if >= 0, lies below n_live and becomes +inf here). cand: [kWarpCand] in
 // shared memory. out: the row's output slots (global; unused when k == 0).
-// scores: optional fp32 row of nb entries. All 32 lanes call this.
+// scores: optional row of nb entries (fp32 or bf16 bits). All 32 lanes call
+// this.
+template <typename S>
 __device__ void topk_warp(uint32_t* __restrict__ keys, int32_t nb, int32_t n_live, int32_t k,
                           int32_t pin_block, uint64_t* __restrict__ cand,
-                          int32_t* __restrict__ out, int32_t topk, float* __restrict__ scores) {
+                          int32_t* __restrict__ out, int32_t topk, S* __restrict__ scores) {
   constexpr int KR = 8;
   const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1u;
@@ -37,7 +39,7 @@ __device__ void topk_warp(uint32_t* __restrict__ keys, int32_t nb, int32_t n_liv
 
   if (scores)
     for (int b = lane; b < nb; b += 32)
-      scores[b] = key_score(b == pin_block ? kKeyPosInf : (b < n_live ? keys[b] : kKeyNegInf));
+      put_score(scores + b, b == pin_block ? kKeyPosInf : (b < n_live ? keys[b] : kKeyNegInf));
 
   uint32_t kr[KR];
   uint32_t cnt = 0, mx = 0;

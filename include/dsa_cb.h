@@ -237,6 +237,53 @@ dsa_status dsa_mask_candidate_logits_sharded(
     int32_t topk_blocks, int64_t ld_candidates, void *stream);
 
 /*
+ * bf16 logits. The same five operations on bf16 logits, held as their 16-bit
+ * patterns (uint16_t, the layout of torch.bfloat16 / __nv_bfloat16). The page
+ * allocates the block scores with the logits' dtype (_block_scores:
+ * logits.new_empty), so scores_out is bf16 too: a block score is the
+ * block's max bf16 value (exact), +inf / -inf (0x7F80 / 0xFF80), or the
+ * canonical bf16 NaN 0x7FC0. Masking writes bf16 -inf (0xFF80). Selection
+ * ranks the exact values, so a bf16 call gives the same ids as the fp32 call
+ * on the widened logits. Arguments (in elements), limits and errors are
+ * those of the fp32 entry points above; the vectorised paths need the row
+ * starts to be 16-byte (8-element) aligned as before, and fall back to
+ * 8-, 4- or 2-byte loads otherwise.
+ */
+dsa_status dsa_block_scores_bf16(const uint16_t *logits, int64_t rows, int64_t width,
+                                 int64_t ld_logits, const int32_t *row_ks,
+                                 const int32_t *row_ke, int32_t block_size,
+                                 int32_t row_repeat, int32_t pin_newest,
+                                 uint16_t *scores_out, int64_t ld_scores, void *stream);
+
+dsa_status dsa_select_candidate_blocks_bf16(
+    const uint16_t *logits, int64_t rows, int64_t width, int64_t ld_logits,
+    const int32_t *row_ks, const int32_t *row_ke, int32_t topk_blocks,
+    int32_t block_size, int32_t row_repeat, int32_t pin_newest, int32_t *out,
+    int64_t ld_out, uint16_t *scores_out, int64_t ld_scores, void *workspace,
+    size_t workspace_bytes, void *stream);
+
+dsa_status dsa_select_candidate_blocks_sharded_bf16(
+    const uint16_t *logits, int32_t shards, int64_t rows, int64_t local_width,
+    int64_t ld_logits, int64_t shard_stride, const int32_t *global_row_ke,
+    int32_t global_block_size, int32_t max_global_blocks, int32_t row_repeat,
+    int32_t topk_blocks, int32_t *out, int64_t ld_out, uint16_t *scores_out,
+    int64_t ld_scores, void *workspace, size_t workspace_bytes, void *stream);
+
+dsa_status dsa_mask_candidate_logits_bf16(uint16_t *logits, int64_t rows, int64_t width,
+                                          int64_t ld_logits, const int32_t *row_ks,
+                                          const int32_t *row_ke,
+                                          const int32_t *candidates,
+                                          int32_t topk_blocks, int64_t ld_candidates,
+                                          int32_t block_size, int32_t row_repeat,
+                                          void *stream);
+
+dsa_status dsa_mask_candidate_logits_sharded_bf16(
+    uint16_t *logits, int32_t shards, int64_t rows, int64_t local_width,
+    int64_t ld_logits, int64_t shard_stride, const int32_t *global_row_ke,
+    int32_t global_block_size, int32_t row_repeat, const int32_t *candidates,
+    int32_t topk_blocks, int64_t ld_candidates, void *stream);
+
+/*
  * dsa_select_candidate_blocks_sharded_static -- dsa_select_candidate_blocks_
  * sharded without a caller-supplied workspace. The pages have no counterpart:
  * this entry point exists for callers that must not allocate device memory

@@ -70,6 +70,7 @@ class Workload:
     seed: int
     notes: dict = dataclasses.field(default_factory=dict)
     logical_width: Optional[int] = None
+    dtype: str = "f32"  # "bf16": the values lie on the bf16 grid, stored as bf16
 
     @property
     def rows(self) -> int:
@@ -100,6 +101,7 @@ class ShardedWorkload:
     row_repeat: int
     seed: int
     notes: dict = dataclasses.field(default_factory=dict)
+    dtype: str = "f32"  # "bf16": the values lie on the bf16 grid, stored as bf16
 
     @property
     def shards(self) -> int:
@@ -175,6 +177,7 @@ def random_nan_bits(rng: np.random.Generator, n: int) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 CONFIG_NAMES = ("tiny", "decode", "prefill", "long", "long_pin", "dcp")
+BF16_NAMES = ("decode_bf16", "dcp_bf16")
 
 
 def make_tiny(seed: int = 0) -> Workload:
@@ -287,6 +290,15 @@ def make(name: str):
         return make_long(pin_newest=True)
     if name == "dcp":
         return make_dcp()
+    if name == "decode_bf16":
+        wl = make_decode()  # already on the bf16 grid
+        wl.name, wl.dtype = "decode_bf16", "bf16"
+        return wl
+    if name == "dcp_bf16":
+        wl = make_dcp()
+        round_to_bf16_grid(wl.logits, inplace=True)
+        wl.name, wl.dtype = "dcp_bf16", "bf16"
+        return wl
     raise KeyError(name)
 
 
