@@ -97,6 +97,10 @@ def bind(path: str):
                                               p, i64, p, i64]
     lib.dsa_oracle_mask.argtypes = [p, i64, i64, i64, p, p, p, i64, i64, i32, i32]
     lib.dsa_oracle_mask_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32, p, i64, i64]
+    lib.dsa_oracle_select_sharded_starts.argtypes = [p, i32, i64, i64, i64, i64, p, p, i32, i32,
+                                                     i32, i32, p, i64, p, i64]
+    lib.dsa_oracle_mask_sharded_starts.argtypes = [p, i32, i64, i64, i64, i64, p, p, i32, i32,
+                                                   p, i64, i64]
     lib.dsa_oracle_block_scores_bf16.argtypes = lib.dsa_oracle_block_scores.argtypes
     lib.dsa_oracle_select_bf16.argtypes = lib.dsa_oracle_select.argtypes
     lib.dsa_oracle_select_sharded_bf16.argtypes = lib.dsa_oracle_select_sharded.argtypes
@@ -109,7 +113,8 @@ def bind(path: str):
               lib.dcp_oracle_correct_attn_out, lib.dcp_oracle_merge_attn_out,
               lib.dsa_oracle_block_scores_bf16, lib.dsa_oracle_select_bf16,
               lib.dsa_oracle_select_sharded_bf16, lib.dsa_oracle_mask_bf16,
-              lib.dsa_oracle_mask_sharded_bf16):
+              lib.dsa_oracle_mask_sharded_bf16, lib.dsa_oracle_select_sharded_starts,
+              lib.dsa_oracle_mask_sharded_starts):
         f.restype = ctypes.c_int
     return lib
 
@@ -212,6 +217,43 @@ def select_sharded(logits: np.ndarray, global_row_ke, global_block_size: int,
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (status {rc})")
     return out, scores
+
+
+def select_sharded_starts(logits: np.ndarray, global_row_ks, global_row_ke,
+                          global_block_size: int, max_global_blocks: int, topk_blocks: int,
+                          row_repeat: int = 1, want_scores: bool = True):
+    """``select_sharded`` with global window starts (reading R12): ids and the
+    merged global block scores."""
+    logits = _f32(logits)
+    shards, rows, lw = logits.shape
+    nbg = max(int(max_global_blocks), 1)
+    out = np.full((rows, topk_blocks), -7, dtype=np.int32)
+    scores = np.zeros((rows, nbg), dtype=np.float32) if want_scores else None
+    rc = _load().dsa_oracle_select_sharded_starts(
+        _ptr(logits), shards, rows, lw, lw, rows * lw, _ptr(_i32(global_row_ks)),
+        _ptr(_i32(global_row_ke)), global_block_size, max_global_blocks, row_repeat,
+        topk_blocks, _ptr(out), topk_blocks, _ptr(scores), nbg)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return out, scores
+
+
+def mask_sharded_starts(logits: np.ndarray, global_row_ks, global_row_ke,
+                        global_block_size: int, candidates: np.ndarray,
+                        row_repeat: int = 1) -> np.ndarray:
+    """Masked copy of a ``[shards, rows, local_width]`` layout with global
+    window starts (reading R12)."""
+    out = np.array(_f32(logits), copy=True)
+    shards, rows, lw = out.shape
+    cand = np.ascontiguousarray(candidates, dtype=np.int32)
+    topk = cand.shape[1] if cand.ndim == 2 else 0
+    rc = _load().dsa_oracle_mask_sharded_starts(
+        _ptr(out), shards, rows, lw, lw, rows * lw, _ptr(_i32(global_row_ks)),
+        _ptr(_i32(global_row_ke)), global_block_size, row_repeat, _ptr(cand), topk,
+        max(topk, 1))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return out
 
 
 def run_workload(wl, want_scores: bool = True):

@@ -37,6 +37,9 @@
  *      else 0 ([SG] interleave-1 placement).
  *   R8 masking (below): a logit outside its window or outside the row's
  *      candidate blocks becomes -inf; the rest are untouched.
+ *   R12 starts in the DCP form (below, select_sharded_impl): each shard's
+ *      window starts at its share of the global start, and blocks count
+ *      from there.
  *
  * Floating-point values are widened to double for every comparison; no
  * arithmetic is done on them, so the results are exact.
@@ -266,14 +269,25 @@ int dsa_oracle_select(const float *logits, int64_t rows, int64_t width,
  *   4. gke <= 0 makes every G[b] = -inf;
  *   5. selection with k = min(topk, nbg).
  */
-int dsa_oracle_select_sharded(const float *logits, int32_t shards,
-                              int64_t rows, int64_t local_width,
-                              int64_t ld_logits, int64_t shard_stride,
-                              const int32_t *global_row_ke,
-                              int32_t global_block_size,
-                              int32_t max_global_blocks, int32_t row_repeat,
-                              int32_t topk_blocks, int32_t *out,
-                              int64_t ld_out, float *scores, int64_t ld_scores)
+/*
+ * R12 (starts in the DCP form; the pages' DCP branch has no starts and pins
+ * (ends - 1) // gbs, which is this rule with a start of 0): a row's global
+ * window is [gs, ge) with ge = gke and gs = min(max(gks, 0), max(gke, 0)).
+ * Shard d holds the global tokens t with t % shards == d, so its window is
+ * local columns [ceil((gs - d) / shards), ceil((ge - d) / shards)) (each 0
+ * when the global bound is <= d), clamped to local_width. Global blocks are
+ * request-local (R1): block b covers tokens [gs + b*gbs, gs + (b+1)*gbs),
+ * and shard d's share of it is local block b counted from the shard's own
+ * window start. The pin is block (ge - gs - 1) // gbs, clamped to nbg - 1,
+ * and a row with ge <= gs selects nothing. Without starts (gks = 0) this is
+ * exactly steps 1-5 above.
+ */
+static int select_sharded_impl(const float *logits, int32_t shards, int64_t rows,
+                               int64_t local_width, int64_t ld_logits, int64_t shard_stride,
+                               const int32_t *global_row_ks, const int32_t *global_row_ke,
+                               int32_t global_block_size, int32_t max_global_blocks,
+                               int32_t row_repeat, int32_t topk_blocks, int32_t *out,
+                               int64_t ld_out, float *scores, int64_t ld_scores)
 {
     int64_t r, b, d, nbg, lbs, nlb, n_use;
     double *global_score, *local_score;
@@ -298,24 +312,28 @@ int dsa_oracle_select_sharded(const float *logits, int32_t shards,
     }
     for (r = 0; r < rows; ++r) {
         int64_t gke = (int64_t)global_row_ke[r / row_repeat];
+        int64_t gks = global_row_ks ? (int64_t)global_row_ks[r / row_repeat] : 0;
+        int64_t gs = imin64(imax64(gks, 0), imax64(gke, 0));
         int64_t pin;
         for (b = 0; b < nbg; ++b)
             global_score[b] = -INFINITY;
         for (d = 0; d < shards; ++d) {
             const float *row = logits + d * shard_stride + r * ld_logits;
+            int64_t lks = gs > d ? (gs - d + shards - 1) / shards : 0;
             int64_t lke = gke > d ? (gke - d + shards - 1) / shards : 0;
             int64_t e = imin64(lke, local_width);
+            int64_t s = imin64(lks, e);
             if (nlb == 0)
                 continue;
-            row_block_scores(row, 0, e, lbs, nlb, 0, local_score);
+            row_block_scores(row, s, e, lbs, nlb, 0, local_score);
             for (b = 0; b < n_use; ++b)
                 if (total_cmp(local_score[b], global_score[b]) > 0)
                     global_score[b] = local_score[b];
         }
-        pin = floor_div(gke - 1, global_block_size);
+        pin = floor_div(gke - gs - 1, global_block_size);
         pin = imin64(imax64(pin, 0), nbg - 1);
         global_score[pin] = INFINITY;
-        if (gke <= 0)
+        if (gke <= gs)
             for (b = 0; b < nbg; ++b)
                 global_score[b] = -INFINITY;
         if (scores)
@@ -327,6 +345,34 @@ int dsa_oracle_select_sharded(const float *logits, int32_t shards,
     free(local_score);
     free(tmp);
     return 0;
+}
+
+int dsa_oracle_select_sharded(const float *logits, int32_t shards,
+                              int64_t rows, int64_t local_width,
+                              int64_t ld_logits, int64_t shard_stride,
+                              const int32_t *global_row_ke,
+                              int32_t global_block_size,
+                              int32_t max_global_blocks, int32_t row_repeat,
+                              int32_t topk_blocks, int32_t *out,
+                              int64_t ld_out, float *scores, int64_t ld_scores)
+{
+    return select_sharded_impl(logits, shards, rows, local_width, ld_logits, shard_stride,
+                               NULL, global_row_ke, global_block_size, max_global_blocks,
+                               row_repeat, topk_blocks, out, ld_out, scores, ld_scores);
+}
+
+int dsa_oracle_select_sharded_starts(const float *logits, int32_t shards, int64_t rows,
+                                     int64_t local_width, int64_t ld_logits,
+                                     int64_t shard_stride, const int32_t *global_row_ks,
+                                     const int32_t *global_row_ke, int32_t global_block_size,
+                                     int32_t max_global_blocks, int32_t row_repeat,
+                                     int32_t topk_blocks, int32_t *out, int64_t ld_out,
+                                     float *scores, int64_t ld_scores)
+{
+    return select_sharded_impl(logits, shards, rows, local_width, ld_logits, shard_stride,
+                               global_row_ks, global_row_ke, global_block_size,
+                               max_global_blocks, row_repeat, topk_blocks, out, ld_out, scores,
+                               ld_scores);
 }
 
 /* ------------------------------------------------------------------ */
@@ -378,11 +424,11 @@ int dsa_oracle_mask(float *logits, int64_t rows, int64_t width, int64_t ld_logit
  * every shard ([CB] masking function: under DCP the local block size is
  * passed and the ids apply unchanged).
  */
-int dsa_oracle_mask_sharded(float *logits, int32_t shards, int64_t rows, int64_t local_width,
-                            int64_t ld_logits, int64_t shard_stride,
-                            const int32_t *global_row_ke, int32_t global_block_size,
-                            int32_t row_repeat, const int32_t *cand, int64_t topk,
-                            int64_t ld_cand)
+static int mask_sharded_impl(float *logits, int32_t shards, int64_t rows,
+                             int64_t local_width, int64_t ld_logits, int64_t shard_stride,
+                             const int32_t *global_row_ks, const int32_t *global_row_ke,
+                             int32_t global_block_size, int32_t row_repeat,
+                             const int32_t *cand, int64_t topk, int64_t ld_cand)
 {
     int64_t r, d, c, lbs;
     if (shards < 1 || rows < 0 || local_width < 0 || global_block_size < 1 ||
@@ -391,16 +437,47 @@ int dsa_oracle_mask_sharded(float *logits, int32_t shards, int64_t rows, int64_t
     lbs = global_block_size / shards;
     for (r = 0; r < rows; ++r) {
         int64_t gke = (int64_t)global_row_ke[r / row_repeat];
+        int64_t gks = global_row_ks ? (int64_t)global_row_ks[r / row_repeat] : 0;
+        int64_t gs = imin64(imax64(gks, 0), imax64(gke, 0));
         for (d = 0; d < shards; ++d) {
             float *row = logits + d * shard_stride + r * ld_logits;
+            int64_t lks = gs > d ? (gs - d + shards - 1) / shards : 0;
             int64_t lke = gke > d ? (gke - d + shards - 1) / shards : 0;
             int64_t e = imin64(lke, local_width);
+            int64_t s = imin64(lks, e);
             for (c = 0; c < local_width; ++c) {
-                int keep = c < e && is_candidate(cand + r * ld_cand, topk, c / lbs);
+                int keep = c >= s && c < e &&
+                           is_candidate(cand + r * ld_cand, topk, (c - s) / lbs);
                 if (!keep)
                     row[c] = -INFINITY;
             }
         }
     }
     return 0;
+}
+
+int dsa_oracle_mask_sharded(float *logits, int32_t shards, int64_t rows, int64_t local_width,
+                            int64_t ld_logits, int64_t shard_stride,
+                            const int32_t *global_row_ke, int32_t global_block_size,
+                            int32_t row_repeat, const int32_t *cand, int64_t topk,
+                            int64_t ld_cand)
+{
+    return mask_sharded_impl(logits, shards, rows, local_width, ld_logits, shard_stride, NULL,
+                             global_row_ke, global_block_size, row_repeat, cand, topk,
+                             ld_cand);
+}
+
+/* The DCP masking with starts (R12): shard d keeps the candidate blocks of
+ * its own window [ceil((gs - d) / shards), ceil((ge - d) / shards)), local
+ * blocks counted from that window's start. */
+int dsa_oracle_mask_sharded_starts(float *logits, int32_t shards, int64_t rows,
+                                   int64_t local_width, int64_t ld_logits,
+                                   int64_t shard_stride, const int32_t *global_row_ks,
+                                   const int32_t *global_row_ke, int32_t global_block_size,
+                                   int32_t row_repeat, const int32_t *cand, int64_t topk,
+                                   int64_t ld_cand)
+{
+    return mask_sharded_impl(logits, shards, rows, local_width, ld_logits, shard_stride,
+                             global_row_ks, global_row_ke, global_block_size, row_repeat, cand,
+                             topk, ld_cand);
 }

@@ -45,6 +45,23 @@ int dsa_oracle_mask_sharded(float *logits, int32_t shards, int64_t rows, int64_t
                             int32_t row_repeat, const int32_t *cand, int64_t topk,
                             int64_t ld_cand);
 
+/* The DCP form with global starts (reading R12 in dsa_oracle.c); a NULL
+ * global_row_ks is the same as the functions above. */
+int dsa_oracle_select_sharded_starts(const float *logits, int32_t shards, int64_t rows,
+                                     int64_t local_width, int64_t ld_logits,
+                                     int64_t shard_stride, const int32_t *global_row_ks,
+                                     const int32_t *global_row_ke, int32_t global_block_size,
+                                     int32_t max_global_blocks, int32_t row_repeat,
+                                     int32_t topk_blocks, int32_t *out, int64_t ld_out,
+                                     float *scores, int64_t ld_scores);
+
+int dsa_oracle_mask_sharded_starts(float *logits, int32_t shards, int64_t rows,
+                                   int64_t local_width, int64_t ld_logits,
+                                   int64_t shard_stride, const int32_t *global_row_ks,
+                                   const int32_t *global_row_ke, int32_t global_block_size,
+                                   int32_t row_repeat, const int32_t *cand, int64_t topk,
+                                   int64_t ld_cand);
+
 /* bf16 logits (dsa_oracle_bf16.c): the same definitions on the exact fp32
  * widening of the bf16 values; scores are bf16 bit patterns. */
 int dsa_oracle_block_scores_bf16(const uint16_t *logits, int64_t rows, int64_t width,

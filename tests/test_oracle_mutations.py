@@ -32,19 +32,32 @@ MUTATIONS = [
     ("block max drops NaN and ignores the zero sign", "if (total_cmp(x, m) > 0)\n                m = x;",
      "if (x > m)\n                m = x;"),
     ("shard end rounds down",
-     "(gke - d + shards - 1) / shards : 0;\n            int64_t e = imin64(lke, local_width);\n            if (nlb == 0)",
-     "(gke - d) / shards : 0;\n            int64_t e = imin64(lke, local_width);\n            if (nlb == 0)"),
-    ("global pin off by one", "pin = floor_div(gke - 1, global_block_size);",
-     "pin = floor_div(gke, global_block_size);"),
-    ("rows without context keep the pin", "if (gke <= 0)\n            for (b = 0; b < nbg; ++b)",
-     "if (gke < 0)\n            for (b = 0; b < nbg; ++b)"),
+     "(gke - d + shards - 1) / shards : 0;\n            int64_t e = imin64(lke, local_width);\n            int64_t s = imin64(lks, e);\n            if (nlb == 0)",
+     "(gke - d) / shards : 0;\n            int64_t e = imin64(lke, local_width);\n            int64_t s = imin64(lks, e);\n            if (nlb == 0)"),
+    ("global pin off by one", "pin = floor_div(gke - gs - 1, global_block_size);",
+     "pin = floor_div(gke - gs, global_block_size);"),
+    ("rows without context keep the pin", "if (gke <= gs)\n            for (b = 0; b < nbg; ++b)",
+     "if (gke < gs)\n            for (b = 0; b < nbg; ++b)"),
+    ("shard start rounds down",
+     "int64_t lks = gs > d ? (gs - d + shards - 1) / shards : 0;\n            int64_t lke = gke > d ? (gke - d + shards - 1) / shards : 0;\n            int64_t e = imin64(lke, local_width);\n            int64_t s = imin64(lks, e);\n            if (nlb == 0)",
+     "int64_t lks = gs > d ? (gs - d) / shards : 0;\n            int64_t lke = gke > d ? (gke - d + shards - 1) / shards : 0;\n            int64_t e = imin64(lke, local_width);\n            int64_t s = imin64(lks, e);\n            if (nlb == 0)"),
+    ("DCP pin ignores the start", "pin = floor_div(gke - gs - 1, global_block_size);",
+     "pin = floor_div(gke - 1, global_block_size);"),
+    ("DCP blocks counted from local column 0", "row_block_scores(row, s, e, lbs, nlb, 0, local_score);",
+     "row_block_scores(row, 0, e, lbs, nlb, 0, local_score);"),
+    ("DCP start not clamped at 0", "int64_t gs = imin64(imax64(gks, 0), imax64(gke, 0));\n        int64_t pin;",
+     "int64_t gs = imin64(gks, imax64(gke, 0));\n        int64_t pin;"),
+    ("DCP mask keeps columns before the shard start",
+     "int keep = c >= s && c < e &&\n                           is_candidate(cand + r * ld_cand, topk, (c - s) / lbs);",
+     "int keep = c < e &&\n                           is_candidate(cand + r * ld_cand, topk, (c - s) / lbs);"),
     ("shard merge takes the min", "if (total_cmp(local_score[b], global_score[b]) > 0)",
      "if (total_cmp(local_score[b], global_score[b]) < 0)"),
     ("canonical NaN not written", "uint32_t bits = 0x7FC00000u;", "uint32_t bits = 0x7FC00001u;"),
     ("mask uses absolute blocks", "is_candidate(cand + r * ld_cand, topk, (c - s) / block_size)",
      "is_candidate(cand + r * ld_cand, topk, c / block_size)"),
-    ("mask keeps columns before the window", "int keep = c >= s && c < e &&",
-     "int keep = c < e &&"),
+    ("mask keeps columns before the window",
+     "int keep = c >= s && c < e &&\n                       is_candidate(cand + r * ld_cand, topk, (c - s) / block_size);",
+     "int keep = c < e &&\n                       is_candidate(cand + r * ld_cand, topk, (c - s) / block_size);"),
     ("mask treats -1 as block 0", "if (cand[j] >= 0 && (int64_t)cand[j] == b)",
      "if ((int64_t)(cand[j] < 0 ? 0 : cand[j]) == b)"),
 ]
@@ -84,6 +97,18 @@ def _battery() -> list:
             mask_pins.test_mask_matches_brute_force(seed)
         except AssertionError:
             failed.append(f"mask-brute:{seed}")
+    import test_oracle_starts as starts
+    checks = [(f"starts-golden:{p.id}", lambda c=p.values[0]: starts.test_golden_starts_case(c))
+              for p in starts._cases()]
+    checks += [(f"starts-brute:{s}", lambda s=s: starts.test_sharded_starts_matches_brute_force(s))
+               for s in range(40)]
+    checks += [("starts-identity", lambda: starts.test_sharded_starts_equals_unsharded_on_global_rows(
+        2, 4, 7, 40, 1))]
+    for name, fn in checks:
+        try:
+            fn()
+        except AssertionError:
+            failed.append(name)
     return failed
 
 
