@@ -76,11 +76,17 @@ def window_elements(wl) -> int:
     if hasattr(wl, "global_row_ke"):
         rows = wl.rows
         g = np.repeat(wl.global_row_ke.astype(np.int64), wl.row_repeat)[:rows]
-        # shard d reads min(ceil((gke - d) / D), lw) columns
+        ks = getattr(wl, "global_row_ks", None)
+        gs = (np.zeros(rows, np.int64) if ks is None else
+              np.minimum(np.maximum(np.repeat(ks.astype(np.int64), wl.row_repeat)[:rows], 0),
+                         np.maximum(g, 0)))
+        # shard d reads columns [ceil((gs - d) / D), ceil((gke - d) / D)), clamped to lw
         total = 0
-        for d in range(wl.shards):
-            lke = np.where(g > d, (g - d + wl.shards - 1) // wl.shards, 0)
-            total += int(np.minimum(lke, wl.local_width).sum())
+        D = wl.shards
+        for d in range(D):
+            lke = np.minimum(np.where(g > d, (g - d + D - 1) // D, 0), wl.local_width)
+            lks = np.minimum(np.where(gs > d, (gs - d + D - 1) // D, 0), lke)
+            total += int((lke - lks).sum())
         return total
     rows, width = wl.rows, wl.width
     ke = np.repeat(wl.row_ke.astype(np.int64), wl.row_repeat)[:rows]
@@ -99,8 +105,10 @@ def esize(wl) -> int:
 def algorithmic_bytes(wl) -> int:
     """Bytes one call must move: in-window logits (fp32 or bf16), the int32
     bounds it reads, the int32 ids it writes."""
-    bounds = wl.global_row_ke.size if hasattr(wl, "global_row_ke") else (
-        wl.row_ke.size + (0 if wl.row_ks is None else wl.row_ks.size))
+    bounds = (wl.global_row_ke.size + (0 if getattr(wl, "global_row_ks", None) is None
+                                       else wl.global_row_ks.size)
+              if hasattr(wl, "global_row_ke") else
+              wl.row_ke.size + (0 if wl.row_ks is None else wl.row_ks.size))
     return esize(wl) * window_elements(wl) + 4 * bounds + 4 * wl.rows * wl.topk_blocks
 
 
@@ -271,10 +279,14 @@ def make_runner(wl, dsa, torch, device):
         ws = torch.zeros(dsa.workspace_bytes(wl.rows, max(wl.max_global_blocks, 1)),
                          dtype=torch.uint8, device=device)
 
+        gks = (None if getattr(wl, "global_row_ks", None) is None
+               else torch.from_numpy(wl.global_row_ks).to(device))
+
         def step():
             dsa.dsa_select_candidate_blocks_sharded(logits, gke, wl.global_block_size,
                                                     wl.max_global_blocks, wl.topk_blocks, out,
-                                                    wl.row_repeat, workspace=ws)
+                                                    wl.row_repeat, workspace=ws,
+                                                    global_row_ks=gks)
         return step, out
     logits = device_logits(wl, torch, device)
     ks = None if wl.row_ks is None else torch.from_numpy(wl.row_ks).to(device)
@@ -298,12 +310,17 @@ def mask_written_elements(wl, ids) -> int:
         D, rows, lw = wl.logits.shape
         lbs = wl.global_block_size // D
         g = np.repeat(wl.global_row_ke.astype(np.int64), wl.row_repeat)[:rows]
+        ks = getattr(wl, "global_row_ks", None)
+        gs = (np.zeros(rows, np.int64) if ks is None else
+              np.minimum(np.maximum(np.repeat(ks.astype(np.int64), wl.row_repeat)[:rows], 0),
+                         np.maximum(g, 0)))
         kept = 0
         for d in range(D):
             e = np.minimum(np.where(g > d, (g - d + D - 1) // D, 0), lw)
+            st = np.minimum(np.where(gs > d, (gs - d + D - 1) // D, 0), e)
             for j in range(ids.shape[1]):
                 b = ids[:, j].astype(np.int64)
-                lo = b * lbs
+                lo = st + b * lbs
                 kept += int(np.where(b >= 0, np.clip(np.minimum(lo + lbs, e) - lo, 0, None),
                                      0).sum())
         return D * rows * lw - kept
@@ -331,9 +348,12 @@ def make_mask_runner(wl, dsa, torch, device):
         logits = device_logits(wl, torch, device)
         gke = torch.from_numpy(wl.global_row_ke).to(device)
 
+        gks = (None if getattr(wl, "global_row_ks", None) is None
+               else torch.from_numpy(wl.global_row_ks).to(device))
+
         def step():
             dsa.dsa_mask_candidate_logits_sharded(logits, gke, wl.global_block_size, ids_dev,
-                                                  wl.row_repeat)
+                                                  wl.row_repeat, global_row_ks=gks)
     else:
         logits = device_logits(wl, torch, device)
         ks = None if wl.row_ks is None else torch.from_numpy(wl.row_ks).to(device)
@@ -434,12 +454,17 @@ def e2e_measure(wl, dsa, torch, device, steps: int):
     if sharded:
         h_b = [torch.from_numpy(wl.global_row_ke).pin_memory()]
         bufs["global_row_ke"] = torch.empty(h_b[0].shape, dtype=torch.int32, device=device)
+        h_ks = None
+        if getattr(wl, "global_row_ks", None) is not None:
+            h_ks = torch.from_numpy(wl.global_row_ks).pin_memory()
+            h_b.append(h_ks)
+            bufs["global_row_ks"] = torch.empty(h_ks.shape, dtype=torch.int32, device=device)
 
         def call():
             dsa.select_candidate_blocks_sharded_host(h_logits, h_b[0], wl.global_block_size,
                                                      wl.max_global_blocks, wl.topk_blocks,
                                                      wl.row_repeat, out=h_out,
-                                                     device_buffers=bufs)
+                                                     device_buffers=bufs, global_row_ks=h_ks)
     else:
         h_b = [None if wl.row_ks is None else torch.from_numpy(wl.row_ks).pin_memory(),
                torch.from_numpy(wl.row_ke).pin_memory()]
@@ -480,6 +505,21 @@ def oracle_cpu_baseline(wl, budget_s: float = 10.0):
     return el / reps, reps
 
 
+def oracle_mask(oracle, wl, ids):
+    """One masking pass of the oracle (the entry point for the workload's
+    layout and dtype) on a copy of the workload's logits."""
+    bf16 = esize(wl) == 2
+    if getattr(wl, "global_row_ks", None) is not None:
+        return oracle.mask_sharded_starts(wl.logits, wl.global_row_ks, wl.global_row_ke,
+                                          wl.global_block_size, ids, wl.row_repeat)
+    if hasattr(wl, "global_row_ke"):
+        return (oracle.mask_sharded_bf16 if bf16 else oracle.mask_sharded)(
+            wl.logits, wl.global_row_ke, wl.global_block_size, ids, wl.row_repeat)
+    return (oracle.mask_bf16 if bf16 else oracle.mask)(
+        wl.logits, wl.row_ks, wl.row_ke, ids, wl.block_size, wl.row_repeat,
+        width=wl.logits.shape[1])
+
+
 def oracle_mask_baseline(wl, ids, budget_s: float = 10.0):
     """The masking oracle as it stands, single-threaded, repeated over the
     whole workload until about budget_s seconds have passed."""
@@ -488,14 +528,7 @@ def oracle_mask_baseline(wl, ids, budget_s: float = 10.0):
     oracle.build()
     reps, t0 = 0, time.perf_counter()
     while True:
-        bf16 = esize(wl) == 2
-        if hasattr(wl, "global_row_ke"):
-            (oracle.mask_sharded_bf16 if bf16 else oracle.mask_sharded)(
-                wl.logits, wl.global_row_ke, wl.global_block_size, ids, wl.row_repeat)
-        else:
-            (oracle.mask_bf16 if bf16 else oracle.mask)(
-                wl.logits, wl.row_ks, wl.row_ke, ids, wl.block_size, wl.row_repeat,
-                        width=wl.width)
+        oracle_mask(oracle, wl, ids)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= 50:
@@ -538,6 +571,14 @@ def run_ours(args):
         flush = window_bytes < 2 * L2_BYTES
     scratch = torch.empty(256 * 1000 * 1000 // 4, dtype=torch.float32, device=device) if flush \
         else None
+    # Read-dominated steps (selection) also read a second 256 MB buffer after
+    # the flush write, so that the flush's own dirty lines are written back
+    # before the timed step rather than during it; write-heavy steps (masking,
+    # LSE) keep the write-only flush, so that their stores cannot sit in a
+    # clean L2 when the step ends.
+    clean = flush and args.op == "select"
+    scratch2 = torch.ones(256 * 1000 * 1000 // 4, dtype=torch.float32, device=device) \
+        if clean else None
 
     for _ in range(args.warmup):
         step()
@@ -565,6 +606,8 @@ def run_ours(args):
                    for _ in range(args.steps)]
             for a, b in evs:
                 scratch.fill_(1.0)
+                if clean:
+                    scratch2.amax()
                 a.record(stream)
                 one.replay()
                 b.record(stream)
@@ -635,7 +678,9 @@ def run_ours(args):
             "data": "synthetic (seeded numpy PCG64; shapes and distributions of the workload)",
             "config": {**config,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": ("flushed before every step (256 MB write)" if flush else
+                       "l2": ("flushed before every step (256 MB write, then 256 MB read of "
+                              "another buffer)" if clean else
+                              "flushed before every step (256 MB write)" if flush else
                               "inputs larger than L2 (bytes per step > 2 x 129 MB)")},
             "rows_per_s": round(rows_per_s, 1),
             "algorithmic_bytes_per_step": nbytes,
@@ -681,13 +726,7 @@ def run_reference(args):
     run_select = oracle.run_workload_bf16 if bf16 else oracle.run_workload
 
     def oracle_mask_step(w, ids):
-        if hasattr(w, "global_row_ke"):
-            (oracle.mask_sharded_bf16 if bf16 else oracle.mask_sharded)(
-                w.logits, w.global_row_ke, w.global_block_size, ids, w.row_repeat)
-        else:
-            (oracle.mask_bf16 if bf16 else oracle.mask)(
-                w.logits, w.row_ks, w.row_ke, ids, w.block_size, w.row_repeat,
-                        width=w.logits.shape[1])
+        oracle_mask(oracle, w, ids)
 
     def prepare(w):
         """(step, algorithmic bytes) of one oracle pass over workload w."""
@@ -804,6 +843,8 @@ def _row_slice(wl, r0: int, r1: int):
     if hasattr(wl, "global_row_ke"):
         s.logits = np.ascontiguousarray(wl.logits[:, r0:r1])
         s.global_row_ke = wl.global_row_ke[g0:g1].copy()
+        if getattr(wl, "global_row_ks", None) is not None:
+            s.global_row_ks = wl.global_row_ks[g0:g1].copy()
     else:
         s.logits = wl.logits[r0:r1]
         s.row_ke = wl.row_ke[g0:g1].copy()
@@ -823,7 +864,7 @@ def main(argv=None):
                         "LSE correction of one shard / merge of all shards")
     p.add_argument("--workload", default=None,
                    choices=("dcp", "decode", "prefill", "long", "long_pin", "tiny",
-                            "dcp_bf16", "decode_bf16") + tuple(LSE_NAMES),
+                            "dcp_bf16", "decode_bf16", "dcp_starts") + tuple(LSE_NAMES),
                    help="default: dcp for select / mask, lse_decode for correct / merge")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")

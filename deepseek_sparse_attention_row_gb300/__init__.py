@@ -71,6 +71,10 @@ EXPORTED_SYMBOLS = (
     "dsa_select_candidate_blocks_sharded_bf16",
     "dsa_mask_candidate_logits_bf16",
     "dsa_mask_candidate_logits_sharded_bf16",
+    "dsa_select_candidate_blocks_sharded_starts",
+    "dsa_select_candidate_blocks_sharded_starts_bf16",
+    "dsa_mask_candidate_logits_sharded_starts",
+    "dsa_mask_candidate_logits_sharded_starts_bf16",
 )
 
 _lib = None
@@ -117,16 +121,25 @@ def library():
                                          i64, i32, p, i64, i64, i64, p, i64, i64, p]
     lib.dsa_merge_attn_out.argtypes = [p, i32, i32, i64, i64, i64, i64, i64, i64, i64, p, i64,
                                        i64, i64, p, i64, i64, i64, p, i64, i64, p]
+    lib.dsa_select_candidate_blocks_sharded_starts.argtypes = [
+        p, i32, i64, i64, i64, i64, p, p, i32, i32, i32, i32, p, i64, p, i64, p, sz, p]
+    lib.dsa_mask_candidate_logits_sharded_starts.argtypes = [p, i32, i64, i64, i64, i64, p, p,
+                                                             i32, i32, p, i32, i64, p]
     for name in ("dsa_block_scores", "dsa_select_candidate_blocks",
                  "dsa_select_candidate_blocks_sharded", "dsa_mask_candidate_logits",
-                 "dsa_mask_candidate_logits_sharded"):
+                 "dsa_mask_candidate_logits_sharded", "dsa_select_candidate_blocks_sharded_starts",
+                 "dsa_mask_candidate_logits_sharded_starts"):
         getattr(lib, name + "_bf16").argtypes = getattr(lib, name).argtypes
     for f in (lib.dsa_block_scores, lib.dsa_select_candidate_blocks,
               lib.dsa_select_candidate_blocks_sharded, lib.dsa_mask_candidate_logits,
               lib.dsa_mask_candidate_logits_sharded, lib.dsa_correct_attn_out,
               lib.dsa_merge_attn_out, lib.dsa_block_scores_bf16,
               lib.dsa_select_candidate_blocks_bf16, lib.dsa_select_candidate_blocks_sharded_bf16,
-              lib.dsa_mask_candidate_logits_bf16, lib.dsa_mask_candidate_logits_sharded_bf16):
+              lib.dsa_mask_candidate_logits_bf16, lib.dsa_mask_candidate_logits_sharded_bf16,
+              lib.dsa_select_candidate_blocks_sharded_starts,
+              lib.dsa_select_candidate_blocks_sharded_starts_bf16,
+              lib.dsa_mask_candidate_logits_sharded_starts,
+              lib.dsa_mask_candidate_logits_sharded_starts_bf16):
         f.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -263,9 +276,10 @@ def dsa_select_candidate_blocks(logits, row_ks, row_ke, topk_blocks: int, block_
 def dsa_select_candidate_blocks_sharded(logits, global_row_ke, global_block_size: int,
                                         max_global_blocks: int, topk_blocks: int, out,
                                         row_repeat: int = 1, scores_out=None, stream=None,
-                                        workspace=None):
+                                        workspace=None, global_row_ks=None):
     """DCP form: ``logits`` is ``[D, rows, local_width]`` (unit stride in the last
-    dimension); writes ranked global block ids into ``out``.
+    dimension); writes ranked global block ids into ``out``. ``global_row_ks``
+    (optional) gives global window starts (the ``_starts`` C entry point).
     ``workspace``: see ``_workspace``."""
     torch = _torch()
     dt, sfx = _logits_kind(logits)
@@ -275,15 +289,19 @@ def dsa_select_candidate_blocks_sharded(logits, global_row_ke, global_block_size
                                   logits.device, handle)
     if logits.stride(2) != 1:
         raise ValueError("logits must have unit stride in its last dimension")
-    st = getattr(library(), "dsa_select_candidate_blocks_sharded" + sfx)(
+    name = "dsa_select_candidate_blocks_sharded" + ("_starts" if global_row_ks is not None
+                                                    else "") + sfx
+    starts = (_dev_ptr(global_row_ks, torch.int32, "global_row_ks"),) \
+        if global_row_ks is not None else ()
+    st = getattr(library(), name)(
         _dev_ptr(logits, dt, "logits"), shards, rows, lw, logits.stride(1),
-        logits.stride(0), _dev_ptr(global_row_ke, torch.int32, "global_row_ke"),
+        logits.stride(0), *starts, _dev_ptr(global_row_ke, torch.int32, "global_row_ke"),
         global_block_size, max_global_blocks, row_repeat, topk_blocks,
         _dev_ptr(out, torch.int32, "out"), _row_major(out, "out") if out.dim() == 2 else topk_blocks,
         _dev_ptr(scores_out, dt, "scores_out", allow_none=True),
         _row_major(scores_out, "scores_out") if scores_out is not None else 0,
         ws_ptr, ws_bytes, handle)
-    _check("dsa_select_candidate_blocks_sharded" + sfx, st)
+    _check(name, st)
     return out
 
 
@@ -307,22 +325,27 @@ def dsa_mask_candidate_logits(logits, row_ks, row_ke, candidates, block_size: in
 
 
 def dsa_mask_candidate_logits_sharded(logits, global_row_ke, global_block_size: int, candidates,
-                                      row_repeat: int = 1, stream=None):
-    """DCP form of ``dsa_mask_candidate_logits`` on ``[D, rows, local_width]``."""
+                                      row_repeat: int = 1, stream=None, global_row_ks=None):
+    """DCP form of ``dsa_mask_candidate_logits`` on ``[D, rows, local_width]``;
+    ``global_row_ks`` (optional) gives global window starts."""
     torch = _torch()
     dt, sfx = _logits_kind(logits)
     shards, rows, lw = logits.shape
     if logits.stride(2) != 1:
         raise ValueError("logits must have unit stride in its last dimension")
     topk = candidates.shape[1] if candidates is not None else 0
-    st = getattr(library(), "dsa_mask_candidate_logits_sharded" + sfx)(
+    name = "dsa_mask_candidate_logits_sharded" + ("_starts" if global_row_ks is not None
+                                                  else "") + sfx
+    starts = (_dev_ptr(global_row_ks, torch.int32, "global_row_ks"),) \
+        if global_row_ks is not None else ()
+    st = getattr(library(), name)(
         _dev_ptr(logits, dt, "logits"), shards, rows, lw, logits.stride(1),
-        logits.stride(0), _dev_ptr(global_row_ke, torch.int32, "global_row_ke"),
+        logits.stride(0), *starts, _dev_ptr(global_row_ke, torch.int32, "global_row_ke"),
         global_block_size, row_repeat,
         _dev_ptr(candidates, torch.int32, "candidates", allow_none=True), topk,
         _row_major(candidates, "candidates") if candidates is not None else 0,
         _stream_handle(stream))
-    _check("dsa_mask_candidate_logits_sharded" + sfx, st)
+    _check(name, st)
     return logits
 
 
@@ -451,20 +474,24 @@ def select_candidate_blocks_host(logits, row_ks, row_ke, topk_blocks: int, block
 def select_candidate_blocks_sharded_host(logits, global_row_ke, global_block_size: int,
                                          max_global_blocks: int, topk_blocks: int,
                                          row_repeat: int = 1, *, out=None,
-                                         device_buffers: Optional[dict] = None, stream=None):
+                                         device_buffers: Optional[dict] = None, stream=None,
+                                         global_row_ks=None):
     """Host-memory form of ``dsa_select_candidate_blocks_sharded`` (see
-    ``select_candidate_blocks_host``)."""
+    ``select_candidate_blocks_host``; ``device_buffers`` may also hold
+    'global_row_ke' and 'global_row_ks')."""
     torch = _torch()
     stream = torch.cuda.current_stream() if stream is None else stream
     db = device_buffers if device_buffers is not None else {}
     d_logits = _to_device(logits, db.get("logits"), stream)
     d_gke = _to_device(global_row_ke, db.get("global_row_ke"), stream)
+    d_gks = _to_device(global_row_ks, db.get("global_row_ks"), stream)
     rows = logits.shape[1]
     d_out = db.get("out")
     if d_out is None:
         d_out = torch.empty((rows, topk_blocks), dtype=torch.int32, device="cuda")
     dsa_select_candidate_blocks_sharded(d_logits, d_gke, global_block_size, max_global_blocks,
-                                        topk_blocks, d_out, row_repeat, stream=stream)
+                                        topk_blocks, d_out, row_repeat, stream=stream,
+                                        global_row_ks=d_gks)
     if out is None:
         out = torch.empty((rows, topk_blocks), dtype=torch.int32, pin_memory=True)
     with torch.cuda.stream(stream):

@@ -41,6 +41,11 @@ constexpr int32_t kSplitUnit = 32;  // blocks per unit of a row split
 constexpr int kMaxSplit = 8;        // CTAs per row at most
 constexpr int kThreads = 256;       // scores-only kernel
 
+// Row layouts of select_kernel.
+constexpr int kUnsharded = 0;       // [rows, ld], window [ks, ke)
+constexpr int kSharded = 1;         // [shards, rows, ld], windows from 0 (the pages' DCP form)
+constexpr int kShardedStarts = 2;   // [shards, rows, ld], windows from each shard's start
+
 struct SelectArgs {
   const void* logits;    // E::T elements
   int64_t ld;            // row stride (elements)
@@ -94,30 +99,21 @@ __device__ __forceinline__ bool arrive_last(uint32_t* counter, uint32_t split) {
   return false;
 }
 
-// Window of an unsharded row: e = min(ke, width), s = min(max(ks, 0), e).
-// Every thread computes the same plan from the row's bounds.
+// The streaming plan of one window: n elements starting at column s of a
+// row whose element 0 is at `base`; blocks counted from s; no pin. A window
+// off the 16-byte grid still reads 16-byte vectors when the block splits
+// into a power of two of them and the aligned base stays inside the row
+// (s >= shift).
 template <typename E>
-__device__ __forceinline__ RowPlan<E> plan_unsharded(const typename E::T* logits, int64_t ld,
-                                                     int32_t width, const int32_t* row_ks,
-                                                     const int32_t* row_ke, int32_t row_repeat,
-                                                     int32_t block_size, int32_t pin_newest,
-                                                     int64_t row) {
+__device__ __forceinline__ RowPlan<E> plan_window(const typename E::T* base, int32_t s,
+                                                  int32_t n, int32_t block_size) {
   constexpr int V16 = 16 / E::kBytes;  // elements per 16-byte vector
-  const int64_t g = row / row_repeat;
-  const int32_t ks = row_ks ? __ldg(row_ks + g) : 0;
-  const int32_t ke = __ldg(row_ke + g);
-  const int32_t e = min(ke, width);
-  const int32_t s = min(max(ks, 0), e);
-  const uint32_t n = e > s ? static_cast<uint32_t>(e - s) : 0u;
   RowPlan<E> p;
-  p.origin = logits + row * ld + s;
-  p.len_max = static_cast<int32_t>(n);
-  p.nblk = static_cast<int32_t>((n + static_cast<uint32_t>(block_size) - 1u) /
-                                static_cast<uint32_t>(block_size));
-  p.pin_block = (pin_newest && n > 0) ? static_cast<int32_t>((n - 1u) / block_size) : -1;
-  // A window off the 16-byte grid still reads 16-byte vectors when the block
-  // splits into a power of two of them and the aligned base stays inside the
-  // row (s >= shift).
+  p.origin = base + s;
+  p.len_max = n;
+  p.nblk = static_cast<int32_t>((static_cast<uint32_t>(n) + static_cast<uint32_t>(block_size) -
+                                 1u) / static_cast<uint32_t>(block_size));
+  p.pin_block = -1;
   p.shift = static_cast<int>((reinterpret_cast<uintptr_t>(p.origin) / E::kBytes) & (V16 - 1));
   const int32_t lpbv = block_size / V16;
   if (p.shift != 0 && s >= p.shift && block_size % V16 == 0 && (lpbv & (lpbv - 1)) == 0) {
@@ -129,6 +125,25 @@ __device__ __forceinline__ RowPlan<E> plan_unsharded(const typename E::T* logits
   return p;
 }
 
+// Window of an unsharded row: e = min(ke, width), s = min(max(ks, 0), e).
+// Every thread computes the same plan from the row's bounds.
+template <typename E>
+__device__ __forceinline__ RowPlan<E> plan_unsharded(const typename E::T* logits, int64_t ld,
+                                                     int32_t width, const int32_t* row_ks,
+                                                     const int32_t* row_ke, int32_t row_repeat,
+                                                     int32_t block_size, int32_t pin_newest,
+                                                     int64_t row) {
+  const int64_t g = row / row_repeat;
+  const int32_t ks = row_ks ? __ldg(row_ks + g) : 0;
+  const int32_t ke = __ldg(row_ke + g);
+  const int32_t e = min(ke, width);
+  const int32_t s = min(max(ks, 0), e);
+  const int32_t n = e > s ? e - s : 0;
+  RowPlan<E> p = plan_window<E>(logits + row * ld, s, n, block_size);
+  p.pin_block = (pin_newest && n > 0) ? (n - 1) / block_size : -1;
+  return p;
+}
+
 // Local end of shard d for global end gke: shard d holds the global tokens
 // t = shards*c + d, so those below gke are its first ceil((gke - d) / shards)
 // local columns; clamped to the local width.
@@ -137,6 +152,30 @@ __device__ __forceinline__ int32_t shard_len(int32_t gke, int32_t d, int32_t sha
   const uint32_t lke = (static_cast<uint32_t>(gke - d) + static_cast<uint32_t>(shards - 1)) /
                        static_cast<uint32_t>(shards);
   return static_cast<int32_t>(min(lke, static_cast<uint32_t>(lw)));
+}
+
+// A group of shards that share their window start (and so its alignment),
+// streamed 8 shards per slab with the group's plan: 16-, 8- or 4-byte
+// vectors, shifted 16-byte vectors, or elements.
+template <typename E>
+__device__ __forceinline__ void stream_group(const Window<E>& w, const RowPlan<E>& p,
+                                             int32_t block_size, int32_t b0, int32_t b1,
+                                             uint32_t* keys) {
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  constexpr int V16 = 16 / E::kBytes, V8 = 8 / E::kBytes, V4 = 4 / E::kBytes;
+  if (b0 >= b1) return;
+  if (p.vec == kVecShift)
+    stream_shift<E, 1, 8>(w, p.shift, p.lpb_log2, b0, b1, keys, 0, warp, nwarps);
+  else if (p.vec == V16)
+    stream_pow2<E, V16, 1, 8>(w, p.lpb_log2, b0, b1, keys, 0, warp, nwarps);
+  else if (p.vec == V8)
+    stream_pow2<E, V8, 2, 8>(w, p.lpb_log2, b0, b1, keys, 0, warp, nwarps);
+  else if (p.vec == V4 && V4 > 1)
+    stream_pow2<E, (V4 > 1 ? V4 : 2), 4, 8>(w, p.lpb_log2, b0, b1, keys, 0, warp, nwarps);
+  else if (p.vec == 1)
+    stream_pow2<E, 1, 4, 8>(w, p.lpb_log2, b0, b1, keys, 0, warp, nwarps);
+  else
+    stream_generic<E, 4, 8>(w, block_size, b0, b1, keys, 0, warp, nwarps);
 }
 
 // SVEC elements per vector (0: generic path); 8 shards per batch and NV
@@ -156,10 +195,10 @@ __device__ __forceinline__ void stream_sharded(const Window<E>& w, int lpb_log2,
 }
 
 // `a.split` CTAs per row.
-// SHARDED = false: unsharded rows, vector width chosen per row.
-// SHARDED = true: DCP rows; SVEC is the vector width fixed by the host
+// MODE kUnsharded: unsharded rows, vector width chosen per row.
+// MODE kSharded: DCP rows; SVEC is the vector width fixed by the host
 // (0 = generic path). T: threads per CTA.
-template <typename E, bool SHARDED, int SVEC, int T>
+template <typename E, int MODE, int SVEC, int T>
 __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a) {
   using TE = typename E::T;
   const TE* logits = static_cast<const TE*>(a.logits);
@@ -167,6 +206,7 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);  // [max(kpad, kRankMax)]
   uint32_t* keys = reinterpret_cast<uint32_t*>(cand + max(a.kpad, kRankMax));  // [nb]
   int32_t* len = reinterpret_cast<int32_t*>(keys + a.nb);                // [shards]
+  int32_t* start = len + a.shards;  // [shards], kShardedStarts only
   __shared__ TopkShared tsh;
   __shared__ int s_last;
 
@@ -175,7 +215,37 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   const int32_t part = static_cast<int32_t>(blockIdx.x % split);
 
   RowPlan<E> plan;
-  if constexpr (SHARDED) {
+  int32_t shard_q = 0, shard_rem = 0;  // kShardedStarts: gs = shard_q * shards + shard_rem
+  if constexpr (MODE == kShardedStarts) {
+    // Each shard's window [start[d], start[d] + len[d]) and its blocks
+    // count from start[d]; the vector width is chosen per shard later.
+    const int64_t g = row / a.row_repeat;
+    const int32_t gke = __ldg(a.row_ke + g);
+    const int32_t gs = min(max(__ldg(a.row_ks + g), 0), max(gke, 0));
+    shard_q = gs / a.shards;
+    shard_rem = gs % a.shards;
+    int32_t len_max = 0;
+    for (int d = 0; d < a.shards; ++d) {
+      const int32_t e = shard_len(gke, d, a.shards, a.width);
+      const int32_t st = min(shard_len(gs, d, a.shards, a.width), e);
+      len_max = max(len_max, e - st);
+      if (d % blockDim.x == threadIdx.x) {
+        len[d] = e - st;
+        start[d] = st;
+      }
+    }
+    plan.origin = logits + row * a.ld;
+    plan.len_max = len_max;
+    plan.nblk = min(static_cast<int32_t>((static_cast<uint32_t>(len_max) + a.block_size - 1u) /
+                                         static_cast<uint32_t>(a.block_size)),
+                    a.nb_data);
+    plan.pin_block = gke > gs ? static_cast<int32_t>(min(
+                                    static_cast<uint32_t>(gke - gs - 1) / a.global_block_size,
+                                    static_cast<uint32_t>(a.nb - 1)))
+                              : -1;
+    plan.vec = 0;
+    plan.lpb_log2 = 0;
+  } else if constexpr (MODE == kSharded) {
     const int32_t gke = __ldg(a.row_ke + row / a.row_repeat);
     const int32_t n0 = shard_len(gke, 0, a.shards, a.width);
     plan.origin = logits + row * a.ld;
@@ -212,14 +282,71 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   w.len = len;
   w.len_max = plan.len_max;
   if (b0 < b1) {
-    if constexpr (SHARDED)
+    if constexpr (MODE == kShardedStarts) {
+      // With gs = q * shards + rg, shards d < rg start at local column
+      // q + 1 and the others at q: two groups whose shards share a start.
+      // When the shard stride keeps 16-byte alignment, each group streams
+      // like the form without starts (all its shards per slab); the second
+      // group merges with atomicMax after a barrier. Otherwise every shard
+      // row streams on its own.
+      const int32_t rg = a.shards > 1 ? shard_rem : 0;
+      const bool grouped = (a.shard_stride * E::kBytes) % 16 == 0;
+      for (int grp = 0; grp < 2; ++grp) {
+        const int d_lo = grp == 0 ? rg : 0, d_hi = grp == 0 ? a.shards : rg;
+        if (d_lo >= d_hi) continue;
+        if (grouped) {
+          int32_t lmax = 0;
+          for (int d = d_lo; d < d_hi; ++d) lmax = max(lmax, len[d]);
+          const int32_t st = grp == 0 ? shard_q : shard_q + 1;
+          const int32_t st_c = min(st, a.width);
+          const RowPlan<E> pg = plan_window<E>(plan.origin + d_lo * a.shard_stride, st_c, lmax,
+                                               a.block_size);
+          Window<E> wg;
+          wg.origin = pg.origin;
+          wg.shard_stride = a.shard_stride;
+          wg.shards = d_hi - d_lo;
+          wg.len = len + d_lo;
+          wg.len_max = lmax;
+          wg.merge = grp == 1;
+          stream_group<E>(wg, pg, a.block_size, b0, min(b1, pg.nblk), keys);
+        } else {
+          for (int d = d_lo; d < d_hi; ++d) {
+            const RowPlan<E> pd = plan_window<E>(plan.origin + d * a.shard_stride, start[d],
+                                                 len[d], a.block_size);
+            Window<E> wd;
+            wd.origin = pd.origin;
+            wd.shard_stride = 0;
+            wd.shards = 1;
+            wd.len = len + d;
+            wd.len_max = len[d];
+            wd.merge = true;
+            stream_row(wd, pd.vec, pd.shift, pd.lpb_log2, a.block_size, b0,
+                       min(b1, pd.nblk), keys, 0, threadIdx.x >> 5, blockDim.x >> 5);
+          }
+        }
+        if (grp == 0) __syncthreads();
+      }
+    } else if constexpr (MODE == kSharded) {
       stream_sharded<E, SVEC>(w, plan.lpb_log2, a.block_size, b0, b1, keys);
-    else
+    } else {
       stream_row(w, plan.vec, plan.shift, plan.lpb_log2, a.block_size, b0, b1, keys, 0,
                  threadIdx.x >> 5, blockDim.x >> 5);
+    }
   }
   __syncthreads();
-  if constexpr (SHARDED) {
+  if constexpr (MODE == kShardedStarts) {
+    for (int d = threadIdx.x; d < a.shards; d += blockDim.x) {
+      const RowPlan<E> pd = plan_window<E>(plan.origin + d * a.shard_stride, start[d], len[d],
+                                           a.block_size);
+      Window<E> wd;
+      wd.origin = pd.origin;
+      wd.shard_stride = 0;
+      wd.shards = 1;
+      wd.len = len + d;
+      wd.len_max = len[d];
+      finish_row(wd, pd.vec, pd.shift, a.block_size, b0, min(b1, pd.nblk), keys, 0);
+    }
+  } else if constexpr (MODE == kSharded) {
     if constexpr (SVEC > 1)
       for (int d = threadIdx.x; d < a.shards; d += blockDim.x)
         commit_partial(load_partial<E, SVEC>(plan.origin + d * a.shard_stride, len[d],
@@ -483,12 +610,12 @@ dsa_status launch_select(K kernel, const SelectArgs& a, int64_t rows, int thread
 }
 
 // Instantiates the kernel for the chosen thread count.
-template <typename E, bool SHARDED, int SVEC>
+template <typename E, int MODE, int SVEC>
 dsa_status launch_shape(const SelectArgs& a, int64_t rows, const Shape& sh, size_t smem,
                         cudaStream_t stream) {
   if (sh.threads == 128)
-    return launch_select(select_kernel<E, SHARDED, SVEC, 128>, a, rows, 128, smem, stream);
-  return launch_select(select_kernel<E, SHARDED, SVEC, 256>, a, rows, 256, smem, stream);
+    return launch_select(select_kernel<E, MODE, SVEC, 128>, a, rows, 128, smem, stream);
+  return launch_select(select_kernel<E, MODE, SVEC, 256>, a, rows, 256, smem, stream);
 }
 
 // Fills the workspace fields of `a` for the chosen shape.
@@ -508,9 +635,11 @@ dsa_status fill_minus_one(int32_t* out, int64_t rows, int32_t cols, int64_t ld, 
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
 }
 
+// Dynamic shared memory of select_kernel: candidates, block keys, and the
+// shard lengths and starts.
 size_t select_smem(int32_t kpad, int32_t nb, int32_t shards) {
   return static_cast<size_t>(std::max(kpad, kRankMax)) * 8 + static_cast<size_t>(nb) * 4 +
-         static_cast<size_t>(shards) * 4;
+         static_cast<size_t>(shards) * 8;
 }
 
 }  // namespace
@@ -638,13 +767,14 @@ dsa_status select_impl(const typename E::T* logits, int64_t rows, int64_t width,
   const bool ws = workspace && workspace_size >= workspace_bytes(rows, a.nb);
   const Shape sh = choose_shape(row_bytes, rows, ws);
   attach_workspace(a, rows, workspace, sh);
-  return launch_shape<E, false, 0>(a, rows, sh, select_smem(a.kpad, a.nb, 1), s);
+  return launch_shape<E, kUnsharded, 0>(a, rows, sh, select_smem(a.kpad, a.nb, 1), s);
 }
 
 template <typename E>
 dsa_status select_sharded_impl(const typename E::T* logits, int32_t shards, int64_t rows,
                                int64_t local_width, int64_t ld_logits, int64_t shard_stride,
-                               const int32_t* global_row_ke, int32_t global_block_size,
+                               const int32_t* global_row_ks, const int32_t* global_row_ke,
+                               int32_t global_block_size,
                                int32_t max_global_blocks, int32_t row_repeat,
                                int32_t topk_blocks, int32_t* out, int64_t ld_out,
                                typename E::T* scores_out, int64_t ld_scores, void* workspace,
@@ -670,7 +800,7 @@ dsa_status select_sharded_impl(const typename E::T* logits, int32_t shards, int6
   a.shard_stride = shard_stride;
   a.shards = shards;
   a.width = static_cast<int32_t>(local_width);
-  a.row_ks = nullptr;
+  a.row_ks = global_row_ks;
   a.row_ke = global_row_ke;
   a.row_repeat = row_repeat;
   a.block_size = lbs;
@@ -699,14 +829,16 @@ dsa_status select_sharded_impl(const typename E::T* logits, int32_t shards, int6
   const Shape sh = choose_shape(local_width * E::kBytes * shards, rows, ws);
   attach_workspace(a, rows, workspace, sh);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // With starts every shard row is planned on its own in the kernel.
+  if (global_row_ks) return launch_shape<E, kShardedStarts, 0>(a, rows, sh, smem, s);
   constexpr int V16 = 16 / E::kBytes, V8 = 8 / E::kBytes, V4 = 4 / E::kBytes;
-  if (aligned(V16)) return launch_shape<E, true, V16>(a, rows, sh, smem, s);
-  if (aligned(V8)) return launch_shape<E, true, V8>(a, rows, sh, smem, s);
+  if (aligned(V16)) return launch_shape<E, kSharded, V16>(a, rows, sh, smem, s);
+  if (aligned(V8)) return launch_shape<E, kSharded, V8>(a, rows, sh, smem, s);
   if constexpr (V4 > 1) {
-    if (aligned(V4)) return launch_shape<E, true, V4>(a, rows, sh, smem, s);
+    if (aligned(V4)) return launch_shape<E, kSharded, V4>(a, rows, sh, smem, s);
   }
-  if (pow2(lbs)) return launch_shape<E, true, 1>(a, rows, sh, smem, s);
-  return launch_shape<E, true, 0>(a, rows, sh, smem, s);
+  if (pow2(lbs)) return launch_shape<E, kSharded, 1>(a, rows, sh, smem, s);
+  return launch_shape<E, kSharded, 0>(a, rows, sh, smem, s);
 }
 
 }  // namespace
@@ -766,7 +898,7 @@ dsa_status dsa_select_candidate_blocks_sharded(const float* logits, int32_t shar
                                                void* workspace, size_t workspace_size,
                                                void* stream) {
   return select_sharded_impl<F32>(logits, shards, rows, local_width, ld_logits, shard_stride,
-                                  global_row_ke, global_block_size, max_global_blocks,
+                                  nullptr, global_row_ke, global_block_size, max_global_blocks,
                                   row_repeat, topk_blocks, out, ld_out, scores_out, ld_scores,
                                   workspace, workspace_size, stream);
 }
@@ -778,9 +910,33 @@ dsa_status dsa_select_candidate_blocks_sharded_bf16(
     int64_t ld_out, uint16_t* scores_out, int64_t ld_scores, void* workspace,
     size_t workspace_size, void* stream) {
   return select_sharded_impl<BF16>(logits, shards, rows, local_width, ld_logits, shard_stride,
-                                   global_row_ke, global_block_size, max_global_blocks,
+                                   nullptr, global_row_ke, global_block_size, max_global_blocks,
                                    row_repeat, topk_blocks, out, ld_out, scores_out, ld_scores,
                                    workspace, workspace_size, stream);
+}
+
+dsa_status dsa_select_candidate_blocks_sharded_starts(
+    const float* logits, int32_t shards, int64_t rows, int64_t local_width, int64_t ld_logits,
+    int64_t shard_stride, const int32_t* global_row_ks, const int32_t* global_row_ke,
+    int32_t global_block_size, int32_t max_global_blocks, int32_t row_repeat,
+    int32_t topk_blocks, int32_t* out, int64_t ld_out, float* scores_out, int64_t ld_scores,
+    void* workspace, size_t workspace_size, void* stream) {
+  return select_sharded_impl<F32>(logits, shards, rows, local_width, ld_logits, shard_stride,
+                                  global_row_ks, global_row_ke, global_block_size,
+                                  max_global_blocks, row_repeat, topk_blocks, out, ld_out,
+                                  scores_out, ld_scores, workspace, workspace_size, stream);
+}
+
+dsa_status dsa_select_candidate_blocks_sharded_starts_bf16(
+    const uint16_t* logits, int32_t shards, int64_t rows, int64_t local_width, int64_t ld_logits,
+    int64_t shard_stride, const int32_t* global_row_ks, const int32_t* global_row_ke,
+    int32_t global_block_size, int32_t max_global_blocks, int32_t row_repeat,
+    int32_t topk_blocks, int32_t* out, int64_t ld_out, uint16_t* scores_out, int64_t ld_scores,
+    void* workspace, size_t workspace_size, void* stream) {
+  return select_sharded_impl<BF16>(logits, shards, rows, local_width, ld_logits, shard_stride,
+                                   global_row_ks, global_row_ke, global_block_size,
+                                   max_global_blocks, row_repeat, topk_blocks, out, ld_out,
+                                   scores_out, ld_scores, workspace, workspace_size, stream);
 }
 
 }  // extern "C"

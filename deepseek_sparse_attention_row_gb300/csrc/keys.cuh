@@ -51,6 +51,16 @@ __device__ __forceinline__ float max_nan(float a, float b, float c) {
   return d;
 }
 
+// Packed bf16 pairs: PTX max.NaN.bf16x2 takes the max of each 16-bit half
+// separately; checked on GB300 to order every pair of special values (signed
+// zeros, infinities, subnormals, NaNs of either sign) as the total order
+// above in both halves, with a NaN result whenever an operand is NaN.
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Read-only streaming loads: each logit is read once per call, so skip L1
 // allocation.
 __device__ __forceinline__ void ld_stream(const float* p, float (&x)[4]) {
@@ -161,6 +171,18 @@ __device__ __forceinline__ float fold(float acc, const Raw<E, VEC>& r) {
     for (int i = 0; i < Raw<E, VEC>::kWords; ++i)
       acc = max_nan(acc, __uint_as_float(r.w[i] << 16), __uint_as_float(r.w[i] & 0xFFFF0000u));
     return acc;
+  }
+}
+
+// Element-wise NaN-propagating max of two loaded vectors, into a.
+template <typename E, int VEC>
+__device__ __forceinline__ void raw_max(Raw<E, VEC>& a, const Raw<E, VEC>& b) {
+#pragma unroll
+  for (int i = 0; i < Raw<E, VEC>::kWords; ++i) {
+    if constexpr (E::kBytes == 4)
+      a.w[i] = __float_as_uint(max_nan(__uint_as_float(a.w[i]), __uint_as_float(b.w[i])));
+    else
+      a.w[i] = max_nan_bf16x2(a.w[i], b.w[i]);
   }
 }
 

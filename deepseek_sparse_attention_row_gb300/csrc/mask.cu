@@ -102,15 +102,19 @@ __global__ void __launch_bounds__(kMaskThreads) mask_kernel(const MaskArgs a) {
     e = min(ke, a.width);
     s = min(max(ks, 0), e);
   } else {
+    // Shard d holds the global tokens t with t % shards == d: its window is
+    // [ceil((gs - d) / shards), ceil((gke - d) / shards)), clamped to the
+    // local width, with gs the clamped global start (0 without starts).
     const int32_t gke = __ldg(a.row_ke + g);
-    s = 0;
-    e = 0;
-    if (gke > d) {
-      const uint32_t lke =
-          (static_cast<uint32_t>(gke - d) + static_cast<uint32_t>(a.shards - 1)) /
-          static_cast<uint32_t>(a.shards);
-      e = static_cast<int32_t>(min(lke, static_cast<uint32_t>(a.width)));
-    }
+    const int32_t gs = a.row_ks ? min(max(__ldg(a.row_ks + g), 0), max(gke, 0)) : 0;
+    auto local = [&](int32_t bound) -> int32_t {
+      if (bound <= d) return 0;
+      const uint32_t c = (static_cast<uint32_t>(bound - d) + static_cast<uint32_t>(a.shards - 1)) /
+                         static_cast<uint32_t>(a.shards);
+      return static_cast<int32_t>(min(c, static_cast<uint32_t>(a.width)));
+    };
+    e = local(gke);
+    s = min(local(gs), e);
   }
   const int32_t c0 = chunk * kMaskChunk;
   const int32_t c1 = min(c0 + kMaskChunk, a.width);
@@ -215,7 +219,8 @@ dsa_status mask_impl(typename E::T* logits, int64_t rows, int64_t width, int64_t
 template <typename E>
 dsa_status mask_sharded_impl(typename E::T* logits, int32_t shards, int64_t rows,
                              int64_t local_width, int64_t ld_logits, int64_t shard_stride,
-                             const int32_t* global_row_ke, int32_t global_block_size,
+                             const int32_t* global_row_ks, const int32_t* global_row_ke,
+                             int32_t global_block_size,
                              int32_t row_repeat, const int32_t* candidates, int32_t topk_blocks,
                              int64_t ld_candidates, void* stream) {
   if (shards < 1 || rows < 0 || local_width < 0 || global_block_size < 1 ||
@@ -233,7 +238,7 @@ dsa_status mask_sharded_impl(typename E::T* logits, int32_t shards, int64_t rows
   a.shards = shards;
   a.rows = rows;
   a.width = static_cast<int32_t>(local_width);
-  a.row_ks = nullptr;
+  a.row_ks = global_row_ks;
   a.row_ke = global_row_ke;
   a.row_repeat = row_repeat;
   a.block_size = global_block_size / shards;
@@ -274,7 +279,7 @@ extern "C" dsa_status dsa_mask_candidate_logits_sharded(
     int32_t row_repeat, const int32_t* candidates, int32_t topk_blocks, int64_t ld_candidates,
     void* stream) {
   return dsa::mask_sharded_impl<dsa::F32>(logits, shards, rows, local_width, ld_logits,
-                                          shard_stride, global_row_ke, global_block_size,
+                                          shard_stride, nullptr, global_row_ke, global_block_size,
                                           row_repeat, candidates, topk_blocks, ld_candidates,
                                           stream);
 }
@@ -285,7 +290,29 @@ extern "C" dsa_status dsa_mask_candidate_logits_sharded_bf16(
     int32_t row_repeat, const int32_t* candidates, int32_t topk_blocks, int64_t ld_candidates,
     void* stream) {
   return dsa::mask_sharded_impl<dsa::BF16>(logits, shards, rows, local_width, ld_logits,
-                                           shard_stride, global_row_ke, global_block_size,
+                                           shard_stride, nullptr, global_row_ke, global_block_size,
                                            row_repeat, candidates, topk_blocks, ld_candidates,
                                            stream);
+}
+
+extern "C" dsa_status dsa_mask_candidate_logits_sharded_starts(
+    float* logits, int32_t shards, int64_t rows, int64_t local_width, int64_t ld_logits,
+    int64_t shard_stride, const int32_t* global_row_ks, const int32_t* global_row_ke,
+    int32_t global_block_size, int32_t row_repeat, const int32_t* candidates,
+    int32_t topk_blocks, int64_t ld_candidates, void* stream) {
+  return dsa::mask_sharded_impl<dsa::F32>(logits, shards, rows, local_width, ld_logits,
+                                          shard_stride, global_row_ks, global_row_ke,
+                                          global_block_size, row_repeat, candidates, topk_blocks,
+                                          ld_candidates, stream);
+}
+
+extern "C" dsa_status dsa_mask_candidate_logits_sharded_starts_bf16(
+    uint16_t* logits, int32_t shards, int64_t rows, int64_t local_width, int64_t ld_logits,
+    int64_t shard_stride, const int32_t* global_row_ks, const int32_t* global_row_ke,
+    int32_t global_block_size, int32_t row_repeat, const int32_t* candidates,
+    int32_t topk_blocks, int64_t ld_candidates, void* stream) {
+  return dsa::mask_sharded_impl<dsa::BF16>(logits, shards, rows, local_width, ld_logits,
+                                           shard_stride, global_row_ks, global_row_ke,
+                                           global_block_size, row_repeat, candidates,
+                                           topk_blocks, ld_candidates, stream);
 }

@@ -237,7 +237,48 @@ dsa_status dsa_mask_candidate_logits_sharded(
     int32_t topk_blocks, int64_t ld_candidates, void *stream);
 
 /*
- * bf16 logits. The same five operations on bf16 logits, held as their 16-bit
+ * dsa_select_candidate_blocks_sharded_starts -- the DCP form with global
+ * window starts (the pages' DCP branch has none; its pin (ends - 1) // gbs is
+ * the start-0 case of the rule below). Row r's global window is [gs, ge)
+ * with ge = global_row_ke[r / row_repeat] and gs = min(max(global_row_ks[...],
+ * 0), max(ge, 0)). Shard d holds the global tokens t with t % shards == d,
+ * so its window is local columns [ceil((gs - d) / shards),
+ * ceil((ge - d) / shards)) (0 when the bound is <= d), clamped to
+ * local_width. Global blocks are request-local: block b covers tokens
+ * [gs + b*gbs, gs + (b+1)*gbs), which is local block b of every shard counted
+ * from the shard's own window start. The pin is block
+ * min((ge - gs - 1) // gbs, nbg - 1); a row with ge <= gs selects nothing.
+ * Local blocks past min(ceil(local_width / lbs), nbg) are dropped as in the
+ * form without starts. A NULL global_row_ks is the form without starts.
+ * Every other argument, limit and error is that of
+ * dsa_select_candidate_blocks_sharded. Each shard row is streamed on its own
+ * (its start sets its alignment), so rows with starts take a slightly slower
+ * path than rows without.
+ */
+dsa_status dsa_select_candidate_blocks_sharded_starts(
+    const float *logits, int32_t shards, int64_t rows, int64_t local_width,
+    int64_t ld_logits, int64_t shard_stride, const int32_t *global_row_ks,
+    const int32_t *global_row_ke, int32_t global_block_size,
+    int32_t max_global_blocks, int32_t row_repeat, int32_t topk_blocks,
+    int32_t *out, int64_t ld_out, float *scores_out, int64_t ld_scores,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * dsa_mask_candidate_logits_sharded_starts -- the DCP masking with global
+ * window starts: shard d keeps the columns of its window (as above) whose
+ * local block, counted from the shard's window start, is a candidate.
+ * Arguments and errors as for dsa_mask_candidate_logits_sharded, plus the
+ * nullable global_row_ks.
+ */
+dsa_status dsa_mask_candidate_logits_sharded_starts(
+    float *logits, int32_t shards, int64_t rows, int64_t local_width,
+    int64_t ld_logits, int64_t shard_stride, const int32_t *global_row_ks,
+    const int32_t *global_row_ke, int32_t global_block_size, int32_t row_repeat,
+    const int32_t *candidates, int32_t topk_blocks, int64_t ld_candidates,
+    void *stream);
+
+/*
+ * bf16 logits. The same operations on bf16 logits, held as their 16-bit
  * patterns (uint16_t, the layout of torch.bfloat16 / __nv_bfloat16). The page
  * allocates the block scores with the logits' dtype (_block_scores:
  * logits.new_empty), so scores_out is bf16 too: a block score is the
@@ -282,6 +323,21 @@ dsa_status dsa_mask_candidate_logits_sharded_bf16(
     int64_t ld_logits, int64_t shard_stride, const int32_t *global_row_ke,
     int32_t global_block_size, int32_t row_repeat, const int32_t *candidates,
     int32_t topk_blocks, int64_t ld_candidates, void *stream);
+
+dsa_status dsa_select_candidate_blocks_sharded_starts_bf16(
+    const uint16_t *logits, int32_t shards, int64_t rows, int64_t local_width,
+    int64_t ld_logits, int64_t shard_stride, const int32_t *global_row_ks,
+    const int32_t *global_row_ke, int32_t global_block_size,
+    int32_t max_global_blocks, int32_t row_repeat, int32_t topk_blocks,
+    int32_t *out, int64_t ld_out, uint16_t *scores_out, int64_t ld_scores,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+dsa_status dsa_mask_candidate_logits_sharded_starts_bf16(
+    uint16_t *logits, int32_t shards, int64_t rows, int64_t local_width,
+    int64_t ld_logits, int64_t shard_stride, const int32_t *global_row_ks,
+    const int32_t *global_row_ke, int32_t global_block_size, int32_t row_repeat,
+    const int32_t *candidates, int32_t topk_blocks, int64_t ld_candidates,
+    void *stream);
 
 /*
  * dsa_select_candidate_blocks_sharded_static -- dsa_select_candidate_blocks_

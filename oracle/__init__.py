@@ -258,6 +258,10 @@ def mask_sharded_starts(logits: np.ndarray, global_row_ks, global_row_ke,
 
 def run_workload(wl, want_scores: bool = True):
     """Run the oracle on a ``workloads.Workload`` or ``ShardedWorkload``."""
+    if getattr(wl, "global_row_ks", None) is not None:
+        return select_sharded_starts(wl.logits, wl.global_row_ks, wl.global_row_ke,
+                                     wl.global_block_size, wl.max_global_blocks, wl.topk_blocks,
+                                     wl.row_repeat, want_scores=want_scores)
     if hasattr(wl, "global_row_ke"):
         return select_sharded(wl.logits, wl.global_row_ke, wl.global_block_size,
                               wl.max_global_blocks, wl.topk_blocks, wl.row_repeat,

@@ -147,6 +147,46 @@ def test_bf16_sharded_sweep(env, seed):
         np.testing.assert_array_equal(s[:, :nbg], want_sc)
 
 
+@pytest.mark.parametrize("seed", range(10))
+def test_bf16_sharded_starts_sweep(env, seed):
+    """bf16 DCP form with global starts against the fp32 oracle on the
+    widened values (ids equal; bf16 scores are the fp32 scores' upper
+    halves)."""
+    torch, dsa = env
+    rng = np.random.default_rng(28000 + seed)
+    shards, lbs = int(rng.choice([2, 3, 8])), int(rng.choice([1, 2, 8, 16]))
+    lw, rows = int(rng.choice([5, 100, 2047, 8192])), int(rng.integers(1, 30))
+    nlb = -(-lw // lbs)
+    max_gb, topk = nlb, int(rng.choice([1, 8, 32]))
+    wl, _ = workloads.small_sharded(28000 + seed, shards=shards, rows=rows,
+                                    global_width=lw * shards, global_block_size=lbs * shards,
+                                    max_global_blocks=max_gb, topk_blocks=topk)
+    bits = to_bf16_bits(wl.logits)
+    gks = rng.integers(-3, shards * lw + 3, size=rows).astype(np.int32)
+    gks[::2] = np.minimum(gks[::2], wl.global_row_ke[::2] - 1)
+    want_ids, want_sc = oracle.select_sharded_starts(widen(bits), gks, wl.global_row_ke,
+                                                     lbs * shards, max_gb, topk)
+    local = dev_bf16(torch, bits, int(rng.choice([0, 1, 5])))
+    for ws in (None, False):
+        out = torch.full((rows, topk), SENTINEL_ID, dtype=torch.int32, device="cuda")
+        sc = torch.empty((rows, max_gb), dtype=torch.bfloat16, device="cuda")
+        dsa.dsa_select_candidate_blocks_sharded(local, _dev(torch, wl.global_row_ke),
+                                                lbs * shards, max_gb, topk, out, scores_out=sc,
+                                                workspace=ws, global_row_ks=_dev(torch, gks))
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out.cpu().numpy(), want_ids)
+        np.testing.assert_array_equal(host_bits(sc),
+                                      (want_sc.view(np.uint32) >> 16).astype(np.uint16))
+    cand = rng.integers(-1, nlb + 1, size=(rows, 4)).astype(np.int32)
+    want_mask = oracle.mask_sharded_starts(widen(bits), gks, wl.global_row_ke, lbs * shards,
+                                           cand)
+    dsa.dsa_mask_candidate_logits_sharded(local, _dev(torch, wl.global_row_ke), lbs * shards,
+                                          _dev(torch, cand), global_row_ks=_dev(torch, gks))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host_bits(local),
+                                  (want_mask.view(np.uint32) >> 16).astype(np.uint16))
+
+
 @pytest.mark.parametrize("seed", range(8))
 def test_bf16_block_scores_sweep(env, seed):
     torch, dsa = env

@@ -167,6 +167,82 @@ def test_sharded_sweep(env, seed):
     check_sharded(env, wl, offset=int(rng.choice([0, 0, 1, 2])))
 
 
+def _run_sharded_starts(env, local, gks, gke, gbs, max_gb, topk, rr, workspace):
+    torch, dsa = env
+    D, rows, lw = local.shape
+    nbg = max(max_gb, 1)
+    out = torch.full((rows, topk + GUARD), SENTINEL_ID, dtype=torch.int32, device="cuda")
+    sc = torch.full((rows, nbg + GUARD), float(SENTINEL_SCORE), dtype=torch.float32,
+                    device="cuda")
+    dsa.dsa_select_candidate_blocks_sharded(local, _dev(torch, gke), gbs, max_gb, topk,
+                                            out[:, :topk], rr, scores_out=sc[:, :nbg],
+                                            workspace=workspace, global_row_ks=_dev(torch, gks))
+    torch.cuda.synchronize()
+    o, c = out.cpu().numpy(), sc.cpu().numpy()
+    assert (o[:, topk:] == SENTINEL_ID).all() and (c[:, nbg:] == SENTINEL_SCORE).all()
+    return o[:, :topk], c[:, :nbg]
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_sharded_starts_sweep(env, seed):
+    """The DCP form with global window starts: each shard streams its own
+    window (its start sets its alignment) and the keys merge."""
+    torch, dsa = env
+    rng = np.random.default_rng(27000 + seed)
+    shards = int(rng.choice([1, 2, 3, 4, 8, 8, 16]))
+    lbs = int(rng.choice([1, 2, 3, 4, 8, 8, 16, 32]))
+    gbs = lbs * shards
+    lw = int(rng.choice([1, 5, 64, 100, 1024, 2047, 8192]))
+    nlb = -(-lw // lbs)
+    max_gb = int(min(rng.choice([0, 1, max(nlb // 2, 1), nlb, nlb + 7]), 16384))
+    rows, rr = int(rng.integers(1, 40)), int(rng.choice([1, 1, 2, 5]))
+    nbg = max(max_gb, 1)
+    topk = int(rng.choice([1, 8, 32, 40, nbg, nbg + 3]))
+    wl, _ = workloads.small_sharded(27000 + seed, shards=shards, rows=rows,
+                                    global_width=lw * shards, global_block_size=gbs,
+                                    max_global_blocks=max_gb, topk_blocks=topk, row_repeat=rr,
+                                    wild_bounds=bool(rng.integers(0, 2)))
+    groups = -(-rows // rr)
+    gks = rng.integers(-4, shards * lw + 6, size=groups).astype(np.int32)
+    gks[::3] = np.minimum(gks[::3], wl.global_row_ke[::3] - 1)  # mostly non-empty windows
+    want_ids, want_sc = oracle.select_sharded_starts(wl.logits, gks, wl.global_row_ke, gbs,
+                                                     max_gb, topk, rr)
+    offset = int(rng.choice([0, 1, 2, 3]))
+    buf = torch.full((shards * rows * lw + offset + 8,), 1e30, dtype=torch.float32,
+                     device="cuda")
+    local = buf[offset:offset + shards * rows * lw].view(shards, rows, lw)
+    local.copy_(torch.from_numpy(wl.logits))
+    for ws in (None, False):
+        ids, sc = _run_sharded_starts(env, local, gks, wl.global_row_ke, gbs, max_gb, topk, rr,
+                                      ws)
+        np.testing.assert_array_equal(ids, want_ids)
+        assert_bits_equal(sc, want_sc)
+    cand = rng.integers(-1, nlb + 2, size=(rows, 6)).astype(np.int32)
+    want_mask = oracle.mask_sharded_starts(wl.logits, gks, wl.global_row_ke, gbs, cand, rr)
+    dsa.dsa_mask_candidate_logits_sharded(local, _dev(torch, wl.global_row_ke), gbs,
+                                          _dev(torch, cand), rr, global_row_ks=_dev(torch, gks))
+    torch.cuda.synchronize()
+    assert_bits_equal(local.cpu().numpy(), want_mask)
+
+
+@pytest.mark.slow
+def test_sharded_starts_full_size(env):
+    """The DCP workload with request starts drawn uniform in [0, gke]."""
+    torch, dsa = env
+    wl = workloads.make("dcp")
+    rng = np.random.default_rng(4004)
+    gks = (rng.random(wl.global_row_ke.size) * (wl.global_row_ke + 1)).astype(np.int32)
+    want_ids, want_sc = oracle.select_sharded_starts(wl.logits, gks, wl.global_row_ke,
+                                                     wl.global_block_size, wl.max_global_blocks,
+                                                     wl.topk_blocks)
+    local = torch.from_numpy(wl.logits).cuda()
+    for ws in (None, False):
+        ids, sc = _run_sharded_starts(env, local, gks, wl.global_row_ke, wl.global_block_size,
+                                      wl.max_global_blocks, wl.topk_blocks, 1, ws)
+        np.testing.assert_array_equal(ids, want_ids)
+        assert_bits_equal(sc, want_sc)
+
+
 @pytest.mark.parametrize("seed", range(12))
 def test_block_scores_sweep(env, seed):
     torch, dsa = env

@@ -102,6 +102,7 @@ class ShardedWorkload:
     seed: int
     notes: dict = dataclasses.field(default_factory=dict)
     dtype: str = "f32"  # "bf16": the values lie on the bf16 grid, stored as bf16
+    global_row_ks: Optional[np.ndarray] = None  # global window starts (None: all 0)
 
     @property
     def shards(self) -> int:
@@ -178,6 +179,7 @@ def random_nan_bits(rng: np.random.Generator, n: int) -> np.ndarray:
 
 CONFIG_NAMES = ("tiny", "decode", "prefill", "long", "long_pin", "dcp")
 BF16_NAMES = ("decode_bf16", "dcp_bf16")
+EXTRA_NAMES = BF16_NAMES + ("dcp_starts",)
 
 
 def make_tiny(seed: int = 0) -> Workload:
@@ -290,6 +292,15 @@ def make(name: str):
         return make_long(pin_newest=True)
     if name == "dcp":
         return make_dcp()
+    if name == "dcp_starts":
+        # The DCP workload with a request start per row, uniform in [0, gke]
+        # (window lengths uniform in [0, gke], so about half the bytes).
+        wl = make_dcp()
+        rng = _rng(40)
+        g = wl.global_row_ke.astype(np.int64)
+        wl.global_row_ks = rng.integers(0, g + 1).astype(np.int32)
+        wl.name = "dcp_starts"
+        return wl
     if name == "decode_bf16":
         wl = make_decode()  # already on the bf16 grid
         wl.name, wl.dtype = "decode_bf16", "bf16"
