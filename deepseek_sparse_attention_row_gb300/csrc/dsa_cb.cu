@@ -155,8 +155,9 @@ __device__ __forceinline__ int32_t shard_len(int32_t gke, int32_t d, int32_t sha
 }
 
 // A group of shards that share their window start (and so its alignment),
-// streamed 8 shards per slab with the group's plan: 16-, 8- or 4-byte
-// vectors, shifted 16-byte vectors, or elements.
+// streamed 8 shards per slab with the group's plan (16-, 8- or 4-byte
+// vectors, or elements), or 4 shards and 2 vectors per lane for shifted
+// 16-byte vectors (measured faster than 8 x 1 there, which spills).
 template <typename E>
 __device__ __forceinline__ void stream_group(const Window<E>& w, const RowPlan<E>& p,
                                              int32_t block_size, int32_t b0, int32_t b1,
@@ -164,9 +165,18 @@ __device__ __forceinline__ void stream_group(const Window<E>& w, const RowPlan<E
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   constexpr int V16 = 16 / E::kBytes, V8 = 8 / E::kBytes, V4 = 4 / E::kBytes;
   if (b0 >= b1) return;
-  if (p.vec == kVecShift)
-    stream_shift<E, 1, 8>(w, p.shift, p.lpb_log2, b0, b1, keys, 0, warp, nwarps);
-  else if (p.vec == V16)
+  if (p.vec == kVecShift) {
+    ShiftGroups<E> sg;
+    sg.base[0] = sg.base[1] = p.origin - p.shift;
+    sg.r[0] = sg.r[1] = p.shift;
+    sg.split = 0;
+    sg.shard_stride = w.shard_stride;
+    sg.shards = w.shards;
+    sg.len = w.len;
+    sg.v_cap = (w.len_max + p.shift) / V16;
+    sg.merge = w.merge;
+    stream_shift<E, 2, 4>(sg, p.lpb_log2, b0, b1, keys, 0, warp, nwarps);
+  } else if (p.vec == V16)
     stream_pow2<E, V16, 1, 8>(w, p.lpb_log2, b0, b1, keys, 0, warp, nwarps);
   else if (p.vec == V8)
     stream_pow2<E, V8, 2, 8>(w, p.lpb_log2, b0, b1, keys, 0, warp, nwarps);
@@ -291,7 +301,36 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
       // row streams on its own.
       const int32_t rg = a.shards > 1 ? shard_rem : 0;
       const bool grouped = (a.shard_stride * E::kBytes) % 16 == 0;
-      for (int grp = 0; grp < 2; ++grp) {
+      // One pass over both groups (stream_shift with two offsets) when the
+      // block is a power of two of 16-byte vectors and each group's aligned
+      // base stays inside its rows.
+      constexpr int V16 = 16 / E::kBytes;
+      const int32_t lpbv = a.block_size / V16;
+      bool paired = grouped && a.block_size % V16 == 0 && (lpbv & (lpbv - 1)) == 0;
+      ShiftGroups<E> sg;
+      if (paired) {
+        for (int g = 0; g < 2; ++g) {
+          const int32_t st = min(g == 0 ? shard_q : shard_q + 1, a.width);
+          const TE* o = plan.origin + st;
+          const int32_t r = static_cast<int32_t>((reinterpret_cast<uintptr_t>(o) / E::kBytes) &
+                                                 (V16 - 1));
+          paired = paired && st >= r;
+          sg.base[g] = o - r;
+          sg.r[g] = r;
+        }
+        sg.split = rg;
+        sg.shard_stride = a.shard_stride;
+        sg.shards = a.shards;
+        sg.len = len;
+        sg.merge = false;
+        int32_t cap = 0;
+        for (int d = 0; d < a.shards; ++d) cap = max(cap, (len[d] + sg.r[d < rg ? 1 : 0]) / V16);
+        sg.v_cap = cap;
+      }
+      if (paired)
+        stream_shift<E, 1, 8>(sg, __ffs(lpbv) - 1, b0, b1, keys, 0, threadIdx.x >> 5,
+                              blockDim.x >> 5);
+      for (int grp = 0; grp < 2 && !paired; ++grp) {
         const int d_lo = grp == 0 ? rg : 0, d_hi = grp == 0 ? a.shards : rg;
         if (d_lo >= d_hi) continue;
         if (grouped) {

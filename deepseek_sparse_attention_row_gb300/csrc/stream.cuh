@@ -148,57 +148,163 @@ __device__ __forceinline__ void stream_pow2(const Window<E>& w, int lpb_log2, in
   }
 }
 
-// Windows whose start lies r = 1..VEC-1 elements past a 16-byte boundary
-// (VEC = 16-byte vector in elements: 4 fp32 or 8 bf16), block size a
-// power-of-two multiple of VEC (LPB = block_size / VEC a power of two), for
-// SB shards at a time that share that offset. Loads aligned 16-byte vectors
-// from base = origin - r. Vector v of base covers window elements
+// One unsharded window whose start lies r = 1..VEC-1 elements past a 16-byte
+// boundary (the same layout as stream_shift below, one row): each lane folds
+// a hi and a lo part per vector, and a lead vector's lo part is merged into
+// the block before with atomicMax; the hi parts reduce per block and merge
+// with atomicMax. Measured on GB300 against the shuffle merge of
+// stream_shift with one shard: equal on prefill-like rows, and faster on
+// long rows and for the rest of the kernel (decode rows do not use it but
+// share the kernel's registers).
+template <typename E, int NV>
+__device__ __forceinline__ void stream_shift_row(const typename E::T* origin, int32_t r,
+                                                 int32_t len, int lpb_log2, int32_t b0, int32_t b1,
+                                                 uint32_t* __restrict__ keys, int32_t kbase,
+                                                 int warp, int nwarps) {
+  constexpr int VEC = 16 / E::kBytes;
+  const int lane = threadIdx.x & 31;
+  const int lpb = 1 << lpb_log2;
+  const typename E::T* base = origin - r;
+  const int32_t nvec = (len + r) / VEC;  // whole vectors of base inside [base, origin + len)
+  const int32_t v_begin = static_cast<int32_t>(static_cast<int64_t>(b0) << lpb_log2);
+  const int32_t v_end = static_cast<int32_t>(min((static_cast<int64_t>(b1) << lpb_log2) + 1,
+                                                 static_cast<int64_t>(nvec)));
+  constexpr int32_t kSlab = 32 * NV;
+  const int32_t step = nwarps * kSlab;
+  for (int32_t slab = v_begin + warp * kSlab; slab < v_end; slab += step) {
+    Raw<E, VEC> x[NV];
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      const int32_t v = slab + m * 32 + lane;
+      if (v < v_end)
+        ld_raw<E, VEC>(base + static_cast<int64_t>(v) * VEC, x[m]);
+      else
+        raw_neg_inf(x[m]);
+    }
+    float hi[NV], lo[NV];
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      const int32_t v = slab + m * 32 + lane;
+      const bool lead = (v & (lpb - 1)) == 0;
+      hi[m] = neg_inf();
+      lo[m] = neg_inf();
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const bool below = lead && i < r;
+        const float xi = raw_elem(x[m], i);
+        hi[m] = max_nan(hi[m], below ? neg_inf() : xi);
+        lo[m] = max_nan(lo[m], below ? xi : neg_inf());
+      }
+    }
+    // lo parts: the lead lane of each block sends them to the block before.
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      const int32_t v = slab + m * 32 + lane;
+      const int32_t blk = (v >> lpb_log2) - 1;
+      if ((v & (lpb - 1)) == 0 && v < v_end && blk >= b0 && blk < b1)
+        atomicMax(&keys[blk - kbase], order_key(lo[m]));
+    }
+    // hi parts, reduced per block as in the aligned path.
+    if (lpb_log2 >= 5) {
+      float carry = neg_inf();
+#pragma unroll
+      for (int m = 0; m < NV; ++m) {
+        carry = max_nan(carry, hi[m]);
+        const int32_t blk = (slab + m * 32) >> lpb_log2;
+        const bool last = (m == NV - 1) || (((slab + (m + 1) * 32) >> lpb_log2) != blk);
+        if (last) {
+          if (blk < b1) {
+            const uint32_t k = __reduce_max_sync(0xffffffffu, order_key(carry));
+            if (lane == 0) atomicMax(&keys[blk - kbase], k);
+          }
+          carry = neg_inf();
+        }
+      }
+    } else {
+#pragma unroll
+      for (int m = 0; m < NV; ++m) {
+        const int32_t vfirst = slab + m * 32;
+        if (vfirst >= v_end) break;
+        uint32_t k = order_key(hi[m]);
+        for (int o = 1; o < lpb; o <<= 1) k = max(k, __shfl_xor_sync(0xffffffffu, k, o));
+        const int32_t v = vfirst + lane;
+        const int32_t blk = v >> lpb_log2;
+        if ((lane & (lpb - 1)) == 0 && v < v_end && blk < b1) atomicMax(&keys[blk - kbase], k);
+      }
+    }
+  }
+}
+
+
+// Shard rows of the DCP form with starts (up to two groups of shards, each
+// group sharing its window start and so its offset r = 0..VEC-1 past a
+// 16-byte boundary; VEC = 16-byte vector in elements, 4 fp32 or 8 bf16),
+// block size a power-of-two multiple of VEC (LPB = block_size / VEC a power
+// of two). Each shard loads aligned 16-byte vectors from its base
+// origin - r. Vector v of a shard covers its window elements
 // [VEC*v - r, VEC*v - r + VEC); all of them belong to block v / LPB except,
 // in the block's first vector (v % LPB == 0), the r elements below the block
 // boundary, which belong to block v / LPB - 1 (and, for v = 0, precede the
-// window and are dropped). Each lane folds its vectors over shards into a
-// "hi" value for block v / LPB and, in a block's first vector, a "lo" value
-// for the block before. A lo value joins the hi value of vector v - 1, which
-// the next lane down (or lane 31 of the previous instruction) holds, through
-// one shuffle; only the lo value of a slab's first vector crosses to another
-// warp's slab and is merged with atomicMax. With several blocks per
-// instruction (LPB < 32) a slab's last block is therefore the one block
-// written with atomicMax (every block when `merge`); larger blocks span
-// slabs and are always merged with atomicMax. Vector b1 * LPB is read only
-// for its lo part (it completes block b1 - 1).
-// Elements past the last whole vector are left to commit_partial_shifted.
+// window and are dropped). Because blocks count from each shard's own
+// start, vector v maps to the same blocks in both groups: the shards of a
+// group are folded element-wise, each group's vector is split at its own r
+// into a "hi" value for block v / LPB and, in a block's first vector, a "lo"
+// value for the block before, and the two groups' parts are combined.
+// A lo value joins the hi value of vector v - 1, which the next lane down
+// (or lane 31 of the previous instruction) holds, through one shuffle; only
+// the lo value of a slab's first vector crosses to another warp's slab and
+// is merged with atomicMax. With several blocks per instruction (LPB < 32) a
+// slab's last block is therefore the one block written with atomicMax (every
+// block when `merge`); larger blocks span slabs and are always merged with
+// atomicMax. Vector b1 * LPB is read only for its lo part (it completes
+// block b1 - 1). Elements past each shard's last whole vector are left to
+// commit_partial_shifted.
+template <typename E>
+struct ShiftGroups {
+  const typename E::T* base[2];  // aligned base of shard 0's row for each group
+  int32_t r[2];                  // the groups' offsets
+  int32_t split;                 // shards [0, split) belong to group 1, the rest to group 0
+  int64_t shard_stride;
+  int32_t shards;
+  const int32_t* len;            // shared memory: in-window length of each shard
+  int32_t v_cap;                 // max over shards of (len + r) / VEC
+  bool merge;
+};
+
 template <typename E, int NV, int SB>
-__device__ __forceinline__ void stream_shift(const Window<E>& w, int32_t r, int lpb_log2,
-                                             int32_t b0, int32_t b1, uint32_t* __restrict__ keys,
+__device__ __forceinline__ void stream_shift(const ShiftGroups<E>& w, int lpb_log2, int32_t b0,
+                                             int32_t b1, uint32_t* __restrict__ keys,
                                              int32_t kbase, int warp, int nwarps) {
   constexpr int VEC = 16 / E::kBytes;
   const int lane = threadIdx.x & 31;
   const int lpb = 1 << lpb_log2;
-  const int32_t nvec = (w.len_max + r) / VEC;  // whole vectors of the longest shard
   const int32_t v_begin = static_cast<int32_t>(static_cast<int64_t>(b0) << lpb_log2);
   const int32_t v_end = static_cast<int32_t>(min((static_cast<int64_t>(b1) << lpb_log2) + 1,
-                                                 static_cast<int64_t>(nvec)));
+                                                 static_cast<int64_t>(w.v_cap)));
   const bool merge = w.shards > SB || w.merge;
   constexpr int32_t kSlab = 32 * NV;
   const int32_t step = nwarps * kSlab;
 
   for (int d0 = 0; d0 < w.shards; d0 += SB) {
     int32_t lim[SB];
+    const typename E::T* src[SB];
 #pragma unroll
-    for (int j = 0; j < SB; ++j)
-      lim[j] = (d0 + j < w.shards) ? min((w.len[d0 + j] + r) / VEC, v_end) : 0;
-    const typename E::T* base = w.origin - r + static_cast<int64_t>(d0) * w.shard_stride;
+    for (int j = 0; j < SB; ++j) {
+      const int d = d0 + j;
+      const int g = d < w.split ? 1 : 0;
+      lim[j] = d < w.shards ? min((w.len[d] + w.r[g]) / VEC, v_end) : 0;
+      src[j] = w.base[g] + static_cast<int64_t>(d) * w.shard_stride;
+    }
 
     for (int32_t slab = v_begin + warp * kSlab; slab < v_end; slab += step) {
       Raw<E, VEC> x[SB][NV];
 #pragma unroll
       for (int j = 0; j < SB; ++j) {
-        const typename E::T* src = base + static_cast<int64_t>(j) * w.shard_stride;
 #pragma unroll
         for (int m = 0; m < NV; ++m) {
           const int32_t v = slab + m * 32 + lane;
           if (v < lim[j])
-            ld_raw<E, VEC>(src + static_cast<int64_t>(v) * VEC, x[j][m]);
+            ld_raw<E, VEC>(src[j] + static_cast<int64_t>(v) * VEC, x[j][m]);
           else
             raw_neg_inf(x[j][m]);
         }
@@ -206,20 +312,27 @@ __device__ __forceinline__ void stream_shift(const Window<E>& w, int32_t r, int 
       float hi[NV], lo[NV];
 #pragma unroll
       for (int m = 0; m < NV; ++m) {
-        // Element-wise max over the shards first (they share the offset),
-        // then one split of the vector into its lo and hi parts.
+        // Element-wise max over each group's shards, then one split per group.
+        Raw<E, VEC> e[2];
+        raw_neg_inf(e[0]);
+        raw_neg_inf(e[1]);
 #pragma unroll
-        for (int j = 1; j < SB; ++j) raw_max(x[0][m], x[j][m]);
+        for (int j = 0; j < SB; ++j) {
+          if (d0 + j < w.split)
+            raw_max(e[1], x[j][m]);
+          else
+            raw_max(e[0], x[j][m]);
+        }
         const int32_t v = slab + m * 32 + lane;
         const bool lead = (v & (lpb - 1)) == 0;
         hi[m] = neg_inf();
         lo[m] = neg_inf();
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
-          const bool below = lead && i < r;
-          const float xi = raw_elem(x[0][m], i);
-          hi[m] = max_nan(hi[m], below ? neg_inf() : xi);
-          lo[m] = max_nan(lo[m], below ? xi : neg_inf());
+          const float x0 = raw_elem(e[0], i), x1 = raw_elem(e[1], i);
+          const bool below0 = lead && i < w.r[0], below1 = lead && i < w.r[1];
+          hi[m] = max_nan(hi[m], below0 ? neg_inf() : x0, below1 ? neg_inf() : x1);
+          lo[m] = max_nan(lo[m], below0 ? x0 : neg_inf(), below1 ? x1 : neg_inf());
         }
       }
       // The slab's first vector sends its lo part to the block before
@@ -412,7 +525,8 @@ __device__ __forceinline__ void stream_row(const Window<E>& w, int vec, int shif
   constexpr int V8 = 8 / E::kBytes;
   constexpr int V4 = 4 / E::kBytes;
   if (vec == kVecShift)
-    stream_shift<E, 8, 1>(w, shift, lpb_log2, b0, b1, keys, kbase, warp, nwarps);
+    stream_shift_row<E, 8>(w.origin, shift, w.len_max, lpb_log2, b0, b1, keys, kbase, warp,
+                           nwarps);
   else if (vec == V16)
     stream_pow2<E, V16, 8, 1>(w, lpb_log2, b0, b1, keys, kbase, warp, nwarps);
   else if (vec == V8)
