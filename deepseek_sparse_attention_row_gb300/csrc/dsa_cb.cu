@@ -577,10 +577,11 @@ int sm_count() {
   return cached[dev];
 }
 
-// Launch shape (measured on GB300 over the five workloads):
-//  - 128 threads per CTA (8 CTAs per SM at 64 registers) unless rows can be
-//    512 KiB long, then 256: a CTA's top-k leaves fewer threads idle and more
-//    rows are in flight; very long rows need the larger CTA's loads in flight.
+// Launch shape (measured on GB300 over the workloads):
+//  - 128 threads per CTA (8 CTAs per SM at 64 registers): a CTA's top-k
+//    leaves fewer threads idle and more rows are in flight. (256 threads
+//    measured slower for the 512 KiB rows of the long workload, 82.6 us
+//    against 78.9 us with 4 CTAs per row.)
 //  - Rows are split over S CTAs (with a workspace) only while there are fewer
 //    than ~3 waves of CTAs, and never below 64 KiB per CTA: small CTA shares
 //    are latency-bound, and a full machine gains nothing from splitting.
@@ -591,7 +592,7 @@ struct Shape {
 
 Shape choose_shape(int64_t max_row_bytes, int64_t rows, bool have_workspace) {
   read_overrides();
-  Shape sh{1, max_row_bytes >= 512 * 1024 ? 256 : 128};
+  Shape sh{1, 128};
   if (g_threads_override) sh.threads = g_threads_override;
   if (have_workspace) {
     const int64_t slots = static_cast<int64_t>(sm_count()) * (1024 / sh.threads);
