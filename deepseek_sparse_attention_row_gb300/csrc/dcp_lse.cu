@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 namespace dsa {
@@ -194,30 +195,33 @@ __global__ void __launch_bounds__(kLseThreads) lse_kernel(const LseArgs a) {
   }
 }
 
+// Streaming multiprocessors of the current device, cached per device.
 int sm_count_lse() {
-  static int n = 0;
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  int n = cached[dev].load(std::memory_order_relaxed);
   if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       return 152;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
   return n;
 }
 
-// Resident CTAs per SM of one kernel instantiation (asked once).
+// Resident CTAs per SM of one kernel instantiation on the current device
+// (asked once per device).
 template <typename T, bool VEC, bool MERGE>
 int resident_ctas() {
-  static int n = 0;
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 4;
+  int n = cached[dev].load(std::memory_order_relaxed);
   if (n == 0) {
-    int v = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, lse_kernel<T, VEC, MERGE>, kLseThreads,
-                                                      0) == cudaSuccess && v > 0)
-      n = v;
-    else
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, lse_kernel<T, VEC, MERGE>, kLseThreads,
+                                                      0) != cudaSuccess || n <= 0)
       return 4;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
   return n;
 }

@@ -10,7 +10,7 @@
 // so the pass never reads the logits: it only writes -inf. It is bound by
 // HBM write bandwidth.
 //
-// One CTA per (shard, row, chunk of kMaskChunk columns). The chunk is cut
+// One CTA per (shard, row, chunk of 32 KiB of logits). The chunk is cut
 // into 16-byte-aligned slots (four fp32 or eight bf16 columns). Before any
 // store, the CTA turns the row's candidate ids into two slot bitmaps in
 // shared memory: `touch` (the slot holds at least one kept column) and
@@ -30,15 +30,19 @@
 namespace dsa {
 namespace {
 
-constexpr int32_t kMaskChunk = 8192;  // columns per CTA
+// Columns per CTA: 32 KiB of logits (8192 fp32 or 16384 bf16 columns).
+template <typename E>
+__host__ __device__ constexpr int32_t mask_chunk() {
+  return 32768 / E::kBytes;
+}
+constexpr int32_t kMaxMaskChunk = 16384;
 constexpr int kMaskThreads = 256;
-// A chunk's columns fall in at most kMaskChunk / 4 + 1 aligned slots (fp32;
-// the chunk may start up to three columns past a 16-byte boundary; bf16
-// needs at most kMaskChunk / 8 + 1).
-constexpr int32_t kSlots = kMaskChunk / 4 + 1;
+// A chunk's columns fall in at most 32768 / 16 + 1 aligned 16-byte slots
+// (the chunk may start up to one slot minus an element past a boundary).
+constexpr int32_t kSlots = 32768 / 16 + 1;
 constexpr int32_t kSlotWords = (kSlots + 31) / 32;
-// Blocks that overlap a chunk: at most kMaskChunk + 1 (block size 1).
-constexpr int32_t kBlockBits = kMaskChunk + 1;
+// Blocks that overlap a chunk: at most its column count + 1 (block size 1).
+constexpr int32_t kBlockBits = kMaxMaskChunk + 1;
 constexpr int32_t kBlockWords = (kBlockBits + 31) / 32;
 
 struct MaskArgs {
@@ -116,8 +120,9 @@ __global__ void __launch_bounds__(kMaskThreads) mask_kernel(const MaskArgs a) {
     e = local(gke);
     s = min(local(gs), e);
   }
-  const int32_t c0 = chunk * kMaskChunk;
-  const int32_t c1 = min(c0 + kMaskChunk, a.width);
+  constexpr int32_t kChunk = mask_chunk<E>();
+  const int32_t c0 = chunk * kChunk;
+  const int32_t c1 = min(c0 + kChunk, a.width);
   typename E::T* rowp = static_cast<typename E::T*>(a.logits) +
                         static_cast<int64_t>(d) * a.shard_stride + row * a.ld;
   // 16-byte slots: slot k covers columns [a0 + P k, a0 + P k + P).
@@ -130,7 +135,9 @@ __global__ void __launch_bounds__(kMaskThreads) mask_kernel(const MaskArgs a) {
     touch[i] = 0u;
     whole[i] = 0u;
   }
-  for (int i = threadIdx.x; i < kBlockWords; i += kMaskThreads) blocks[i] = 0u;
+  // Only the words of the blocks that can overlap this chunk are used.
+  const int32_t nbw = (kChunk / a.block_size + 2 + 31) / 32;
+  for (int i = threadIdx.x; i < min(nbw, kBlockWords); i += kMaskThreads) blocks[i] = 0u;
   __syncthreads();
 
   // Kept columns of this chunk lie in [lo_c, hi_c), in blocks [blo, bhi).
@@ -181,7 +188,8 @@ __global__ void __launch_bounds__(kMaskThreads) mask_kernel(const MaskArgs a) {
 
 template <typename E>
 dsa_status launch_mask(MaskArgs& a, cudaStream_t stream) {
-  a.chunks = static_cast<int32_t>((static_cast<int64_t>(a.width) + kMaskChunk - 1) / kMaskChunk);
+  a.chunks = static_cast<int32_t>((static_cast<int64_t>(a.width) + mask_chunk<E>() - 1) /
+                                  mask_chunk<E>());
   const int64_t grid = static_cast<int64_t>(a.shards) * a.rows * a.chunks;
   if (grid > INT32_MAX) return DSA_EUNSUPPORTED;
   mask_kernel<E><<<static_cast<unsigned>(grid), kMaskThreads, 0, stream>>>(a);
@@ -198,7 +206,7 @@ dsa_status mask_impl(typename E::T* logits, int64_t rows, int64_t width, int64_t
   if (rows == 0 || width == 0) return DSA_OK;
   if (!logits || !row_ke || ld_logits < width) return DSA_EINVAL;
   if (topk_blocks > 0 && (!candidates || ld_candidates < topk_blocks)) return DSA_EINVAL;
-  if (width > INT32_MAX - kMaskChunk) return DSA_EUNSUPPORTED;
+  if (width > INT32_MAX - kMaxMaskChunk) return DSA_EUNSUPPORTED;
   MaskArgs a{};
   a.logits = logits;
   a.ld = ld_logits;
@@ -230,7 +238,7 @@ dsa_status mask_sharded_impl(typename E::T* logits, int32_t shards, int64_t rows
   if (rows == 0 || local_width == 0) return DSA_OK;
   if (!logits || !global_row_ke) return DSA_EINVAL;
   if (topk_blocks > 0 && (!candidates || ld_candidates < topk_blocks)) return DSA_EINVAL;
-  if (local_width > INT32_MAX - kMaskChunk) return DSA_EUNSUPPORTED;
+  if (local_width > INT32_MAX - kMaxMaskChunk) return DSA_EUNSUPPORTED;
   MaskArgs a{};
   a.logits = logits;
   a.ld = ld_logits;
