@@ -66,10 +66,12 @@ struct SelectArgs {
   int64_t ld_out;
   void* scores;          // E::T elements, nullable
   int64_t ld_scores;
-  int32_t split;        // CTAs per row
+  int32_t split;        // CTAs per row at most (grid = rows * split)
+  int32_t chunk;        // blocks per CTA of a split row (>= nb when split == 1)
   uint32_t* ws_keys;    // split > 1: [rows, nb] block keys
   uint32_t* ws_count;   // split > 1: [rows] arrival counters (zero between calls)
-  int64_t rows;         // select_warp_kernel: rows to handle
+  int64_t rows;         // rows of the call
+  int32_t reverse;      // select_warp_kernel: take rows last to first
 };
 
 template <typename E>
@@ -82,18 +84,19 @@ struct RowPlan {
   int shift;          // vec == kVecShift: elements past the 16-byte boundary
 };
 
-// Counts one arrival on a row's counter and returns true for the last of
-// `split`. The last arrival writes 0 back, so a completed call leaves its
-// counters at zero. A counter word can also hold block-key data left by an
-// earlier call of another shape; every block key is >= key(-inf) while a
-// count is <= kMaxSplit, so such a word is read as zero. Each failed CAS means
-// another CTA of the row succeeded, so at most `split` + 1 attempts are made.
-__device__ __forceinline__ bool arrive_last(uint32_t* counter, uint32_t split) {
+// Adds `units` of a row's `total` to the row's counter and returns true for
+// the CTA whose addition completes the total. That CTA writes 0 back, so a
+// completed call leaves its counters at zero. A counter word can also hold
+// block-key data left by an earlier call of another shape; every block key
+// is >= key(-inf) while a count is < total <= 16384 / 32, so such a word is
+// read as zero. Each failed CAS but the first means another CTA of the row
+// succeeded, so at most `total` + 1 attempts are made.
+__device__ __forceinline__ bool arrive_units(uint32_t* counter, uint32_t units, uint32_t total) {
   uint32_t seen = 0u;
-  for (int i = 0; i < kMaxSplit + 2; ++i) {
-    const uint32_t count = (seen >= kKeyNegInf ? 0u : seen) + 1u;
-    const uint32_t prev = atomicCAS(counter, seen, count == split ? 0u : count);
-    if (prev == seen) return count == split;
+  for (uint32_t i = 0; i < total + 2u; ++i) {
+    const uint32_t count = (seen >= kKeyNegInf ? 0u : seen) + units;
+    const uint32_t prev = atomicCAS(counter, seen, count == total ? 0u : count);
+    if (prev == seen) return count == total;
     seen = prev;
   }
   return false;
@@ -204,28 +207,17 @@ __device__ __forceinline__ void stream_sharded(const Window<E>& w, int lpb_log2,
   }
 }
 
-// `a.split` CTAs per row.
-// MODE kUnsharded: unsharded rows, vector width chosen per row.
-// MODE kSharded: DCP rows; SVEC is the vector width fixed by the host
-// (0 = generic path). T: threads per CTA.
-template <typename E, int MODE, int SVEC, int T>
-__global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a) {
+// The row's streaming plan (every thread computes the same one from the
+// row's bounds); fills the per-shard window lengths (and, with starts, the
+// window starts) in shared memory, which other threads may read only after
+// the next barrier.
+template <typename E, int MODE, int SVEC>
+__device__ __forceinline__ RowPlan<E> plan_row(const SelectArgs& a, int64_t row, int32_t* len,
+                                               int32_t* start, int32_t& shard_q,
+                                               int32_t& shard_rem) {
   using TE = typename E::T;
   const TE* logits = static_cast<const TE*>(a.logits);
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);  // [max(kpad, kRankMax)]
-  uint32_t* keys = reinterpret_cast<uint32_t*>(cand + max(a.kpad, kRankMax));  // [nb]
-  int32_t* len = reinterpret_cast<int32_t*>(keys + a.nb);                // [shards]
-  int32_t* start = len + a.shards;  // [shards], kShardedStarts only
-  __shared__ TopkShared tsh;
-  __shared__ int s_last;
-
-  const int32_t split = a.split;
-  const int64_t row = blockIdx.x / split;
-  const int32_t part = static_cast<int32_t>(blockIdx.x % split);
-
   RowPlan<E> plan;
-  int32_t shard_q = 0, shard_rem = 0;  // kShardedStarts: gs = shard_q * shards + shard_rem
   if constexpr (MODE == kShardedStarts) {
     // Each shard's window [start[d], start[d] + len[d]) and its blocks
     // count from start[d]; the vector width is chosen per shard later.
@@ -277,14 +269,18 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
     if (threadIdx.x == 0) len[0] = plan.len_max;
   }
 
-  const int32_t nblk = plan.nblk;
-  const int32_t units = (nblk + kSplitUnit - 1) / kSplitUnit;
-  const int32_t b0 = min(part * units / split * kSplitUnit, nblk);
-  const int32_t b1 = min((part + 1) * units / split * kSplitUnit, nblk);
+  return plan;
+}
 
-  for (int32_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) keys[b] = kKeyNegInf;
-  __syncthreads();
-
+// Streams blocks [b0, b1) of `row` into keys[b0, b1) (initialised to
+// key(-inf) by the caller before a barrier), the window-end tails included.
+// Called by every thread of the CTA; ends with a barrier.
+template <typename E, int MODE, int SVEC>
+__device__ __forceinline__ void stream_range(const SelectArgs& a, const RowPlan<E>& plan,
+                                             int32_t shard_q, int32_t shard_rem, int32_t b0,
+                                             int32_t b1, uint32_t* keys, int32_t* len,
+                                             int32_t* start) {
+  using TE = typename E::T;
   Window<E> w;
   w.origin = plan.origin;
   w.shard_stride = a.shard_stride;
@@ -396,28 +392,80 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   }
   __syncthreads();
 
-  if (split > 1) {
-    // Publish this share, count in; only the last CTA of the row goes on.
-    uint32_t* wrow = a.ws_keys + row * a.nb;
-    for (int32_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) __stcg(wrow + b, keys[b]);
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = arrive_last(a.ws_count + row, static_cast<uint32_t>(split));
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    for (int32_t b = threadIdx.x; b < nblk; b += blockDim.x)
-      if (b < b0 || b >= b1) keys[b] = __ldcg(wrow + b);
-  }
+}
+
+// Pins, ranks and stores one row whose block keys [0, nblk) are final in
+// shared memory. Called by every thread of the CTA.
+template <typename E>
+__device__ __forceinline__ void rank_row(const SelectArgs& a, int64_t row, int32_t nblk,
+                                         int32_t pin_block, uint32_t* keys, uint64_t* cand,
+                                         TopkShared& tsh) {
+  using TE = typename E::T;
   // Blocks past the data blocks up to the pin are -inf (the pin can lie past
   // the data in the DCP form); topk_store never reads further.
-  for (int32_t b = nblk + threadIdx.x; b <= plan.pin_block; b += blockDim.x) keys[b] = kKeyNegInf;
+  for (int32_t b = nblk + threadIdx.x; b <= pin_block; b += blockDim.x) keys[b] = kKeyNegInf;
   __syncthreads();
-
-  topk_store(keys, a.nb, max(nblk, plan.pin_block + 1), min(a.topk, a.nb), plan.pin_block,
-             cand, a.kpad,
+  topk_store(keys, a.nb, max(nblk, pin_block + 1), min(a.topk, a.nb), pin_block, cand, a.kpad,
              a.topk > 0 ? a.out + row * a.ld_out : nullptr, a.topk,
              a.scores ? static_cast<TE*>(a.scores) + row * a.ld_scores : nullptr, tsh);
+}
+
+// Publishes keys [b0, b1) of `row` to the workspace and counts `units` of the
+// row's `total` in; returns (to every thread) whether this CTA was the last
+// to arrive, in which case keys [0, nblk) now hold the whole row.
+__device__ __forceinline__ bool merge_shares(const SelectArgs& a, int64_t row, int32_t nblk,
+                                             int32_t b0, int32_t b1, uint32_t units,
+                                             uint32_t total, uint32_t* keys, int* s_last) {
+  uint32_t* wrow = a.ws_keys + row * a.nb;
+  for (int32_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) __stcg(wrow + b, keys[b]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *s_last = arrive_units(a.ws_count + row, units, total);
+  __syncthreads();
+  if (!*s_last) return false;
+  __threadfence();
+  for (int32_t b = threadIdx.x; b < nblk; b += blockDim.x)
+    if (b < b0 || b >= b1) keys[b] = __ldcg(wrow + b);
+  return true;
+}
+
+// Up to `a.split` CTAs per row. A row's in-window blocks are cut from its
+// start into parts of `a.chunk` blocks, and CTA i takes part i / rows of row
+// i % rows (chunk-major): a short row uses only the parts its data reaches,
+// and the CTAs launched last hold the far parts of the longest rows.
+// MODE kUnsharded: unsharded rows, vector width chosen per row.
+// MODE kSharded: DCP rows; SVEC is the vector width fixed by the host
+// (0 = generic path). T: threads per CTA.
+template <typename E, int MODE, int SVEC, int T>
+__global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);  // [max(kpad, kRankMax)]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(cand + max(a.kpad, kRankMax));  // [nb]
+  int32_t* len = reinterpret_cast<int32_t*>(keys + a.nb);                // [shards]
+  int32_t* start = len + a.shards;  // [shards], kShardedStarts only
+  __shared__ TopkShared tsh;
+  __shared__ int s_last;
+
+  const uint32_t rows = static_cast<uint32_t>(a.rows);
+  const int64_t row = blockIdx.x % rows;
+  const int32_t part = static_cast<int32_t>(blockIdx.x / rows);
+
+  int32_t shard_q = 0, shard_rem = 0;  // kShardedStarts: gs = shard_q * shards + shard_rem
+  const RowPlan<E> plan = plan_row<E, MODE, SVEC>(a, row, len, start, shard_q, shard_rem);
+  const int32_t nblk = plan.nblk;
+  const int32_t parts = max(1, (nblk + a.chunk - 1) / a.chunk);
+  if (part >= parts) return;  // past the row's data
+  const int32_t b0 = part * a.chunk;
+  const int32_t b1 = min(b0 + a.chunk, nblk);
+
+  for (int32_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) keys[b] = kKeyNegInf;
+  __syncthreads();
+  stream_range<E, MODE, SVEC>(a, plan, shard_q, shard_rem, b0, b1, keys, len, start);
+  // Publish this share, count in; only the last CTA of the row goes on.
+  if (parts > 1 &&
+      !merge_shares(a, row, nblk, b0, b1, 1u, static_cast<uint32_t>(parts), keys, &s_last))
+    return;
+  rank_row<E>(a, row, nblk, plan.pin_block, keys, cand, tsh);
 }
 
 // Shared memory per warp in select_warp_kernel: candidates, keys, length.
@@ -434,8 +482,12 @@ __global__ void __launch_bounds__(W * 32, 1024 / (W * 32)) select_warp_kernel(co
   using TE = typename E::T;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * W + warp;
-  if (row >= a.rows) return;
+  // Rows are taken last to first: in a causally ordered chunk (packed
+  // prefill) later rows are longer, so the longest rows start first and the
+  // launch ends on short ones.
+  const int64_t slot = static_cast<int64_t>(blockIdx.x) * W + warp;
+  if (slot >= a.rows) return;
+  const int64_t row = a.reverse ? a.rows - 1 - slot : slot;
   unsigned char* slice = smem_raw + warp * warp_slice_bytes(a.nb);
   uint64_t* cand = reinterpret_cast<uint64_t*>(slice);
   uint32_t* keys = reinterpret_cast<uint32_t*>(cand + kWarpCand);
@@ -528,9 +580,11 @@ __global__ void fill_minus_one_kernel(int32_t* out, int64_t rows, int32_t cols, 
 // ---------------------------------------------------------------------------
 
 // Tuning overrides, read once: DSA_CB_SPLIT (CTAs per row, 1..8, used only
-// with a workspace), DSA_CB_THREADS (128 or 256 threads per CTA) and
-// DSA_CB_WARP=0 (never one row per warp).
+// with a workspace), DSA_CB_THREADS (128 or 256 threads per CTA),
+// DSA_CB_WARP=0 (never one row per warp) and DSA_CB_WARP_REV=0 (one row per
+// warp in row order).
 int g_split_override = 0, g_threads_override = 0, g_warp_off = 0;
+int g_warp_rev = 1;
 std::once_flag g_env_once;
 
 void read_overrides() {
@@ -543,6 +597,8 @@ void read_overrides() {
     g_threads_override = (u == 128 || u == 256) ? u : 0;
     const char* wv = std::getenv("DSA_CB_WARP");
     g_warp_off = wv && std::atoi(wv) == 0;
+    const char* rv = std::getenv("DSA_CB_WARP_REV");
+    if (rv) g_warp_rev = std::atoi(rv) != 0;
   });
 }
 
@@ -661,6 +717,11 @@ dsa_status launch_shape(const SelectArgs& a, int64_t rows, const Shape& sh, size
 // Fills the workspace fields of `a` for the chosen shape.
 void attach_workspace(SelectArgs& a, int64_t rows, void* workspace, const Shape& sh) {
   a.split = sh.split;
+  a.rows = rows;
+  // The part size of an even split of the longest row, in whole units.
+  const int32_t units = (a.nb_data + kSplitUnit - 1) / kSplitUnit;
+  a.chunk = sh.split > 1 ? std::max(1, (units + sh.split - 1) / sh.split) * kSplitUnit
+                         : std::max(a.nb, 1);
   if (sh.split == 1) return;
   a.ws_count = static_cast<uint32_t*>(workspace);
   a.ws_keys = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
@@ -681,6 +742,7 @@ size_t select_smem(int32_t kpad, int32_t nb, int32_t shards) {
   return static_cast<size_t>(std::max(kpad, kRankMax)) * 8 + static_cast<size_t>(nb) * 4 +
          static_cast<size_t>(shards) * 8;
 }
+
 
 }  // namespace
 }  // namespace dsa
@@ -799,15 +861,17 @@ dsa_status select_impl(const typename E::T* logits, int64_t rows, int64_t width,
     constexpr int W = 4;
     a.split = 1;
     a.rows = rows;
+    a.reverse = g_warp_rev;
     const size_t smem = W * warp_slice_bytes(a.nb);
     if (set_smem_attr(select_warp_kernel<E, W>, smem) != cudaSuccess) return DSA_ECUDA;
     select_warp_kernel<E, W><<<static_cast<unsigned>((rows + W - 1) / W), W * 32, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
   }
   const bool ws = workspace && workspace_size >= workspace_bytes(rows, a.nb);
+  const size_t smem = select_smem(a.kpad, a.nb, 1);
   const Shape sh = choose_shape(row_bytes, rows, ws);
   attach_workspace(a, rows, workspace, sh);
-  return launch_shape<E, kUnsharded, 0>(a, rows, sh, select_smem(a.kpad, a.nb, 1), s);
+  return launch_shape<E, kUnsharded, 0>(a, rows, sh, smem, s);
 }
 
 template <typename E>
