@@ -440,9 +440,15 @@ def steps_per_graph(k: int) -> int:
     return max(d for d in range(1, min(k, 64) + 1) if k % d == 0)
 
 
-def e2e_measure(wl, dsa, torch, device, steps: int):
-    """Same metric through the host-buffer API: pinned host inputs copied in
-    and ids copied out inside every timed step."""
+def e2e_measure(wl, dsa, torch, device, steps: int, flush=None):
+    """Same metric through the host-buffer API, one call per step from pinned
+    host inputs to the ids in pinned host memory, each step timed on its own
+    (the call waits for its result). ``in_place`` (the headline): the kernel
+    reads the in-window logits and the bounds across the host link and
+    writes the ids straight into host memory. ``staged``: the whole logits
+    tensor and the bounds are copied to the device first and the ids copied
+    back. ``flush`` (a callable) runs untimed between steps when the bytes a
+    step reads fit in L2."""
     sharded = hasattr(wl, "global_row_ke")
     h_logits = torch.from_numpy(wl.logits)
     if esize(wl) == 2:
@@ -452,6 +458,7 @@ def e2e_measure(wl, dsa, torch, device, steps: int):
     bufs = {"logits": torch.empty(h_logits.shape, dtype=h_logits.dtype, device=device),
             "out": torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)}
     if sharded:
+        nb = max(wl.max_global_blocks, 1)
         h_b = [torch.from_numpy(wl.global_row_ke).pin_memory()]
         bufs["global_row_ke"] = torch.empty(h_b[0].shape, dtype=torch.int32, device=device)
         h_ks = None
@@ -460,32 +467,46 @@ def e2e_measure(wl, dsa, torch, device, steps: int):
             h_b.append(h_ks)
             bufs["global_row_ks"] = torch.empty(h_ks.shape, dtype=torch.int32, device=device)
 
-        def call():
+        def call(in_place):
             dsa.select_candidate_blocks_sharded_host(h_logits, h_b[0], wl.global_block_size,
                                                      wl.max_global_blocks, wl.topk_blocks,
                                                      wl.row_repeat, out=h_out,
-                                                     device_buffers=bufs, global_row_ks=h_ks)
+                                                     device_buffers=bufs, global_row_ks=h_ks,
+                                                     in_place=in_place)
     else:
+        nb = -(-wl.width // wl.block_size)
         h_b = [None if wl.row_ks is None else torch.from_numpy(wl.row_ks).pin_memory(),
                torch.from_numpy(wl.row_ke).pin_memory()]
         if h_b[0] is not None:
             bufs["row_ks"] = torch.empty(h_b[0].shape, dtype=torch.int32, device=device)
         bufs["row_ke"] = torch.empty(h_b[1].shape, dtype=torch.int32, device=device)
 
-        def call():
+        def call(in_place):
             dsa.select_candidate_blocks_host(h_logits, h_b[0], h_b[1], wl.topk_blocks,
                                              wl.block_size, wl.row_repeat, wl.pin_newest,
-                                             out=h_out, device_buffers=bufs)
-    h2d = h_logits.numel() * esize(wl) + sum(b.numel() * 4 for b in h_b if b is not None)
+                                             out=h_out, device_buffers=bufs, in_place=in_place)
+    bufs["workspace"] = torch.zeros(dsa.workspace_bytes(wl.rows, nb), dtype=torch.uint8,
+                                    device=device)
+    bound_bytes = sum(b.numel() * 4 for b in h_b if b is not None)
     d2h = h_out.numel() * 4
-    call()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        call()
-    torch.cuda.synchronize()
-    sec = (time.perf_counter() - t0) / steps
-    return sec, h2d, d2h
+    res = {}
+    for in_place in (True, False):
+        call(in_place)
+        torch.cuda.synchronize()
+        total = 0.0
+        for _ in range(steps):
+            if flush is not None:
+                flush()
+                torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            call(in_place)
+            total += time.perf_counter() - t0
+        # in place: the bytes the kernel reads across the link; staged: the
+        # tensors copied in
+        h2d = (esize(wl) * window_elements(wl) if in_place else h_logits.numel() * esize(wl)) \
+            + bound_bytes
+        res["in_place" if in_place else "staged"] = (total / steps, h2d, d2h)
+    return res
 
 
 def oracle_cpu_baseline(wl, budget_s: float = 10.0):
@@ -637,10 +658,24 @@ def run_ours(args):
     e2e = None
     cpu = None
     if rank == 0 and not args.no_e2e and args.op == "select":
-        sec, h2d, d2h = e2e_measure(wl, dsa, torch, device, args.e2e_steps)
+        def flush_l2():
+            scratch.fill_(1.0)
+            if clean:
+                scratch2.amax()
+        res = e2e_measure(wl, dsa, torch, device, args.e2e_steps,
+                          flush=flush_l2 if flush else None)
+        sec, h2d, d2h = res["in_place"]
+        ssec, sh2d, sd2h = res["staged"]
         e2e = {"value": round(nbytes / sec / 1e9 * world, 3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(sec * 1e3, 4), "steps": args.e2e_steps}
+               "ms_per_step": round(sec * 1e3, 4), "steps": args.e2e_steps,
+               "path": "pinned host inputs read in place by the kernel (in-window logits and "
+                       "bounds across the host link), ids written to pinned host memory",
+               "staged": {"value": round(nbytes / ssec / 1e9 * world, 3), "unit": UNIT,
+                          "h2d_bytes_per_step": sh2d, "d2h_bytes_per_step": sd2h,
+                          "ms_per_step": round(ssec * 1e3, 4),
+                          "path": "whole logits tensor and bounds copied to the device, "
+                                  "ids copied back"}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.op in LSE_OPS:
         sec, reps = oracle_lse_baseline(wl, args.op, args.cpu_budget)
         cpu = {"value": round(nbytes / sec / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",

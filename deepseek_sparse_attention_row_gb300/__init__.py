@@ -21,9 +21,13 @@ Functions carry the C ABI's names:
   C ABI in ``include/dsa_dcp_attn.h``) and the sum over shards after it.
 
 Tensors are PyTorch CUDA tensors (PyTorch supplies device memory and the
-current stream). Logits may be float32 or bfloat16 (the ``*_bf16`` C entry
-points); scores follow the logits' dtype. ``select_candidate_blocks_host`` accepts host tensors and
-moves them through the device around one call.
+current stream) or pinned host tensors, which the kernels read and write in
+place through ``dsa_mapped_host_pointer`` (across NVLink-C2C on Grace
+systems). Logits may be float32 or bfloat16 (the ``*_bf16`` C entry points);
+scores follow the logits' dtype. ``select_candidate_blocks[_sharded]_host``
+take host tensors and wait for the ids: pinned inputs are read in place
+(only the in-window logits cross the link), other host tensors are copied to
+the device first.
 """
 
 from __future__ import annotations
@@ -46,6 +50,7 @@ __all__ = [
     "select_candidate_blocks_host",
     "select_candidate_blocks_sharded_host",
     "max_select_blocks",
+    "mapped_host_pointer",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -63,6 +68,7 @@ EXPORTED_SYMBOLS = (
     "dsa_mask_candidate_logits",
     "dsa_mask_candidate_logits_sharded",
     "dsa_select_candidate_blocks_sharded_static",
+    "dsa_mapped_host_pointer",
     "dsa_attn_max_shards",
     "dsa_correct_attn_out",
     "dsa_merge_attn_out",
@@ -115,6 +121,8 @@ def library():
     lib.dsa_mask_candidate_logits.argtypes = [p, i64, i64, i64, p, p, p, i32, i64, i32, i32, p]
     lib.dsa_mask_candidate_logits_sharded.argtypes = [p, i32, i64, i64, i64, i64, p, i32, i32, p,
                                                       i32, i64, p]
+    lib.dsa_mapped_host_pointer.argtypes = [p, ctypes.POINTER(ctypes.c_void_p)]
+    lib.dsa_mapped_host_pointer.restype = ctypes.c_int
     lib.dsa_attn_max_shards.argtypes = []
     lib.dsa_attn_max_shards.restype = i32
     lib.dsa_correct_attn_out.argtypes = [p, i32, i64, i64, i64, i64, i64, i64, p, i32, i64, i64,
@@ -198,17 +206,47 @@ def _stream_handle(stream) -> Optional[int]:
     return s.cuda_stream or None
 
 
+def mapped_host_pointer(t) -> int:
+    """Device address of a pinned (page-locked) host tensor's data, under
+    which kernels read and write it in place (``dsa_mapped_host_pointer``)."""
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("expected a pinned host tensor")
+    dev = ctypes.c_void_p()
+    _check("dsa_mapped_host_pointer", library().dsa_mapped_host_pointer(t.data_ptr(),
+                                                                         ctypes.byref(dev)))
+    return dev.value
+
+
 def _dev_ptr(t, dtype, name, *, allow_none=False):
-    torch = _torch()
+    """Device address of a CUDA tensor, or of a pinned host tensor (read and
+    written in place across the host link)."""
     if t is None:
         if allow_none:
             return None
         raise ValueError(f"{name} is required")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
+        return (mapped_host_pointer(t) if t.numel() else None) or None
     return t.data_ptr() or None
+
+
+def _empty_beside(shape, dtype, t):
+    """An output tensor where input ``t`` lives: on its CUDA device, or in
+    pinned host memory for a host input."""
+    torch = _torch()
+    if t.is_cuda:
+        return torch.empty(shape, dtype=dtype, device=t.device)
+    return torch.empty(shape, dtype=dtype, pin_memory=True)
+
+
+def _cuda_device(t):
+    """The device a call on tensor ``t`` runs on: its own, or the current
+    CUDA device for a pinned host tensor."""
+    torch = _torch()
+    return t.device if t.is_cuda else torch.device("cuda", torch.cuda.current_device())
 
 
 def _logits_kind(t, name="logits"):
@@ -236,7 +274,7 @@ def dsa_block_scores(logits, row_ks, row_ke, block_size: int, row_repeat: int = 
     rows, width = logits.shape
     nb = -(-width // block_size) if block_size > 0 else 0
     if scores_out is None:
-        scores_out = torch.empty((rows, nb), dtype=dt, device=logits.device)
+        scores_out = _empty_beside((rows, nb), dt, logits)
     st = getattr(library(), "dsa_block_scores" + sfx)(
         _dev_ptr(logits, dt, "logits"), rows, width, _row_major(logits, "logits"),
         _dev_ptr(row_ks, torch.int32, "row_ks", allow_none=True),
@@ -259,7 +297,7 @@ def dsa_select_candidate_blocks(logits, row_ks, row_ke, topk_blocks: int, block_
     rows, width = logits.shape
     nb = -(-width // block_size) if block_size > 0 else 0
     handle = _stream_handle(stream)
-    ws_ptr, ws_bytes = _workspace(workspace, rows, nb, logits.device, handle)
+    ws_ptr, ws_bytes = _workspace(workspace, rows, nb, _cuda_device(logits), handle)
     st = getattr(library(), "dsa_select_candidate_blocks" + sfx)(
         _dev_ptr(logits, dt, "logits"), rows, width, _row_major(logits, "logits"),
         _dev_ptr(row_ks, torch.int32, "row_ks", allow_none=True),
@@ -286,7 +324,7 @@ def dsa_select_candidate_blocks_sharded(logits, global_row_ke, global_block_size
     shards, rows, lw = logits.shape
     handle = _stream_handle(stream)
     ws_ptr, ws_bytes = _workspace(workspace, rows, max(int(max_global_blocks), 1),
-                                  logits.device, handle)
+                                  _cuda_device(logits), handle)
     if logits.stride(2) != 1:
         raise ValueError("logits must have unit stride in its last dimension")
     name = "dsa_select_candidate_blocks_sharded" + ("_starts" if global_row_ks is not None
@@ -390,9 +428,9 @@ def dsa_correct_attn_out(out, lses, rank: int, new_out=None, lse_out=None, strea
         raise ValueError(f"lses {tuple(lses.shape)} does not match out {tuple(out.shape)}")
     code = _attn_dtype(out, "out")
     if new_out is None:
-        new_out = torch.empty((H, B, D), dtype=out.dtype, device=out.device)
+        new_out = _empty_beside((H, B, D), out.dtype, out)
     if lse_out is None:
-        lse_out = torch.empty((B, H), dtype=torch.float32, device=out.device)
+        lse_out = _empty_beside((B, H), torch.float32, out)
     if tuple(new_out.shape) != (H, B, D) or tuple(lse_out.shape) != (B, H):
         raise ValueError("new_out must be [H, B, Dh] and lse_out [B, H]")
     st = library().dsa_correct_attn_out(
@@ -418,9 +456,9 @@ def dsa_merge_attn_out(outs, lses, merged=None, lse_out=None, stream=None):
         raise ValueError(f"lses {tuple(lses.shape)} does not match outs {tuple(outs.shape)}")
     code = _attn_dtype(outs, "outs")
     if merged is None:
-        merged = torch.empty((H, B, D), dtype=outs.dtype, device=outs.device)
+        merged = _empty_beside((H, B, D), outs.dtype, outs)
     if lse_out is None:
-        lse_out = torch.empty((B, H), dtype=torch.float32, device=outs.device)
+        lse_out = _empty_beside((B, H), torch.float32, outs)
     if tuple(merged.shape) != (H, B, D) or tuple(lse_out.shape) != (B, H):
         raise ValueError("merged must be [H, B, Dh] and lse_out [B, H]")
     st = library().dsa_merge_attn_out(
@@ -443,28 +481,46 @@ def _to_device(host, dev_buf, stream):
     return dev_buf
 
 
+def _all_pinned(*ts) -> bool:
+    return all(t is None or (not t.is_cuda and t.is_pinned()) for t in ts)
+
+
 def select_candidate_blocks_host(logits, row_ks, row_ke, topk_blocks: int, block_size: int,
                                  row_repeat: int = 1, pin_newest: bool = True, *,
-                                 out=None, device_buffers: Optional[dict] = None, stream=None):
-    """Host-memory form of ``dsa_select_candidate_blocks``: copies the host
-    (ideally pinned) inputs to the device, selects, and copies the ids back
-    into host tensor ``out`` (allocated when None). ``device_buffers`` may hold
-    preallocated device tensors under 'logits', 'row_ks', 'row_ke', 'out' so
-    that repeated calls allocate nothing. Waits for the result."""
+                                 out=None, device_buffers: Optional[dict] = None, stream=None,
+                                 in_place: bool = True):
+    """Host-memory form of ``dsa_select_candidate_blocks``; waits for the
+    result and returns the ids in host tensor ``out`` (pinned; allocated when
+    None).
+
+    Pinned inputs are read in place (unless ``in_place`` is False): the
+    kernel reads only the in-window logits across the host link and writes
+    the ids straight into ``out``. Other host tensors are first copied to the
+    device whole; ``device_buffers``
+    may then hold preallocated device tensors under 'logits', 'row_ks',
+    'row_ke', 'out' so that repeated calls allocate nothing. A device
+    tensor under 'workspace' is passed on as the call's workspace."""
     torch = _torch()
     stream = torch.cuda.current_stream() if stream is None else stream
     db = device_buffers if device_buffers is not None else {}
+    rows = logits.shape[0]
+    if out is None:
+        out = torch.empty((rows, topk_blocks), dtype=torch.int32, pin_memory=True)
+    if in_place and _all_pinned(logits, row_ks, row_ke, out):
+        dsa_select_candidate_blocks(logits, row_ks, row_ke, topk_blocks, block_size, out,
+                                    row_repeat, pin_newest, stream=stream,
+                                    workspace=db.get("workspace"))
+        stream.synchronize()
+        return out
     d_logits = _to_device(logits, db.get("logits"), stream)
     d_ks = _to_device(row_ks, db.get("row_ks"), stream)
     d_ke = _to_device(row_ke, db.get("row_ke"), stream)
-    rows = logits.shape[0]
     d_out = db.get("out")
     if d_out is None:
         d_out = torch.empty((rows, topk_blocks), dtype=torch.int32, device="cuda")
     dsa_select_candidate_blocks(d_logits, d_ks, d_ke, topk_blocks, block_size, d_out,
-                                row_repeat, pin_newest, stream=stream)
-    if out is None:
-        out = torch.empty((rows, topk_blocks), dtype=torch.int32, pin_memory=True)
+                                row_repeat, pin_newest, stream=stream,
+                                workspace=db.get("workspace"))
     with torch.cuda.stream(stream):
         out.copy_(d_out, non_blocking=True)
     stream.synchronize()
@@ -475,25 +531,32 @@ def select_candidate_blocks_sharded_host(logits, global_row_ke, global_block_siz
                                          max_global_blocks: int, topk_blocks: int,
                                          row_repeat: int = 1, *, out=None,
                                          device_buffers: Optional[dict] = None, stream=None,
-                                         global_row_ks=None):
+                                         global_row_ks=None, in_place: bool = True):
     """Host-memory form of ``dsa_select_candidate_blocks_sharded`` (see
-    ``select_candidate_blocks_host``; ``device_buffers`` may also hold
-    'global_row_ke' and 'global_row_ks')."""
+    ``select_candidate_blocks_host``: pinned inputs are read in place;
+    ``device_buffers`` may also hold 'global_row_ke' and 'global_row_ks')."""
     torch = _torch()
     stream = torch.cuda.current_stream() if stream is None else stream
     db = device_buffers if device_buffers is not None else {}
+    rows = logits.shape[1]
+    if out is None:
+        out = torch.empty((rows, topk_blocks), dtype=torch.int32, pin_memory=True)
+    if in_place and _all_pinned(logits, global_row_ke, global_row_ks, out):
+        dsa_select_candidate_blocks_sharded(logits, global_row_ke, global_block_size,
+                                            max_global_blocks, topk_blocks, out, row_repeat,
+                                            stream=stream, workspace=db.get("workspace"),
+                                            global_row_ks=global_row_ks)
+        stream.synchronize()
+        return out
     d_logits = _to_device(logits, db.get("logits"), stream)
     d_gke = _to_device(global_row_ke, db.get("global_row_ke"), stream)
     d_gks = _to_device(global_row_ks, db.get("global_row_ks"), stream)
-    rows = logits.shape[1]
     d_out = db.get("out")
     if d_out is None:
         d_out = torch.empty((rows, topk_blocks), dtype=torch.int32, device="cuda")
     dsa_select_candidate_blocks_sharded(d_logits, d_gke, global_block_size, max_global_blocks,
                                         topk_blocks, d_out, row_repeat, stream=stream,
-                                        global_row_ks=d_gks)
-    if out is None:
-        out = torch.empty((rows, topk_blocks), dtype=torch.int32, pin_memory=True)
+                                        global_row_ks=d_gks, workspace=db.get("workspace"))
     with torch.cuda.stream(stream):
         out.copy_(d_out, non_blocking=True)
     stream.synchronize()

@@ -1093,6 +1093,24 @@ cudaError_t static_scratch_address(void** addr) {
 }  // namespace
 }  // namespace dsa
 
+// Host memory that the GPU reads in place: page-locked memory is mapped into
+// the device's address space (across NVLink-C2C on Grace systems), so a
+// kernel can be handed its device address instead of a device copy.
+extern "C" dsa_status dsa_mapped_host_pointer(const void* host, void** device) {
+  if (!host || !device) return DSA_EINVAL;
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, host) != cudaSuccess) {
+    cudaGetLastError();  // the lookup's error is not sticky: clear it
+    return DSA_EINVAL;
+  }
+  // The attributes must describe this very address (not only its
+  // allocation), so that the device address maps the same byte.
+  if (attr.type != cudaMemoryTypeHost || !attr.devicePointer || attr.hostPointer != host)
+    return DSA_EINVAL;
+  *device = attr.devicePointer;
+  return DSA_OK;
+}
+
 extern "C" dsa_status dsa_select_candidate_blocks_sharded_static(
     const float* logits, int32_t shards, int64_t rows, int64_t local_width, int64_t ld_logits,
     int64_t shard_stride, const int32_t* global_row_ke, int32_t global_block_size,

@@ -17,8 +17,11 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Pointers named logits, row_ks, row_ke, global_row_ke, out, scores_out
- *    and workspace are DEVICE pointers owned by the caller. The library
- *    allocates no memory and keeps no pointer after a call returns.
+ *    and workspace are DEVICE addresses of memory owned by the caller:
+ *    device memory, or page-locked host memory under the address that
+ *    dsa_mapped_host_pointer gives (the kernels then read and write it
+ *    across the host link). The library allocates no memory and keeps no
+ *    pointer after a call returns.
  *  - Matrices are row-major with an explicit row stride in elements (ld_*).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL means the legacy
  *    default stream) and the call returns without synchronising. Results are
@@ -370,6 +373,28 @@ dsa_status dsa_select_candidate_blocks_sharded_static(
     int32_t global_block_size, int32_t max_global_blocks, int32_t row_repeat,
     int32_t topk_blocks, int32_t *out, int64_t ld_out, float *scores_out,
     int64_t ld_scores, void *stream);
+
+/*
+ * dsa_mapped_host_pointer -- the device address of page-locked host memory.
+ * The pages have no counterpart: it lets a caller whose logits sit in host
+ * memory hand them to the selecting, scoring and masking entry points
+ * without copying the tensor to the device first. Page-locked memory
+ * (cudaHostAlloc / cudaMallocHost, cudaHostRegister, a pinned torch tensor)
+ * is mapped into every device's address space; on Grace systems the GPU
+ * reads it across NVLink-C2C, so a selecting call reads only the in-window
+ * logits across the link instead of the caller copying the whole tensor.
+ *
+ *   host    a pointer into page-locked host memory (any offset).
+ *   device  receives the address under which the current device's kernels
+ *           read and write the same bytes.
+ *
+ * Nothing is launched. DSA_EINVAL when host or device is NULL, or when host
+ * is not page-locked memory mapped for the current device (pageable and
+ * device memory included); *device is then unchanged. The memory stays the
+ * caller's: it must stay allocated and page-locked until the calls that use
+ * the address have finished on the GPU.
+ */
+dsa_status dsa_mapped_host_pointer(const void *host, void **device);
 
 #ifdef __cplusplus
 }

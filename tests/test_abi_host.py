@@ -252,3 +252,11 @@ def test_merge_attn_out_validation(lib, kw, want):
 
 def test_attn_limits(lib):
     assert lib.dsa_attn_max_shards() == 32
+
+
+def test_mapped_host_pointer_null_arguments(lib):
+    out = ctypes.c_void_p(7)
+    assert lib.dsa_mapped_host_pointer(None, ctypes.byref(out)) == DSA_EINVAL
+    buf = ctypes.create_string_buffer(64)
+    assert lib.dsa_mapped_host_pointer(ctypes.addressof(buf), None) == DSA_EINVAL
+    assert out.value == 7
