@@ -98,3 +98,29 @@ def test_algorithmic_bytes_count_only_windows():
     swl.global_row_ke[:] = [10, 100]
     # shard ends for gke 10 over 4 shards: 3, 3, 2, 2; gke 100 clamps to 16 each
     assert bench.window_elements(swl) == 10 + 64
+
+
+def test_window_elements_with_starts_by_brute_force():
+    """The bytes a DCP call with starts reads (and the in-place end-to-end call
+    moves across the host link): every global token t in a row's window
+    [gs, ge) whose local column t // D lies inside the shard width."""
+    import numpy as np
+
+    import bench
+    import workloads
+
+    for seed in range(6):
+        rng = np.random.default_rng(70 + seed)
+        D = int(rng.choice([1, 3, 8]))
+        lw = int(rng.choice([5, 64, 100]))
+        swl, _ = workloads.small_sharded(70 + seed, shards=D, rows=7, global_width=D * lw,
+                                         global_block_size=D * 4, max_global_blocks=32,
+                                         topk_blocks=4, row_repeat=2, wild_bounds=True)
+        groups = swl.global_row_ke.size
+        swl.global_row_ks = rng.integers(-5, D * lw + 9, size=groups).astype(np.int32)
+        want = 0
+        for r in range(swl.rows):
+            ge = int(swl.global_row_ke[r // 2])
+            gs = min(max(int(swl.global_row_ks[r // 2]), 0), max(ge, 0))
+            want += sum(1 for t in range(gs, max(ge, 0)) if t // D < lw)
+        assert bench.window_elements(swl) == want, seed
