@@ -33,6 +33,7 @@ import hashlib
 import io
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -142,11 +143,23 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_only(text: str) -> str:
+    """C / CUDA source without its comments and blank lines, each line
+    stripped: what decides the compiled kernel (no string literal in the
+    kernel sources holds a comment marker)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.strip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(op: str = "select") -> str:
+    """Hash of the code (comments and blank lines removed) of the sources the
+    op's kernel is built from: a committed traffic figure stays valid across
+    comment edits and lapses with any change to the code."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[op]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

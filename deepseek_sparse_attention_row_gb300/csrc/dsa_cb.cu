@@ -4,16 +4,17 @@
 // stay in shared memory, the top-k runs on them in place, and only ids (and,
 // on request, block scores) are written back.
 //
-// Selecting kernel (select_kernel): `split` CTAs per row (1 without a
-// workspace). The row's blocks that hold in-window data are divided among
-// them in units of 32 blocks; each CTA streams its share (stream.cuh) into a
-// shared-memory key array. With split = 1 the CTA then pins, writes scores if
-// asked, and runs the top-k (topk.cuh) on its own keys. With split > 1 every
-// CTA publishes its keys to the row's slice of the workspace and counts
-// itself in on the row's counter (arrive_last); the last CTA to arrive reads
-// the other shares back (they are in L2) and runs the pin and the top-k.
-// The others exit as soon as they have published, so their slots go back to
-// streaming. The DCP form is the same kernel reading `shards` slices per row
+// Selecting kernel (select_kernel): up to `split` CTAs per row (1 without a
+// workspace). The row's blocks that hold in-window data are cut from its
+// start into parts of `chunk` blocks (whole units of 32 blocks), launched
+// chunk-major, and a row uses only the parts its data reaches; each CTA
+// streams its part (stream.cuh) into a shared-memory key array. A row held
+// by one CTA is then pinned, its scores written if asked, and ranked
+// (topk.cuh) in place. Otherwise every CTA of the row publishes its keys to
+// the row's slice of the workspace and counts itself in on the row's counter
+// (arrive_units); the last CTA to arrive reads the other parts back (they
+// are in L2) and runs the pin and the top-k. The others exit as soon as they
+// have published, so their slots go back to streaming. The DCP form is the same kernel reading `shards` slices per row
 // and taking the max over them before the reduction, i.e. the all-reduce MAX
 // of candidate_blocks.py's DCP branch happens in registers.
 //

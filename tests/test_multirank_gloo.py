@@ -124,3 +124,17 @@ def test_window_elements_with_starts_by_brute_force():
             gs = min(max(int(swl.global_row_ks[r // 2]), 0), max(ge, 0))
             want += sum(1 for t in range(gs, max(ge, 0)) if t // D < lw)
         assert bench.window_elements(swl) == want, seed
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The traffic figures are keyed by a hash of the kernel code with its
+    comments and blank lines removed: comment edits keep it, code edits
+    change it."""
+    import bench
+
+    src = "int f(int x) {  // doubles\n  /* the\n  answer */\n  return 2 * x;\n}\n"
+    same = "// header\nint f(int x) {\n\n    return 2 * x;   /* twice */\n}\n"
+    other = "int f(int x) {\n  return 3 * x;\n}\n"
+    assert bench.code_only(src) == bench.code_only(same) == "int f(int x) {\nreturn 2 * x;\n}"
+    assert bench.code_only(other) != bench.code_only(src)
+    assert "ld.global.nc" in bench.code_only('asm("ld.global.nc.b32 %0, [%1];");')
