@@ -53,8 +53,9 @@ def call_static(env, local, gke, wl, out, scores):
 
 def test_static_matches_workspace_entry_point_twice(env):
     torch, dsa, _ = env
-    # 256 rows of up to 256 KiB: the launcher splits each row over 4 CTAs, so
-    # the shares meet in the fixed array.
+    # 256 rows of up to 256 KiB: the launcher cuts each row into parts of
+    # 64 KiB, one CTA each (up to 4 per row), and the parts meet in the fixed
+    # array.
     wl, _ = workloads.small_sharded(2024, shards=8, rows=256, global_width=65536,
                                     global_block_size=64, max_global_blocks=1024,
                                     topk_blocks=32, row_repeat=2)
