@@ -41,4 +41,5 @@ def test_forced_launch_shape(name):
                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert res.returncode == 0, res.stdout[-4000:] + res.stderr[-2000:]
     passed = re.search(r"(\d+) passed", res.stdout)
-    assert passed and int(passed.group(1)) >= least and " failed" not in res.stdout, res.stdout[-2000:]
+    ok = passed and int(passed.group(1)) >= least and " failed" not in res.stdout
+    assert ok, res.stdout[-2000:]
