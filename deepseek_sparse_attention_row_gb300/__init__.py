@@ -51,6 +51,7 @@ __all__ = [
     "select_candidate_blocks_sharded_host",
     "max_select_blocks",
     "mapped_host_pointer",
+    "set_launch_override",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -81,7 +82,11 @@ EXPORTED_SYMBOLS = (
     "dsa_select_candidate_blocks_sharded_starts_bf16",
     "dsa_mask_candidate_logits_sharded_starts",
     "dsa_mask_candidate_logits_sharded_starts_bf16",
+    "dsa_select_set_launch_override",
 )
+
+# Knobs of dsa_select_set_launch_override (include/dsa_cb.h).
+LAUNCH_KNOBS = {"split": 1, "threads": 2, "warp_rows": 3, "warp_order": 4}
 
 _lib = None
 
@@ -112,6 +117,8 @@ def library():
     lib.dsa_select_max_shards.restype = i32
     lib.dsa_select_workspace_bytes.argtypes = [i64, i64]
     lib.dsa_select_workspace_bytes.restype = ctypes.c_size_t
+    lib.dsa_select_set_launch_override.argtypes = [i32, i32]
+    lib.dsa_select_set_launch_override.restype = ctypes.c_int
     lib.dsa_block_scores.argtypes = [p, i64, i64, i64, p, p, i32, i32, i32, p, i64, p]
     sz = ctypes.c_size_t
     lib.dsa_select_candidate_blocks.argtypes = [p, i64, i64, i64, p, p, i32, i32, i32, i32,
@@ -151,6 +158,13 @@ def library():
         f.restype = ctypes.c_int
     _lib = lib
     return lib
+
+
+def set_launch_override(knob: str, value: int) -> None:
+    """Pin one launch-shape choice of the selecting calls for this process
+    (value 0 hands it back to the launcher); for tests and tuning sweeps."""
+    _check("dsa_select_set_launch_override",
+           library().dsa_select_set_launch_override(LAUNCH_KNOBS[knob], int(value)))
 
 
 def _check(fn: str, status: int):

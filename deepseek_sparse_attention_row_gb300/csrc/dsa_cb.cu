@@ -24,8 +24,9 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
-#include <cstdlib>
+#include <atomic>
 #include <mutex>
 
 #include "keys.cuh"
@@ -580,28 +581,13 @@ __global__ void fill_minus_one_kernel(int32_t* out, int64_t rows, int32_t cols, 
 // Host side
 // ---------------------------------------------------------------------------
 
-// Tuning overrides, read once: DSA_CB_SPLIT (CTAs per row, 1..8, used only
-// with a workspace), DSA_CB_THREADS (128 or 256 threads per CTA),
-// DSA_CB_WARP=0 (never one row per warp) and DSA_CB_WARP_REV=0 (one row per
-// warp in row order).
-int g_split_override = 0, g_threads_override = 0, g_warp_off = 0;
-int g_warp_rev = 1;
-std::once_flag g_env_once;
-
-void read_overrides() {
-  std::call_once(g_env_once, [] {
-    const char* s = std::getenv("DSA_CB_SPLIT");
-    const int v = s ? std::atoi(s) : 0;
-    g_split_override = (v >= 1 && v <= kMaxSplit) ? v : 0;
-    const char* t = std::getenv("DSA_CB_THREADS");
-    const int u = t ? std::atoi(t) : 0;
-    g_threads_override = (u == 128 || u == 256) ? u : 0;
-    const char* wv = std::getenv("DSA_CB_WARP");
-    g_warp_off = wv && std::atoi(wv) == 0;
-    const char* rv = std::getenv("DSA_CB_WARP_REV");
-    if (rv) g_warp_rev = std::atoi(rv) != 0;
-  });
-}
+// Launch-shape overrides (dsa_select_set_launch_override): 0 leaves the
+// choice to the launcher. Set explicitly by tests and tuning sweeps; nothing
+// in the library reads them from the process settings.
+std::atomic<int> g_split_override{0};    // CTAs per row with a workspace, 1..8
+std::atomic<int> g_threads_override{0};  // 128 or 256 threads per CTA
+std::atomic<int> g_warp_off{0};          // 1: never one row per warp
+std::atomic<int> g_warp_in_order{0};     // 1: one row per warp, rows in order
 
 int32_t next_pow2(int32_t x) {
   int32_t p = 1;
@@ -648,16 +634,16 @@ struct Shape {
 };
 
 Shape choose_shape(int64_t max_row_bytes, int64_t rows, bool have_workspace) {
-  read_overrides();
   Shape sh{1, 128};
-  if (g_threads_override) sh.threads = g_threads_override;
+  if (const int t = g_threads_override.load(std::memory_order_relaxed)) sh.threads = t;
   if (have_workspace) {
     const int64_t slots = static_cast<int64_t>(sm_count()) * (1024 / sh.threads);
     int split = 1;
     while (split < kMaxSplit && rows * split < 3 * slots &&
            max_row_bytes / (2 * split) >= 64 * 1024)
       split <<= 1;
-    sh.split = g_split_override ? g_split_override : split;
+    const int forced = g_split_override.load(std::memory_order_relaxed);
+    sh.split = forced ? forced : split;
   }
   return sh;
 }
@@ -770,6 +756,29 @@ size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks) {
   return workspace_bytes(rows, nblocks);
 }
 
+dsa_status dsa_select_set_launch_override(int32_t knob, int32_t value) {
+  switch (knob) {
+    case DSA_LAUNCH_SPLIT:
+      if (value < 0 || value > kMaxSplit) return DSA_EINVAL;
+      g_split_override.store(value);
+      return DSA_OK;
+    case DSA_LAUNCH_THREADS:
+      if (value != 0 && value != 128 && value != 256) return DSA_EINVAL;
+      g_threads_override.store(value);
+      return DSA_OK;
+    case DSA_LAUNCH_WARP_ROWS:
+      if (value < 0 || value > 1) return DSA_EINVAL;
+      g_warp_off.store(value);
+      return DSA_OK;
+    case DSA_LAUNCH_WARP_ORDER:
+      if (value < 0 || value > 1) return DSA_EINVAL;
+      g_warp_in_order.store(value);
+      return DSA_OK;
+    default:
+      return DSA_EINVAL;
+  }
+}
+
 }  // extern "C"
 
 namespace dsa {
@@ -856,13 +865,12 @@ dsa_status select_impl(const typename E::T* logits, int64_t rows, int64_t width,
   const int64_t row_bytes = width * E::kBytes;
   // Many short rows: one row per warp (32 rows in flight per SM instead of
   // 8). With few rows a CTA per row keeps more of the GPU busy.
-  read_overrides();
-  if (!g_warp_off && row_bytes <= 64 * 1024 && topk_blocks <= 32 && a.nb <= 2048 &&
-      rows >= 8 * static_cast<int64_t>(sm_count())) {
+  if (!g_warp_off.load(std::memory_order_relaxed) && row_bytes <= 64 * 1024 &&
+      topk_blocks <= 32 && a.nb <= 2048 && rows >= 8 * static_cast<int64_t>(sm_count())) {
     constexpr int W = 4;
     a.split = 1;
     a.rows = rows;
-    a.reverse = g_warp_rev;
+    a.reverse = !g_warp_in_order.load(std::memory_order_relaxed);
     const size_t smem = W * warp_slice_bytes(a.nb);
     if (set_smem_attr(select_warp_kernel<E, W>, smem) != cudaSuccess) return DSA_ECUDA;
     select_warp_kernel<E, W><<<static_cast<unsigned>((rows + W - 1) / W), W * 32, smem, s>>>(a);

@@ -87,6 +87,33 @@ int32_t dsa_select_max_shards(void);
 size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks);
 
 /*
+ * dsa_select_set_launch_override -- pins one launch-shape choice of the
+ * selecting entry points for every later call in this process, or hands it
+ * back to the launcher (value 0). The pages have no counterpart: the
+ * launcher picks a shape from each call's sizes, results never depend on
+ * the shape (only the speed does), and tests and tuning sweeps use this to
+ * run shapes that the automatic choice reaches only at other sizes. Normal
+ * callers never need it. The setting is process-wide; set it while no other
+ * host thread is issuing selecting calls.
+ *
+ *   DSA_LAUNCH_SPLIT       CTAs per row when a workspace is given, 1..8
+ *   DSA_LAUNCH_THREADS     threads per row-per-CTA block, 128 or 256
+ *   DSA_LAUNCH_WARP_ROWS   1: never take the one-row-per-warp kernel
+ *   DSA_LAUNCH_WARP_ORDER  1: one-row-per-warp rows in order (default: last
+ *                          to first)
+ *
+ * DSA_EINVAL for an unknown knob or a value outside its range (nothing
+ * changes then).
+ */
+enum {
+    DSA_LAUNCH_SPLIT = 1,
+    DSA_LAUNCH_THREADS = 2,
+    DSA_LAUNCH_WARP_ROWS = 3,
+    DSA_LAUNCH_WARP_ORDER = 4
+};
+dsa_status dsa_select_set_launch_override(int32_t knob, int32_t value);
+
+/*
  * dsa_block_scores -- per-block scores of every row (candidate_blocks.py:
  * _block_scores and _block_scores_kernel, with the PIN_NEWEST switch).
  *

@@ -75,6 +75,32 @@ def test_limits(lib):
     assert lib.dsa_select_max_shards() >= 8
 
 
+def test_launch_override_validation(lib):
+    # Only the explicit call sets a launch shape: out-of-range values and
+    # unknown knobs are refused, and 0 hands every knob back to the launcher.
+    set_ = lib.dsa_select_set_launch_override
+    set_.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    set_.restype = ctypes.c_int
+    for knob, good, bad in ((1, (0, 1, 3, 8), (-1, 9)), (2, (0, 128, 256), (64, 512, -1)),
+                            (3, (0, 1), (2, -1)), (4, (0, 1), (2, -1))):
+        for v in good:
+            assert set_(knob, v) == DSA_OK
+        for v in bad:
+            assert set_(knob, v) == DSA_EINVAL
+        assert set_(knob, 0) == DSA_OK
+    for knob in (0, 5, 99, -3):
+        assert set_(knob, 0) == DSA_EINVAL
+
+
+def test_library_reads_no_environment():
+    # Launch shapes are plain function arguments or explicit calls: no source
+    # of the library asks the process environment for anything.
+    csrc = os.path.join(ROOT, "deepseek_sparse_attention_row_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        text = open(os.path.join(csrc, f)).read()
+        assert "getenv" not in text and "environ" not in text, f
+
+
 FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails validation first
 
 
