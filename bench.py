@@ -282,36 +282,42 @@ def device_logits(wl, torch, device):
     return t.to(torch.bfloat16) if esize(wl) == 2 else t
 
 
-def make_runner(wl, dsa, torch, device):
+def make_runner(wl, dsa, torch, device, copies: int = 1):
     """Device-resident inputs, an explicit workspace (so that graph capture
-    allocates nothing) and a one-call step function."""
+    allocates nothing) and one-call step functions. With copies = 2 the
+    logits are held twice and the two steps read different copies, so that a
+    step never finds the previous step's lines in L2."""
+    out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)
     if hasattr(wl, "global_row_ke"):
-        logits = device_logits(wl, torch, device)
         gke = torch.from_numpy(wl.global_row_ke).to(device)
-        out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)
         ws = torch.zeros(dsa.workspace_bytes(wl.rows, max(wl.max_global_blocks, 1)),
                          dtype=torch.uint8, device=device)
-
         gks = (None if getattr(wl, "global_row_ks", None) is None
                else torch.from_numpy(wl.global_row_ks).to(device))
 
-        def step():
-            dsa.dsa_select_candidate_blocks_sharded(logits, gke, wl.global_block_size,
-                                                    wl.max_global_blocks, wl.topk_blocks, out,
-                                                    wl.row_repeat, workspace=ws,
-                                                    global_row_ks=gks)
-        return step, out
-    logits = device_logits(wl, torch, device)
-    ks = None if wl.row_ks is None else torch.from_numpy(wl.row_ks).to(device)
-    ke = torch.from_numpy(wl.row_ke).to(device)
-    out = torch.empty((wl.rows, wl.topk_blocks), dtype=torch.int32, device=device)
-    ws = torch.zeros(dsa.workspace_bytes(wl.rows, -(-wl.width // wl.block_size)),
-                     dtype=torch.uint8, device=device)
+        def make_step(logits):
+            def step():
+                dsa.dsa_select_candidate_blocks_sharded(logits, gke, wl.global_block_size,
+                                                        wl.max_global_blocks, wl.topk_blocks,
+                                                        out, wl.row_repeat, workspace=ws,
+                                                        global_row_ks=gks)
+            return step
+    else:
+        ks = None if wl.row_ks is None else torch.from_numpy(wl.row_ks).to(device)
+        ke = torch.from_numpy(wl.row_ke).to(device)
+        ws = torch.zeros(dsa.workspace_bytes(wl.rows, -(-wl.width // wl.block_size)),
+                         dtype=torch.uint8, device=device)
 
-    def step():
-        dsa.dsa_select_candidate_blocks(logits, ks, ke, wl.topk_blocks, wl.block_size, out,
-                                        wl.row_repeat, wl.pin_newest, workspace=ws)
-    return step, out
+        def make_step(logits):
+            def step():
+                dsa.dsa_select_candidate_blocks(logits, ks, ke, wl.topk_blocks, wl.block_size,
+                                                out, wl.row_repeat, wl.pin_newest, workspace=ws)
+            return step
+    first = device_logits(wl, torch, device)
+    steps = [make_step(first)] + [make_step(first.clone()) for _ in range(copies - 1)]
+    if copies == 1:
+        return steps[0], out
+    return steps, out
 
 
 def mask_written_elements(wl, ids) -> int:
@@ -440,11 +446,13 @@ def oracle_lse_baseline(wl, op: str, budget_s: float = 10.0):
 
 def graph_of(step, n: int, torch):
     """A CUDA graph of n consecutive steps (launch cost paid once per replay,
-    not per step). The step must have run once before, outside capture."""
+    not per step); ``step`` is one callable or a list taken in turn. Every
+    step must have run once before, outside capture."""
+    steps = step if isinstance(step, (list, tuple)) else [step]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for _ in range(n):
-            step()
+        for i in range(n):
+            steps[i % len(steps)]()
     return g
 
 
@@ -539,6 +547,39 @@ def oracle_cpu_baseline(wl, budget_s: float = 10.0):
     return el / reps, reps
 
 
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_cpu_baseline_threads(wl, budget_s: float = 10.0, threads: int = 0):
+    """The same oracle function over ``threads`` contiguous row ranges on as
+    many host threads (the C calls release the GIL), repeated over the whole
+    workload until about budget_s seconds have passed; seconds per pass."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    oracle.build()
+    run = oracle.run_workload_bf16 if esize(wl) == 2 else oracle.run_workload
+    threads = max(1, threads or host_threads())
+    groups = -(-wl.rows // wl.row_repeat)
+    cuts = [min(wl.rows, (groups * i // threads) * wl.row_repeat) for i in range(threads + 1)]
+    parts = [_row_slice(wl, a, b) for a, b in zip(cuts, cuts[1:]) if b > a]
+    reps, t0 = 0, time.perf_counter()
+    with ThreadPoolExecutor(max_workers=len(parts)) as pool:
+        while True:
+            list(pool.map(lambda w: run(w, want_scores=False), parts))
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or reps >= 50:
+                break
+    return el / reps, reps
+
+
 def oracle_mask(oracle, wl, ids):
     """One masking pass of the oracle (the entry point for the workload's
     layout and dtype) on a copy of the workload's logits."""
@@ -570,6 +611,112 @@ def oracle_mask_baseline(wl, ids, budget_s: float = 10.0):
     return el / reps, reps
 
 
+class StepTimer:
+    """Times K steps on the device with CUDA events on the launching stream.
+
+    Steps whose inputs fit in L2 twice over (``flush``) are timed one by one
+    with L2 flushed before each (a 256 MB write, and for read-dominated steps
+    a 256 MB read of another buffer after it); the others are replayed from
+    a CUDA graph of up to 64 steps so that host launch cost never starves
+    the GPU between short steps. ``step`` is one callable or a list taken in
+    turn (e.g. two copies of the inputs, so that no step finds the previous
+    step's lines in L2)."""
+
+    def __init__(self, torch, device, read_after_flush: bool):
+        self.torch = torch
+        self.read_after_flush = read_after_flush
+        self.scratch = torch.empty(256 * 1000 * 1000 // 4, dtype=torch.float32, device=device)
+        self.scratch2 = (torch.ones(256 * 1000 * 1000 // 4, dtype=torch.float32, device=device)
+                         if read_after_flush else None)
+        self.flush = False
+        self.clean = False
+
+    def flush_l2(self):
+        self.scratch.fill_(1.0)
+        if self.clean:
+            self.scratch2.amax()
+
+    def prepare(self, step, steps: int, warmup: int, flush: bool):
+        torch = self.torch
+        self.flush = flush
+        self.clean = flush and self.read_after_flush
+        seq = list(step) if isinstance(step, (list, tuple)) else [step]
+        for i in range(max(warmup, len(seq))):
+            seq[i % len(seq)]()
+        torch.cuda.synchronize()
+        self.one = graph_of(seq[0], 1, torch)
+        self.per = steps_per_graph(steps)
+        self.many = graph_of(seq, self.per, torch)
+        for _ in range(2):
+            self.one.replay()
+            self.many.replay()
+        torch.cuda.synchronize()
+
+    def run(self, steps: int, stream) -> float:
+        """Device milliseconds of ``steps`` steps (prepare() first)."""
+        torch = self.torch
+        if self.flush:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(steps)]
+            for a, b in evs:
+                self.flush_l2()
+                a.record(stream)
+                self.one.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            return sum(a.elapsed_time(b) for a, b in evs)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps // self.per):
+            self.many.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    def l2_note(self) -> str:
+        if self.clean:
+            return "flushed before every step (256 MB write, then 256 MB read of another buffer)"
+        if self.flush:
+            return "flushed before every step (256 MB write)"
+        return ("inputs larger than L2 (bytes per step > 2 x 129 MB); two copies of the logits "
+                "read in turn" if self.read_after_flush else
+                "inputs larger than L2 (bytes per step > 2 x 129 MB)")
+
+
+# The configurations besides the headline one, each timed briefly in the same
+# run (selection only, one GPU) so that the bench line carries all of them.
+OTHER_WORKLOADS = ("tiny", "decode", "prefill", "long", "long_pin", "decode_bf16", "dcp_bf16",
+                   "dcp_starts")
+
+
+def time_other_workloads(names, dsa, torch, device, timer, steps: int, warmup: int,
+                         peak: float):
+    """ms per step, GB/s, roofline fraction and rows/s of each workload's
+    selection, by the headline's method (flushed per step when its window
+    bytes fit in L2 twice over, else graph-replayed over two logits copies)."""
+    import workloads
+
+    res = {}
+    stream = torch.cuda.current_stream()
+    for name in names:
+        wl = workloads.make(name)
+        nbytes = algorithmic_bytes(wl)
+        flush = esize(wl) * window_elements(wl) < 2 * L2_BYTES
+        step, _ = make_runner(wl, dsa, torch, device, copies=1 if flush else 2)
+        n = steps if not flush else max(steps // 4, 20)
+        timer.prepare(step, n, warmup, flush)
+        ms = timer.run(n, stream) / n
+        res[name] = {"ms_per_step": round(ms, 5), "value": round(nbytes / ms / 1e6, 3),
+                     "unit": UNIT, "frac": round(nbytes / ms / 1e6 / peak, 4),
+                     "rows_per_s": round(wl.rows / ms * 1e3, 1),
+                     "algorithmic_bytes_per_step": nbytes, "steps": n,
+                     "workload": workload_config(wl, name)["workload"], "l2": timer.l2_note()}
+        del step, wl
+        timer.one = timer.many = None
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -599,62 +746,26 @@ def run_ours(args):
         flush = nbytes < 2 * L2_BYTES
     else:
         wl = workloads.make(args.workload)
-        step, out = make_runner(wl, dsa, torch, device)
         nbytes = algorithmic_bytes(wl)
         window_bytes = esize(wl) * window_elements(wl)
         flush = window_bytes < 2 * L2_BYTES
-    scratch = torch.empty(256 * 1000 * 1000 // 4, dtype=torch.float32, device=device) if flush \
-        else None
+        step, out = make_runner(wl, dsa, torch, device, copies=1 if flush else 2)
     # Read-dominated steps (selection) also read a second 256 MB buffer after
     # the flush write, so that the flush's own dirty lines are written back
     # before the timed step rather than during it; write-heavy steps (masking,
     # LSE) keep the write-only flush, so that their stores cannot sit in a
     # clean L2 when the step ends.
-    clean = flush and args.op == "select"
-    scratch2 = torch.ones(256 * 1000 * 1000 // 4, dtype=torch.float32, device=device) \
-        if clean else None
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    # Steps are replayed from CUDA graphs so that host launch cost never
-    # starves the GPU between short steps.
-    one = graph_of(step, 1, torch)
-    per = steps_per_graph(args.steps)
-    many = graph_of(step, per, torch)
-    for _ in range(2):
-        one.replay()
-        many.replay()
-    torch.cuda.synchronize()
+    timer = StepTimer(torch, device, read_after_flush=args.op == "select")
     stream = torch.cuda.current_stream()
     props = torch.cuda.get_device_properties(device)
     uuid = str(getattr(props, "uuid", "") or "")
+    timer.prepare(step, args.steps, args.warmup, flush)
 
     with ClockSampler(uuid) as sampler:
         dist_barrier(world)
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
-        if flush:
-            # L2 flushed before every step; each step timed on its own.
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(args.steps)]
-            for a, b in evs:
-                scratch.fill_(1.0)
-                if clean:
-                    scratch2.amax()
-                a.record(stream)
-                one.replay()
-                b.record(stream)
-            torch.cuda.synchronize()
-            gpu_ms = sum(a.elapsed_time(b) for a, b in evs)
-        else:
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(args.steps // per):
-                many.replay()
-            b.record(stream)
-            torch.cuda.synchronize()
-            gpu_ms = a.elapsed_time(b)
+        gpu_ms = timer.run(args.steps, stream)
         dist_barrier(world)
         wall_s = time.perf_counter() - t_wall
     clocks = sampler.summary()
@@ -671,12 +782,8 @@ def run_ours(args):
     e2e = None
     cpu = None
     if rank == 0 and not args.no_e2e and args.op == "select":
-        def flush_l2():
-            scratch.fill_(1.0)
-            if clean:
-                scratch2.amax()
         res = e2e_measure(wl, dsa, torch, device, args.e2e_steps,
-                          flush=flush_l2 if flush else None)
+                          flush=timer.flush_l2 if flush else None)
         sec, h2d, d2h = res["in_place"]
         ssec, sh2d, sd2h = res["staged"]
         e2e = {"value": round(nbytes / sec / 1e9 * world, 3), "unit": UNIT,
@@ -700,10 +807,20 @@ def run_ours(args):
                "sample": f"the whole {args.workload} workload, {reps} pass(es), single-threaded "
                          f"C oracle masking, {sec:.3f} s per pass"}
     elif rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nthr = host_threads()
+        msec, mreps = oracle_cpu_baseline_threads(wl, args.cpu_budget, nthr)
         sec, reps = oracle_cpu_baseline(wl, args.cpu_budget)
-        cpu = {"value": round(nbytes / sec / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"the whole {args.workload} workload, {reps} pass(es), single-threaded "
-                         f"C oracle, {sec:.3f} s per pass"}
+        cpu = {"value": round(nbytes / msec / 1e9, 4), "unit": UNIT, "cores": nthr,
+               "kind": "oracle",
+               "sample": f"the whole {args.workload} workload, {mreps} pass(es), the C oracle "
+                         f"over {nthr} row ranges on {nthr} threads, {msec:.3f} s per pass",
+               "single_core": {"value": round(nbytes / sec / 1e9, 4), "unit": UNIT, "cores": 1,
+                               "sample": f"the whole {args.workload} workload, {reps} pass(es), "
+                                         f"single-threaded C oracle, {sec:.3f} s per pass"}}
+    others = None
+    if rank == 0 and world == 1 and args.op == "select" and not args.no_other_workloads:
+        others = time_other_workloads([n for n in OTHER_WORKLOADS if n != args.workload], dsa,
+                                      torch, device, timer, 500, 5, peak)
 
     if rank == 0:
         metric = {"select": METRIC, "mask": MASK_METRIC}.get(args.op) or LSE_METRICS[args.op]
@@ -726,10 +843,7 @@ def run_ours(args):
             "data": "synthetic (seeded numpy PCG64; shapes and distributions of the workload)",
             "config": {**config,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": ("flushed before every step (256 MB write, then 256 MB read of "
-                              "another buffer)" if clean else
-                              "flushed before every step (256 MB write)" if flush else
-                              "inputs larger than L2 (bytes per step > 2 x 129 MB)")},
+                       "l2": timer.l2_note()},
             "rows_per_s": round(rows_per_s, 1),
             "algorithmic_bytes_per_step": nbytes,
             "full_tensor_equivalent_gbs": full_gbs,
@@ -745,6 +859,8 @@ def run_ours(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if others is not None:
+            line["workloads"] = others
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -787,24 +903,37 @@ def run_reference(args):
                 esize(w) * mask_written_elements(w, ids) + 4 * nb + 4 * ids.size)
 
     # Calibrate on a slice of rows, then size each step's sample so that the
-    # whole run stays within about args.ref_budget seconds.
+    # whole run stays within about args.ref_budget seconds. The sample's rows
+    # are cut into one contiguous range per host thread and each step runs
+    # the oracle on all ranges at once (the C calls release the GIL).
+    from concurrent.futures import ThreadPoolExecutor
+
     rows = wl.rows
-    probe = max(1, rows // 64)
+    nthr = host_threads()
+    rr = wl.row_repeat
+    probe = max(rr, (rows // 64) // rr * rr)
     probe_step, _ = prepare(_row_slice(wl, 0, probe))
     t0 = time.perf_counter()
     probe_step()
     per_row = max((time.perf_counter() - t0) / probe, 1e-7)
     total_steps = args.steps + args.warmup
-    sample_rows = int(max(1, min(rows, args.ref_budget / total_steps / per_row)))
-    ref_step, sample_bytes = prepare(_row_slice(wl, 0, sample_rows))
-    for _ in range(args.warmup):
-        ref_step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        ref_step()
-    sec = (time.perf_counter() - t0) / args.steps
+    sample_rows = int(max(1, min(rows, args.ref_budget * nthr / total_steps / per_row)))
+    groups = -(-sample_rows // rr)
+    cuts = [min(sample_rows, (groups * i // nthr) * rr) for i in range(nthr + 1)]
+    parts = [prepare(_row_slice(wl, a, b)) for a, b in zip(cuts, cuts[1:]) if b > a]
+    sample_bytes = sum(nb for _, nb in parts)
+    with ThreadPoolExecutor(max_workers=len(parts)) as pool:
+        def ref_step():
+            list(pool.map(lambda part: part[0](), parts))
+        for _ in range(args.warmup):
+            ref_step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            ref_step()
+        sec = (time.perf_counter() - t0) / args.steps
     value = sample_bytes / sec / 1e9
-    desc = (f"first {sample_rows} of {rows} rows of the {args.workload} workload per step "
+    desc = (f"first {sample_rows} of {rows} rows of the {args.workload} workload per step, "
+            f"cut into {len(parts)} row ranges run on {len(parts)} host threads "
             f"({sample_bytes} algorithmic bytes)")
     line = {
         "impl": "reference", "metric": METRIC if args.op == "select" else MASK_METRIC,
@@ -813,10 +942,11 @@ def run_reference(args):
         "ms_per_step": round(sec * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32" if esize(wl) == 4 else "bf16 data, exact compares",
         "data": "synthetic (seeded numpy PCG64; shapes and distributions of the workload)",
-        "config": {**workload_config(wl, args.workload), "parallelism": "host, 1 thread"},
+        "config": {**workload_config(wl, args.workload),
+                   "parallelism": f"host, {len(parts)} threads"},
         "rows_per_s": round(sample_rows / sec, 1),
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": len(parts),
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -917,6 +1047,8 @@ def main(argv=None):
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-other-workloads", action="store_true",
+                   help="select only: skip timing the other configurations after the headline")
     p.add_argument("--cpu-budget", type=float, default=10.0)
     p.add_argument("--ref-budget", type=float, default=90.0)
     args = p.parse_args(argv)

@@ -1,9 +1,10 @@
 // mask.cu -- masking packed logits to the selected candidate blocks: the C
 // ABI dsa_mask_candidate_logits[_sharded][_bf16] of include/dsa_cb.h.
 //
-// candidate_blocks.py diff, the masking function after selection ("mask
-// packed logits outside causal bounds and request-local candidates"; under
-// DCP the local block size is passed and the candidate ids apply unchanged).
+// candidate_blocks.py diff, the masking function after selection: its
+// docstring masks every packed logit outside the row's causal window or
+// outside the row's request-local candidate blocks; under DCP the local
+// block size is passed and the candidate ids apply unchanged.
 // In place: logit c of a row becomes -inf when c is outside the row's window
 // [s, e) or its request-local block (c - s) / block_size is not one of the
 // row's candidate ids (ids < 0 are empty slots). Kept logits are not touched,

@@ -224,8 +224,8 @@ dsa_status dsa_select_candidate_blocks_sharded(
 /*
  * dsa_mask_candidate_logits -- mask packed logits to the selected candidate
  * blocks, in place (candidate_blocks.py: the masking function after
- * selection, "mask packed logits outside causal bounds and request-local
- * candidates"; its body is not on the page).
+ * selection, whose docstring masks logits outside the causal window or
+ * outside the request-local candidate blocks; its body is not on the page).
  *
  *   logits       [rows, ld_logits] fp32, modified in place over columns
  *                [0, width): column c becomes -inf when it lies outside the

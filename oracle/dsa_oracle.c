@@ -30,7 +30,7 @@
  *      < NaN (all NaNs equal).
  *   R5 equal scores rank the lower block id first.
  *   R6 an output slot is -1 when it is past k = min(topk, nblocks) or its
- *      block's score is -inf ([CB] "Output is -1 padded"; the DCP branch
+ *      block's score is -inf ([CB] docstring: the output is padded with -1; the DCP branch
  *      deselects rows without context only by filling -inf).
  *   R7 DCP local ends: shard d holds the global tokens t < gke with
  *      t % D == d, so its local end is ceil((gke - d) / D) when gke > d,
