@@ -59,7 +59,8 @@ _CSRC = "deepseek_sparse_attention_row_gb300/csrc/"
 # counts only while their hash still matches.
 KERNEL_SOURCES = {
     "select": tuple(_CSRC + f for f in ("dsa_cb.cu", "stream.cuh", "topk.cuh", "topk_warp.cuh",
-                                        "keys.cuh")),
+                                        "keys.cuh", "select_pipe.cu", "select_pipe.h",
+                                        "pipe.cuh")),
     "mask": tuple(_CSRC + f for f in ("mask.cu", "keys.cuh")),
     "correct": (_CSRC + "dcp_lse.cu",),
     "merge": (_CSRC + "dcp_lse.cu",),
@@ -735,6 +736,9 @@ def run_ours(args):
     __graft_entry__.build()
     import deepseek_sparse_attention_row_gb300 as dsa
 
+    for item in filter(None, args.launch.split(",")):
+        knob, val = item.split("=")
+        dsa.set_launch_override(knob.strip(), int(val))
     if args.op in LSE_OPS:
         wl = workloads.make_lse_named(args.workload)
         step = make_lse_runner(wl, args.op, dsa, torch, device)
@@ -1047,6 +1051,9 @@ def main(argv=None):
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--launch", default="",
+                   help="tuning sweeps: knob=value,... pinned through the library's launch "
+                        "overrides (see dsa_select_set_launch_override)")
     p.add_argument("--no-other-workloads", action="store_true",
                    help="select only: skip timing the other configurations after the headline")
     p.add_argument("--cpu-budget", type=float, default=10.0)

@@ -52,6 +52,7 @@ __all__ = [
     "max_select_blocks",
     "mapped_host_pointer",
     "set_launch_override",
+    "pipeline_error",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -83,10 +84,13 @@ EXPORTED_SYMBOLS = (
     "dsa_mask_candidate_logits_sharded_starts",
     "dsa_mask_candidate_logits_sharded_starts_bf16",
     "dsa_select_set_launch_override",
+    "dsa_pipeline_error",
 )
 
 # Knobs of dsa_select_set_launch_override (include/dsa_cb.h).
-LAUNCH_KNOBS = {"split": 1, "threads": 2, "warp_rows": 3, "warp_order": 4}
+LAUNCH_KNOBS = {"split": 1, "threads": 2, "warp_rows": 3, "warp_order": 4, "pipeline": 5,
+                "pipe_split": 6, "pipe_stages": 7, "pipe_stage_kb": 8, "pipe_sched": 9,
+                "pipe_warps": 10, "pipe_ctas": 11}
 
 _lib = None
 
@@ -117,6 +121,8 @@ def library():
     lib.dsa_select_max_shards.restype = i32
     lib.dsa_select_workspace_bytes.argtypes = [i64, i64]
     lib.dsa_select_workspace_bytes.restype = ctypes.c_size_t
+    lib.dsa_pipeline_error.argtypes = [ctypes.c_int]
+    lib.dsa_pipeline_error.restype = ctypes.c_int
     lib.dsa_select_set_launch_override.argtypes = [i32, i32]
     lib.dsa_select_set_launch_override.restype = ctypes.c_int
     lib.dsa_block_scores.argtypes = [p, i64, i64, i64, p, p, i32, i32, i32, p, i64, p]
@@ -165,6 +171,12 @@ def set_launch_override(knob: str, value: int) -> None:
     (value 0 hands it back to the launcher); for tests and tuning sweeps."""
     _check("dsa_select_set_launch_override",
            library().dsa_select_set_launch_override(LAUNCH_KNOBS[knob], int(value)))
+
+
+def pipeline_error(clear: bool = False) -> int:
+    """The pipelined kernels' give-up flag (0: none of their waits ever gave
+    up); see dsa_pipeline_error."""
+    return int(library().dsa_pipeline_error(1 if clear else 0))
 
 
 def _check(fn: str, status: int):

@@ -24,7 +24,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 def sources() -> list:
     return (sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
-                   if f.endswith((".cu", ".cuh")))
+                   if f.endswith((".cu", ".cuh", ".h")))
             + sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")))
 
 

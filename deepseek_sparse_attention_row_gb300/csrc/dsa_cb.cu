@@ -30,6 +30,7 @@
 #include <mutex>
 
 #include "keys.cuh"
+#include "select_pipe.h"
 #include "stream.cuh"
 #include "topk.cuh"
 #include "topk_warp.cuh"
@@ -595,14 +596,10 @@ int32_t next_pow2(int32_t x) {
   return p;
 }
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
-// Workspace layout: rows arrival counters (uint32), then rows * nb block keys
-// (uint32), each part 256-byte aligned.
-size_t workspace_bytes(int64_t rows, int64_t nb) {
-  return align256(static_cast<size_t>(rows) * 4) +
-         align256(static_cast<size_t>(rows) * static_cast<size_t>(nb) * 4);
-}
+// Workspace layout (select_pipe.h): a 256-byte header (the pipelined
+// kernels' unit queue), rows arrival counters (uint32), then rows * nb block
+// keys (uint32), each part 256-byte aligned.
+size_t workspace_bytes(int64_t rows, int64_t nb) { return ws_total_bytes(rows, nb); }
 
 // Streaming multiprocessors of the current device, cached per device.
 int sm_count() {
@@ -710,9 +707,8 @@ void attach_workspace(SelectArgs& a, int64_t rows, void* workspace, const Shape&
   a.chunk = sh.split > 1 ? std::max(1, (units + sh.split - 1) / sh.split) * kSplitUnit
                          : std::max(a.nb, 1);
   if (sh.split == 1) return;
-  a.ws_count = static_cast<uint32_t*>(workspace);
-  a.ws_keys = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
-                                          align256(static_cast<size_t>(rows) * 4));
+  a.ws_count = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws_counts_offset());
+  a.ws_keys = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws_keys_offset(rows));
 }
 
 dsa_status fill_minus_one(int32_t* out, int64_t rows, int32_t cols, int64_t ld, cudaStream_t s) {
@@ -773,6 +769,34 @@ dsa_status dsa_select_set_launch_override(int32_t knob, int32_t value) {
     case DSA_LAUNCH_WARP_ORDER:
       if (value < 0 || value > 1) return DSA_EINVAL;
       g_warp_in_order.store(value);
+      return DSA_OK;
+    case DSA_LAUNCH_PIPELINE:
+      if (value < 0 || value > 3) return DSA_EINVAL;
+      pipe_set_override(knob, value);
+      return DSA_OK;
+    case DSA_LAUNCH_PIPE_SPLIT:
+      if (value < 0 || value > 8) return DSA_EINVAL;
+      pipe_set_override(knob, value);
+      return DSA_OK;
+    case DSA_LAUNCH_PIPE_STAGES:
+      if (value != 0 && (value < 2 || value > 16)) return DSA_EINVAL;
+      pipe_set_override(knob, value);
+      return DSA_OK;
+    case DSA_LAUNCH_PIPE_STAGE_KB:
+      if (value != 0 && (value < 4 || value > 64)) return DSA_EINVAL;
+      pipe_set_override(knob, value);
+      return DSA_OK;
+    case DSA_LAUNCH_PIPE_SCHED:
+      if (value < 0 || value > 1) return DSA_EINVAL;
+      pipe_set_override(knob, value);
+      return DSA_OK;
+    case DSA_LAUNCH_PIPE_WARPS:
+      if (value != 0 && value != 4 && value != 8) return DSA_EINVAL;
+      pipe_set_override(knob, value);
+      return DSA_OK;
+    case DSA_LAUNCH_PIPE_CTAS:
+      if (value < 0 || value > 4) return DSA_EINVAL;
+      pipe_set_override(knob, value);
       return DSA_OK;
     default:
       return DSA_EINVAL;
@@ -840,8 +864,8 @@ dsa_status select_impl(const typename E::T* logits, int64_t rows, int64_t width,
   const int64_t nb = (width + block_size - 1) / block_size;
   if (scores_out && ld_scores < nb) return DSA_EINVAL;
   if (topk_blocks == 0 && !scores_out) return DSA_OK;
-  if (nb > kMaxSelectBlocks || width > INT32_MAX - 64) return DSA_EUNSUPPORTED;
-  if (rows * kMaxSplit > INT32_MAX) return DSA_EUNSUPPORTED;
+  if (nb > kMaxSelectBlocks || width > INT32_MAX - 8192) return DSA_EUNSUPPORTED;
+  if (rows > INT32_MAX / kMaxSplit) return DSA_EUNSUPPORTED;
 
   SelectArgs a{};
   a.logits = logits;
@@ -863,6 +887,33 @@ dsa_status select_impl(const typename E::T* logits, int64_t rows, int64_t width,
   a.scores = scores_out;
   a.ld_scores = ld_scores;
   const int64_t row_bytes = width * E::kBytes;
+  {
+    PipeCall pc{};
+    pc.elem_bytes = E::kBytes;
+    pc.mode = kPipeUnsharded;
+    pc.logits = logits;
+    pc.ld = ld_logits;
+    pc.shard_stride = 0;
+    pc.shards = 1;
+    pc.width = a.width;
+    pc.row_ks = row_ks;
+    pc.row_ke = row_ke;
+    pc.row_repeat = row_repeat;
+    pc.block_size = block_size;
+    pc.global_block_size = block_size;
+    pc.nb = a.nb;
+    pc.nb_data = a.nb;
+    pc.pin_newest = a.pin_newest;
+    pc.topk = topk_blocks;
+    pc.out = out;
+    pc.ld_out = ld_out;
+    pc.scores = scores_out;
+    pc.ld_scores = ld_scores;
+    pc.rows = rows;
+    pc.workspace = workspace;
+    pc.workspace_size = workspace_size;
+    if (pipe_takes(pc)) return pipe_select(pc, stream);
+  }
   // Many short rows: one row per warp (32 rows in flight per SM instead of
   // 8). With few rows a CTA per row keeps more of the GPU busy.
   if (!g_warp_off.load(std::memory_order_relaxed) && row_bytes <= 64 * 1024 &&
@@ -883,6 +934,32 @@ dsa_status select_impl(const typename E::T* logits, int64_t rows, int64_t width,
   return launch_shape<E, kUnsharded, 0>(a, rows, sh, smem, s);
 }
 
+// Argument checks of the sharded selection, done on the host before anything
+// is enqueued: a status < 0 is the call's error, kNoWork means DSA_OK with
+// nothing to do, DSA_OK means go on.
+constexpr int kNoWork = 1;
+
+int sharded_precheck(const void* logits, int32_t shards, int64_t rows, int64_t local_width,
+                     int64_t ld_logits, int64_t shard_stride, const int32_t* global_row_ke,
+                     int32_t global_block_size, int32_t max_global_blocks, int32_t row_repeat,
+                     int32_t topk_blocks, const int32_t* out, int64_t ld_out,
+                     const void* scores_out, int64_t ld_scores) {
+  if (shards < 1 || rows < 0 || local_width < 0 || topk_blocks < 0 || global_block_size < 1 ||
+      global_block_size % shards != 0 || row_repeat < 1 || ld_logits < local_width ||
+      shard_stride < 0)
+    return DSA_EINVAL;
+  if (rows == 0) return kNoWork;
+  if (!global_row_ke || (topk_blocks > 0 && (!out || ld_out < topk_blocks))) return DSA_EINVAL;
+  if (local_width > 0 && !logits) return DSA_EINVAL;
+  const int32_t nbg = std::max<int32_t>(max_global_blocks, 1);
+  if (scores_out && ld_scores < nbg) return DSA_EINVAL;
+  if (topk_blocks == 0 && !scores_out) return kNoWork;
+  if (nbg > kMaxSelectBlocks || shards > kMaxShards || local_width > INT32_MAX - 8192)
+    return DSA_EUNSUPPORTED;
+  if (rows > INT32_MAX / kMaxSplit) return DSA_EUNSUPPORTED;
+  return DSA_OK;
+}
+
 template <typename E>
 dsa_status select_sharded_impl(const typename E::T* logits, int32_t shards, int64_t rows,
                                int64_t local_width, int64_t ld_logits, int64_t shard_stride,
@@ -892,19 +969,12 @@ dsa_status select_sharded_impl(const typename E::T* logits, int32_t shards, int6
                                int32_t topk_blocks, int32_t* out, int64_t ld_out,
                                typename E::T* scores_out, int64_t ld_scores, void* workspace,
                                size_t workspace_size, void* stream) {
-  if (shards < 1 || rows < 0 || local_width < 0 || topk_blocks < 0 || global_block_size < 1 ||
-      global_block_size % shards != 0 || row_repeat < 1 || ld_logits < local_width ||
-      shard_stride < 0)
-    return DSA_EINVAL;
-  if (rows == 0) return DSA_OK;
-  if (!global_row_ke || (topk_blocks > 0 && (!out || ld_out < topk_blocks))) return DSA_EINVAL;
-  if (local_width > 0 && !logits) return DSA_EINVAL;
+  const int pre = sharded_precheck(logits, shards, rows, local_width, ld_logits, shard_stride,
+                                   global_row_ke, global_block_size, max_global_blocks,
+                                   row_repeat, topk_blocks, out, ld_out, scores_out, ld_scores);
+  if (pre < 0) return static_cast<dsa_status>(pre);
+  if (pre == kNoWork) return DSA_OK;
   const int32_t nbg = std::max<int32_t>(max_global_blocks, 1);
-  if (scores_out && ld_scores < nbg) return DSA_EINVAL;
-  if (topk_blocks == 0 && !scores_out) return DSA_OK;
-  if (nbg > kMaxSelectBlocks || shards > kMaxShards || local_width > INT32_MAX - 64)
-    return DSA_EUNSUPPORTED;
-  if (rows * kMaxSplit > INT32_MAX) return DSA_EUNSUPPORTED;
 
   const int32_t lbs = global_block_size / shards;
   SelectArgs a{};
@@ -937,6 +1007,33 @@ dsa_status select_sharded_impl(const typename E::T* logits, int32_t shards, int6
     return lbs % vec == 0 && pow2(lbs / vec) && (base % (E::kBytes * vec)) == 0 &&
            ld_logits % vec == 0 && shard_stride % vec == 0;
   };
+  {
+    PipeCall pc{};
+    pc.elem_bytes = E::kBytes;
+    pc.mode = global_row_ks ? kPipeShardedStarts : kPipeSharded;
+    pc.logits = logits;
+    pc.ld = ld_logits;
+    pc.shard_stride = shard_stride;
+    pc.shards = shards;
+    pc.width = a.width;
+    pc.row_ks = global_row_ks;
+    pc.row_ke = global_row_ke;
+    pc.row_repeat = row_repeat;
+    pc.block_size = lbs;
+    pc.global_block_size = global_block_size;
+    pc.nb = a.nb;
+    pc.nb_data = a.nb_data;
+    pc.pin_newest = 0;
+    pc.topk = topk_blocks;
+    pc.out = out;
+    pc.ld_out = ld_out;
+    pc.scores = scores_out;
+    pc.ld_scores = ld_scores;
+    pc.rows = rows;
+    pc.workspace = workspace;
+    pc.workspace_size = workspace_size;
+    if (local_width > 0 && pipe_takes(pc)) return pipe_select(pc, stream);
+  }
   const size_t smem = select_smem(a.kpad, a.nb, shards);
   const bool ws = workspace && workspace_size >= workspace_bytes(rows, a.nb);
   const Shape sh = choose_shape(local_width * E::kBytes * shards, rows, ws);
@@ -1069,35 +1166,15 @@ dsa_status dsa_select_candidate_blocks_sharded_starts_bf16(
 // The array (kStaticScratchBytes) is created when the library's device code
 // is loaded on a GPU and stays there until the process exits; every call on
 // that GPU shares it. In host code the array's name is only a host-side
-// stand-in, so its device address is looked up once per device with
-// cudaGetSymbolAddress, with that device current.
+// stand-in, so every call looks up its device address with
+// cudaGetSymbolAddress, with the call's device current (a lookup is cheap, and
+// nothing cached can go stale when a context is torn down and rebuilt).
 
 namespace dsa {
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
-
-std::mutex g_static_mu;
-void* g_static_addr[64] = {};
-
-// Device address of g_static_scratch on the current device (looked up on
-// the first call per device).
-cudaError_t static_scratch_address(void** addr) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_addr[dev]) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (err != cudaSuccess) return err;
-    g_static_addr[dev] = p;
-  }
-  *addr = g_static_addr[dev];
-  return cudaSuccess;
-}
 
 }  // namespace
 }  // namespace dsa
@@ -1125,21 +1202,32 @@ extern "C" dsa_status dsa_select_candidate_blocks_sharded_static(
     int64_t shard_stride, const int32_t* global_row_ke, int32_t global_block_size,
     int32_t max_global_blocks, int32_t row_repeat, int32_t topk_blocks, int32_t* out,
     int64_t ld_out, float* scores_out, int64_t ld_scores, void* stream) {
-  if (rows <= 0)
-    return dsa_select_candidate_blocks_sharded(
-        logits, shards, rows, local_width, ld_logits, shard_stride, global_row_ke,
-        global_block_size, max_global_blocks, row_repeat, topk_blocks, out, ld_out, scores_out,
-        ld_scores, nullptr, 0, stream);
+  // Every argument error is returned before anything is enqueued.
+  const int pre = dsa::sharded_precheck(logits, shards, rows, local_width, ld_logits,
+                                        shard_stride, global_row_ke, global_block_size,
+                                        max_global_blocks, row_repeat, topk_blocks, out, ld_out,
+                                        scores_out, ld_scores);
+  if (pre < 0) return static_cast<dsa_status>(pre);
+  if (pre == dsa::kNoWork) return DSA_OK;
   const int64_t nbg = max_global_blocks > 1 ? max_global_blocks : 1;
-  if (dsa::workspace_bytes(rows, nbg) > dsa::kStaticScratchBytes) return DSA_EUNSUPPORTED;
+  const size_t need = dsa::workspace_bytes(rows, nbg);
   void* scratch = nullptr;
-  if (dsa::static_scratch_address(&scratch) != cudaSuccess) return DSA_ECUDA;
-  // The array keeps the previous call's contents: clear the arrival counters.
-  if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(rows) * 4,
-                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return DSA_ECUDA;
+  if (need <= dsa::kStaticScratchBytes) {
+    if (cudaGetSymbolAddress(&scratch, dsa::g_static_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return DSA_ECUDA;
+    }
+    // The array keeps whatever the previous call left: clear the part of it
+    // that must start at zero (the queue header and the arrival counters).
+    if (cudaMemsetAsync(scratch, 0, dsa::ws_keys_offset(rows),
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return DSA_ECUDA;
+  }
+  // A call whose workspace does not fit in the array runs without one: rows
+  // are dealt to CTAs in a fixed order and none is split, with the same
+  // results.
   return dsa_select_candidate_blocks_sharded(
       logits, shards, rows, local_width, ld_logits, shard_stride, global_row_ke,
       global_block_size, max_global_blocks, row_repeat, topk_blocks, out, ld_out, scores_out,
-      ld_scores, scratch, dsa::kStaticScratchBytes, stream);
+      ld_scores, scratch, scratch ? dsa::kStaticScratchBytes : 0, stream);
 }

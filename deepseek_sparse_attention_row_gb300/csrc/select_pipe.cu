@@ -1,0 +1,1083 @@
+// select_pipe.cu -- pipelined candidate-block selection: persistent CTAs that
+// stage in-window logits into a shared-memory ring with the bulk-copy engine
+// (cp.async.bulk, pipe.cuh) while their consumer warps reduce the previous
+// stages and rank finished rows.
+//
+// What is computed is that of select_kernel (dsa_cb.cu) and of
+// candidate_blocks.py's _block_scores_kernel, _select_candidate_blocks_impl
+// and _store_candidates_kernel: per row the window [s, e) cut into blocks of
+// block_size counted from s, each block's NaN-propagating max (-inf when
+// empty), the optional pin, the ranked top-k with ties to the lower id, -1
+// padded; in the DCP form the max over the shards' local blocks, the global
+// pin and the rows without context. Only the way the bytes move differs.
+//
+// Layout of a CTA: warps 0 .. NW-1 consume, warp NW produces. The producer
+// takes work units (a row, or a part of a long row), plans each unit's
+// window from the row's bounds and cuts it into stages of whole blocks. A
+// stage holds, for every shard of the row (one piece when unsharded), the
+// piece of that shard's window that covers the stage's blocks, copied with
+// one cp.async.bulk from the 16-byte aligned address at or below the
+// piece's first element to the one at or above its end. The granules read
+// beyond the piece hold at least one in-window element each, so no byte is
+// read from a 16-byte granule (or page) that the window does not touch; the
+// consumers never look at the extra elements. The stage's descriptor (the
+// row, the block range, where each piece's first element landed and how
+// many elements it has) is written before the stage's "full" barrier is
+// armed with the bytes in flight.
+//
+// Consumers read a stage's elements from shared memory with consecutive
+// lanes on consecutive elements (no bank conflicts whatever the window's
+// alignment), fold the pieces with max.NaN, reduce each block across lanes
+// as order keys (keys.cuh) and store the block's key once: a stage holds
+// whole blocks, so no key is written twice and none needs an atomic.
+//
+//  - coop (all warps on one row): every consumer warp takes a share of every
+//    stage's blocks; when a unit's last stage is in, the warps rank the row
+//    together (topk.cuh with a named barrier, so the producer keeps
+//    filling the ring meanwhile). A long row cut into parts meets in the
+//    workspace as in select_kernel: each part publishes its keys, counts
+//    itself in, and the last part to arrive ranks the row.
+//  - solo (one row per warp): each consumer warp owns a sub-ring; the
+//    producer hands whole rows to the warps in turn and each warp ranks its
+//    own rows with topk_warp, without any CTA barrier.
+//
+// Work units: rows * S of them, unit u being part u % S of row u / S. With
+// a workspace the producer takes units from a queue counter in the
+// workspace (the last CTA to finish resets it to zero); without one, CTA b
+// takes units b, b + grid, ... and S is 1.
+#include "select_pipe.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "keys.cuh"
+#include "pipe.cuh"
+#include "topk.cuh"
+#include "topk_warp.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kMaxShardLanes = 32;  // shards per row: one producer lane each
+constexpr int kPipeMaxBlocks = 4096;
+constexpr int kPipeMaxTopk = 256;
+constexpr int32_t kPartUnit = 32;  // blocks: a part of a split row is a multiple
+
+// Stage flags.
+constexpr int32_t kFirst = 1;  // first stage of a unit
+constexpr int32_t kLast = 2;   // last stage of a unit: rank or merge after it
+constexpr int32_t kDone = 4;   // no more units for this consumer
+
+// Wait sites recorded in g_pipe_error on a timeout.
+constexpr unsigned kSiteFull = 1u, kSiteEmpty = 2u;
+
+struct StageDesc {
+  int32_t row;
+  int32_t c0;       // first block of the stage (row-relative)
+  int32_t n;        // blocks in the stage
+  int32_t flags;
+  int32_t npieces;
+  int32_t nblk;     // blocks of the row holding data
+  int32_t pin;      // pinned block, or -1
+  int32_t b0, b1;   // the unit's blocks
+  int32_t parts;    // parts of the row (1: the unit is the whole row)
+  uint32_t off;     // byte offset in the stage of the piece's first element
+  int32_t cnt;      // elements of the piece
+};
+
+struct PipeArgs {
+  const void* logits;
+  int64_t ld;
+  int64_t shard_stride;
+  int32_t shards;
+  int32_t width;
+  const int32_t* row_ks;
+  const int32_t* row_ke;
+  int32_t row_repeat;
+  int32_t block_size;
+  int32_t bs_log2;  // log2(block_size) when block_size < 32
+  int32_t global_block_size;
+  int32_t nb;
+  int32_t nb_data;
+  int32_t pin_newest;
+  int32_t topk;
+  int32_t kpad;
+  int32_t* out;
+  int64_t ld_out;
+  void* scores;
+  int64_t ld_scores;
+  int32_t rows;
+  int32_t split;        // S
+  uint32_t* queue;      // [0]: next unit, [1]: CTAs done; null: static schedule
+  uint32_t* ws_count;   // [rows] arrival counters (S > 1)
+  uint32_t* ws_keys;    // [rows, nb] (S > 1)
+  int32_t stages;       // ring depth (coop) or depth of each warp's ring (solo)
+  int32_t stage_bytes;  // multiple of 128
+  int32_t cap;          // blocks per stage
+};
+
+// ---------------------------------------------------------------------------
+// Shared-memory element loads
+// ---------------------------------------------------------------------------
+
+// Element of a stage, widened to fp32. `p` points into the CTA's shared
+// memory (derived from the kernel's shared array, so the compiler emits
+// shared loads and may batch them).
+template <typename E>
+__device__ __forceinline__ float stage_elem(const unsigned char* p) {
+  if constexpr (E::kBytes == 4) {
+    return *reinterpret_cast<const float*>(p);
+  } else {
+    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Row plans (producer side)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int32_t shard_cols(int32_t gke, int32_t d, int32_t shards, int32_t lw) {
+  if (gke <= d) return 0;
+  const uint32_t lke = (static_cast<uint32_t>(gke - d) + static_cast<uint32_t>(shards - 1)) /
+                       static_cast<uint32_t>(shards);
+  return static_cast<int32_t>(min(lke, static_cast<uint32_t>(lw)));
+}
+
+// One row's plan as the producer warp holds it: lane d < shards knows shard
+// d's window (first element and length); every lane knows the row totals.
+template <typename E>
+struct LanePlan {
+  const typename E::T* origin;  // shard `lane`'s first in-window element
+  int32_t len;                  // its window length (0 for lanes >= shards)
+  int32_t nblk;                 // the row's blocks holding data
+  int32_t pin;                  // pinned block or -1
+};
+
+// A row's bounds as read from memory: (ks or 0, ke) unsharded, (0, gke) in
+// the DCP form, (gks, gke) in the DCP form with starts.
+struct Bounds {
+  int32_t lo, hi;
+};
+
+template <int MODE>
+__device__ __forceinline__ Bounds load_bounds(const PipeArgs& a, int32_t row) {
+  const int32_t g = row / a.row_repeat;
+  Bounds b;
+  b.lo = (MODE != kPipeSharded && a.row_ks) ? __ldg(a.row_ks + g) : 0;
+  b.hi = __ldg(a.row_ke + g);
+  return b;
+}
+
+template <typename E, int MODE>
+__device__ __forceinline__ LanePlan<E> plan_lane(const PipeArgs& a, int32_t row, Bounds bnd,
+                                                 int lane) {
+  using TE = typename E::T;
+  const TE* logits = static_cast<const TE*>(a.logits);
+  LanePlan<E> p;
+  if constexpr (MODE == kPipeUnsharded) {
+    const int32_t ks = bnd.lo;
+    const int32_t ke = bnd.hi;
+    const int32_t e = min(ke, a.width);
+    const int32_t s = min(max(ks, 0), e);
+    const int32_t n = e > s ? e - s : 0;
+    p.origin = logits + static_cast<int64_t>(row) * a.ld + s;
+    p.len = lane == 0 ? n : 0;
+    p.nblk = static_cast<int32_t>((static_cast<uint32_t>(n) + a.block_size - 1u) /
+                                  static_cast<uint32_t>(a.block_size));
+    p.pin = (a.pin_newest && n > 0) ? (n - 1) / a.block_size : -1;
+  } else if constexpr (MODE == kPipeSharded) {
+    const int32_t gke = bnd.hi;
+    const int32_t n0 = shard_cols(gke, 0, a.shards, a.width);
+    p.origin = logits + static_cast<int64_t>(min(lane, a.shards - 1)) * a.shard_stride +
+               static_cast<int64_t>(row) * a.ld;
+    p.len = lane < a.shards ? shard_cols(gke, lane, a.shards, a.width) : 0;
+    p.nblk = min(static_cast<int32_t>((static_cast<uint32_t>(n0) + a.block_size - 1u) /
+                                      static_cast<uint32_t>(a.block_size)),
+                 a.nb_data);
+    p.pin = gke >= 1 ? static_cast<int32_t>(min(static_cast<uint32_t>(gke - 1) /
+                                                    static_cast<uint32_t>(a.global_block_size),
+                                                static_cast<uint32_t>(a.nb - 1)))
+                     : -1;
+  } else {
+    const int32_t gke = bnd.hi;
+    const int32_t gs = min(max(bnd.lo, 0), max(gke, 0));
+    const int32_t d = min(lane, a.shards - 1);
+    const int32_t e = shard_cols(gke, d, a.shards, a.width);
+    const int32_t st = min(shard_cols(gs, d, a.shards, a.width), e);
+    p.origin = logits + static_cast<int64_t>(d) * a.shard_stride +
+               static_cast<int64_t>(row) * a.ld + st;
+    p.len = lane < a.shards ? e - st : 0;
+    const int32_t lmax = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(p.len));
+    p.nblk = min(static_cast<int32_t>((static_cast<uint32_t>(lmax) + a.block_size - 1u) /
+                                      static_cast<uint32_t>(a.block_size)),
+                 a.nb_data);
+    p.pin = gke > gs ? static_cast<int32_t>(min(static_cast<uint32_t>(gke - gs - 1) /
+                                                    static_cast<uint32_t>(a.global_block_size),
+                                                static_cast<uint32_t>(a.nb - 1)))
+                     : -1;
+  }
+  return p;
+}
+
+// Emits the stages of blocks [b0, b1) of one row into a ring (all lanes of
+// the producer warp). ring: `stages` buffers of a.stage_bytes at `buf`;
+// full / empty: their barriers; desc: their descriptors; k: this ring's
+// stage counter. Returns false when a wait gave up.
+// `after_first` runs (on every lane) once the first stage's copies are in
+// flight: the producer fetches the next unit's bounds there, so that their
+// round trip overlaps this unit's stages.
+//
+// ONE_SHARD: every stage carries one shard's piece (its consumers merge the
+// shards into the keys with atomicMax), so that each bulk copy moves up to a
+// whole stage instead of 1 / shards of it; the stages go chunk by chunk,
+// shard by shard within a chunk.
+template <typename E, bool ONE_SHARD, typename Hook>
+__device__ __forceinline__ bool emit_unit(const PipeArgs& a, const LanePlan<E>& p, int32_t row,
+                                          int32_t b0, int32_t b1, int32_t parts, int npieces,
+                                          unsigned char* buf, uint64_t* full, uint64_t* empty,
+                                          StageDesc* desc, int stages, uint32_t& k,
+                                          Hook&& after_first) {
+  const int lane = threadIdx.x & 31;
+  const int32_t bs = a.block_size;
+  int32_t c = b0;
+  int shard = 0;  // ONE_SHARD: the shard of the next stage
+  bool first = true;
+  for (;;) {
+    const int32_t n = min(a.cap, b1 - c);
+    const bool last = c + n >= b1 && (!ONE_SHARD || shard == npieces - 1);
+    const bool mine = ONE_SHARD ? lane == shard : lane < npieces;
+    const uint32_t slot = k % static_cast<uint32_t>(stages);
+    const uint32_t round = k / static_cast<uint32_t>(stages);
+    int ok = 1;
+    if (lane == 0 && round > 0) ok = mbar_wait(&empty[slot], (round - 1u) & 1u, kSiteEmpty);
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+    // This lane's piece: elements [c*bs, min((c+n)*bs, len)) of its window.
+    const int32_t j0 = c * bs;
+    const int32_t j1 = min((c + n) * bs, p.len);
+    uintptr_t A = 0;
+    uint32_t bytes = 0, head = 0;
+    if (mine && j1 > j0) {
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(p.origin + j0);
+      const uintptr_t hi = reinterpret_cast<uintptr_t>(p.origin + j1);
+      A = lo & ~static_cast<uintptr_t>(15);
+      bytes = static_cast<uint32_t>(((hi + 15) & ~static_cast<uintptr_t>(15)) - A);
+      head = static_cast<uint32_t>(lo - A);
+    }
+    // Pieces are packed in lane order; every size is a multiple of 16.
+    uint32_t pos = bytes;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, pos, o);
+      if (lane >= o) pos += t;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, pos, 31);
+    pos -= bytes;  // exclusive prefix: this piece's offset in the stage
+    StageDesc& d = desc[slot];
+    if (mine) {
+      d.off = pos + head;
+      d.cnt = j1 > j0 ? j1 - j0 : 0;
+    }
+    if (lane == 0) {
+      d.row = row;
+      d.c0 = c;
+      d.n = n;
+      d.flags = (first ? kFirst : 0) | (last ? kLast : 0);
+      d.npieces = 1;
+      d.nblk = p.nblk;
+      d.pin = p.pin;
+      d.b0 = b0;
+      d.b1 = b1;
+      d.parts = parts;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      if (total > 0)
+        mbar_arrive_expect_tx(&full[slot], total);
+      else
+        mbar_arrive(&full[slot]);
+    }
+    __syncwarp();
+    if (bytes > 0)
+      bulk_load(buf + static_cast<size_t>(slot) * a.stage_bytes + pos,
+                reinterpret_cast<const void*>(A), bytes, &full[slot]);
+    ++k;
+    if (first) after_first();
+    first = false;
+    if (last) return true;
+    if (ONE_SHARD && shard + 1 < npieces) {
+      ++shard;
+    } else {
+      shard = 0;
+      c += n;
+    }
+  }
+}
+
+// A stage with no data that tells its consumer(s) to stop.
+__device__ __forceinline__ bool emit_done(unsigned char* buf, uint64_t* full, uint64_t* empty,
+                                          StageDesc* desc, int stages, uint32_t& k) {
+  (void)buf;
+  const int lane = threadIdx.x & 31;
+  const uint32_t slot = k % static_cast<uint32_t>(stages);
+  const uint32_t round = k / static_cast<uint32_t>(stages);
+  int ok = 1;
+  if (lane == 0) {
+    if (round > 0) ok = mbar_wait(&empty[slot], (round - 1u) & 1u, kSiteEmpty);
+    if (ok) {
+      desc[slot].flags = kDone;
+      mbar_arrive(&full[slot]);
+    }
+  }
+  ++k;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// ---------------------------------------------------------------------------
+// Consumer side
+// ---------------------------------------------------------------------------
+
+// Folds the blocks of one stage that belong to this warp into keys[c0 + b].
+//
+// Lane per block (the common block sizes, see fold_stage): a warp takes 32
+// consecutive blocks at a time and lane l folds block 32g + l on its own,
+// over every piece, with no exchange between lanes. Lane l visits the
+// elements of its block in its own order: element i ^ l for blocks of 32 or
+// more (i ^ l stays inside the same aligned run of 32), (i + l / (32 / bs))
+// mod bs for smaller ones. The 32 lanes of every load then ask for 32
+// different banks whatever the pieces' alignment (checked exhaustively on the
+// CPU for every block size and offset, fp32; bf16 lanes pair up on words).
+// A lane keeps a whole block's loads in flight, and each key is stored once.
+// Groups go to the consumer warps in turn across stages (`gbase`: groups in
+// the earlier stages).
+// MERGE: several stages hold pieces of the same blocks (one shard each), so
+// keys are merged with atomicMax into keys that start at key(-inf).
+template <typename E, int BS, bool MERGE>
+__device__ __forceinline__ void fold_lane_blocks(const unsigned char* stage, const StageDesc& d,
+                                                 int g0, int gstep,
+                                                 uint32_t* __restrict__ keys) {
+  constexpr int ES = E::kBytes;
+  constexpr int T = BS < 32 ? BS : 32;  // offsets in the lane's table
+  constexpr int CH = BS < 32 ? 1 : BS / 32;
+  constexpr int LB = BS <= 1 ? 0 : BS == 2 ? 1 : BS == 4 ? 2 : BS == 8 ? 3 : 4;
+  const int lane = threadIdx.x & 31;
+  const int32_t c0 = d.c0, n = d.n;
+  // Byte offsets of this lane's visiting order within a run of T elements.
+  uint32_t offs[T];
+#pragma unroll
+  for (int i = 0; i < T; ++i)
+    offs[i] = static_cast<uint32_t>(BS >= 32 ? (i ^ lane) : ((i + (lane >> (5 - LB))) & (BS - 1))) *
+              ES;
+  const int32_t ngroups = (n + 31) >> 5;
+  for (int32_t g = g0; g < ngroups; g += gstep) {
+    const int32_t blk = g * 32 + lane;
+    if (blk >= n) continue;
+    float acc[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+    {
+      const int32_t valid = d.cnt - blk * BS;
+      if (valid <= 0) continue;
+      const unsigned char* pb = stage + d.off + static_cast<uint32_t>(blk * BS) * ES;
+      if (valid >= BS) {
+#pragma unroll
+        for (int i = 0; i < T; ++i)
+#pragma unroll
+          for (int c = 0; c < CH; ++c)
+            acc[(i + c) & 3] =
+                max_nan(acc[(i + c) & 3], stage_elem<E>(pb + offs[i] + c * 32 * ES));
+      } else {
+        // The window's last block: only its first `valid` elements.
+        for (int32_t e = 0; e < valid; ++e) acc[0] = max_nan(acc[0], stage_elem<E>(pb + e * ES));
+      }
+    }
+    const uint32_t key = order_key(max_nan(max_nan(acc[0], acc[1], acc[2]), acc[3]));
+    if (MERGE)
+      atomicMax(&keys[c0 + blk], key);
+    else
+      keys[c0 + blk] = key;
+  }
+}
+
+// Other block sizes: lanes on consecutive elements, unconditional loads (an
+// index past a piece's end reads the piece's first element, inside the CTA's
+// shared memory, and a select drops it), one warp reduction per block (a
+// redux, or xor shuffles over bs lanes for blocks below 32).
+template <typename E, bool MERGE>
+__device__ __forceinline__ void fold_elems(const unsigned char* stage, const StageDesc& d,
+                                           int32_t bs, int32_t bs_log2, int t0, int tstep,
+                                           uint32_t* __restrict__ keys) {
+  constexpr int ES = E::kBytes;
+  const int lane = threadIdx.x & 31;
+  const int32_t c0 = d.c0, n = d.n;
+  if (bs >= 32) {
+    for (int32_t b = t0; b < n; b += tstep) {
+      float acc = neg_inf();
+      for (int32_t i = 0; i < bs; i += 32) {
+        const int32_t j = b * bs + i + lane;
+        const int32_t lim = d.cnt;
+        const float v = stage_elem<E>(stage + d.off + (j < lim ? j : 0) * ES);
+        acc = j < lim ? max_nan(acc, v) : acc;
+      }
+      const uint32_t key = __reduce_max_sync(0xffffffffu, order_key(acc));
+      if (lane == 0) {
+        if (MERGE)
+          atomicMax(&keys[c0 + b], key);
+        else
+          keys[c0 + b] = key;
+      }
+    }
+  } else {
+    const int32_t ntile = (n * bs + 31) >> 5;
+    for (int32_t tt = t0; tt < ntile; tt += tstep) {
+      const int32_t j = tt * 32 + lane;
+      const int32_t lim = d.cnt;
+      const float v = stage_elem<E>(stage + d.off + (j < lim ? j : 0) * ES);
+      const float acc = j < lim ? v : neg_inf();
+      uint32_t key = order_key(acc);
+      for (int o = 1; o < bs; o <<= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+      const int32_t blk = j >> bs_log2;
+      if ((lane & (bs - 1)) == 0 && blk < n) {
+        if (MERGE)
+          atomicMax(&keys[c0 + blk], key);
+        else
+          keys[c0 + blk] = key;
+      }
+    }
+  }
+}
+
+// Whether a block size takes the lane-per-block path (one piece per stage in
+// every mode).
+__host__ __device__ __forceinline__ bool lane_per_block(int32_t bs) {
+  return bs >= 2 && bs <= 128 && (bs & (bs - 1)) == 0;
+}
+
+// The warp's share of one stage: the lane-per-block groups (gbase + g) %
+// gstep == g0, or every gstep-th block / tile of the element path.
+template <typename E, int MODE>
+__device__ __forceinline__ void fold_stage(const PipeArgs& a, const unsigned char* stage,
+                                           const StageDesc& d, int g0, int gstep, uint32_t gbase,
+                                           uint32_t* __restrict__ keys) {
+  constexpr bool M = MODE != kPipeUnsharded;  // one shard per stage: merge
+  const int first = static_cast<int>((static_cast<uint32_t>(g0) + gstep - gbase % gstep) % gstep);
+  switch (a.block_size) {
+    case 2: fold_lane_blocks<E, 2, M>(stage, d, first, gstep, keys); return;
+    case 4: fold_lane_blocks<E, 4, M>(stage, d, first, gstep, keys); return;
+    case 8: fold_lane_blocks<E, 8, M>(stage, d, first, gstep, keys); return;
+    case 16: fold_lane_blocks<E, 16, M>(stage, d, first, gstep, keys); return;
+    case 32: fold_lane_blocks<E, 32, M>(stage, d, first, gstep, keys); return;
+    case 64: fold_lane_blocks<E, 64, M>(stage, d, first, gstep, keys); return;
+    case 128: fold_lane_blocks<E, 128, M>(stage, d, first, gstep, keys); return;
+    default: fold_elems<E, M>(stage, d, a.block_size, a.bs_log2, g0, gstep, keys); return;
+  }
+}
+
+// Lane-per-block groups in a stage of n blocks (0 for the element path,
+// whose work is split by block or tile and needs no rotation).
+__device__ __forceinline__ uint32_t stage_groups(int32_t bs, int32_t n) {
+  return lane_per_block(bs) ? static_cast<uint32_t>((n + 31) >> 5) : 0u;
+}
+
+// The keys of a part [b0, b1) of a row that is split over several units:
+// published to the workspace; the last part to arrive reads the others back
+// and goes on to rank (returns true to every consumer thread).
+template <typename Sync>
+__device__ __forceinline__ bool merge_parts(const PipeArgs& a, int32_t row, int32_t nblk,
+                                            int32_t b0, int32_t b1, int32_t parts, uint32_t* keys,
+                                            int* s_last) {
+  uint32_t* wrow = a.ws_keys + static_cast<int64_t>(row) * a.nb;
+  for (int32_t b = b0 + threadIdx.x; b < b1; b += Sync::count()) __stcg(wrow + b, keys[b]);
+  __threadfence();
+  Sync::sync();
+  if (threadIdx.x == 0) {
+    // Count this part in; a counter word can hold an earlier call's block key
+    // (>= key(-inf)), which reads as zero. Each failed CAS but the first
+    // means another part arrived, so parts + 1 attempts suffice.
+    uint32_t* counter = a.ws_count + row;
+    uint32_t seen = 0u;
+    int last = 0;
+    for (int32_t i = 0; i < parts + 2; ++i) {
+      const uint32_t count = (seen >= kKeyNegInf ? 0u : seen) + 1u;
+      const uint32_t want = count == static_cast<uint32_t>(parts) ? 0u : count;
+      const uint32_t prev = atomicCAS(counter, seen, want);
+      if (prev == seen) {
+        last = count == static_cast<uint32_t>(parts);
+        break;
+      }
+      seen = prev;
+    }
+    *s_last = last;
+  }
+  Sync::sync();
+  if (!*s_last) return false;
+  __threadfence();
+  for (int32_t b = threadIdx.x; b < nblk; b += Sync::count())
+    if (b < b0 || b >= b1) keys[b] = __ldcg(wrow + b);
+  return true;
+}
+
+template <typename E>
+__device__ __forceinline__ typename E::T* score_row(const PipeArgs& a, int32_t row) {
+  return a.scores ? static_cast<typename E::T*>(a.scores) + static_cast<int64_t>(row) * a.ld_scores
+                  : nullptr;
+}
+
+// Takes the next unit: from the workspace queue, or the static stride.
+__device__ __forceinline__ uint32_t next_unit(const PipeArgs& a, uint32_t cur) {
+  return a.queue ? atomicAdd(a.queue, 1u) : cur + gridDim.x;
+}
+
+// After a CTA's last (failing) take: the last CTA to finish resets the queue.
+__device__ __forceinline__ void retire_queue(const PipeArgs& a) {
+  if (!a.queue) return;
+  __threadfence();
+  if (atomicAdd(a.queue + 1, 1u) == gridDim.x - 1u) {
+    atomicExch(a.queue, 0u);
+    atomicExch(a.queue + 1, 0u);
+  }
+}
+
+// Shared memory of a coop CTA: ring, barriers, descriptors, keys [nb],
+// candidates [max(kpad, kRankMax)].
+__host__ __device__ __forceinline__ size_t coop_keys_offset(int stages, int stage_bytes) {
+  return static_cast<size_t>(stages) * stage_bytes +
+         ((static_cast<size_t>(stages) * (16 + sizeof(StageDesc)) + 127) & ~static_cast<size_t>(127));
+}
+
+template <typename E, int MODE, int NW>
+__global__ void __launch_bounds__((NW + 1) * 32, NW == 4 ? 4 : 2) pipe_coop_kernel(const PipeArgs a) {
+  using Sync = NamedSync<NW * 32>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(a.stages) * a.stage_bytes);
+  uint64_t* empty = full + a.stages;
+  StageDesc* desc = reinterpret_cast<StageDesc*>(empty + a.stages);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + coop_keys_offset(a.stages, a.stage_bytes));
+  uint64_t* cand = reinterpret_cast<uint64_t*>(keys + ((a.nb + 3) & ~3));
+  __shared__ TopkShared tsh;
+  __shared__ int s_last;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.stages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], NW);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (warp == NW) {
+    // Producer warp.
+    const uint32_t total = static_cast<uint32_t>(a.rows) * static_cast<uint32_t>(a.split);
+    const int npieces = MODE == kPipeUnsharded ? 1 : a.shards;
+    uint32_t k = 0;
+    uint32_t u = 0;
+    if (lane == 0) u = a.queue ? atomicAdd(a.queue, 1u) : blockIdx.x;
+    u = __shfl_sync(0xffffffffu, u, 0);
+    const uint32_t S = static_cast<uint32_t>(a.split);
+    Bounds bnd{0, 0};
+    if (u < total) bnd = load_bounds<MODE>(a, static_cast<int32_t>(u / S));
+    bool ok = true;
+    while (ok && u < total) {
+      uint32_t nu = 0;
+      if (lane == 0) nu = next_unit(a, u);  // in flight while this unit's stages go out
+      Bounds nbnd{0, 0};
+      bool fetched = false;
+      auto prefetch = [&]() {
+        nu = __shfl_sync(0xffffffffu, nu, 0);
+        if (nu < total) nbnd = load_bounds<MODE>(a, static_cast<int32_t>(nu / S));
+        fetched = true;
+      };
+      const int32_t row = static_cast<int32_t>(u / S);
+      const int32_t part = static_cast<int32_t>(u % S);
+      const LanePlan<E> p = plan_lane<E, MODE>(a, row, bnd, lane);
+      int32_t b0 = 0, b1 = p.nblk, parts = 1;
+      if (a.split > 1) {
+        const int32_t per = max(kPartUnit, ((p.nblk + a.split - 1) / a.split + kPartUnit - 1) /
+                                               kPartUnit * kPartUnit);
+        parts = max(1, (p.nblk + per - 1) / per);
+        b0 = min(part * per, p.nblk);
+        b1 = min(b0 + per, p.nblk);
+      }
+      if (part < parts)
+        ok = emit_unit<E, MODE != kPipeUnsharded>(a, p, row, b0, b1, parts, npieces, ring, full,
+                                                  empty, desc, a.stages, k, prefetch);
+      if (!fetched) prefetch();
+      u = nu;
+      bnd = nbnd;
+    }
+    if (lane == 0) retire_queue(a);
+    if (ok) emit_done(ring, full, empty, desc, a.stages, k);
+    return;
+  }
+
+  // Consumer warps. In the shard forms every stage holds one shard, and its
+  // keys are merged into keys that start at key(-inf) for every row.
+  constexpr bool kMerge = MODE != kPipeUnsharded;
+  if (kMerge) {
+    for (int32_t b = threadIdx.x; b < a.nb; b += Sync::count()) keys[b] = kKeyNegInf;
+    Sync::sync();
+  }
+  uint32_t gbase = 0;  // lane-per-block groups in the stages before this one
+  for (uint32_t k = 0;; ++k) {
+    const uint32_t slot = k % static_cast<uint32_t>(a.stages);
+    // A phase that never completes (a fault in the byte accounting) makes
+    // every waiter give up; the warp leaves as one.
+    const bool ok = mbar_wait(&full[slot], (k / static_cast<uint32_t>(a.stages)) & 1u, kSiteFull);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const StageDesc& d = desc[slot];
+    const int32_t flags = d.flags;
+    if (flags & kDone) return;
+    const int32_t row = d.row, nblk = d.nblk, pin = d.pin, b0 = d.b0, b1 = d.b1,
+                  parts = d.parts;
+    fold_stage<E, MODE>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d, warp, NW, gbase,
+                        keys);
+    gbase += stage_groups(a.block_size, d.n);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (!(flags & kLast)) continue;
+    Sync::sync();  // every block of the unit is in keys
+    if (parts > 1 && !merge_parts<Sync>(a, row, nblk, b0, b1, parts, keys, &s_last)) {
+      if (kMerge)
+        for (int32_t b = threadIdx.x; b < a.nb; b += Sync::count()) keys[b] = kKeyNegInf;
+      Sync::sync();
+      continue;
+    }
+    for (int32_t b = nblk + threadIdx.x; b <= pin; b += Sync::count()) keys[b] = kKeyNegInf;
+    Sync::sync();
+    topk_store<typename E::T, Sync>(keys, a.nb, max(nblk, pin + 1), min(a.topk, a.nb), pin, cand,
+                                    a.kpad,
+                                    a.topk > 0 ? a.out + static_cast<int64_t>(row) * a.ld_out
+                                               : nullptr,
+                                    a.topk, score_row<E>(a, row), tsh);
+    Sync::sync();  // keys and candidates are free for the next unit
+    if (kMerge) {
+      for (int32_t b = threadIdx.x; b < a.nb; b += Sync::count()) keys[b] = kKeyNegInf;
+      Sync::sync();
+    }
+  }
+}
+
+// Shared memory of a solo CTA: NW rings of `stages`, their full barriers and
+// descriptors, then per warp its keys [nb] and candidates [kWarpCand].
+__host__ __device__ __forceinline__ size_t solo_warp_offset(int nw, int stages, int stage_bytes) {
+  const size_t nst = static_cast<size_t>(nw) * stages;
+  return nst * stage_bytes + ((nst * (8 + sizeof(StageDesc)) + 127) & ~static_cast<size_t>(127));
+}
+__host__ __device__ __forceinline__ size_t solo_warp_bytes(int32_t nb) {
+  return static_cast<size_t>(kWarpCand) * 8 + static_cast<size_t>((nb + 3) & ~3) * 4;
+}
+
+// One stage of an unsharded row for a warp that produces for itself: lane
+// 0 copies blocks [c, c + n) of the window and arms the stage's barrier.
+template <typename E>
+__device__ __forceinline__ void solo_emit(const PipeArgs& a, const LanePlan<E>& p, int32_t row,
+                                          int32_t c, int32_t n, bool last,
+                                          unsigned char* buf, uint64_t* full, StageDesc& d) {
+  const int32_t j0 = c * a.block_size;
+  const int32_t j1 = min((c + n) * a.block_size, p.len);
+  uintptr_t A = 0;
+  uint32_t bytes = 0, head = 0;
+  if (j1 > j0) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p.origin + j0);
+    const uintptr_t hi = reinterpret_cast<uintptr_t>(p.origin + j1);
+    A = lo & ~static_cast<uintptr_t>(15);
+    bytes = static_cast<uint32_t>(((hi + 15) & ~static_cast<uintptr_t>(15)) - A);
+    head = static_cast<uint32_t>(lo - A);
+  }
+  d.row = row;
+  d.c0 = c;
+  d.n = n;
+  d.flags = last ? kLast : 0;
+  d.npieces = 1;
+  d.nblk = p.nblk;
+  d.pin = p.pin;
+  d.b0 = 0;
+  d.b1 = p.nblk;
+  d.parts = 1;
+  d.off = head;
+  d.cnt = j1 > j0 ? j1 - j0 : 0;
+  if (bytes > 0) {
+    mbar_arrive_expect_tx(full, bytes);
+    bulk_load(buf, reinterpret_cast<const void*>(A), bytes, full);
+  } else {
+    mbar_arrive(full);
+  }
+}
+
+// One row per warp, each warp its own producer: warp g of the grid takes rows
+// g, g + G, ... (G warps in all). Lane 0 keeps the warp's ring full: it
+// issues the stages of the rows ahead (fetching each next row's bounds while
+// the current one goes out) whenever a slot is free, so the copies of the
+// next rows are in flight while the warp folds and ranks this one. A slot is
+// free once the warp has folded it (the warp's own program order, with a
+// __syncwarp before lane 0 reuses it), so no empty barriers are needed and no
+// warp waits for another.
+template <typename E, int NW>
+__global__ void __launch_bounds__(NW * 32, 2) pipe_solo_kernel(const PipeArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int nst = NW * a.stages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* ring = smem + static_cast<size_t>(warp) * a.stages * a.stage_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(nst) * a.stage_bytes) +
+                   warp * a.stages;
+  StageDesc* desc = reinterpret_cast<StageDesc*>(
+                        reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(nst) * a.stage_bytes) +
+                        nst) +
+                    warp * a.stages;
+  unsigned char* wbase = smem + solo_warp_offset(NW, a.stages, a.stage_bytes);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(wbase + static_cast<size_t>(warp) * solo_warp_bytes(a.nb));
+  uint32_t* keys = reinterpret_cast<uint32_t*>(cand + kWarpCand);
+  if (lane == 0) {
+    for (int i = 0; i < a.stages; ++i) mbar_init(&full[i], 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+
+  const uint32_t rows = static_cast<uint32_t>(a.rows);
+  const uint32_t G = gridDim.x * NW;
+  // Producer state (lane 0's values are the ones used): the row being issued,
+  // its plan, the next block to issue, and the next row's bounds.
+  uint32_t prow = blockIdx.x * NW + warp;
+  Bounds bnd{0, 0}, nbnd{0, 0};
+  if (prow < rows) bnd = load_bounds<kPipeUnsharded>(a, static_cast<int32_t>(prow));
+  if (prow + G < rows) nbnd = load_bounds<kPipeUnsharded>(a, static_cast<int32_t>(prow + G));
+  LanePlan<E> p = plan_lane<E, kPipeUnsharded>(a, static_cast<int32_t>(prow), bnd, 0);
+  int32_t pc = 0;
+  uint32_t kp = 0;  // stages issued
+  for (uint32_t kc = 0;; ++kc) {
+    // Issue while slots are free and rows remain.
+    if (lane == 0) {
+      while (prow < rows && kp - kc < static_cast<uint32_t>(a.stages)) {
+        const uint32_t slot = kp % static_cast<uint32_t>(a.stages);
+        const int32_t n = min(a.cap, p.nblk - pc);
+        const bool last = pc + n >= p.nblk;
+        solo_emit<E>(a, p, static_cast<int32_t>(prow), pc, n, last,
+                     ring + static_cast<size_t>(slot) * a.stage_bytes, &full[slot], desc[slot]);
+        ++kp;
+        pc += n;
+        if (last) {
+          prow += G;
+          pc = 0;
+          if (prow < rows) {
+            p = plan_lane<E, kPipeUnsharded>(a, static_cast<int32_t>(prow), nbnd, 0);
+            if (prow + G < rows) nbnd = load_bounds<kPipeUnsharded>(a, static_cast<int32_t>(prow + G));
+          }
+        }
+      }
+    }
+    kp = __shfl_sync(0xffffffffu, kp, 0);
+    if (kc >= kp) break;  // nothing issued beyond what was consumed: done
+    const uint32_t slot = kc % static_cast<uint32_t>(a.stages);
+    const bool ok = mbar_wait(&full[slot], (kc / static_cast<uint32_t>(a.stages)) & 1u, kSiteFull);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const StageDesc& d = desc[slot];
+    const int32_t flags = d.flags;
+    const int32_t row = d.row, nblk = d.nblk, pin = d.pin;
+    fold_stage<E, kPipeUnsharded>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d, 0, 1,
+                                  0u, keys);
+    __syncwarp();  // the slot and its descriptor are free for lane 0
+    if (!(flags & kLast)) continue;
+    topk_warp(keys, a.nb, nblk, min(a.topk, a.nb), pin, cand,
+              a.topk > 0 ? a.out + static_cast<int64_t>(row) * a.ld_out : nullptr, a.topk,
+              score_row<E>(a, row));
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+std::atomic<int> g_over[16];
+
+int sm_count_now() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+int max_smem_optin() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      n = 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+int max_smem_per_sm() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+        cudaSuccess)
+      n = 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Remembers the largest dynamic shared memory set per (kernel, device).
+std::mutex g_attr_mu;
+struct AttrEntry {
+  const void* fn;
+  int dev;
+  size_t bytes;
+};
+AttrEntry g_attr[64];
+int g_attr_n = 0;
+
+template <typename K>
+cudaError_t opt_in_smem(K kernel, size_t bytes) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const void* fn = reinterpret_cast<const void*>(kernel);
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  for (int i = 0; i < g_attr_n; ++i)
+    if (g_attr[i].fn == fn && g_attr[i].dev == dev) {
+      if (g_attr[i].bytes >= bytes) return cudaSuccess;
+      err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(bytes));
+      if (err == cudaSuccess) g_attr[i].bytes = bytes;
+      return err;
+    }
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bytes));
+  if (err == cudaSuccess && g_attr_n < 64) g_attr[g_attr_n++] = {fn, dev, bytes};
+  return err;
+}
+
+constexpr int kSoloWarps = 8;
+
+bool pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+int log2i(int64_t x) {
+  int l = 0;
+  while ((int64_t(1) << (l + 1)) <= x) ++l;
+  return l;
+}
+
+bool logits_on_device(const void* p) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return attr.type == cudaMemoryTypeDevice;
+}
+
+// Whether to hand short unsharded rows one per warp.
+bool want_solo(const PipeCall& c) {
+  const int forced = g_over[DSA_LAUNCH_PIPELINE].load(std::memory_order_relaxed);
+  if (forced == 2) return false;
+  const bool fits = c.mode == kPipeUnsharded && c.topk <= 32 && c.nb <= 2048;
+  if (forced == 3) return fits;
+  return fits && static_cast<int64_t>(c.width) * c.elem_bytes <= 64 * 1024 &&
+         c.rows >= 8 * static_cast<int64_t>(sm_count_now());
+}
+
+}  // namespace
+
+void pipe_set_override(int knob, int value) {
+  if (knob >= 0 && knob < 16) g_over[knob].store(value);
+}
+int pipe_get_override(int knob) { return (knob >= 0 && knob < 16) ? g_over[knob].load() : 0; }
+
+bool pipe_takes(const PipeCall& c) {
+  const int forced = g_over[DSA_LAUNCH_PIPELINE].load(std::memory_order_relaxed);
+  if (forced == 1) return false;
+  // The shard forms stay on select_kernel unless the pipelined kernels are
+  // asked for: there select_kernel's eight shard streams per CTA measured
+  // faster (DCP 85.8 us against 116 us and more).
+  if (c.mode != kPipeUnsharded && forced == 0) return false;
+  const int32_t bs = c.block_size;
+  if (!(bs % 32 == 0 || (pow2(bs) && bs < 32))) return false;
+  if (c.shards > kMaxShardLanes || c.nb > kPipeMaxBlocks || c.topk > kPipeMaxTopk) return false;
+  if (c.rows * 8 > INT32_MAX) return false;
+  if (static_cast<int64_t>(bs) * c.elem_bytes > 4096) return false;
+  return logits_on_device(c.logits);
+}
+
+namespace {
+
+// Shared memory a CTA may use when `ctas` of them share an SM (each CTA
+// also pays the SM's 1 KiB reservation), less `static_bytes` of static
+// shared memory.
+size_t smem_budget(int ctas, size_t static_bytes) {
+  const size_t per_sm = static_cast<size_t>(max_smem_per_sm());
+  const size_t per_cta = std::min<size_t>(static_cast<size_t>(max_smem_optin()),
+                                          per_sm / ctas - 1024);
+  return per_cta > static_bytes + 64 ? per_cta - static_bytes - 64 : 0;
+}
+
+template <typename E, int MODE, int NW>
+dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int ctas,
+                          cudaStream_t s) {
+  const int sms = sm_count_now();
+  const int pieces = 1;  // one piece per stage (one shard in the shard forms)
+  // A stage carries `payload` bytes of whole blocks; its buffer adds 32 bytes
+  // for the 16-byte rounding at both ends of the piece.
+  const int kb = g_over[DSA_LAUNCH_PIPE_STAGE_KB].load(std::memory_order_relaxed);
+  const int payload = (kb >= 4 && kb <= 64 ? kb : 32) * 1024;
+  a.stage_bytes = (payload + 32 * pieces + 127) & ~127;
+  a.cap = static_cast<int32_t>(payload /
+                               (static_cast<int64_t>(pieces) * a.block_size * E::kBytes));
+  if (a.cap < 1) return DSA_EUNSUPPORTED;
+  const int slots = sms * ctas;
+  // Parts per row: only when there are fewer rows than CTAs, never below
+  // 64 KiB per part, at most 8; only with a workspace. (Merging parts costs
+  // each part a fence, an atomic and a read-back: decode measured 30.7 us
+  // unsplit against 45 us in 4 parts.)
+  int split = 1;
+  if (have_ws) {
+    while (split < 8 && a.rows * split < slots && max_row_bytes / (2 * split) >= 64 * 1024)
+      split <<= 1;
+    const int forced = g_over[DSA_LAUNCH_PIPE_SPLIT].load(std::memory_order_relaxed);
+    if (forced >= 1 && forced <= 8) split = forced;
+  }
+  a.split = split;
+  const size_t tail = static_cast<size_t>((a.nb + 3) & ~3) * 4 +
+                      static_cast<size_t>(std::max(a.kpad, kRankMax)) * 8;
+  const size_t limit = smem_budget(ctas, sizeof(TopkShared) + 16);
+  int stages = 16;
+  while (stages >= 2 && coop_keys_offset(stages, a.stage_bytes) + tail > limit) --stages;
+  const int fst = g_over[DSA_LAUNCH_PIPE_STAGES].load(std::memory_order_relaxed);
+  if (fst >= 2 && fst < stages) stages = fst;
+  if (stages < 2) return DSA_EUNSUPPORTED;
+  a.stages = stages;
+  const size_t smem = coop_keys_offset(stages, a.stage_bytes) + tail;
+  auto kernel = pipe_coop_kernel<E, MODE, NW>;
+  if (opt_in_smem(kernel, smem) != cudaSuccess) return DSA_ECUDA;
+  const int64_t units = a.rows * static_cast<int64_t>(split);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(units, slots));
+  kernel<<<grid, (NW + 1) * 32, smem, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
+}
+
+template <typename E, int MODE>
+dsa_status launch_coop(const PipeArgs& a, int64_t max_row_bytes, bool have_ws, cudaStream_t s) {
+  const int warps = g_over[DSA_LAUNCH_PIPE_WARPS].load(std::memory_order_relaxed);
+  const int fc = g_over[DSA_LAUNCH_PIPE_CTAS].load(std::memory_order_relaxed);
+  if (warps == 8)
+    return launch_coop_nw<E, MODE, 8>(a, max_row_bytes, have_ws, fc >= 1 ? std::min(fc, 2) : 1,
+                                      s);
+  return launch_coop_nw<E, MODE, 4>(a, max_row_bytes, have_ws, fc >= 1 ? fc : 2, s);
+}
+
+template <typename E>
+dsa_status launch_solo(PipeArgs a, cudaStream_t s) {
+  const int sms = sm_count_now();
+  const int fc = g_over[DSA_LAUNCH_PIPE_CTAS].load(std::memory_order_relaxed);
+  const int ctas = fc >= 1 ? std::min(fc, 2) : 2;
+  const int kb = g_over[DSA_LAUNCH_PIPE_STAGE_KB].load(std::memory_order_relaxed);
+  const size_t limit = smem_budget(ctas, 0);
+  const size_t fixed = static_cast<size_t>(kSoloWarps) * solo_warp_bytes(a.nb);
+  a.split = 1;
+  a.queue = nullptr;
+  // Stages of 8 KiB (4 KiB when two per warp do not fit), up to 4 per warp.
+  int stages = 0;
+  for (int payload = kb >= 4 && kb <= 64 ? kb * 1024 : 8192; payload >= 4096; payload /= 2) {
+    a.stage_bytes = (payload + 32 + 127) & ~127;
+    a.cap = static_cast<int32_t>(payload / (static_cast<int64_t>(a.block_size) * E::kBytes));
+    stages = 4;
+    while (stages >= 2 && solo_warp_offset(kSoloWarps, stages, a.stage_bytes) + fixed > limit)
+      --stages;
+    if ((stages >= 2 && a.cap >= 1) || kb != 0) break;
+  }
+  const int fst = g_over[DSA_LAUNCH_PIPE_STAGES].load(std::memory_order_relaxed);
+  if (fst >= 2 && fst < stages) stages = fst;
+  if (stages < 2 || a.cap < 1) return DSA_EUNSUPPORTED;
+  a.stages = stages;
+  const size_t smem = solo_warp_offset(kSoloWarps, stages, a.stage_bytes) + fixed;
+  auto kernel = pipe_solo_kernel<E, kSoloWarps>;
+  if (opt_in_smem(kernel, smem) != cudaSuccess) return DSA_ECUDA;
+  const unsigned grid = static_cast<unsigned>(
+      std::min<int64_t>((a.rows + kSoloWarps - 1) / kSoloWarps, static_cast<int64_t>(sms) * ctas));
+  kernel<<<grid, kSoloWarps * 32, smem, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
+}
+
+template <typename E>
+dsa_status dispatch(const PipeCall& c, cudaStream_t s) {
+  PipeArgs a{};
+  a.logits = c.logits;
+  a.ld = c.ld;
+  a.shard_stride = c.shard_stride;
+  a.shards = c.shards;
+  a.width = c.width;
+  a.row_ks = c.row_ks;
+  a.row_ke = c.row_ke;
+  a.row_repeat = c.row_repeat;
+  a.block_size = c.block_size;
+  a.bs_log2 = c.block_size < 32 ? log2i(c.block_size) : 0;
+  a.global_block_size = c.global_block_size;
+  a.nb = c.nb;
+  a.nb_data = c.nb_data;
+  a.pin_newest = c.pin_newest;
+  a.topk = c.topk;
+  int32_t kp = 1;
+  while (kp < std::max<int32_t>(1, std::min(c.topk, c.nb))) kp <<= 1;
+  a.kpad = kp;
+  a.out = c.out;
+  a.ld_out = c.ld_out;
+  a.scores = c.scores;
+  a.ld_scores = c.ld_scores;
+  a.rows = static_cast<int32_t>(c.rows);
+  // A workspace of full size gives split rows their keys and counters and,
+  // unless a fixed order is forced, the unit queue.
+  const bool have_ws = c.workspace && c.workspace_size >= ws_total_bytes(c.rows, c.nb);
+  if (have_ws) {
+    if (g_over[DSA_LAUNCH_PIPE_SCHED].load(std::memory_order_relaxed) != 1)
+      a.queue = static_cast<uint32_t*>(c.workspace);
+    a.ws_count = reinterpret_cast<uint32_t*>(static_cast<char*>(c.workspace) + ws_counts_offset());
+    a.ws_keys = reinterpret_cast<uint32_t*>(static_cast<char*>(c.workspace) + ws_keys_offset(c.rows));
+  }
+  const int64_t max_row_bytes = static_cast<int64_t>(c.width) * c.elem_bytes * c.shards;
+  if (want_solo(c)) return launch_solo<E>(a, s);
+  switch (c.mode) {
+    case kPipeUnsharded: return launch_coop<E, kPipeUnsharded>(a, max_row_bytes, have_ws, s);
+    case kPipeSharded: return launch_coop<E, kPipeSharded>(a, max_row_bytes, have_ws, s);
+    default: return launch_coop<E, kPipeShardedStarts>(a, max_row_bytes, have_ws, s);
+  }
+}
+
+}  // namespace
+
+dsa_status pipe_select(const PipeCall& c, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return c.elem_bytes == 4 ? dispatch<F32>(c, s) : dispatch<BF16>(c, s);
+}
+
+}  // namespace dsa
+
+extern "C" int dsa_pipeline_error(int clear) {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, dsa::g_pipe_error, sizeof(v)) != cudaSuccess) return -1;
+  if (clear && v) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(dsa::g_pipe_error, &zero, sizeof(zero)) != cudaSuccess) return -1;
+  }
+  return static_cast<int>(v);
+}

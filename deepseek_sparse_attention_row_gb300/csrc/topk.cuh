@@ -35,6 +35,21 @@ namespace dsa {
 
 constexpr int kRankMax = 256;  // candidates ranked by counting
 
+// Which threads take part in a row's top-k, and how they meet. CtaSync: every
+// thread of the CTA, __syncthreads(). NamedSync<N>: threads 0 .. N - 1 (whole
+// warps), named barrier 1, so that other warps of the CTA (a producer) carry
+// on meanwhile.
+struct CtaSync {
+  __device__ __forceinline__ static void sync() { __syncthreads(); }
+  __device__ __forceinline__ static int count() { return blockDim.x; }
+};
+template <int N>
+struct NamedSync {
+  static_assert(N % 32 == 0, "whole warps");
+  __device__ __forceinline__ static void sync() { asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory"); }
+  __device__ __forceinline__ static constexpr int count() { return N; }
+};
+
 struct TopkShared {
   uint32_t hist[256];
   uint32_t warp_count[32], warp_kth[32], warp_max[32], warp_min[32];
@@ -52,31 +67,33 @@ __device__ __forceinline__ int32_t candidate_id(uint64_t c) {
 
 // Stores ranks of cand[0 .. n) (distinct composites): rank r < K goes to
 // out[r]; out[K .. topk) becomes -1. No barrier inside.
+template <typename Sync = CtaSync>
 __device__ __forceinline__ void rank_store(const uint64_t* __restrict__ cand, int32_t n, int32_t K,
                                            int32_t* __restrict__ out, int32_t topk) {
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+  for (int i = threadIdx.x; i < n; i += Sync::count()) {
     const uint64_t ci = cand[i];
     int32_t r = 0;
     for (int j = 0; j < n; ++j) r += cand[j] > ci;
     if (r < K) out[r] = candidate_id(ci);
   }
-  for (int j = K + threadIdx.x; j < topk; j += blockDim.x) out[j] = -1;
+  for (int j = K + threadIdx.x; j < topk; j += Sync::count()) out[j] = -1;
 }
 
 // Exact path. Preconditions: keys final; total = number of keys above -inf,
 // m / M their min / max, 0 < K <= total. Ends with the row stored.
+template <typename Sync = CtaSync>
 __device__ void topk_exact(const uint32_t* __restrict__ keys, int32_t nb, int32_t K, uint32_t total,
                            uint32_t m, uint32_t M, uint64_t* __restrict__ cand, int32_t kpad,
                            int32_t* __restrict__ out, int32_t topk, TopkShared& sh) {
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int nthreads = blockDim.x;
+  const int nthreads = Sync::count();
   const int nwarps = nthreads >> 5;
 
   if (tid == 0) sh.count = 0;
   for (int i = tid; i < 256; i += nthreads) sh.hist[i] = 0;
-  __syncthreads();
+  Sync::sync();
 
   uint32_t prefix = kKeyNegInf + 1u;  // selected: keys >= prefix (take_all) or
   bool take_all = true;               // keys > prefix plus `need` tied keys
@@ -96,13 +113,13 @@ __device__ void topk_exact(const uint32_t* __restrict__ keys, int32_t nb, int32_
         const uint32_t wmask = (2u << (hi - lo)) - 1u;
         if (pass > 0) {
           for (int i = tid; i < 256; i += nthreads) sh.hist[i] = 0;
-          __syncthreads();
+          Sync::sync();
         }
         for (int b = tid; b < nb; b += nthreads) {
           const uint32_t key = keys[b];
           if (key > kKeyNegInf && (key & mask) == prefix) atomicAdd(&sh.hist[(key >> lo) & wmask], 1u);
         }
-        __syncthreads();
+        Sync::sync();
         if (warp == 0) {
           // Lane l owns digits 255 - 8l down to 248 - 8l (highest first).
           uint32_t c[8], sum = 0;
@@ -132,7 +149,7 @@ __device__ void topk_exact(const uint32_t* __restrict__ keys, int32_t nb, int32_
             }
           }
         }
-        __syncthreads();
+        Sync::sync();
         prefix |= sh.digit << lo;
         mask |= wmask << lo;
         need -= static_cast<int32_t>(sh.above);
@@ -163,7 +180,7 @@ __device__ void topk_exact(const uint32_t* __restrict__ keys, int32_t nb, int32_
       mine += __popc(__ballot_sync(0xffffffffu, b < hi_id && keys[b] == prefix));
     }
     if (lane == 0) sh.warp_count[warp] = mine;
-    __syncthreads();
+    Sync::sync();
     int32_t rank0 = 0;
     for (int i = 0; i < warp; ++i) rank0 += static_cast<int32_t>(sh.warp_count[i]);
     const int32_t count_gt = static_cast<int32_t>(sh.count);
@@ -176,14 +193,14 @@ __device__ void topk_exact(const uint32_t* __restrict__ keys, int32_t nb, int32_
       rank0 += __popc(bal);
     }
   }
-  __syncthreads();
+  Sync::sync();
 
   if (K <= kRankMax) {
-    rank_store(cand, K, K, out, topk);
+    rank_store<Sync>(cand, K, K, out, topk);
     return;
   }
   for (int i = K + tid; i < kpad; i += nthreads) cand[i] = 0ull;
-  __syncthreads();
+  Sync::sync();
   for (int size = 2; size <= kpad; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int i = tid; i < (kpad >> 1); i += nthreads) {
@@ -196,7 +213,7 @@ __device__ void topk_exact(const uint32_t* __restrict__ keys, int32_t nb, int32_
           cand[hi] = a;
         }
       }
-      __syncthreads();
+      Sync::sync();
     }
   }
   for (int j = tid; j < topk; j += nthreads) out[j] = (j < K) ? candidate_id(cand[j]) : -1;
@@ -208,7 +225,7 @@ __device__ void topk_exact(const uint32_t* __restrict__ keys, int32_t nb, int32_
 // power of two >= min(k, nb). out: this row's output slots (global; unused
 // when k == 0). scores: optional row (nb entries, fp32 or bf16 bits like the
 // logits) written with the final scores. Every thread of the CTA calls this.
-template <typename S>
+template <typename S, typename Sync = CtaSync>
 __device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t n_live, int32_t k,
                            int32_t pin_block, uint64_t* __restrict__ cand, int32_t kpad,
                            int32_t* __restrict__ out, int32_t topk, S* __restrict__ scores,
@@ -217,7 +234,7 @@ __device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t n_li
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int nthreads = blockDim.x;
+  const int nthreads = Sync::count();
   const int nwarps = nthreads >> 5;
   const bool in_regs = n_live <= KR * nthreads;
   const bool fast = k > 0 && k <= 32 * nwarps && in_regs;
@@ -285,7 +302,7 @@ __device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t n_li
     sh.warp_kth[warp] = kth;
   }
   if (tid == 0) sh.count = 0;
-  __syncthreads();
+  Sync::sync();
   if (k <= 0) return;
 
   uint32_t total = 0, M = 0, m = 0xFFFFFFFFu, L = 0xFFFFFFFFu;
@@ -312,16 +329,16 @@ __device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t n_li
         if (pos < cap) cand[pos] = pack_candidate(kr[i], tid + i * nthreads);
       }
     }
-    __syncthreads();
+    Sync::sync();
     const uint32_t n = sh.count;
     if (n <= static_cast<uint32_t>(kRankMax)) {
       // 3. Rank by counting.
-      rank_store(cand, static_cast<int32_t>(n), K, out, topk);
+      rank_store<Sync>(cand, static_cast<int32_t>(n), K, out, topk);
       return;
     }
-    __syncthreads();  // every thread has read sh.count before it is reset
+    Sync::sync();  // every thread has read sh.count before it is reset
   }
-  topk_exact(keys, n_live, K, total, m, M, cand, kpad, out, topk, sh);
+  topk_exact<Sync>(keys, n_live, K, total, m, M, cand, kpad, out, topk, sh);
 }
 
 }  // namespace dsa

@@ -70,19 +70,20 @@ int32_t dsa_select_max_shards(void);
 
 /*
  * Bytes of optional device workspace that lets the selecting entry points
- * split each row over several CTAs: one arrival counter per row, then
- * rows * nblocks block keys, each part 256-byte aligned. nblocks is
- * ceil(width / block_size) for dsa_select_candidate_blocks and
- * max(max_global_blocks, 1) for the sharded form. Returns 0 for negative
- * arguments.
+ * deal rows to CTAs as they free up and split long rows over several CTAs:
+ * a 256-byte header (a work counter and a count of finished CTAs), one
+ * arrival counter per row, then rows * nblocks block keys, each part
+ * 256-byte aligned. nblocks is ceil(width / block_size) for
+ * dsa_select_candidate_blocks and max(max_global_blocks, 1) for the sharded
+ * form. Returns 0 for negative arguments and for rows == 0.
  *
  * Workspace contract: caller-owned device memory of at least this many bytes,
  * all zero bytes before its first use (e.g. one cudaMemset), and written by
- * nothing but these calls afterwards. Every completed call leaves its
- * counters at zero; block keys that a call of another shape left where this
- * call's counters are can never be mistaken for a count, so one workspace
- * serves calls of any shape in turn. Two calls that may run at the same
- * time (different streams) must not share a workspace.
+ * nothing but these calls afterwards. Every completed call leaves its header
+ * and counters at zero; block keys that a call of another shape left where
+ * this call's counters are can never be mistaken for a count, so one
+ * workspace serves calls of any shape in turn. Two calls that may run at the
+ * same time (different streams) must not share a workspace.
  */
 size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks);
 
@@ -101,6 +102,23 @@ size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks);
  *   DSA_LAUNCH_WARP_ROWS   1: never take the one-row-per-warp kernel
  *   DSA_LAUNCH_WARP_ORDER  1: one-row-per-warp rows in order (default: last
  *                          to first)
+ *   DSA_LAUNCH_PIPELINE    0 (automatic): the pipelined (bulk-copy staged)
+ *                          kernels take the unsharded calls they support, the
+ *                          DCP forms stay on the row-per-CTA kernel; 1: never
+ *                          take the pipelined kernels; 2: take them (DCP
+ *                          forms included) with every warp on one row; 3:
+ *                          take them with one row per warp (unsharded rows
+ *                          with top-k <= 32 and <= 2048 blocks)
+ *   DSA_LAUNCH_PIPE_SPLIT  pipelined kernels: parts per row, 1..8 (only
+ *                          with a workspace)
+ *   DSA_LAUNCH_PIPE_STAGES pipelined kernels: ring depth, 2..16
+ *   DSA_LAUNCH_PIPE_STAGE_KB  pipelined kernels: KiB per stage, 4..64
+ *   DSA_LAUNCH_PIPE_SCHED  pipelined kernels: 1 = rows dealt to CTAs in a
+ *                          fixed order even when a workspace is given
+ *   DSA_LAUNCH_PIPE_WARPS  pipelined kernels, every warp on one row: 4 or 8
+ *                          consumer warps per CTA
+ *   DSA_LAUNCH_PIPE_CTAS   pipelined kernels: CTAs per SM, 1..4 (at most 2
+ *                          with 8 consumer warps or one row per warp)
  *
  * DSA_EINVAL for an unknown knob or a value outside its range (nothing
  * changes then).
@@ -109,9 +127,30 @@ enum {
     DSA_LAUNCH_SPLIT = 1,
     DSA_LAUNCH_THREADS = 2,
     DSA_LAUNCH_WARP_ROWS = 3,
-    DSA_LAUNCH_WARP_ORDER = 4
+    DSA_LAUNCH_WARP_ORDER = 4,
+    DSA_LAUNCH_PIPELINE = 5,
+    DSA_LAUNCH_PIPE_SPLIT = 6,
+    DSA_LAUNCH_PIPE_STAGES = 7,
+    DSA_LAUNCH_PIPE_STAGE_KB = 8,
+    DSA_LAUNCH_PIPE_SCHED = 9,
+    DSA_LAUNCH_PIPE_WARPS = 10,
+    DSA_LAUNCH_PIPE_CTAS = 11
 };
 dsa_status dsa_select_set_launch_override(int32_t knob, int32_t value);
+
+/*
+ * dsa_pipeline_error -- whether a pipelined selecting kernel has given up a
+ * wait since the process started (or since the last clear). The pages have
+ * no counterpart. The pipelined kernels stage logits through shared memory
+ * with the bulk-copy engine and wait on mbarriers; every such wait ends
+ * after one second, records a nonzero site code in a device-wide flag and
+ * lets the kernel finish instead of hanging the GPU. Such a call's outputs
+ * are not valid. Returns that flag (0: no wait ever gave up; 1: a consumer's
+ * wait for data; 2: the producer's wait for a free stage), or -1 if the flag
+ * could not be read. clear != 0 resets it to 0 after reading. Synchronises
+ * with the current device (a plain device-to-host copy of 4 bytes).
+ */
+int dsa_pipeline_error(int clear);
 
 /*
  * dsa_block_scores -- per-block scores of every row (candidate_blocks.py:
@@ -154,19 +193,20 @@ dsa_status dsa_block_scores(const float *logits, int64_t rows, int64_t width,
  *               ld_scores >= nb receives the block scores that were ranked
  *               (pin applied), as dsa_block_scores would write them.
  *   workspace   nullable; see dsa_select_workspace_bytes. With a workspace
- *               of sufficient size long rows are split over several CTAs
- *               (their block keys meet in the workspace and the last CTA of
- *               the row to finish ranks them); without one, one CTA handles
- *               each row. Results are identical either way.
+ *               of sufficient size rows are dealt to CTAs as they free up
+ *               and long rows are split over several CTAs (their block keys
+ *               meet in the workspace and the last CTA of the row to finish
+ *               ranks them); without one, rows are dealt in a fixed order
+ *               and none is split. Results are identical either way.
  *
  * rows == 0: DSA_OK, nothing written. width == 0: every slot of out is -1.
  * topk_blocks == 0 and no scores_out: DSA_OK, nothing written. A workspace
- * smaller than dsa_select_workspace_bytes is not used (one CTA per row).
+ * smaller than dsa_select_workspace_bytes is not used.
  * DSA_EINVAL for negative rows / width / topk_blocks, block_size < 1,
  * row_repeat < 1, ld_logits < width, ld_out < topk_blocks, ld_scores < nb
  * (with scores_out), or a NULL logits / row_ke / out (out only when
- * topk_blocks > 0). DSA_EUNSUPPORTED when nb > dsa_select_max_blocks() or
- * width >= 2^31.
+ * topk_blocks > 0). DSA_EUNSUPPORTED when nb > dsa_select_max_blocks(),
+ * width > 2^31 - 8193 or rows > 2^28 - 1.
  */
 dsa_status dsa_select_candidate_blocks(const float *logits, int64_t rows,
                                        int64_t width, int64_t ld_logits,
@@ -212,7 +252,8 @@ dsa_status dsa_select_candidate_blocks(const float *logits, int64_t rows,
  * topk_blocks, ld_scores < nbg (with scores_out), or a NULL
  * global_row_ke / out (out only when topk_blocks > 0) / logits (when
  * local_width > 0). DSA_EUNSUPPORTED when nbg > dsa_select_max_blocks(),
- * shards > dsa_select_max_shards() or local_width >= 2^31.
+ * shards > dsa_select_max_shards(), local_width > 2^31 - 8193 or
+ * rows > 2^28 - 1.
  */
 dsa_status dsa_select_candidate_blocks_sharded(
     const float *logits, int32_t shards, int64_t rows, int64_t local_width,
@@ -384,15 +425,20 @@ dsa_status dsa_mask_candidate_logits_sharded_starts_bf16(
  *
  *   Arguments, results and errors are those of
  *   dsa_select_candidate_blocks_sharded (without workspace and
- *   workspace_bytes), plus DSA_EUNSUPPORTED when
- *   dsa_select_workspace_bytes(rows, max(max_global_blocks, 1)) exceeds
- *   8 MiB (8388608 bytes).
+ *   workspace_bytes); every argument error is returned before anything is
+ *   enqueued. When dsa_select_workspace_bytes(rows, max(max_global_blocks,
+ *   1)) is at most 8 MiB (8388608 bytes) the call uses the array as its
+ *   workspace; above that it runs without a workspace (rows dealt to CTAs
+ *   in a fixed order, none split), with the same results. Row counts beyond
+ *   the selecting calls' limit (2^28 - 1) return DSA_EUNSUPPORTED.
  *
- * The first call on each device looks up the array's device address with that
- * device current; make that first call before any stream capture. Each call
- * clears the array's arrival counters with cudaMemsetAsync on `stream`.
- * Calls that overlap on the GPU (different streams, or different host
- * threads) race on the shared array and must not be issued.
+ * Each call that uses the array looks up its device address with
+ * cudaGetSymbolAddress, with the call's device current; the first such call
+ * on a device may load the library's device code there, so make it before
+ * any stream capture. Each such call clears the array's header and arrival
+ * counters with cudaMemsetAsync on `stream`. Calls that overlap on the GPU
+ * (different streams, or different host threads) race on the shared array
+ * and must not be issued.
  */
 dsa_status dsa_select_candidate_blocks_sharded_static(
     const float *logits, int32_t shards, int64_t rows, int64_t local_width,

@@ -63,9 +63,10 @@ def test_status_strings(lib):
 
 
 def test_workspace_bytes(lib):
-    # one counter per row and rows * nblocks keys, each part 256-byte aligned
-    assert lib.dsa_select_workspace_bytes(4096, 1024) == 16384 + 4096 * 1024 * 4
-    assert lib.dsa_select_workspace_bytes(3, 5) == 256 + 256
+    # a 256-byte queue header, one counter per row and rows * nblocks keys,
+    # each part 256-byte aligned
+    assert lib.dsa_select_workspace_bytes(4096, 1024) == 256 + 16384 + 4096 * 1024 * 4
+    assert lib.dsa_select_workspace_bytes(3, 5) == 256 + 256 + 256
     assert lib.dsa_select_workspace_bytes(0, 7) == 0
     assert lib.dsa_select_workspace_bytes(-1, 7) == 0
 
@@ -88,7 +89,16 @@ def test_launch_override_validation(lib):
         for v in bad:
             assert set_(knob, v) == DSA_EINVAL
         assert set_(knob, 0) == DSA_OK
-    for knob in (0, 5, 99, -3):
+    for knob, good, bad in ((5, (0, 1, 2, 3), (4, -1)), (6, (0, 1, 8), (9, -1)),
+                            (7, (0, 2, 16), (1, 17)), (8, (0, 4, 64), (3, 65)),
+                            (9, (0, 1), (2, -1)), (10, (0, 4, 8), (2, 16)),
+                            (11, (0, 1, 4), (5, -1))):
+        for v in good:
+            assert set_(knob, v) == DSA_OK
+        for v in bad:
+            assert set_(knob, v) == DSA_EINVAL
+        assert set_(knob, 0) == DSA_OK
+    for knob in (0, 12, 99, -3):
         assert set_(knob, 0) == DSA_EINVAL
 
 

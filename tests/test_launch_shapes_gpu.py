@@ -3,10 +3,12 @@ through the library's explicit override call (dsa_select_set_launch_override,
 applied by conftest.py from DSA_TEST_LAUNCH in a child run), must give the
 oracle's results bit for bit like the default ones:
 
-- every row split into 3 or 8 chunk-major parts (long rows normally split
-  only when there are few rows), whose keys meet in the workspace;
-- short rows handled one per warp in row order instead of last to first;
-- short rows handled one per CTA instead of one per warp.
+- the row-per-CTA kernel with every row split into 3 or 8 chunk-major parts
+  (long rows normally split only when there are few rows), the row-per-warp
+  kernel in row order, and short rows one per CTA instead of one per warp;
+- the pipelined kernels with every warp of a CTA on one row or one row per
+  warp, rows cut into 3 or 8 parts that meet in the workspace, the smallest
+  rings (2 stages of 4 KiB), and rows dealt to CTAs in a fixed order.
 
 The overrides are process-wide, so each setting re-runs the relevant parity
 sweeps in a child process.
@@ -24,12 +26,27 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 FILES = ["tests/test_parity_gpu.py", "tests/test_bf16_gpu.py"]
 # setting -> (overrides, pytest -k selection, least number of tests it must run)
+SWEEPS = "unsharded_sweep or sharded_sweep or starts_sweep"
 CASES = {
-    "split3": ("split=3", "unsharded_sweep or sharded_sweep or starts_sweep", 150),
-    "split8": ("split=8", "unsharded_sweep or sharded_sweep or starts_sweep or workspace_reuse",
-               150),
-    "warp_rows_in_order": ("warp_order=1", "warp", 8),
-    "no_warp_kernel": ("warp_rows=1", "warp", 8),
+    # The row-per-CTA and row-per-warp kernels, which take the calls that the
+    # pipelined kernels do not (host-mapped logits, odd block sizes, more
+    # than 16 shards, more than 4096 blocks or top-256).
+    "legacy": ("pipeline=1", SWEEPS + " or warp or workspace_reuse or graph", 190),
+    "legacy_split3": ("pipeline=1,split=3", SWEEPS, 150),
+    "legacy_split8": ("pipeline=1,split=8", SWEEPS + " or workspace_reuse", 150),
+    "legacy_warp_rows_in_order": ("pipeline=1,warp_order=1", "warp", 8),
+    "legacy_no_warp_kernel": ("pipeline=1,warp_rows=1", "warp", 8),
+    # The pipelined kernels in shapes the automatic choice reaches only for
+    # some sizes.
+    "pipe_coop": ("pipeline=2", SWEEPS + " or warp or graph", 190),
+    "pipe_solo": ("pipeline=3", "unsharded_sweep or warp", 80),
+    "pipe_split3": ("pipeline=2,pipe_split=3", SWEEPS + " or workspace_reuse", 150),
+    "pipe_split8": ("pipeline=2,pipe_split=8", SWEEPS, 150),
+    "pipe_small_stages": ("pipeline=2,pipe_stage_kb=4,pipe_stages=2", SWEEPS + " or warp", 150),
+    "pipe_fixed_order": ("pipeline=2,pipe_sched=1,pipe_split=2", SWEEPS, 150),
+    "pipe_8_warps": ("pipeline=2,pipe_warps=8,pipe_ctas=1", SWEEPS + " or graph", 150),
+    "pipe_solo_small_stages": ("pipeline=3,pipe_stage_kb=4,pipe_ctas=1", "unsharded_sweep or warp",
+                               80),
 }
 
 

@@ -594,3 +594,11 @@ def test_full_size_dcp(env):
     want_ids, _ = oracle.run_workload(wl, want_scores=False)
     got_ids, _ = run_sharded(env, wl, want_scores=False)
     np.testing.assert_array_equal(got_ids, want_ids)
+
+
+def test_no_pipelined_wait_gave_up(env):
+    # Every bounded wait of the pipelined kernels in the calls above (this
+    # file and the ones collected before it) completed: none recorded a
+    # give-up in the library's device-wide flag.
+    _, dsa = env
+    assert dsa.pipeline_error() == 0
