@@ -912,7 +912,10 @@ dsa_status select_impl(const typename E::T* logits, int64_t rows, int64_t width,
     pc.rows = rows;
     pc.workspace = workspace;
     pc.workspace_size = workspace_size;
-    if (pipe_takes(pc)) return pipe_select(pc, stream);
+    if (pipe_takes(pc)) {
+      const dsa_status st = pipe_select(pc, stream);
+      if (st != kPipeDeclined) return st;
+    }
   }
   // Many short rows: one row per warp (32 rows in flight per SM instead of
   // 8). With few rows a CTA per row keeps more of the GPU busy.
@@ -1032,7 +1035,10 @@ dsa_status select_sharded_impl(const typename E::T* logits, int32_t shards, int6
     pc.rows = rows;
     pc.workspace = workspace;
     pc.workspace_size = workspace_size;
-    if (local_width > 0 && pipe_takes(pc)) return pipe_select(pc, stream);
+    if (local_width > 0 && pipe_takes(pc)) {
+      const dsa_status st = pipe_select(pc, stream);
+      if (st != kPipeDeclined) return st;
+    }
   }
   const size_t smem = select_smem(a.kpad, a.nb, shards);
   const bool ws = workspace && workspace_size >= workspace_bytes(rows, a.nb);

@@ -67,12 +67,11 @@ constexpr int kPipeMaxTopk = 256;
 constexpr int32_t kPartUnit = 32;  // blocks: a part of a split row is a multiple
 
 // Stage flags.
-constexpr int32_t kFirst = 1;  // first stage of a unit
 constexpr int32_t kLast = 2;   // last stage of a unit: rank or merge after it
 constexpr int32_t kDone = 4;   // no more units for this consumer
 
 // Wait sites recorded in g_pipe_error on a timeout.
-constexpr unsigned kSiteFull = 1u, kSiteEmpty = 2u;
+constexpr unsigned kSiteFull = 1u, kSiteEmpty = 2u, kSiteKeys = 3u;
 
 struct StageDesc {
   int32_t row;
@@ -222,92 +221,71 @@ __device__ __forceinline__ LanePlan<E> plan_lane(const PipeArgs& a, int32_t row,
   return p;
 }
 
-// Emits the stages of blocks [b0, b1) of one row into a ring (all lanes of
-// the producer warp). ring: `stages` buffers of a.stage_bytes at `buf`;
-// full / empty: their barriers; desc: their descriptors; k: this ring's
-// stage counter. Returns false when a wait gave up.
-// `after_first` runs (on every lane) once the first stage's copies are in
-// flight: the producer fetches the next unit's bounds there, so that their
-// round trip overlaps this unit's stages.
-//
-// ONE_SHARD: every stage carries one shard's piece (its consumers merge the
-// shards into the keys with atomicMax), so that each bulk copy moves up to a
-// whole stage instead of 1 / shards of it; the stages go chunk by chunk,
-// shard by shard within a chunk.
-template <typename E, bool ONE_SHARD, typename Hook>
-__device__ __forceinline__ bool emit_unit(const PipeArgs& a, const LanePlan<E>& p, int32_t row,
-                                          int32_t b0, int32_t b1, int32_t parts, int npieces,
-                                          unsigned char* buf, uint64_t* full, uint64_t* empty,
-                                          StageDesc* desc, int stages, uint32_t& k,
-                                          Hook&& after_first) {
-  const int lane = threadIdx.x & 31;
+// The pieces of one row as the producer's lane 0 reads them, one per shard
+// (one in all for unsharded rows): written by the producer warp's lanes
+// (lane d: shard d) once per row.
+struct PieceTable {
+  const unsigned char* origin[kMaxShardLanes];  // first in-window element
+  int32_t len[kMaxShardLanes];                  // window length (elements)
+};
+
+// Emits the stages of blocks [b0, b1) of one row into the ring, one piece per
+// stage, in the order chunk by chunk, shard by shard within a chunk (a shard
+// form's consumers merge the shards into the keys). Lane 0 alone does the
+// work, so that no shuffle or warp barrier lengthens the path between two
+// stages: wait for the stage's slot, write its descriptor (the unit's fields
+// only on its last stage), arm its barrier and issue the one bulk copy.
+// Returns false (on lane 0) when a wait gave up.
+template <typename E>
+__device__ __forceinline__ bool emit_unit(const PipeArgs& a, const PieceTable& pt, int npieces,
+                                          int32_t row, int32_t nblk, int32_t pin, int32_t b0,
+                                          int32_t b1, int32_t parts, unsigned char* buf,
+                                          uint64_t* full, uint64_t* empty, StageDesc* desc,
+                                          int stages, uint32_t& k) {
   const int32_t bs = a.block_size;
   int32_t c = b0;
-  int shard = 0;  // ONE_SHARD: the shard of the next stage
-  bool first = true;
+  int shard = 0;
   for (;;) {
     const int32_t n = min(a.cap, b1 - c);
-    const bool last = c + n >= b1 && (!ONE_SHARD || shard == npieces - 1);
-    const bool mine = ONE_SHARD ? lane == shard : lane < npieces;
+    const bool last = c + n >= b1 && shard == npieces - 1;
     const uint32_t slot = k % static_cast<uint32_t>(stages);
     const uint32_t round = k / static_cast<uint32_t>(stages);
-    int ok = 1;
-    if (lane == 0 && round > 0) ok = mbar_wait(&empty[slot], (round - 1u) & 1u, kSiteEmpty);
-    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-    // This lane's piece: elements [c*bs, min((c+n)*bs, len)) of its window.
+    if (round > 0 && !mbar_wait(&empty[slot], (round - 1u) & 1u, kSiteEmpty)) return false;
+    // The piece: elements [c*bs, min((c+n)*bs, len)) of the shard's window,
+    // copied from the 16-byte granule holding its first element through the
+    // one holding its last.
     const int32_t j0 = c * bs;
-    const int32_t j1 = min((c + n) * bs, p.len);
-    uintptr_t A = 0;
-    uint32_t bytes = 0, head = 0;
-    if (mine && j1 > j0) {
-      const uintptr_t lo = reinterpret_cast<uintptr_t>(p.origin + j0);
-      const uintptr_t hi = reinterpret_cast<uintptr_t>(p.origin + j1);
-      A = lo & ~static_cast<uintptr_t>(15);
-      bytes = static_cast<uint32_t>(((hi + 15) & ~static_cast<uintptr_t>(15)) - A);
-      head = static_cast<uint32_t>(lo - A);
-    }
-    // Pieces are packed in lane order; every size is a multiple of 16.
-    uint32_t pos = bytes;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t t = __shfl_up_sync(0xffffffffu, pos, o);
-      if (lane >= o) pos += t;
-    }
-    const uint32_t total = __shfl_sync(0xffffffffu, pos, 31);
-    pos -= bytes;  // exclusive prefix: this piece's offset in the stage
+    const int32_t j1 = min((c + n) * bs, pt.len[shard]);
     StageDesc& d = desc[slot];
-    if (mine) {
-      d.off = pos + head;
-      d.cnt = j1 > j0 ? j1 - j0 : 0;
-    }
-    if (lane == 0) {
+    d.c0 = c;
+    d.n = n;
+    d.flags = last ? kLast : 0;
+    if (last) {
       d.row = row;
-      d.c0 = c;
-      d.n = n;
-      d.flags = (first ? kFirst : 0) | (last ? kLast : 0);
-      d.npieces = 1;
-      d.nblk = p.nblk;
-      d.pin = p.pin;
+      d.nblk = nblk;
+      d.pin = pin;
       d.b0 = b0;
       d.b1 = b1;
       d.parts = parts;
     }
-    __syncwarp();
-    if (lane == 0) {
-      if (total > 0)
-        mbar_arrive_expect_tx(&full[slot], total);
-      else
-        mbar_arrive(&full[slot]);
+    if (j1 > j0) {
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(pt.origin[shard] + j0 * E::kBytes);
+      const uintptr_t hi = reinterpret_cast<uintptr_t>(pt.origin[shard] + j1 * E::kBytes);
+      const uintptr_t A = lo & ~static_cast<uintptr_t>(15);
+      const uint32_t bytes = static_cast<uint32_t>(((hi + 15) & ~static_cast<uintptr_t>(15)) - A);
+      d.off = static_cast<uint32_t>(lo - A);
+      d.cnt = j1 - j0;
+      mbar_arrive_expect_tx(&full[slot], bytes);
+      bulk_load(buf + static_cast<size_t>(slot) * a.stage_bytes, reinterpret_cast<const void*>(A),
+                bytes, &full[slot]);
+    } else {
+      d.off = 0;
+      d.cnt = 0;
+      mbar_arrive(&full[slot]);
     }
-    __syncwarp();
-    if (bytes > 0)
-      bulk_load(buf + static_cast<size_t>(slot) * a.stage_bytes + pos,
-                reinterpret_cast<const void*>(A), bytes, &full[slot]);
     ++k;
-    if (first) after_first();
-    first = false;
     if (last) return true;
-    if (ONE_SHARD && shard + 1 < npieces) {
+    if (shard + 1 < npieces) {
       ++shard;
     } else {
       shard = 0;
@@ -316,23 +294,16 @@ __device__ __forceinline__ bool emit_unit(const PipeArgs& a, const LanePlan<E>& 
   }
 }
 
-// A stage with no data that tells its consumer(s) to stop.
-__device__ __forceinline__ bool emit_done(unsigned char* buf, uint64_t* full, uint64_t* empty,
-                                          StageDesc* desc, int stages, uint32_t& k) {
-  (void)buf;
-  const int lane = threadIdx.x & 31;
+// A stage with no data that tells its consumer(s) to stop (lane 0).
+__device__ __forceinline__ bool emit_done(uint64_t* full, uint64_t* empty, StageDesc* desc,
+                                          int stages, uint32_t& k) {
   const uint32_t slot = k % static_cast<uint32_t>(stages);
   const uint32_t round = k / static_cast<uint32_t>(stages);
-  int ok = 1;
-  if (lane == 0) {
-    if (round > 0) ok = mbar_wait(&empty[slot], (round - 1u) & 1u, kSiteEmpty);
-    if (ok) {
-      desc[slot].flags = kDone;
-      mbar_arrive(&full[slot]);
-    }
-  }
+  if (round > 0 && !mbar_wait(&empty[slot], (round - 1u) & 1u, kSiteEmpty)) return false;
+  desc[slot].flags = kDone;
+  mbar_arrive(&full[slot]);
   ++k;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -392,6 +363,71 @@ __device__ __forceinline__ void fold_lane_blocks(const unsigned char* stage, con
       }
     }
     const uint32_t key = order_key(max_nan(max_nan(acc[0], acc[1], acc[2]), acc[3]));
+    if (MERGE)
+      atomicMax(&keys[c0 + blk], key);
+    else
+      keys[c0 + blk] = key;
+  }
+}
+
+// The same with 16-byte loads, for a piece whose first element sits on a
+// 16-byte boundary of the stage and blocks of whole 16-byte chunks (CH per
+// block): lane l reads chunk c ^ (l & 7) of its block (8 chunks or more) or
+// (c + l / (8 / CH)) mod CH (fewer), so that every 8-lane phase of a 16-byte
+// load spreads over the 8 bank groups (checked exhaustively on the CPU). A
+// chunk is four fp32 values, or eight bf16 values folded in pairs with
+// max.NaN.bf16x2 and widened once per block.
+template <typename E, int BS, bool MERGE>
+__device__ __forceinline__ void fold_lane_blocks_vec(const unsigned char* stage,
+                                                     const StageDesc& d, int g0, int gstep,
+                                                     uint32_t* __restrict__ keys) {
+  constexpr int ES = E::kBytes;
+  constexpr int CH = BS * ES / 16;
+  static_assert(CH >= 1 && (BS * ES) % 16 == 0, "whole 16-byte chunks");
+  constexpr int SH = CH >= 8 ? 0 : CH == 4 ? 1 : CH == 2 ? 2 : 3;
+  const int lane = threadIdx.x & 31;
+  const int32_t c0 = d.c0, n = d.n;
+  uint32_t offs[CH];
+#pragma unroll
+  for (int c = 0; c < CH; ++c)
+    offs[c] = static_cast<uint32_t>(CH >= 8 ? (c ^ (lane & 7)) : ((c + (lane >> SH)) % CH)) * 16;
+  const int32_t ngroups = (n + 31) >> 5;
+  for (int32_t g = g0; g < ngroups; g += gstep) {
+    const int32_t blk = g * 32 + lane;
+    if (blk >= n) continue;
+    const int32_t valid = d.cnt - blk * BS;
+    if (valid <= 0) continue;
+    const unsigned char* pb = stage + d.off + static_cast<uint32_t>(blk * BS) * ES;
+    float acc;
+    if (valid >= BS) {
+      if constexpr (ES == 4) {
+        float a4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const float4 v = *reinterpret_cast<const float4*>(pb + offs[c]);
+          a4[(c & 1) * 2] = max_nan(a4[(c & 1) * 2], v.x, v.y);
+          a4[(c & 1) * 2 + 1] = max_nan(a4[(c & 1) * 2 + 1], v.z, v.w);
+        }
+        acc = max_nan(max_nan(a4[0], a4[1], a4[2]), a4[3]);
+      } else {
+        uint32_t w[2] = {BF16::kNegInfWord, BF16::kNegInfWord};
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(pb + offs[c]);
+          w[0] = max_nan_bf16x2(w[0], v.x);
+          w[1] = max_nan_bf16x2(w[1], v.y);
+          w[0] = max_nan_bf16x2(w[0], v.z);
+          w[1] = max_nan_bf16x2(w[1], v.w);
+        }
+        const uint32_t m = max_nan_bf16x2(w[0], w[1]);
+        acc = max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+      }
+    } else {
+      // The window's last block: only its first `valid` elements.
+      acc = neg_inf();
+      for (int32_t e = 0; e < valid; ++e) acc = max_nan(acc, stage_elem<E>(pb + e * ES));
+    }
+    const uint32_t key = order_key(acc);
     if (MERGE)
       atomicMax(&keys[c0 + blk], key);
     else
@@ -460,7 +496,25 @@ __device__ __forceinline__ void fold_stage(const PipeArgs& a, const unsigned cha
                                            const StageDesc& d, int g0, int gstep, uint32_t gbase,
                                            uint32_t* __restrict__ keys) {
   constexpr bool M = MODE != kPipeUnsharded;  // one shard per stage: merge
+  constexpr int ES = E::kBytes;
   const int first = static_cast<int>((static_cast<uint32_t>(g0) + gstep - gbase % gstep) % gstep);
+  if ((d.off & 15u) == 0) {
+    // The piece starts on a 16-byte boundary: whole 16-byte chunks per block.
+    switch (a.block_size) {
+      case 4:
+        if constexpr (ES == 4) {
+          fold_lane_blocks_vec<E, 4, M>(stage, d, first, gstep, keys);
+          return;
+        }
+        break;
+      case 8: fold_lane_blocks_vec<E, 8, M>(stage, d, first, gstep, keys); return;
+      case 16: fold_lane_blocks_vec<E, 16, M>(stage, d, first, gstep, keys); return;
+      case 32: fold_lane_blocks_vec<E, 32, M>(stage, d, first, gstep, keys); return;
+      case 64: fold_lane_blocks_vec<E, 64, M>(stage, d, first, gstep, keys); return;
+      case 128: fold_lane_blocks_vec<E, 128, M>(stage, d, first, gstep, keys); return;
+      default: break;
+    }
+  }
   switch (a.block_size) {
     case 2: fold_lane_blocks<E, 2, M>(stage, d, first, gstep, keys); return;
     case 4: fold_lane_blocks<E, 4, M>(stage, d, first, gstep, keys); return;
@@ -487,10 +541,10 @@ __device__ __forceinline__ bool merge_parts(const PipeArgs& a, int32_t row, int3
                                             int32_t b0, int32_t b1, int32_t parts, uint32_t* keys,
                                             int* s_last) {
   uint32_t* wrow = a.ws_keys + static_cast<int64_t>(row) * a.nb;
-  for (int32_t b = b0 + threadIdx.x; b < b1; b += Sync::count()) __stcg(wrow + b, keys[b]);
+  for (int32_t b = b0 + Sync::tid(); b < b1; b += Sync::count()) __stcg(wrow + b, keys[b]);
   __threadfence();
   Sync::sync();
-  if (threadIdx.x == 0) {
+  if (Sync::tid() == 0) {
     // Count this part in; a counter word can hold an earlier call's block key
     // (>= key(-inf)), which reads as zero. Each failed CAS but the first
     // means another part arrived, so parts + 1 attempts suffice.
@@ -512,7 +566,7 @@ __device__ __forceinline__ bool merge_parts(const PipeArgs& a, int32_t row, int3
   Sync::sync();
   if (!*s_last) return false;
   __threadfence();
-  for (int32_t b = threadIdx.x; b < nblk; b += Sync::count())
+  for (int32_t b = Sync::tid(); b < nblk; b += Sync::count())
     if (b < b0 || b >= b1) keys[b] = __ldcg(wrow + b);
   return true;
 }
@@ -521,11 +575,6 @@ template <typename E>
 __device__ __forceinline__ typename E::T* score_row(const PipeArgs& a, int32_t row) {
   return a.scores ? static_cast<typename E::T*>(a.scores) + static_cast<int64_t>(row) * a.ld_scores
                   : nullptr;
-}
-
-// Takes the next unit: from the workspace queue, or the static stride.
-__device__ __forceinline__ uint32_t next_unit(const PipeArgs& a, uint32_t cur) {
-  return a.queue ? atomicAdd(a.queue, 1u) : cur + gridDim.x;
 }
 
 // After a CTA's last (failing) take: the last CTA to finish resets the queue.
@@ -538,58 +587,85 @@ __device__ __forceinline__ void retire_queue(const PipeArgs& a) {
   }
 }
 
-// Shared memory of a coop CTA: ring, barriers, descriptors, keys [nb],
-// candidates [max(kpad, kRankMax)].
+// A finished unit handed from the fold warps to the rank warps.
+struct UnitMeta {
+  int32_t row, nblk, pin, b0, b1, parts, done;
+};
+
+constexpr int kRankWarps = 4;
+
+// Shared memory of a coop CTA: ring, its barriers and descriptors, then two
+// key buffers [nb] (padded to 4) and the candidates [max(kpad, kRankMax)].
 __host__ __device__ __forceinline__ size_t coop_keys_offset(int stages, int stage_bytes) {
   return static_cast<size_t>(stages) * stage_bytes +
          ((static_cast<size_t>(stages) * (16 + sizeof(StageDesc)) + 127) & ~static_cast<size_t>(127));
 }
 
+// Warps 0 .. NW-1 fold, NW .. NW+3 rank, warp NW+4 produces. The fold warps
+// fill one of two key buffers with a unit's block keys and hand it to the
+// rank warps (mbarrier kfull, with the unit in `meta`); the rank warps merge
+// split rows, pin, rank and store it, reset the buffer (key(-inf), in the
+// shard forms whose stages merge into it) and hand it back (kempty), while
+// the fold warps go on with the next unit in the other buffer. A row's top-k
+// thus never stops the fold, and no barrier joins the fold warps.
 template <typename E, int MODE, int NW>
-__global__ void __launch_bounds__((NW + 1) * 32, NW == 4 ? 4 : 2) pipe_coop_kernel(const PipeArgs a) {
-  using Sync = NamedSync<NW * 32>;
+__global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
+    pipe_coop_kernel(const PipeArgs a) {
+  constexpr int NR = kRankWarps;
+  using RankSync = NamedSync<NR * 32, 2, NW * 32>;
+  constexpr bool kMerge = MODE != kPipeUnsharded;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(a.stages) * a.stage_bytes);
   uint64_t* empty = full + a.stages;
   StageDesc* desc = reinterpret_cast<StageDesc*>(empty + a.stages);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + coop_keys_offset(a.stages, a.stage_bytes));
-  uint64_t* cand = reinterpret_cast<uint64_t*>(keys + ((a.nb + 3) & ~3));
+  const int32_t nbp = (a.nb + 3) & ~3;
+  uint32_t* keys0 = reinterpret_cast<uint32_t*>(smem + coop_keys_offset(a.stages, a.stage_bytes));
+  uint64_t* cand = reinterpret_cast<uint64_t*>(keys0 + 2 * nbp);
   __shared__ TopkShared tsh;
   __shared__ int s_last;
+  __shared__ __align__(8) uint64_t kfull[2], kempty[2];
+  __shared__ UnitMeta meta[2];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int32_t b = threadIdx.x; b < 2 * nbp; b += blockDim.x) keys0[b] = kKeyNegInf;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.stages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], NW);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kfull[i], NW);
+      mbar_init(&kempty[i], 1);
+    }
     mbar_init_fence();
   }
   __syncthreads();
 
-  if (warp == NW) {
-    // Producer warp.
-    const uint32_t total = static_cast<uint32_t>(a.rows) * static_cast<uint32_t>(a.split);
-    const int npieces = MODE == kPipeUnsharded ? 1 : a.shards;
-    uint32_t k = 0;
-    uint32_t u = 0;
-    if (lane == 0) u = a.queue ? atomicAdd(a.queue, 1u) : blockIdx.x;
-    u = __shfl_sync(0xffffffffu, u, 0);
+  if (warp == NW + NR) {
+    // Producer warp. Units are fetched two ahead: while the stages of unit u
+    // go out, the bounds of the next unit and the index of the one after it
+    // are in flight, so a unit boundary waits on no memory round trip.
+    __shared__ PieceTable pt;
     const uint32_t S = static_cast<uint32_t>(a.split);
+    const uint32_t total = static_cast<uint32_t>(a.rows) * S;
+    const int npieces = MODE == kPipeUnsharded ? 1 : a.shards;
+    uint32_t u = 0, u1 = 0;
+    if (lane == 0) {
+      u = a.queue ? atomicAdd(a.queue, 1u) : blockIdx.x;
+      u1 = a.queue ? atomicAdd(a.queue, 1u) : blockIdx.x + gridDim.x;
+    }
+    u = __shfl_sync(0xffffffffu, u, 0);
+    u1 = __shfl_sync(0xffffffffu, u1, 0);
     Bounds bnd{0, 0};
     if (u < total) bnd = load_bounds<MODE>(a, static_cast<int32_t>(u / S));
-    bool ok = true;
+    uint32_t k = 0;  // stages issued (lane 0)
+    int ok = 1;
     while (ok && u < total) {
-      uint32_t nu = 0;
-      if (lane == 0) nu = next_unit(a, u);  // in flight while this unit's stages go out
       Bounds nbnd{0, 0};
-      bool fetched = false;
-      auto prefetch = [&]() {
-        nu = __shfl_sync(0xffffffffu, nu, 0);
-        if (nu < total) nbnd = load_bounds<MODE>(a, static_cast<int32_t>(nu / S));
-        fetched = true;
-      };
+      if (u1 < total) nbnd = load_bounds<MODE>(a, static_cast<int32_t>(u1 / S));
+      uint32_t u2 = 0;
+      if (lane == 0) u2 = a.queue ? (u1 < total ? atomicAdd(a.queue, 1u) : u1) : u1 + gridDim.x;
       const int32_t row = static_cast<int32_t>(u / S);
       const int32_t part = static_cast<int32_t>(u % S);
       const LanePlan<E> p = plan_lane<E, MODE>(a, row, bnd, lane);
@@ -601,62 +677,100 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == 4 ? 4 : 2) pipe_coop_kern
         b0 = min(part * per, p.nblk);
         b1 = min(b0 + per, p.nblk);
       }
-      if (part < parts)
-        ok = emit_unit<E, MODE != kPipeUnsharded>(a, p, row, b0, b1, parts, npieces, ring, full,
-                                                  empty, desc, a.stages, k, prefetch);
-      if (!fetched) prefetch();
-      u = nu;
+      if (part < parts) {
+        if (lane < npieces) {
+          pt.origin[lane] = reinterpret_cast<const unsigned char*>(p.origin);
+          pt.len[lane] = p.len;
+        }
+        __syncwarp();
+        if (lane == 0)
+          ok = emit_unit<E>(a, pt, npieces, row, p.nblk, p.pin, b0, b1, parts, ring, full, empty,
+                            desc, a.stages, k);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();  // the table is read before it is rewritten
+      }
+      u = u1;
       bnd = nbnd;
+      u1 = __shfl_sync(0xffffffffu, u2, 0);
     }
-    if (lane == 0) retire_queue(a);
-    if (ok) emit_done(ring, full, empty, desc, a.stages, k);
+    if (lane == 0) {
+      retire_queue(a);
+      if (ok) emit_done(full, empty, desc, a.stages, k);
+    }
     return;
   }
 
-  // Consumer warps. In the shard forms every stage holds one shard, and its
-  // keys are merged into keys that start at key(-inf) for every row.
-  constexpr bool kMerge = MODE != kPipeUnsharded;
-  if (kMerge) {
-    for (int32_t b = threadIdx.x; b < a.nb; b += Sync::count()) keys[b] = kKeyNegInf;
-    Sync::sync();
+  if (warp >= NW) {
+    // Rank warps: units in the order the fold warps finish them.
+    uint32_t rounds0 = 0, rounds1 = 0;  // units taken from each buffer
+    for (int rb = 0;; rb ^= 1) {
+      uint32_t& rounds = rb ? rounds1 : rounds0;
+      const bool ok = mbar_wait(&kfull[rb], rounds & 1u, kSiteKeys);
+      if (!__all_sync(0xffffffffu, ok)) return;
+      const UnitMeta m = meta[rb];
+      if (m.done) return;
+      uint32_t* keys = keys0 + rb * nbp;
+      if (m.parts == 1 || merge_parts<RankSync>(a, m.row, m.nblk, m.b0, m.b1, m.parts, keys,
+                                                &s_last)) {
+        for (int32_t b = m.nblk + RankSync::tid(); b <= m.pin; b += RankSync::count())
+          keys[b] = kKeyNegInf;
+        RankSync::sync();
+        topk_store<typename E::T, RankSync>(
+            keys, a.nb, max(m.nblk, m.pin + 1), min(a.topk, a.nb), m.pin, cand, a.kpad,
+            a.topk > 0 ? a.out + static_cast<int64_t>(m.row) * a.ld_out : nullptr, a.topk,
+            score_row<E>(a, m.row), tsh);
+      }
+      RankSync::sync();  // every rank thread is done with the keys
+      if (kMerge) {
+        for (int32_t b = RankSync::tid(); b < a.nb; b += RankSync::count()) keys[b] = kKeyNegInf;
+        RankSync::sync();
+      }
+      if (RankSync::tid() == 0) mbar_arrive(&kempty[rb]);
+      ++rounds;
+    }
   }
-  uint32_t gbase = 0;  // lane-per-block groups in the stages before this one
+
+  // Fold warps.
+  uint32_t gbase = 0;        // lane-per-block groups in the stages before this one
+  int ub = 0;                // key buffer of the current unit
+  uint32_t uses0 = 0, uses1 = 0;
+  bool have = false;         // the current unit's buffer is ours
   for (uint32_t k = 0;; ++k) {
     const uint32_t slot = k % static_cast<uint32_t>(a.stages);
     // A phase that never completes (a fault in the byte accounting) makes
     // every waiter give up; the warp leaves as one.
     const bool ok = mbar_wait(&full[slot], (k / static_cast<uint32_t>(a.stages)) & 1u, kSiteFull);
     if (!__all_sync(0xffffffffu, ok)) return;
+    if (!have) {
+      const uint32_t uses = ub ? uses1 : uses0;
+      const bool free_ok = uses == 0 || mbar_wait(&kempty[ub], (uses - 1u) & 1u, kSiteKeys);
+      if (!__all_sync(0xffffffffu, free_ok)) return;
+      have = true;
+    }
     const StageDesc& d = desc[slot];
     const int32_t flags = d.flags;
-    if (flags & kDone) return;
+    if (flags & kDone) {
+      // The done marker goes to the rank warps through the next buffer.
+      if (warp == 0 && lane == 0) meta[ub].done = 1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&kfull[ub]);
+      return;
+    }
     const int32_t row = d.row, nblk = d.nblk, pin = d.pin, b0 = d.b0, b1 = d.b1,
                   parts = d.parts;
+    uint32_t* keys = keys0 + ub * nbp;
     fold_stage<E, MODE>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d, warp, NW, gbase,
                         keys);
     gbase += stage_groups(a.block_size, d.n);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
     if (!(flags & kLast)) continue;
-    Sync::sync();  // every block of the unit is in keys
-    if (parts > 1 && !merge_parts<Sync>(a, row, nblk, b0, b1, parts, keys, &s_last)) {
-      if (kMerge)
-        for (int32_t b = threadIdx.x; b < a.nb; b += Sync::count()) keys[b] = kKeyNegInf;
-      Sync::sync();
-      continue;
-    }
-    for (int32_t b = nblk + threadIdx.x; b <= pin; b += Sync::count()) keys[b] = kKeyNegInf;
-    Sync::sync();
-    topk_store<typename E::T, Sync>(keys, a.nb, max(nblk, pin + 1), min(a.topk, a.nb), pin, cand,
-                                    a.kpad,
-                                    a.topk > 0 ? a.out + static_cast<int64_t>(row) * a.ld_out
-                                               : nullptr,
-                                    a.topk, score_row<E>(a, row), tsh);
-    Sync::sync();  // keys and candidates are free for the next unit
-    if (kMerge) {
-      for (int32_t b = threadIdx.x; b < a.nb; b += Sync::count()) keys[b] = kKeyNegInf;
-      Sync::sync();
-    }
+    if (warp == 0 && lane == 0) meta[ub] = UnitMeta{row, nblk, pin, b0, b1, parts, 0};
+    __syncwarp();  // this warp's keys (and the unit) before the hand-over
+    if (lane == 0) mbar_arrive(&kfull[ub]);
+    if (ub) ++uses1; else ++uses0;
+    ub ^= 1;
+    have = false;
   }
 }
 
@@ -944,7 +1058,7 @@ dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int c
   a.stage_bytes = (payload + 32 * pieces + 127) & ~127;
   a.cap = static_cast<int32_t>(payload /
                                (static_cast<int64_t>(pieces) * a.block_size * E::kBytes));
-  if (a.cap < 1) return DSA_EUNSUPPORTED;
+  if (a.cap < 1) return kPipeDeclined;
   const int slots = sms * ctas;
   // Parts per row: only when there are fewer rows than CTAs, never below
   // 64 KiB per part, at most 8; only with a workspace. (Merging parts costs
@@ -958,21 +1072,22 @@ dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int c
     if (forced >= 1 && forced <= 8) split = forced;
   }
   a.split = split;
-  const size_t tail = static_cast<size_t>((a.nb + 3) & ~3) * 4 +
+  const size_t tail = 2 * static_cast<size_t>((a.nb + 3) & ~3) * 4 +
                       static_cast<size_t>(std::max(a.kpad, kRankMax)) * 8;
-  const size_t limit = smem_budget(ctas, sizeof(TopkShared) + 16);
+  const size_t limit =
+      smem_budget(ctas, sizeof(TopkShared) + sizeof(PieceTable) + 2 * sizeof(UnitMeta) + 128);
   int stages = 16;
   while (stages >= 2 && coop_keys_offset(stages, a.stage_bytes) + tail > limit) --stages;
   const int fst = g_over[DSA_LAUNCH_PIPE_STAGES].load(std::memory_order_relaxed);
   if (fst >= 2 && fst < stages) stages = fst;
-  if (stages < 2) return DSA_EUNSUPPORTED;
+  if (stages < 2) return kPipeDeclined;
   a.stages = stages;
   const size_t smem = coop_keys_offset(stages, a.stage_bytes) + tail;
   auto kernel = pipe_coop_kernel<E, MODE, NW>;
   if (opt_in_smem(kernel, smem) != cudaSuccess) return DSA_ECUDA;
   const int64_t units = a.rows * static_cast<int64_t>(split);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(units, slots));
-  kernel<<<grid, (NW + 1) * 32, smem, s>>>(a);
+  kernel<<<grid, (NW + kRankWarps + 1) * 32, smem, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
 }
 
@@ -981,16 +1096,15 @@ dsa_status launch_coop(const PipeArgs& a, int64_t max_row_bytes, bool have_ws, c
   const int warps = g_over[DSA_LAUNCH_PIPE_WARPS].load(std::memory_order_relaxed);
   const int fc = g_over[DSA_LAUNCH_PIPE_CTAS].load(std::memory_order_relaxed);
   if (warps == 8)
-    return launch_coop_nw<E, MODE, 8>(a, max_row_bytes, have_ws, fc >= 1 ? std::min(fc, 2) : 1,
-                                      s);
-  return launch_coop_nw<E, MODE, 4>(a, max_row_bytes, have_ws, fc >= 1 ? fc : 2, s);
+    return launch_coop_nw<E, MODE, 8>(a, max_row_bytes, have_ws, 1, s);
+  return launch_coop_nw<E, MODE, 4>(a, max_row_bytes, have_ws, fc >= 1 ? std::min(fc, 2) : 2, s);
 }
 
+// Solo launch with `ctas` CTAs per SM; kPipeDeclined (nothing enqueued) when
+// the rings and the warps' keys do not fit.
 template <typename E>
-dsa_status launch_solo(PipeArgs a, cudaStream_t s) {
+dsa_status launch_solo_ctas(PipeArgs a, int ctas, cudaStream_t s) {
   const int sms = sm_count_now();
-  const int fc = g_over[DSA_LAUNCH_PIPE_CTAS].load(std::memory_order_relaxed);
-  const int ctas = fc >= 1 ? std::min(fc, 2) : 2;
   const int kb = g_over[DSA_LAUNCH_PIPE_STAGE_KB].load(std::memory_order_relaxed);
   const size_t limit = smem_budget(ctas, 0);
   const size_t fixed = static_cast<size_t>(kSoloWarps) * solo_warp_bytes(a.nb);
@@ -1008,7 +1122,7 @@ dsa_status launch_solo(PipeArgs a, cudaStream_t s) {
   }
   const int fst = g_over[DSA_LAUNCH_PIPE_STAGES].load(std::memory_order_relaxed);
   if (fst >= 2 && fst < stages) stages = fst;
-  if (stages < 2 || a.cap < 1) return DSA_EUNSUPPORTED;
+  if (stages < 2 || a.cap < 1) return kPipeDeclined;
   a.stages = stages;
   const size_t smem = solo_warp_offset(kSoloWarps, stages, a.stage_bytes) + fixed;
   auto kernel = pipe_solo_kernel<E, kSoloWarps>;
@@ -1017,6 +1131,16 @@ dsa_status launch_solo(PipeArgs a, cudaStream_t s) {
       std::min<int64_t>((a.rows + kSoloWarps - 1) / kSoloWarps, static_cast<int64_t>(sms) * ctas));
   kernel<<<grid, kSoloWarps * 32, smem, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
+}
+
+// Two CTAs per SM (measured faster on packed prefill rows), one when the
+// keys of rows with many blocks leave no room for two.
+template <typename E>
+dsa_status launch_solo(const PipeArgs& a, cudaStream_t s) {
+  const int fc = g_over[DSA_LAUNCH_PIPE_CTAS].load(std::memory_order_relaxed);
+  if (fc >= 1) return launch_solo_ctas<E>(a, std::min(fc, 2), s);
+  const dsa_status st = launch_solo_ctas<E>(a, 2, s);
+  return st == kPipeDeclined ? launch_solo_ctas<E>(a, 1, s) : st;
 }
 
 template <typename E>
@@ -1055,7 +1179,10 @@ dsa_status dispatch(const PipeCall& c, cudaStream_t s) {
     a.ws_keys = reinterpret_cast<uint32_t*>(static_cast<char*>(c.workspace) + ws_keys_offset(c.rows));
   }
   const int64_t max_row_bytes = static_cast<int64_t>(c.width) * c.elem_bytes * c.shards;
-  if (want_solo(c)) return launch_solo<E>(a, s);
+  if (want_solo(c)) {
+    const dsa_status st = launch_solo<E>(a, s);
+    if (st != kPipeDeclined) return st;
+  }
   switch (c.mode) {
     case kPipeUnsharded: return launch_coop<E, kPipeUnsharded>(a, max_row_bytes, have_ws, s);
     case kPipeSharded: return launch_coop<E, kPipeSharded>(a, max_row_bytes, have_ws, s);

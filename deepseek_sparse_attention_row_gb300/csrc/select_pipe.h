@@ -45,7 +45,10 @@ struct PipeCall {
 // block size they reduce, at most 16 shards, up to 4096 blocks and top-256).
 bool pipe_takes(const PipeCall& c);
 
-// Launches the pipelined selection. Call only when pipe_takes(c).
+// Launches the pipelined selection. Call only when pipe_takes(c). Returns
+// kPipeDeclined, with nothing enqueued, when no pipelined launch shape fits
+// the call (shared memory); the caller then takes another kernel.
+constexpr dsa_status kPipeDeclined = static_cast<dsa_status>(-100);
 dsa_status pipe_select(const PipeCall& c, void* stream);
 
 // Workspace layout shared by every selecting kernel: a 256-byte header whose

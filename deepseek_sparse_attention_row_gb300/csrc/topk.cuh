@@ -36,18 +36,23 @@ namespace dsa {
 constexpr int kRankMax = 256;  // candidates ranked by counting
 
 // Which threads take part in a row's top-k, and how they meet. CtaSync: every
-// thread of the CTA, __syncthreads(). NamedSync<N>: threads 0 .. N - 1 (whole
-// warps), named barrier 1, so that other warps of the CTA (a producer) carry
-// on meanwhile.
+// thread of the CTA, __syncthreads(). NamedSync<N, ID, BASE>: the N threads
+// BASE .. BASE + N - 1 (whole warps), named barrier ID, so that the CTA's
+// other warps (a producer, the warps folding the next row) carry on
+// meanwhile. tid() is a thread's index within the group.
 struct CtaSync {
   __device__ __forceinline__ static void sync() { __syncthreads(); }
   __device__ __forceinline__ static int count() { return blockDim.x; }
+  __device__ __forceinline__ static int tid() { return threadIdx.x; }
 };
-template <int N>
+template <int N, int ID = 1, int BASE = 0>
 struct NamedSync {
-  static_assert(N % 32 == 0, "whole warps");
-  __device__ __forceinline__ static void sync() { asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory"); }
+  static_assert(N % 32 == 0 && BASE % 32 == 0, "whole warps");
+  __device__ __forceinline__ static void sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
+  }
   __device__ __forceinline__ static constexpr int count() { return N; }
+  __device__ __forceinline__ static int tid() { return static_cast<int>(threadIdx.x) - BASE; }
 };
 
 struct TopkShared {
@@ -70,13 +75,13 @@ __device__ __forceinline__ int32_t candidate_id(uint64_t c) {
 template <typename Sync = CtaSync>
 __device__ __forceinline__ void rank_store(const uint64_t* __restrict__ cand, int32_t n, int32_t K,
                                            int32_t* __restrict__ out, int32_t topk) {
-  for (int i = threadIdx.x; i < n; i += Sync::count()) {
+  for (int i = Sync::tid(); i < n; i += Sync::count()) {
     const uint64_t ci = cand[i];
     int32_t r = 0;
     for (int j = 0; j < n; ++j) r += cand[j] > ci;
     if (r < K) out[r] = candidate_id(ci);
   }
-  for (int j = K + threadIdx.x; j < topk; j += Sync::count()) out[j] = -1;
+  for (int j = K + Sync::tid(); j < topk; j += Sync::count()) out[j] = -1;
 }
 
 // Exact path. Preconditions: keys final; total = number of keys above -inf,
@@ -85,7 +90,7 @@ template <typename Sync = CtaSync>
 __device__ void topk_exact(const uint32_t* __restrict__ keys, int32_t nb, int32_t K, uint32_t total,
                            uint32_t m, uint32_t M, uint64_t* __restrict__ cand, int32_t kpad,
                            int32_t* __restrict__ out, int32_t topk, TopkShared& sh) {
-  const int tid = threadIdx.x;
+  const int tid = Sync::tid();
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int nthreads = Sync::count();
@@ -231,7 +236,7 @@ __device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t n_li
                            int32_t* __restrict__ out, int32_t topk, S* __restrict__ scores,
                            TopkShared& sh) {
   constexpr int KR = 8;  // live keys per thread held in registers
-  const int tid = threadIdx.x;
+  const int tid = Sync::tid();
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int nthreads = Sync::count();
