@@ -134,6 +134,21 @@ def workload_config(wl, name: str) -> dict:
     return cfg
 
 
+def selection_kernel(wl, sms: int = 152) -> str:
+    """The selecting kernel the library's default launch choice takes for a
+    workload (the rule of select_impl / pipe_takes, restated for the report):
+    the DCP forms stay on select_kernel; unsharded rows go to the pipelined
+    kernels, one row per warp for many short rows with top-k <= 32."""
+    if hasattr(wl, "global_row_ke"):
+        return "select_kernel (row per CTA, one launch per step)"
+    nb = -(-wl.width // wl.block_size)
+    solo = (wl.topk_blocks <= 32 and nb <= 2048 and wl.width * esize(wl) <= 64 * 1024
+            and wl.rows >= 8 * sms)
+    return ("pipe_solo_kernel (bulk-copy staged, one row per warp, one launch per step)" if solo
+            else "pipe_coop_kernel (bulk-copy staged, warps of a CTA on one row, one launch "
+                 "per step)")
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -711,7 +726,10 @@ def time_other_workloads(names, dsa, torch, device, timer, steps: int, warmup: i
                      "unit": UNIT, "frac": round(nbytes / ms / 1e6 / peak, 4),
                      "rows_per_s": round(wl.rows / ms * 1e3, 1),
                      "algorithmic_bytes_per_step": nbytes, "steps": n,
-                     "workload": workload_config(wl, name)["workload"], "l2": timer.l2_note()}
+                     "workload": workload_config(wl, name)["workload"], "l2": timer.l2_note(),
+                     "kernel": selection_kernel(wl, torch.cuda.get_device_properties(device)
+                                                .multi_processor_count),
+                     "traffic": profiled_traffic("select", name)}
         del step, wl
         timer.one = timer.many = None
         torch.cuda.empty_cache()
@@ -837,8 +855,9 @@ def run_ours(args):
             config = workload_config(wl, args.workload)
             full_gbs = round(whole_job_rate(wl.logits.size * esize(wl) * args.steps, world,
                                             max_ms / 1e3) / 1e9, 3)
-            kernel = ("select_kernel (one launch per step)" if args.op == "select"
-                      else "mask_kernel (one launch per step)")
+            kernel = (selection_kernel(wl, torch.cuda.get_device_properties(device)
+                                       .multi_processor_count)
+                      if args.op == "select" else "mask_kernel (one launch per step)")
             dtype = "f32" if esize(wl) == 4 else "bf16 data, exact compares"
         line = {
             "metric": metric, "value": round(value, 3), "unit": UNIT, "n_gpus": world,

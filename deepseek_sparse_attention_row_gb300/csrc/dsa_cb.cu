@@ -798,6 +798,10 @@ dsa_status dsa_select_set_launch_override(int32_t knob, int32_t value) {
       if (value < 0 || value > 4) return DSA_EINVAL;
       pipe_set_override(knob, value);
       return DSA_OK;
+    case DSA_LAUNCH_PIPE_STAGE_OWNER:
+      if (value < 0 || value > 1) return DSA_EINVAL;
+      pipe_set_override(knob, value);
+      return DSA_OK;
     default:
       return DSA_EINVAL;
   }

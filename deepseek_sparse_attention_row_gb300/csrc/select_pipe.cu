@@ -116,6 +116,7 @@ struct PipeArgs {
   int32_t stages;       // ring depth (coop) or depth of each warp's ring (solo)
   int32_t stage_bytes;  // multiple of 128
   int32_t cap;          // blocks per stage
+  int32_t own_stages;   // coop: each fold warp folds whole stages in turn
 };
 
 // ---------------------------------------------------------------------------
@@ -334,7 +335,10 @@ __device__ __forceinline__ void fold_lane_blocks(const unsigned char* stage, con
   constexpr int CH = BS < 32 ? 1 : BS / 32;
   constexpr int LB = BS <= 1 ? 0 : BS == 2 ? 1 : BS == 4 ? 2 : BS == 8 ? 3 : 4;
   const int lane = threadIdx.x & 31;
-  const int32_t c0 = d.c0, n = d.n;
+  // The descriptor's fields in registers: key stores may alias shared
+  // memory, so the compiler would reload them on every block.
+  const int32_t c0 = d.c0, n = d.n, cnt = d.cnt;
+  const unsigned char* __restrict__ const piece = stage + d.off;
   // Byte offsets of this lane's visiting order within a run of T elements.
   uint32_t offs[T];
 #pragma unroll
@@ -347,9 +351,9 @@ __device__ __forceinline__ void fold_lane_blocks(const unsigned char* stage, con
     if (blk >= n) continue;
     float acc[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
     {
-      const int32_t valid = d.cnt - blk * BS;
+      const int32_t valid = cnt - blk * BS;
       if (valid <= 0) continue;
-      const unsigned char* pb = stage + d.off + static_cast<uint32_t>(blk * BS) * ES;
+      const unsigned char* pb = piece + static_cast<uint32_t>(blk * BS) * ES;
       if (valid >= BS) {
 #pragma unroll
         for (int i = 0; i < T; ++i)
@@ -386,7 +390,10 @@ __device__ __forceinline__ void fold_lane_blocks_vec(const unsigned char* stage,
   static_assert(CH >= 1 && (BS * ES) % 16 == 0, "whole 16-byte chunks");
   constexpr int SH = CH >= 8 ? 0 : CH == 4 ? 1 : CH == 2 ? 2 : 3;
   const int lane = threadIdx.x & 31;
-  const int32_t c0 = d.c0, n = d.n;
+  // The descriptor's fields in registers: key stores may alias shared
+  // memory, so the compiler would reload them on every block.
+  const int32_t c0 = d.c0, n = d.n, cnt = d.cnt;
+  const unsigned char* __restrict__ const piece = stage + d.off;
   uint32_t offs[CH];
 #pragma unroll
   for (int c = 0; c < CH; ++c)
@@ -395,9 +402,9 @@ __device__ __forceinline__ void fold_lane_blocks_vec(const unsigned char* stage,
   for (int32_t g = g0; g < ngroups; g += gstep) {
     const int32_t blk = g * 32 + lane;
     if (blk >= n) continue;
-    const int32_t valid = d.cnt - blk * BS;
+    const int32_t valid = cnt - blk * BS;
     if (valid <= 0) continue;
-    const unsigned char* pb = stage + d.off + static_cast<uint32_t>(blk * BS) * ES;
+    const unsigned char* pb = piece + static_cast<uint32_t>(blk * BS) * ES;
     float acc;
     if (valid >= BS) {
       if constexpr (ES == 4) {
@@ -445,14 +452,17 @@ __device__ __forceinline__ void fold_elems(const unsigned char* stage, const Sta
                                            uint32_t* __restrict__ keys) {
   constexpr int ES = E::kBytes;
   const int lane = threadIdx.x & 31;
-  const int32_t c0 = d.c0, n = d.n;
+  // The descriptor's fields in registers: key stores may alias shared
+  // memory, so the compiler would reload them on every block.
+  const int32_t c0 = d.c0, n = d.n, cnt = d.cnt;
+  const unsigned char* __restrict__ const piece = stage + d.off;
   if (bs >= 32) {
     for (int32_t b = t0; b < n; b += tstep) {
       float acc = neg_inf();
       for (int32_t i = 0; i < bs; i += 32) {
         const int32_t j = b * bs + i + lane;
-        const int32_t lim = d.cnt;
-        const float v = stage_elem<E>(stage + d.off + (j < lim ? j : 0) * ES);
+        const int32_t lim = cnt;
+        const float v = stage_elem<E>(piece + (j < lim ? j : 0) * ES);
         acc = j < lim ? max_nan(acc, v) : acc;
       }
       const uint32_t key = __reduce_max_sync(0xffffffffu, order_key(acc));
@@ -467,8 +477,8 @@ __device__ __forceinline__ void fold_elems(const unsigned char* stage, const Sta
     const int32_t ntile = (n * bs + 31) >> 5;
     for (int32_t tt = t0; tt < ntile; tt += tstep) {
       const int32_t j = tt * 32 + lane;
-      const int32_t lim = d.cnt;
-      const float v = stage_elem<E>(stage + d.off + (j < lim ? j : 0) * ES);
+      const int32_t lim = cnt;
+      const float v = stage_elem<E>(piece + (j < lim ? j : 0) * ES);
       const float acc = j < lim ? v : neg_inf();
       uint32_t key = order_key(acc);
       for (int o = 1; o < bs; o <<= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
@@ -759,8 +769,11 @@ __global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
     const int32_t row = d.row, nblk = d.nblk, pin = d.pin, b0 = d.b0, b1 = d.b1,
                   parts = d.parts;
     uint32_t* keys = keys0 + ub * nbp;
-    fold_stage<E, MODE>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d, warp, NW, gbase,
-                        keys);
+    if (!a.own_stages)
+      fold_stage<E, MODE>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d, warp, NW, gbase,
+                          keys);
+    else if (k % NW == static_cast<uint32_t>(warp))
+      fold_stage<E, MODE>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d, 0, 1, 0u, keys);
     gbase += stage_groups(a.block_size, d.n);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
@@ -1072,6 +1085,7 @@ dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int c
     if (forced >= 1 && forced <= 8) split = forced;
   }
   a.split = split;
+  a.own_stages = g_over[DSA_LAUNCH_PIPE_STAGE_OWNER].load(std::memory_order_relaxed) == 1;
   const size_t tail = 2 * static_cast<size_t>((a.nb + 3) & ~3) * 4 +
                       static_cast<size_t>(std::max(a.kpad, kRankMax)) * 8;
   const size_t limit =

@@ -119,6 +119,9 @@ size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks);
  *                          consumer warps per CTA
  *   DSA_LAUNCH_PIPE_CTAS   pipelined kernels: CTAs per SM, 1..4 (at most 2
  *                          with 8 consumer warps or one row per warp)
+ *   DSA_LAUNCH_PIPE_STAGE_OWNER  pipelined kernels, every warp on one row:
+ *                          1 = each folding warp takes whole stages in turn
+ *                          (default: every stage's blocks shared by all)
  *
  * DSA_EINVAL for an unknown knob or a value outside its range (nothing
  * changes then).
@@ -134,7 +137,8 @@ enum {
     DSA_LAUNCH_PIPE_STAGE_KB = 8,
     DSA_LAUNCH_PIPE_SCHED = 9,
     DSA_LAUNCH_PIPE_WARPS = 10,
-    DSA_LAUNCH_PIPE_CTAS = 11
+    DSA_LAUNCH_PIPE_CTAS = 11,
+    DSA_LAUNCH_PIPE_STAGE_OWNER = 12
 };
 dsa_status dsa_select_set_launch_override(int32_t knob, int32_t value);
 
