@@ -90,7 +90,8 @@ EXPORTED_SYMBOLS = (
 # Knobs of dsa_select_set_launch_override (include/dsa_cb.h).
 LAUNCH_KNOBS = {"split": 1, "threads": 2, "warp_rows": 3, "warp_order": 4, "pipeline": 5,
                 "pipe_split": 6, "pipe_stages": 7, "pipe_stage_kb": 8, "pipe_sched": 9,
-                "pipe_warps": 10, "pipe_ctas": 11, "pipe_stage_owner": 12}
+                "pipe_warps": 10, "pipe_ctas": 11, "pipe_stage_owner": 12, "pipe_order": 13,
+                "rank_cta": 14}
 
 _lib = None
 

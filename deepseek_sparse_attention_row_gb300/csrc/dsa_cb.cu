@@ -75,6 +75,7 @@ struct SelectArgs {
   uint32_t* ws_count;   // split > 1: [rows] arrival counters (zero between calls)
   int64_t rows;         // rows of the call
   int32_t reverse;      // select_warp_kernel: take rows last to first
+  int32_t rank_cta;     // select_kernel: the whole CTA ranks every row
 };
 
 template <typename E>
@@ -224,20 +225,32 @@ __device__ __forceinline__ RowPlan<E> plan_row(const SelectArgs& a, int64_t row,
   if constexpr (MODE == kShardedStarts) {
     // Each shard's window [start[d], start[d] + len[d]) and its blocks
     // count from start[d]; the vector width is chosen per shard later.
+    // With x = q * shards + r (0 <= r < shards), shard d holds
+    // ceil((x - d) / shards) = q + (d < r) of the global tokens below x, so
+    // two divisions give every shard's start and end.
     const int64_t g = row / a.row_repeat;
-    const int32_t gke = __ldg(a.row_ke + g);
-    const int32_t gs = min(max(__ldg(a.row_ks + g), 0), max(gke, 0));
-    shard_q = gs / a.shards;
-    shard_rem = gs % a.shards;
-    int32_t len_max = 0;
-    for (int d = 0; d < a.shards; ++d) {
-      const int32_t e = shard_len(gke, d, a.shards, a.width);
-      const int32_t st = min(shard_len(gs, d, a.shards, a.width), e);
-      len_max = max(len_max, e - st);
-      if (d % blockDim.x == threadIdx.x) {
-        len[d] = e - st;
-        start[d] = st;
-      }
+    const int32_t gke = max(__ldg(a.row_ke + g), 0);
+    const int32_t gs = min(max(__ldg(a.row_ks + g), 0), gke);
+    const uint32_t D = static_cast<uint32_t>(a.shards);
+    const int32_t qe = static_cast<int32_t>(static_cast<uint32_t>(gke) / D);
+    const int32_t re = gke - qe * a.shards;
+    shard_q = static_cast<int32_t>(static_cast<uint32_t>(gs) / D);
+    shard_rem = gs - shard_q * a.shards;
+    auto window = [&](int d, int32_t& st) {
+      const int32_t e = min(qe + (d < re ? 1 : 0), a.width);
+      st = min(shard_q + (d < shard_rem ? 1 : 0), e);
+      return e - st;
+    };
+    // A shard's window length is constant on the runs of d cut at
+    // shard_rem and re, so its largest value is taken at one of d = 0,
+    // shard_rem, re and shards - 1.
+    int32_t st;
+    const int32_t last = a.shards - 1;
+    const int32_t len_max = max(max(window(0, st), window(min(shard_rem, last), st)),
+                                max(window(min(re, last), st), window(last, st)));
+    for (int d = threadIdx.x; d < a.shards; d += blockDim.x) {
+      len[d] = window(d, st);
+      start[d] = st;
     }
     plan.origin = logits + row * a.ld;
     plan.len_max = len_max;
@@ -300,35 +313,33 @@ __device__ __forceinline__ void stream_range(const SelectArgs& a, const RowPlan<
       // row streams on its own.
       const int32_t rg = a.shards > 1 ? shard_rem : 0;
       const bool grouped = (a.shard_stride * E::kBytes) % 16 == 0;
-      // One pass over both groups (stream_shift with two offsets) when the
-      // block is a power of two of 16-byte vectors and each group's aligned
-      // base stays inside its rows.
+      // One pass over both groups, read from one aligned base
+      // (stream_shift_paired), when the block is a power of two of 16-byte
+      // vectors and the base stays inside the rows.
       constexpr int V16 = 16 / E::kBytes;
       const int32_t lpbv = a.block_size / V16;
       bool paired = grouped && a.block_size % V16 == 0 && (lpbv & (lpbv - 1)) == 0;
-      ShiftGroups<E> sg;
+      PairedShift<E> ps;
       if (paired) {
-        for (int g = 0; g < 2; ++g) {
-          const int32_t st = min(g == 0 ? shard_q : shard_q + 1, a.width);
-          const TE* o = plan.origin + st;
-          const int32_t r = static_cast<int32_t>((reinterpret_cast<uintptr_t>(o) / E::kBytes) &
-                                                 (V16 - 1));
-          paired = paired && st >= r;
-          sg.base[g] = o - r;
-          sg.r[g] = r;
-        }
-        sg.split = rg;
-        sg.shard_stride = a.shard_stride;
-        sg.shards = a.shards;
-        sg.len = len;
-        sg.merge = false;
-        int32_t cap = 0;
-        for (int d = 0; d < a.shards; ++d) cap = max(cap, (len[d] + sg.r[d < rg ? 1 : 0]) / V16);
-        sg.v_cap = cap;
+        const int32_t q = min(shard_q, a.width);
+        const TE* o = plan.origin + q;
+        const int32_t r0 = static_cast<int32_t>((reinterpret_cast<uintptr_t>(o) / E::kBytes) &
+                                                (V16 - 1));
+        paired = q >= r0;
+        ps.base = o - r0;
+        ps.r0 = r0;
+        ps.split = rg;
+        ps.shard_stride = a.shard_stride;
+        ps.shards = a.shards;
+        ps.len = len;
+        ps.merge = false;
+        // A bound on every shard's whole vectors (each shard's own limit is
+        // applied in the loop).
+        ps.v_cap = (plan.len_max + r0 + 1) / V16;
       }
       if (paired)
-        stream_shift<E, 1, 8>(sg, __ffs(lpbv) - 1, b0, b1, keys, 0, threadIdx.x >> 5,
-                              blockDim.x >> 5);
+        stream_shift_paired<E, 8>(ps, __ffs(lpbv) - 1, b0, b1, keys, 0, threadIdx.x >> 5,
+                                  blockDim.x >> 5);
       for (int grp = 0; grp < 2 && !paired; ++grp) {
         const int d_lo = grp == 0 ? rg : 0, d_hi = grp == 0 ? a.shards : rg;
         if (d_lo >= d_hi) continue;
@@ -398,19 +409,35 @@ __device__ __forceinline__ void stream_range(const SelectArgs& a, const RowPlan<
 }
 
 // Pins, ranks and stores one row whose block keys [0, nblk) are final in
-// shared memory. Called by every thread of the CTA.
+// shared memory. Called by every thread of the CTA. Rows of up to 1024 live
+// blocks with k <= 32 are ranked by warp 0 alone (topk_warp_wide): the
+// other warps leave, and the ranking costs a quarter of the instructions of
+// the CTA-wide topk_store.
 template <typename E>
 __device__ __forceinline__ void rank_row(const SelectArgs& a, int64_t row, int32_t nblk,
                                          int32_t pin_block, uint32_t* keys, uint64_t* cand,
                                          TopkShared& tsh) {
   using TE = typename E::T;
+  const int32_t n_live = max(nblk, pin_block + 1);
+  const int32_t k = min(a.topk, a.nb);
+  int32_t* out = a.topk > 0 ? a.out + row * a.ld_out : nullptr;
+  TE* scores = a.scores ? static_cast<TE*>(a.scores) + row * a.ld_scores : nullptr;
+  if (!a.rank_cta && k <= 32 && n_live <= 1024) {
+    // Blocks between the data and the pin are -inf; after the barrier (the
+    // last CTA of a split row may still be reading other parts' keys back)
+    // the ranking warp makes the pin +inf.
+    for (int32_t b = nblk + threadIdx.x; b < pin_block; b += blockDim.x) keys[b] = kKeyNegInf;
+    __syncthreads();
+    if (threadIdx.x < 32)
+      topk_warp_wide(keys, a.nb, n_live, k, pin_block, cand, max(a.kpad, kRankMax), out, a.topk,
+                     scores);
+    return;
+  }
   // Blocks past the data blocks up to the pin are -inf (the pin can lie past
   // the data in the DCP form); topk_store never reads further.
   for (int32_t b = nblk + threadIdx.x; b <= pin_block; b += blockDim.x) keys[b] = kKeyNegInf;
   __syncthreads();
-  topk_store(keys, a.nb, max(nblk, pin_block + 1), min(a.topk, a.nb), pin_block, cand, a.kpad,
-             a.topk > 0 ? a.out + row * a.ld_out : nullptr, a.topk,
-             a.scores ? static_cast<TE*>(a.scores) + row * a.ld_scores : nullptr, tsh);
+  topk_store(keys, a.nb, n_live, k, pin_block, cand, a.kpad, out, a.topk, scores, tsh);
 }
 
 // Publishes keys [b0, b1) of `row` to the workspace and counts `units` of the
@@ -444,7 +471,7 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);  // [max(kpad, kRankMax)]
   uint32_t* keys = reinterpret_cast<uint32_t*>(cand + max(a.kpad, kRankMax));  // [nb]
-  int32_t* len = reinterpret_cast<int32_t*>(keys + a.nb);                // [shards]
+  int32_t* len = reinterpret_cast<int32_t*>(keys + ((a.nb + 3) & ~3));   // [shards]
   int32_t* start = len + a.shards;  // [shards], kShardedStarts only
   __shared__ TopkShared tsh;
   __shared__ int s_last;
@@ -589,6 +616,7 @@ std::atomic<int> g_split_override{0};    // CTAs per row with a workspace, 1..8
 std::atomic<int> g_threads_override{0};  // 128 or 256 threads per CTA
 std::atomic<int> g_warp_off{0};          // 1: never one row per warp
 std::atomic<int> g_warp_in_order{0};     // 1: one row per warp, rows in order
+std::atomic<int> g_rank_cta{0};          // select_kernel ranking: 1 whole CTA, 2 one warp
 
 int32_t next_pow2(int32_t x) {
   int32_t p = 1;
@@ -719,11 +747,11 @@ dsa_status fill_minus_one(int32_t* out, int64_t rows, int32_t cols, int64_t ld, 
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
 }
 
-// Dynamic shared memory of select_kernel: candidates, block keys, and the
-// shard lengths and starts.
+// Dynamic shared memory of select_kernel: candidates, block keys (padded to
+// a multiple of 4 for 16-byte loads), and the shard lengths and starts.
 size_t select_smem(int32_t kpad, int32_t nb, int32_t shards) {
-  return static_cast<size_t>(std::max(kpad, kRankMax)) * 8 + static_cast<size_t>(nb) * 4 +
-         static_cast<size_t>(shards) * 8;
+  return static_cast<size_t>(std::max(kpad, kRankMax)) * 8 +
+         static_cast<size_t>((nb + 3) & ~3) * 4 + static_cast<size_t>(shards) * 8;
 }
 
 
@@ -801,6 +829,14 @@ dsa_status dsa_select_set_launch_override(int32_t knob, int32_t value) {
     case DSA_LAUNCH_PIPE_STAGE_OWNER:
       if (value < 0 || value > 1) return DSA_EINVAL;
       pipe_set_override(knob, value);
+      return DSA_OK;
+    case DSA_LAUNCH_PIPE_ORDER:
+      if (value < 0 || value > 2) return DSA_EINVAL;
+      pipe_set_override(knob, value);
+      return DSA_OK;
+    case DSA_LAUNCH_RANK_CTA:
+      if (value < 0 || value > 2) return DSA_EINVAL;
+      g_rank_cta.store(value);
       return DSA_OK;
     default:
       return DSA_EINVAL;
@@ -886,6 +922,7 @@ dsa_status select_impl(const typename E::T* logits, int64_t rows, int64_t width,
   a.pin_newest = pin_newest != 0;
   a.topk = topk_blocks;
   a.kpad = next_pow2(std::max<int32_t>(1, std::min<int32_t>(topk_blocks, a.nb)));
+  a.rank_cta = g_rank_cta.load(std::memory_order_relaxed) == 1;
   a.out = out;
   a.ld_out = ld_out;
   a.scores = scores_out;
@@ -1000,6 +1037,14 @@ dsa_status select_sharded_impl(const typename E::T* logits, int32_t shards, int6
   a.pin_newest = 0;
   a.topk = topk_blocks;
   a.kpad = next_pow2(std::max<int32_t>(1, std::min<int32_t>(topk_blocks, nbg)));
+  // The fp32 DCP form without starts streams at about 0.91 of the copy
+  // bandwidth: there the whole CTA ranks, which frees the CTA's slot sooner
+  // (86.0 against 86.7 us on the [8, 4096, 8192] workload). The other forms
+  // are issue-bound and rank with one warp.
+  {
+    const int rc = g_rank_cta.load(std::memory_order_relaxed);
+    a.rank_cta = rc == 1 || (rc == 0 && !global_row_ks && sizeof(typename E::T) == 4);
+  }
   a.out = out;
   a.ld_out = ld_out;
   a.scores = scores_out;

@@ -156,6 +156,19 @@ __device__ __forceinline__ float raw_elem(const Raw<E, VEC>& r, int i) {
   }
 }
 
+// Element r of a loaded 16-byte vector, r a runtime index (0 .. VEC-1),
+// widened to fp32; selects on the bits of r, no local memory.
+template <typename E, int VEC>
+__device__ __forceinline__ float raw_elem_at(const Raw<E, VEC>& x, int r) {
+  static_assert(VEC * E::kBytes == 16, "16-byte vectors");
+  const int wi = E::kBytes == 4 ? r : (r >> 1);  // word holding element r
+  const uint32_t lo2 = (wi & 1) ? x.w[1] : x.w[0];
+  const uint32_t hi2 = (wi & 1) ? x.w[3] : x.w[2];
+  const uint32_t w = (wi & 2) ? hi2 : lo2;
+  if constexpr (E::kBytes == 4) return __uint_as_float(w);
+  else return __uint_as_float((r & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
 // Fold a loaded vector into an accumulator with the NaN-propagating max.
 template <typename E, int VEC>
 __device__ __forceinline__ float fold(float acc, const Raw<E, VEC>& r) {

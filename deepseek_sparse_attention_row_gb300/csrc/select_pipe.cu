@@ -117,6 +117,7 @@ struct PipeArgs {
   int32_t stage_bytes;  // multiple of 128
   int32_t cap;          // blocks per stage
   int32_t own_stages;   // coop: each fold warp folds whole stages in turn
+  int32_t lpt;          // coop, unsharded, S = 1: unit u is row order[u], longest first
 };
 
 // ---------------------------------------------------------------------------
@@ -236,13 +237,15 @@ struct PieceTable {
 // work, so that no shuffle or warp barrier lengthens the path between two
 // stages: wait for the stage's slot, write its descriptor (the unit's fields
 // only on its last stage), arm its barrier and issue the one bulk copy.
-// Returns false (on lane 0) when a wait gave up.
+// With `claim`, the next unit is claimed from the unit counter as the last
+// stage's turn comes (before waiting for its slot). Returns false (on lane
+// 0) when a wait gave up.
 template <typename E>
 __device__ __forceinline__ bool emit_unit(const PipeArgs& a, const PieceTable& pt, int npieces,
                                           int32_t row, int32_t nblk, int32_t pin, int32_t b0,
                                           int32_t b1, int32_t parts, unsigned char* buf,
                                           uint64_t* full, uint64_t* empty, StageDesc* desc,
-                                          int stages, uint32_t& k) {
+                                          int stages, uint32_t& k, uint32_t* claim = nullptr) {
   const int32_t bs = a.block_size;
   int32_t c = b0;
   int shard = 0;
@@ -251,6 +254,7 @@ __device__ __forceinline__ bool emit_unit(const PipeArgs& a, const PieceTable& p
     const bool last = c + n >= b1 && shard == npieces - 1;
     const uint32_t slot = k % static_cast<uint32_t>(stages);
     const uint32_t round = k / static_cast<uint32_t>(stages);
+    if (last && claim) *claim = atomicAdd(a.queue, 1u);
     if (round > 0 && !mbar_wait(&empty[slot], (round - 1u) & 1u, kSiteEmpty)) return false;
     // The piece: elements [c*bs, min((c+n)*bs, len)) of the shard's window,
     // copied from the 16-byte granule holding its first element through the
@@ -597,6 +601,105 @@ __device__ __forceinline__ void retire_queue(const PipeArgs& a) {
   }
 }
 
+// Longest rows first. With rows handed out by the unit counter, CTAs that
+// start on long rows and pick up short ones when they free up finish close
+// together (greedy list scheduling in longest-first order); in index order a
+// CTA can draw two of the longest rows while others idle. Every CTA computes
+// the same order: a stable counting sort of the rows by window length, cut
+// into kLptClasses classes of width/(kLptClasses - 1) elements, longest class
+// first and row index ascending within a class. Warp w sorts a contiguous
+// range of 32-row chunks; __match_any_sync gives each lane its peers in the
+// same class. Scratch (per-warp class counts and the rows' classes) lives in
+// the ring, which no copy touches before the order is built.
+constexpr int kLptClasses = 128;
+constexpr int kLptMaxRows = 4096;
+
+__host__ __device__ __forceinline__ size_t lpt_scratch_bytes(int warps, int32_t rows) {
+  return static_cast<size_t>(warps + 1) * kLptClasses * 4 + static_cast<size_t>(rows);
+}
+
+template <int NWARPS>
+__device__ void longest_first_order(const PipeArgs& a, uint16_t* __restrict__ order,
+                                    unsigned char* __restrict__ scratch) {
+  uint32_t* hist = reinterpret_cast<uint32_t*>(scratch);  // [NWARPS][kLptClasses]
+  uint32_t* start = hist + NWARPS * kLptClasses;           // [kLptClasses]
+  unsigned char* cls = reinterpret_cast<unsigned char*>(start + kLptClasses);  // [rows]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < NWARPS * kLptClasses; i += blockDim.x) hist[i] = 0u;
+  const int32_t rows = a.rows;
+  // Every row's class (independent loads, all in flight together).
+  const uint64_t width = static_cast<uint64_t>(max(a.width, 1));
+#pragma unroll 4
+  for (int32_t r = threadIdx.x; r < rows; r += blockDim.x) {
+    const Bounds bnd = load_bounds<kPipeUnsharded>(a, r);
+    const int32_t e = min(bnd.hi, a.width);
+    const int32_t st = min(max(bnd.lo, 0), e);
+    const uint64_t n = e > st ? static_cast<uint64_t>(e - st) : 0u;
+    cls[r] = static_cast<unsigned char>((kLptClasses - 1) -
+                                        static_cast<int>(n * (kLptClasses - 1) / width));
+  }
+  __syncthreads();
+  const int32_t nch = (rows + 31) >> 5;
+  const int32_t cpw = (nch + NWARPS - 1) / NWARPS;
+  const int32_t c0 = warp * cpw, c1 = min(c0 + cpw, nch);
+  uint32_t* h = hist + warp * kLptClasses;
+  for (int32_t c = c0; c < c1; ++c) {
+    const int32_t r = c * 32 + lane;
+    const int b = r < rows ? static_cast<int>(cls[r]) : -1;  // 0: longest
+    const uint32_t peers = __match_any_sync(0xffffffffu, b);
+    if (b >= 0 && lane == __ffs(peers) - 1) h[b] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // Each class's start in the order (an exclusive scan over classes, longest
+  // first), then each warp's start within the class.
+  if (warp == 0) {
+    constexpr int PER = kLptClasses / 32;
+    uint32_t t[PER], sum = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      t[i] = 0;
+      for (int w = 0; w < NWARPS; ++w) t[i] += hist[w * kLptClasses + lane * PER + i];
+      sum += t[i];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    uint32_t run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      start[lane * PER + i] = run;
+      run += t[i];
+    }
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < kLptClasses; b += blockDim.x) {
+    uint32_t off = start[b];
+    for (int w = 0; w < NWARPS; ++w) {
+      const uint32_t c = hist[w * kLptClasses + b];
+      hist[w * kLptClasses + b] = off;
+      off += c;
+    }
+  }
+  __syncthreads();
+  for (int32_t c = c0; c < c1; ++c) {
+    const int32_t r = c * 32 + lane;
+    const int b = r < rows ? static_cast<int>(cls[r]) : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, b);
+    if (b >= 0) order[h[b] + __popc(peers & ((1u << lane) - 1u))] = static_cast<uint16_t>(r);
+    __syncwarp();
+    if (b >= 0 && lane == __ffs(peers) - 1) h[b] += __popc(peers);
+    __syncwarp();
+  }
+  // The ring's generic-proxy accesses come before the copies that later
+  // write it.
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+}
+
 // A finished unit handed from the fold warps to the rank warps.
 struct UnitMeta {
   int32_t row, nblk, pin, b0, b1, parts, done;
@@ -605,7 +708,8 @@ struct UnitMeta {
 constexpr int kRankWarps = 4;
 
 // Shared memory of a coop CTA: ring, its barriers and descriptors, then two
-// key buffers [nb] (padded to 4) and the candidates [max(kpad, kRankMax)].
+// key buffers [nb] (padded to 4), the candidates [max(kpad, kRankMax)] and,
+// with a.lpt, the row order [rows] (uint16).
 __host__ __device__ __forceinline__ size_t coop_keys_offset(int stages, int stage_bytes) {
   return static_cast<size_t>(stages) * stage_bytes +
          ((static_cast<size_t>(stages) * (16 + sizeof(StageDesc)) + 127) & ~static_cast<size_t>(127));
@@ -632,10 +736,12 @@ __global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
   const int32_t nbp = (a.nb + 3) & ~3;
   uint32_t* keys0 = reinterpret_cast<uint32_t*>(smem + coop_keys_offset(a.stages, a.stage_bytes));
   uint64_t* cand = reinterpret_cast<uint64_t*>(keys0 + 2 * nbp);
+  uint16_t* order = reinterpret_cast<uint16_t*>(cand + max(a.kpad, kRankMax));
   __shared__ TopkShared tsh;
   __shared__ int s_last;
   __shared__ __align__(8) uint64_t kfull[2], kempty[2];
   __shared__ UnitMeta meta[2];
+  __shared__ PieceTable pt;  // the producer's current unit
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int32_t b = threadIdx.x; b < 2 * nbp; b += blockDim.x) keys0[b] = kKeyNegInf;
@@ -651,12 +757,44 @@ __global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
     mbar_init_fence();
   }
   __syncthreads();
+  if constexpr (MODE == kPipeUnsharded)
+    if (a.lpt) longest_first_order<NW + NR + 1>(a, order, ring);
+
+  if (MODE == kPipeUnsharded && a.lpt && warp == NW + NR) {
+    // Producer warp, longest rows first: a CTA claims its next row only when
+    // the current row's last stage is due (the ring still holds the row's
+    // last stages, which hides the claim's round trip), so rows go to CTAs
+    // as they free up. The row's bounds were read by the order pass and are
+    // cached.
+    const uint32_t total = static_cast<uint32_t>(a.rows);
+    uint32_t u = 0;
+    if (lane == 0) u = atomicAdd(a.queue, 1u);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    uint32_t k = 0;
+    int ok = 1;
+    while (ok && u < total) {
+      const int32_t row = order[u];
+      const LanePlan<E> p = plan_lane<E, MODE>(a, row, load_bounds<MODE>(a, row), lane);
+      if (lane == 0) {
+        pt.origin[0] = reinterpret_cast<const unsigned char*>(p.origin);
+        pt.len[0] = p.len;
+        ok = emit_unit<E>(a, pt, 1, row, p.nblk, p.pin, 0, p.nblk, 1, ring, full, empty, desc,
+                          a.stages, k, &u);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      u = __shfl_sync(0xffffffffu, u, 0);
+    }
+    if (lane == 0) {
+      retire_queue(a);
+      if (ok) emit_done(full, empty, desc, a.stages, k);
+    }
+    return;
+  }
 
   if (warp == NW + NR) {
     // Producer warp. Units are fetched two ahead: while the stages of unit u
     // go out, the bounds of the next unit and the index of the one after it
     // are in flight, so a unit boundary waits on no memory round trip.
-    __shared__ PieceTable pt;
     const uint32_t S = static_cast<uint32_t>(a.split);
     const uint32_t total = static_cast<uint32_t>(a.rows) * S;
     const int npieces = MODE == kPipeUnsharded ? 1 : a.shards;
@@ -1086,8 +1224,14 @@ dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int c
   }
   a.split = split;
   a.own_stages = g_over[DSA_LAUNCH_PIPE_STAGE_OWNER].load(std::memory_order_relaxed) == 1;
+  // Longest rows first when rows outnumber the CTAs (unsharded, unsplit,
+  // through the unit counter).
+  const int ord = g_over[DSA_LAUNCH_PIPE_ORDER].load(std::memory_order_relaxed);
+  a.lpt = MODE == kPipeUnsharded && split == 1 && a.queue != nullptr && a.rows <= kLptMaxRows &&
+          ord != 1 && (ord == 2 || a.rows > slots);
   const size_t tail = 2 * static_cast<size_t>((a.nb + 3) & ~3) * 4 +
-                      static_cast<size_t>(std::max(a.kpad, kRankMax)) * 8;
+                      static_cast<size_t>(std::max(a.kpad, kRankMax)) * 8 +
+                      (a.lpt ? ((static_cast<size_t>(a.rows) * 2 + 15) & ~static_cast<size_t>(15)) : 0);
   const size_t limit =
       smem_budget(ctas, sizeof(TopkShared) + sizeof(PieceTable) + 2 * sizeof(UnitMeta) + 128);
   int stages = 16;
@@ -1096,6 +1240,9 @@ dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int c
   if (fst >= 2 && fst < stages) stages = fst;
   if (stages < 2) return kPipeDeclined;
   a.stages = stages;
+  // The order pass's scratch lives in the ring.
+  if (static_cast<size_t>(stages) * a.stage_bytes < lpt_scratch_bytes(NW + kRankWarps + 1, a.rows))
+    a.lpt = 0;
   const size_t smem = coop_keys_offset(stages, a.stage_bytes) + tail;
   auto kernel = pipe_coop_kernel<E, MODE, NW>;
   if (opt_in_smem(kernel, smem) != cudaSuccess) return DSA_ECUDA;

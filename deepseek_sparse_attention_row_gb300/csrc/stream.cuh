@@ -67,9 +67,12 @@ __device__ __forceinline__ void stream_pow2(const Window<E>& w, int lpb_log2, in
 
   for (int d0 = 0; d0 < w.shards; d0 += SB) {
     int32_t lim[SB];
+    int32_t lim_min = v_end;  // slabs below it lie inside every shard's window
 #pragma unroll
-    for (int j = 0; j < SB; ++j)
+    for (int j = 0; j < SB; ++j) {
       lim[j] = (d0 + j < w.shards) ? min(w.len[d0 + j] / VEC, v_end) : 0;
+      lim_min = min(lim_min, lim[j]);
+    }
     const typename E::T* base = w.origin + static_cast<int64_t>(d0) * w.shard_stride;
 
     const int32_t step = nwarps * kSlab;
@@ -78,16 +81,27 @@ __device__ __forceinline__ void stream_pow2(const Window<E>& w, int lpb_log2, in
 #pragma unroll
       for (int m = 0; m < NV; ++m) acc[m] = neg_inf();
       Raw<E, VEC> x[SB][NV];
+      if (slab + kSlab <= lim_min) {
+        // A full slab: every load is inside its shard's window.
 #pragma unroll
-      for (int j = 0; j < SB; ++j) {
-        const typename E::T* src = base + static_cast<int64_t>(j) * w.shard_stride;
+        for (int j = 0; j < SB; ++j) {
+          const typename E::T* src = base + static_cast<int64_t>(j) * w.shard_stride;
 #pragma unroll
-        for (int m = 0; m < NV; ++m) {
-          const int32_t v = slab + m * 32 + lane;
-          if (v < lim[j])
-            ld_raw<E, VEC>(src + static_cast<int64_t>(v) * VEC, x[j][m]);
-          else
-            raw_neg_inf(x[j][m]);
+          for (int m = 0; m < NV; ++m)
+            ld_raw<E, VEC>(src + static_cast<int64_t>(slab + m * 32 + lane) * VEC, x[j][m]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < SB; ++j) {
+          const typename E::T* src = base + static_cast<int64_t>(j) * w.shard_stride;
+#pragma unroll
+          for (int m = 0; m < NV; ++m) {
+            const int32_t v = slab + m * 32 + lane;
+            if (v < lim[j])
+              ld_raw<E, VEC>(src + static_cast<int64_t>(v) * VEC, x[j][m]);
+            else
+              raw_neg_inf(x[j][m]);
+          }
         }
       }
       if constexpr (E::kBytes == 2 && VEC >= 2) {
@@ -291,9 +305,9 @@ __device__ __forceinline__ void stream_shift(const ShiftGroups<E>& w, int lpb_lo
 #pragma unroll
     for (int j = 0; j < SB; ++j) {
       const int d = d0 + j;
-      const int g = d < w.split ? 1 : 0;
-      lim[j] = d < w.shards ? min((w.len[d] + w.r[g]) / VEC, v_end) : 0;
-      src[j] = w.base[g] + static_cast<int64_t>(d) * w.shard_stride;
+      const bool g1 = d < w.split;  // constant indices keep w in registers
+      lim[j] = d < w.shards ? min((w.len[d] + (g1 ? w.r[1] : w.r[0])) / VEC, v_end) : 0;
+      src[j] = (g1 ? w.base[1] : w.base[0]) + static_cast<int64_t>(d) * w.shard_stride;
     }
 
     for (int32_t slab = v_begin + warp * kSlab; slab < v_end; slab += step) {
@@ -386,6 +400,168 @@ __device__ __forceinline__ void stream_shift(const ShiftGroups<E>& w, int lpb_lo
             else
               keys[blk - kbase] = k;
           }
+        }
+      }
+    }
+  }
+}
+
+// The DCP form with starts, both shard groups read from ONE aligned base.
+// With gs = q * shards + rg, shards d < rg (group 1) start at local column
+// q + 1 and the others (group 0) at q; every shard row is read from column
+// q - r0, r0 = q's offset past a 16-byte boundary (0 <= r0 < VEC). Window
+// element t of a group-g shard then sits at stream position t + r0 + g, in
+// block (t) / block_size. For stream position p = VEC*v + i the two groups
+// put element i in the same block unless p - r0 is a multiple of the block
+// size, i.e. unless v is a block's first vector (v % LPB == 0) and i = r0:
+// there group 0 starts block v / LPB while group 1 ends block v / LPB - 1.
+// So a lane folds its 16-byte vectors of all shards element-wise (no group
+// routing), splits the result at r0 into a "lo" part (the block before) and
+// a "hi" part, and routes only element r0 by group: the group-0 maximum of
+// that element joins hi, the group-1 maximum joins lo. Vectors past a
+// shard's window load as -inf (only in the slab that crosses the shortest
+// shard's end; full slabs load unconditionally). lo and hi then meet as in
+// stream_shift: lo joins the hi of the vector below (one shuffle), a slab's
+// first lo goes to the previous slab's block with atomicMax, and a slab's
+// last block is written with atomicMax. Elements past each shard's last
+// whole vector are left to commit_partial_shifted.
+template <typename E>
+struct PairedShift {
+  const typename E::T* base;  // shard 0's row at column q - r0 (16-byte aligned)
+  int32_t r0;                 // 0 .. VEC-1
+  int32_t split;              // shards [0, split) belong to group 1
+  int64_t shard_stride;
+  int32_t shards;
+  const int32_t* len;         // shared memory: in-window length of each shard
+  int32_t v_cap;              // max over shards of (len + r0 + group) / VEC
+  bool merge;
+};
+
+template <typename E, int SB>
+__device__ __forceinline__ void stream_shift_paired(const PairedShift<E>& w, int lpb_log2,
+                                                    int32_t b0, int32_t b1,
+                                                    uint32_t* __restrict__ keys, int32_t kbase,
+                                                    int warp, int nwarps) {
+  constexpr int VEC = 16 / E::kBytes;
+  const int lane = threadIdx.x & 31;
+  const int lpb = 1 << lpb_log2;
+  const int32_t v_begin = static_cast<int32_t>(static_cast<int64_t>(b0) << lpb_log2);
+  const int32_t v_end = static_cast<int32_t>(min((static_cast<int64_t>(b1) << lpb_log2) + 1,
+                                                 static_cast<int64_t>(w.v_cap)));
+  const bool merge = w.shards > SB || w.merge;
+  const int r0 = w.r0;
+  constexpr int32_t kSlab = 32;
+  const int32_t step = nwarps * kSlab;
+
+  for (int d0 = 0; d0 < w.shards; d0 += SB) {
+    int32_t lim[SB];
+    bool g1[SB];
+    // Shard j of the batch is read at row0 + j * shard_stride (no pointer per
+    // shard held across the loop).
+    const typename E::T* row0 = w.base + static_cast<int64_t>(d0) * w.shard_stride;
+    int32_t lim_min = v_end;
+#pragma unroll
+    for (int j = 0; j < SB; ++j) {
+      const int d = d0 + j;
+      g1[j] = d < w.split;
+      const int32_t n = d < w.shards ? w.len[d] : 0;
+      lim[j] = n > 0 ? min((n + r0 + (g1[j] ? 1 : 0)) / VEC, v_end) : 0;
+      if (d < w.shards) lim_min = min(lim_min, lim[j]);
+    }
+    // In the last batch, shards past the end load nothing.
+    if (d0 + SB > w.shards) lim_min = 0;
+
+    for (int32_t slab = v_begin + warp * kSlab; slab < v_end; slab += step) {
+      const int32_t v = slab + lane;
+      const typename E::T* at = row0 + static_cast<int64_t>(v) * VEC;
+      Raw<E, VEC> x[SB];
+      if (slab + kSlab <= lim_min) {
+#pragma unroll
+        for (int j = 0; j < SB; ++j) ld_raw<E, VEC>(at + j * w.shard_stride, x[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < SB; ++j) {
+          if (v < lim[j])
+            ld_raw<E, VEC>(at + j * w.shard_stride, x[j]);
+          else
+            raw_neg_inf(x[j]);
+        }
+      }
+      // Element-wise max over every shard (three-operand max for fp32, the
+      // packed bf16 pair max for bf16), and element r0 by group.
+      float ae[VEC];
+      if constexpr (E::kBytes == 4) {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+          float m = __uint_as_float(x[0].w[i]);
+#pragma unroll
+          for (int j = 1; j < SB; j += 2)
+            m = j + 1 < SB ? max_nan(m, __uint_as_float(x[j].w[i]), __uint_as_float(x[j + 1].w[i]))
+                           : max_nan(m, __uint_as_float(x[j].w[i]));
+          ae[i] = m;
+        }
+      } else {
+        Raw<E, VEC> a = x[0];
+#pragma unroll
+        for (int j = 1; j < SB; ++j) raw_max(a, x[j]);
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) ae[i] = raw_elem(a, i);
+      }
+      float xr[SB];
+#pragma unroll
+      for (int j = 0; j < SB; ++j) xr[j] = raw_elem_at(x[j], r0);
+      float gr0 = neg_inf(), gr1 = neg_inf();
+#pragma unroll
+      for (int j = 0; j < SB; j += 2) {
+        if (j + 1 < SB) {
+          gr1 = max_nan(gr1, g1[j] ? xr[j] : neg_inf(), g1[j + 1] ? xr[j + 1] : neg_inf());
+          gr0 = max_nan(gr0, g1[j] ? neg_inf() : xr[j], g1[j + 1] ? neg_inf() : xr[j + 1]);
+        } else {
+          gr1 = max_nan(gr1, g1[j] ? xr[j] : neg_inf());
+          gr0 = max_nan(gr0, g1[j] ? neg_inf() : xr[j]);
+        }
+      }
+      float lo = neg_inf(), hi = neg_inf(), all = neg_inf();
+#pragma unroll
+      for (int i = 0; i < VEC; i += 2) {
+        all = max_nan(all, ae[i], ae[i + 1]);
+        lo = max_nan(lo, i < r0 ? ae[i] : neg_inf(), i + 1 < r0 ? ae[i + 1] : neg_inf());
+        hi = max_nan(hi, i > r0 ? ae[i] : neg_inf(), i + 1 > r0 ? ae[i + 1] : neg_inf());
+      }
+      const bool lead = (v & (lpb - 1)) == 0;
+      hi = lead ? max_nan(hi, gr0) : all;
+      lo = lead ? max_nan(lo, gr1) : neg_inf();
+      // The slab's first vector sends its lo part to the block before (in
+      // another warp's slab) with an atomic; every other lo part joins the
+      // hi part of the vector below it.
+      if (lane == 0) {
+        const int32_t blk = (slab >> lpb_log2) - 1;
+        if ((slab & (lpb - 1)) == 0 && blk >= b0 && blk < b1)
+          atomicMax(&keys[blk - kbase], order_key(lo));
+      }
+      float nxt = __shfl_down_sync(0xffffffffu, lo, 1);
+      if (lane == 31) nxt = neg_inf();
+      hi = max_nan(hi, nxt);
+      if (lpb_log2 >= 5) {
+        // A block spans whole slabs: one warp reduction and one atomicMax per
+        // block and slab.
+        const int32_t blk = slab >> lpb_log2;
+        if (blk < b1) {
+          const uint32_t k = __reduce_max_sync(0xffffffffu, order_key(hi));
+          if (lane == 0) atomicMax(&keys[blk - kbase], k);
+        }
+      } else {
+        // Several blocks per slab: one reduction per block; only the slab's
+        // last block can also receive a lo part from another slab.
+        const int32_t last_blk = (slab + kSlab - 1) >> lpb_log2;
+        uint32_t k = order_key(hi);
+        for (int o = 1; o < lpb; o <<= 1) k = max(k, __shfl_xor_sync(0xffffffffu, k, o));
+        const int32_t blk = v >> lpb_log2;
+        if ((lane & (lpb - 1)) == 0 && v < v_end && blk < b1) {
+          if (merge || blk == last_blk)
+            atomicMax(&keys[blk - kbase], k);
+          else
+            keys[blk - kbase] = k;
         }
       }
     }

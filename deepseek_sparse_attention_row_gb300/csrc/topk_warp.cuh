@@ -128,4 +128,156 @@ __device__ void topk_warp(uint32_t* __restrict__ keys, int32_t nb, int32_t n_liv
   for (int j = K + lane; j < topk; j += 32) out[j] = -1;
 }
 
+// R-th largest of the 32 lanes' values v, counted with multiplicity, or 0
+// when fewer than R lanes hold a value above key(-inf). At most R rounds of a
+// warp max, each dropping the lanes that hold it. Warp-uniform result.
+__device__ __forceinline__ uint32_t warp_kth_largest(uint32_t v, int R) {
+  for (int need = R; need > 0;) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, v);
+    if (m <= kKeyNegInf) return 0u;
+    const int c = __popc(__ballot_sync(0xffffffffu, v == m));
+    if (c >= need) return m;
+    need -= c;
+    if (v == m) v = 0u;
+  }
+  return 0u;
+}
+
+// Ranked top-k of one row by one warp for rows of up to 1024 block keys
+// (32 per lane) and k <= 32; same result as topk_store. Lane l reads keys
+// 4l + 128i .. 4l + 128i + 3 with one 16-byte shared load per i (conflict
+// free) and keeps its two largest keys t1 >= t2. Bound: ceil(k/2) lanes with
+// t2 >= L hold at least k keys >= L, so every top-k key is >= L (L from t1
+// and k lanes when too few lanes have two live keys; all live keys when even
+// that fails). Keys >= L (typically k plus a few dozen) are compacted from
+// per-lane bit masks and a warp scan, and ranked by counting the composites
+// above each. More candidates than `cand_cap` (long runs of equal keys): k
+// rounds of a warp max.
+//
+// keys: [n_live] final keys in shared memory (no other warp writes them any
+// more), 16-byte aligned, padded to a multiple of 4 words (n_live <= padded
+// size); block pin_block (if >= 0, below n_live) becomes key(+inf) here.
+// cand: [cand_cap >= 64] in shared memory. All 32 lanes call this.
+template <typename S>
+__device__ void topk_warp_wide(uint32_t* __restrict__ keys, int32_t nb, int32_t n_live, int32_t k,
+                               int32_t pin_block, uint64_t* __restrict__ cand, int32_t cand_cap,
+                               int32_t* __restrict__ out, int32_t topk, S* __restrict__ scores) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0 && pin_block >= 0) keys[pin_block] = kKeyPosInf;
+  __syncwarp();
+  if (scores)
+    for (int b = lane; b < nb; b += 32) put_score(scores + b, b < n_live ? keys[b] : kKeyNegInf);
+  if (k <= 0) return;
+
+  // 1. Each lane's two largest keys (0 stands for none: every key is >=
+  // key(-inf) > 0).
+  uint32_t t1 = 0u, t2 = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int base = 4 * lane + 128 * i;
+    if (base < n_live) {
+      uint4 v = *reinterpret_cast<const uint4*>(keys + base);
+      if (base + 4 > n_live) {
+        if (base + 1 >= n_live) v.y = 0u;
+        if (base + 2 >= n_live) v.z = 0u;
+        v.w = 0u;
+      }
+      t2 = max(t2, min(t1, v.x)); t1 = max(t1, v.x);
+      t2 = max(t2, min(t1, v.y)); t1 = max(t1, v.y);
+      t2 = max(t2, min(t1, v.z)); t1 = max(t1, v.z);
+      t2 = max(t2, min(t1, v.w)); t1 = max(t1, v.w);
+    }
+  }
+
+  // 2. The bound.
+  int32_t K = k;
+  uint32_t thr = warp_kth_largest(t2, (k + 1) >> 1);
+  if (thr == 0u) thr = warp_kth_largest(t1, k);
+  if (thr == 0u) {
+    // Fewer than k lanes hold a live key: take every live key.
+    uint32_t cnt = 0;
+    for (int i = 0; i < 8; ++i)
+      for (int j = 0; j < 4; ++j) {
+        const int b = 4 * lane + 128 * i + j;
+        cnt += (b < n_live && keys[b] > kKeyNegInf) ? 1u : 0u;
+      }
+    const uint32_t total = __reduce_add_sync(0xffffffffu, cnt);
+    K = static_cast<int32_t>(min(static_cast<uint32_t>(k), total));
+    thr = kKeyNegInf + 1u;
+  }
+  if (K == 0) {
+    for (int j = lane; j < topk; j += 32) out[j] = -1;
+    return;
+  }
+
+  // 3. Candidates: a bit per key at or above the bound, then a warp scan of
+  // the counts gives each lane its slots.
+  uint32_t bits = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int base = 4 * lane + 128 * i;
+    if (base < n_live) {
+      const uint4 v = *reinterpret_cast<const uint4*>(keys + base);
+      uint32_t m = (v.x >= thr ? 1u : 0u) | (v.y >= thr ? 2u : 0u) | (v.z >= thr ? 4u : 0u) |
+                   (v.w >= thr ? 8u : 0u);
+      if (base + 4 > n_live) m &= (1u << (n_live - base)) - 1u;
+      bits |= m << (4 * i);
+    }
+  }
+  const uint32_t mine = __popc(bits);
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int32_t n = static_cast<int32_t>(__shfl_sync(0xffffffffu, incl, 31));
+  if (n <= cand_cap) {
+    int32_t pos = static_cast<int32_t>(incl - mine);
+    while (bits) {
+      const int q = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      const int b = 4 * lane + 128 * (q >> 2) + (q & 3);
+      cand[pos++] = pack_candidate(keys[b], b);
+    }
+    __syncwarp();
+    // 4. Rank by counting; two candidates per lane per pass.
+    for (int i0 = 0; i0 < n; i0 += 64) {
+      const int ia = i0 + lane, ib = i0 + 32 + lane;
+      const uint64_t ca = ia < n ? cand[ia] : 0ull;
+      const uint64_t cb = ib < n ? cand[ib] : 0ull;
+      int32_t ra = 0, rb = 0;
+      for (int j = 0; j < n; ++j) {
+        const uint64_t cj = cand[j];
+        ra += cj > ca;
+        rb += cj > cb;
+      }
+      if (ia < n && ra < K) out[ra] = candidate_id(ca);
+      if (ib < n && rb < K) out[rb] = candidate_id(cb);
+    }
+    for (int j = K + lane; j < topk; j += 32) out[j] = -1;
+    return;
+  }
+
+  // Fallback: K rounds, each taking the largest composite below the last.
+  uint64_t last = ~0ull;
+  for (int32_t j = 0; j < K; ++j) {
+    uint64_t best = 0ull;
+    for (int b = lane; b < n_live; b += 32) {
+      const uint32_t key = keys[b];
+      if (key > kKeyNegInf) {
+        const uint64_t c = pack_candidate(key, b);
+        if (c < last && c > best) best = c;
+      }
+    }
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(best >> 32));
+    const uint32_t lo = __reduce_max_sync(
+        0xffffffffu, static_cast<uint32_t>(best >> 32) == hi ? static_cast<uint32_t>(best) : 0u);
+    best = (static_cast<uint64_t>(hi) << 32) | lo;
+    if (lane == 0) out[j] = candidate_id(best);
+    last = best;
+  }
+  for (int j = K + lane; j < topk; j += 32) out[j] = -1;
+}
+
 }  // namespace dsa

@@ -122,6 +122,14 @@ size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks);
  *   DSA_LAUNCH_PIPE_STAGE_OWNER  pipelined kernels, every warp on one row:
  *                          1 = each folding warp takes whole stages in turn
  *                          (default: every stage's blocks shared by all)
+ *   DSA_LAUNCH_PIPE_ORDER  pipelined kernels, every warp on one row: 1 = rows
+ *                          handed out in index order, 2 = longest rows first
+ *                          whenever the call allows it (default: longest
+ *                          first when the rows outnumber the CTAs)
+ *   DSA_LAUNCH_RANK_CTA    row-per-CTA kernel: 1 = every warp of the CTA
+ *                          ranks each row, 2 = one warp ranks every row of
+ *                          up to 1024 live blocks with k <= 32 (default: one
+ *                          warp, except the fp32 DCP form without starts)
  *
  * DSA_EINVAL for an unknown knob or a value outside its range (nothing
  * changes then).
@@ -138,7 +146,9 @@ enum {
     DSA_LAUNCH_PIPE_SCHED = 9,
     DSA_LAUNCH_PIPE_WARPS = 10,
     DSA_LAUNCH_PIPE_CTAS = 11,
-    DSA_LAUNCH_PIPE_STAGE_OWNER = 12
+    DSA_LAUNCH_PIPE_STAGE_OWNER = 12,
+    DSA_LAUNCH_PIPE_ORDER = 13,
+    DSA_LAUNCH_RANK_CTA = 14
 };
 dsa_status dsa_select_set_launch_override(int32_t knob, int32_t value);
 

@@ -92,13 +92,14 @@ def test_launch_override_validation(lib):
     for knob, good, bad in ((5, (0, 1, 2, 3), (4, -1)), (6, (0, 1, 8), (9, -1)),
                             (7, (0, 2, 16), (1, 17)), (8, (0, 4, 64), (3, 65)),
                             (9, (0, 1), (2, -1)), (10, (0, 4, 8), (2, 16)),
-                            (11, (0, 1, 4), (5, -1)), (12, (0, 1), (2, -1))):
+                            (11, (0, 1, 4), (5, -1)), (12, (0, 1), (2, -1)),
+                            (13, (0, 1, 2), (3, -1)), (14, (0, 1, 2), (3, -1))):
         for v in good:
             assert set_(knob, v) == DSA_OK
         for v in bad:
             assert set_(knob, v) == DSA_EINVAL
         assert set_(knob, 0) == DSA_OK
-    for knob in (0, 13, 99, -3):
+    for knob in (0, 15, 99, -3):
         assert set_(knob, 0) == DSA_EINVAL
 
 

@@ -4,11 +4,13 @@ applied by conftest.py from DSA_TEST_LAUNCH in a child run), must give the
 oracle's results bit for bit like the default ones:
 
 - the row-per-CTA kernel with every row split into 3 or 8 chunk-major parts
-  (long rows normally split only when there are few rows), the row-per-warp
-  kernel in row order, and short rows one per CTA instead of one per warp;
+  (long rows normally split only when there are few rows), every row ranked
+  by the whole CTA or by one warp, the row-per-warp kernel in row order,
+  and short rows one per CTA instead of one per warp;
 - the pipelined kernels with every warp of a CTA on one row or one row per
   warp, rows cut into 3 or 8 parts that meet in the workspace, the smallest
-  rings (2 stages of 4 KiB), and rows dealt to CTAs in a fixed order.
+  rings (2 stages of 4 KiB), rows dealt to CTAs in a fixed order, and rows
+  handed out longest first on every call.
 
 The overrides are process-wide, so each setting re-runs the relevant parity
 sweeps in a child process.
@@ -36,6 +38,8 @@ CASES = {
     "legacy_split8": ("pipeline=1,split=8", SWEEPS + " or workspace_reuse", 150),
     "legacy_warp_rows_in_order": ("pipeline=1,warp_order=1", "warp", 8),
     "legacy_no_warp_kernel": ("pipeline=1,warp_rows=1", "warp", 8),
+    "legacy_rank_cta": ("pipeline=1,rank_cta=1", SWEEPS + " or workspace_reuse", 150),
+    "legacy_rank_warp": ("pipeline=1,rank_cta=2", SWEEPS + " or workspace_reuse", 150),
     # The pipelined kernels in shapes the automatic choice reaches only for
     # some sizes.
     "pipe_coop": ("pipeline=2", SWEEPS + " or warp or graph", 190),
@@ -46,6 +50,7 @@ CASES = {
     "pipe_fixed_order": ("pipeline=2,pipe_sched=1,pipe_split=2", SWEEPS, 150),
     "pipe_8_warps": ("pipeline=2,pipe_warps=8,pipe_ctas=1", SWEEPS + " or graph", 150),
     "pipe_stage_owner": ("pipeline=2,pipe_stage_owner=1", SWEEPS, 150),
+    "pipe_longest_first": ("pipeline=2,pipe_order=2", SWEEPS + " or graph", 150),
     "pipe_solo_small_stages": ("pipeline=3,pipe_stage_kb=4,pipe_ctas=1", "unsharded_sweep or warp",
                                80),
 }
