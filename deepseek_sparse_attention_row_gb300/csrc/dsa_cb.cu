@@ -49,6 +49,27 @@ constexpr int kUnsharded = 0;       // [rows, ld], window [ks, ke)
 constexpr int kSharded = 1;         // [shards, rows, ld], windows from 0 (the pages' DCP form)
 constexpr int kShardedStarts = 2;   // [shards, rows, ld], windows from each shard's start
 
+// A divisor fixed for a whole call: division is a shift when it is a power
+// of two (the usual block sizes, shard counts and row repeats), else the
+// plain division. Only for non-negative dividends.
+struct Divisor {
+  uint32_t d;
+  int32_t log2;  // -1: not a power of two
+  __device__ __forceinline__ uint32_t div(uint32_t x) const {
+    return log2 >= 0 ? x >> log2 : x / d;
+  }
+};
+
+inline Divisor make_divisor(int64_t d) {
+  Divisor v{static_cast<uint32_t>(d), -1};
+  if (d > 0 && (d & (d - 1)) == 0) {
+    int l = 0;
+    while ((int64_t{1} << l) < d) ++l;
+    v.log2 = l;
+  }
+  return v;
+}
+
 struct SelectArgs {
   const void* logits;    // E::T elements
   int64_t ld;            // row stride (elements)
@@ -76,6 +97,10 @@ struct SelectArgs {
   int64_t rows;         // rows of the call
   int32_t reverse;      // select_warp_kernel: take rows last to first
   int32_t rank_cta;     // select_kernel: the whole CTA ranks every row
+  Divisor by_repeat;    // row_repeat
+  Divisor by_block;     // block_size
+  Divisor by_gblock;    // global_block_size
+  Divisor by_shards;    // shards
 };
 
 template <typename E>
@@ -113,13 +138,13 @@ __device__ __forceinline__ bool arrive_units(uint32_t* counter, uint32_t units, 
 // (s >= shift).
 template <typename E>
 __device__ __forceinline__ RowPlan<E> plan_window(const typename E::T* base, int32_t s,
-                                                  int32_t n, int32_t block_size) {
+                                                  int32_t n, int32_t block_size, Divisor by_block) {
   constexpr int V16 = 16 / E::kBytes;  // elements per 16-byte vector
   RowPlan<E> p;
   p.origin = base + s;
   p.len_max = n;
-  p.nblk = static_cast<int32_t>((static_cast<uint32_t>(n) + static_cast<uint32_t>(block_size) -
-                                 1u) / static_cast<uint32_t>(block_size));
+  p.nblk = static_cast<int32_t>(
+      by_block.div(static_cast<uint32_t>(n) + static_cast<uint32_t>(block_size) - 1u));
   p.pin_block = -1;
   p.shift = static_cast<int>((reinterpret_cast<uintptr_t>(p.origin) / E::kBytes) & (V16 - 1));
   const int32_t lpbv = block_size / V16;
@@ -137,28 +162,18 @@ __device__ __forceinline__ RowPlan<E> plan_window(const typename E::T* base, int
 template <typename E>
 __device__ __forceinline__ RowPlan<E> plan_unsharded(const typename E::T* logits, int64_t ld,
                                                      int32_t width, const int32_t* row_ks,
-                                                     const int32_t* row_ke, int32_t row_repeat,
-                                                     int32_t block_size, int32_t pin_newest,
-                                                     int64_t row) {
-  const int64_t g = row / row_repeat;
+                                                     const int32_t* row_ke, Divisor by_repeat,
+                                                     int32_t block_size, Divisor by_block,
+                                                     int32_t pin_newest, int64_t row) {
+  const uint32_t g = by_repeat.div(static_cast<uint32_t>(row));
   const int32_t ks = row_ks ? __ldg(row_ks + g) : 0;
   const int32_t ke = __ldg(row_ke + g);
   const int32_t e = min(ke, width);
   const int32_t s = min(max(ks, 0), e);
   const int32_t n = e > s ? e - s : 0;
-  RowPlan<E> p = plan_window<E>(logits + row * ld, s, n, block_size);
-  p.pin_block = (pin_newest && n > 0) ? (n - 1) / block_size : -1;
+  RowPlan<E> p = plan_window<E>(logits + row * ld, s, n, block_size, by_block);
+  p.pin_block = (pin_newest && n > 0) ? static_cast<int32_t>(by_block.div(n - 1)) : -1;
   return p;
-}
-
-// Local end of shard d for global end gke: shard d holds the global tokens
-// t = shards*c + d, so those below gke are its first ceil((gke - d) / shards)
-// local columns; clamped to the local width.
-__device__ __forceinline__ int32_t shard_len(int32_t gke, int32_t d, int32_t shards, int32_t lw) {
-  if (gke <= d) return 0;
-  const uint32_t lke = (static_cast<uint32_t>(gke - d) + static_cast<uint32_t>(shards - 1)) /
-                       static_cast<uint32_t>(shards);
-  return static_cast<int32_t>(min(lke, static_cast<uint32_t>(lw)));
 }
 
 // A group of shards that share their window start (and so its alignment),
@@ -228,13 +243,12 @@ __device__ __forceinline__ RowPlan<E> plan_row(const SelectArgs& a, int64_t row,
     // With x = q * shards + r (0 <= r < shards), shard d holds
     // ceil((x - d) / shards) = q + (d < r) of the global tokens below x, so
     // two divisions give every shard's start and end.
-    const int64_t g = row / a.row_repeat;
+    const uint32_t g = a.by_repeat.div(static_cast<uint32_t>(row));
     const int32_t gke = max(__ldg(a.row_ke + g), 0);
     const int32_t gs = min(max(__ldg(a.row_ks + g), 0), gke);
-    const uint32_t D = static_cast<uint32_t>(a.shards);
-    const int32_t qe = static_cast<int32_t>(static_cast<uint32_t>(gke) / D);
+    const int32_t qe = static_cast<int32_t>(a.by_shards.div(static_cast<uint32_t>(gke)));
     const int32_t re = gke - qe * a.shards;
-    shard_q = static_cast<int32_t>(static_cast<uint32_t>(gs) / D);
+    shard_q = static_cast<int32_t>(a.by_shards.div(static_cast<uint32_t>(gs)));
     shard_rem = gs - shard_q * a.shards;
     auto window = [&](int d, int32_t& st) {
       const int32_t e = min(qe + (d < re ? 1 : 0), a.width);
@@ -254,34 +268,37 @@ __device__ __forceinline__ RowPlan<E> plan_row(const SelectArgs& a, int64_t row,
     }
     plan.origin = logits + row * a.ld;
     plan.len_max = len_max;
-    plan.nblk = min(static_cast<int32_t>((static_cast<uint32_t>(len_max) + a.block_size - 1u) /
-                                         static_cast<uint32_t>(a.block_size)),
+    plan.nblk = min(static_cast<int32_t>(
+                        a.by_block.div(static_cast<uint32_t>(len_max) + a.block_size - 1u)),
                     a.nb_data);
     plan.pin_block = gke > gs ? static_cast<int32_t>(min(
-                                    static_cast<uint32_t>(gke - gs - 1) / a.global_block_size,
+                                    a.by_gblock.div(static_cast<uint32_t>(gke - gs - 1)),
                                     static_cast<uint32_t>(a.nb - 1)))
                               : -1;
     plan.vec = 0;
     plan.lpb_log2 = 0;
   } else if constexpr (MODE == kSharded) {
-    const int32_t gke = __ldg(a.row_ke + row / a.row_repeat);
-    const int32_t n0 = shard_len(gke, 0, a.shards, a.width);
+    // Shard d holds q + (d < r) of the global tokens below gke = q * shards + r.
+    const int32_t gke = max(__ldg(a.row_ke + a.by_repeat.div(static_cast<uint32_t>(row))), 0);
+    const int32_t qe = static_cast<int32_t>(a.by_shards.div(static_cast<uint32_t>(gke)));
+    const int32_t re = gke - qe * a.shards;
+    const int32_t n0 = min(qe + (re > 0 ? 1 : 0), a.width);
     plan.origin = logits + row * a.ld;
     plan.len_max = n0;
-    plan.nblk = min(static_cast<int32_t>((static_cast<uint32_t>(n0) + a.block_size - 1u) /
-                                         static_cast<uint32_t>(a.block_size)),
+    plan.nblk = min(static_cast<int32_t>(
+                        a.by_block.div(static_cast<uint32_t>(n0) + a.block_size - 1u)),
                     a.nb_data);
     plan.pin_block = gke >= 1 ? static_cast<int32_t>(min(
-                                    static_cast<uint32_t>(gke - 1) / a.global_block_size,
+                                    a.by_gblock.div(static_cast<uint32_t>(gke - 1)),
                                     static_cast<uint32_t>(a.nb - 1)))
                               : -1;
     plan.vec = SVEC;
     plan.lpb_log2 = SVEC ? __ffs(a.block_size / (SVEC ? SVEC : 1)) - 1 : 0;
     for (int d = threadIdx.x; d < a.shards; d += blockDim.x)
-      len[d] = shard_len(gke, d, a.shards, a.width);
+      len[d] = min(qe + (d < re ? 1 : 0), a.width);
   } else {
-    plan = plan_unsharded<E>(logits, a.ld, a.width, a.row_ks, a.row_ke, a.row_repeat,
-                             a.block_size, a.pin_newest, row);
+    plan = plan_unsharded<E>(logits, a.ld, a.width, a.row_ks, a.row_ke, a.by_repeat,
+                             a.block_size, a.by_block, a.pin_newest, row);
     if (threadIdx.x == 0) len[0] = plan.len_max;
   }
 
@@ -349,7 +366,7 @@ __device__ __forceinline__ void stream_range(const SelectArgs& a, const RowPlan<
           const int32_t st = grp == 0 ? shard_q : shard_q + 1;
           const int32_t st_c = min(st, a.width);
           const RowPlan<E> pg = plan_window<E>(plan.origin + d_lo * a.shard_stride, st_c, lmax,
-                                               a.block_size);
+                                               a.block_size, a.by_block);
           Window<E> wg;
           wg.origin = pg.origin;
           wg.shard_stride = a.shard_stride;
@@ -361,7 +378,7 @@ __device__ __forceinline__ void stream_range(const SelectArgs& a, const RowPlan<
         } else {
           for (int d = d_lo; d < d_hi; ++d) {
             const RowPlan<E> pd = plan_window<E>(plan.origin + d * a.shard_stride, start[d],
-                                                 len[d], a.block_size);
+                                                 len[d], a.block_size, a.by_block);
             Window<E> wd;
             wd.origin = pd.origin;
             wd.shard_stride = 0;
@@ -386,7 +403,7 @@ __device__ __forceinline__ void stream_range(const SelectArgs& a, const RowPlan<
   if constexpr (MODE == kShardedStarts) {
     for (int d = threadIdx.x; d < a.shards; d += blockDim.x) {
       const RowPlan<E> pd = plan_window<E>(plan.origin + d * a.shard_stride, start[d], len[d],
-                                           a.block_size);
+                                           a.block_size, a.by_block);
       Window<E> wd;
       wd.origin = pd.origin;
       wd.shard_stride = 0;
@@ -477,8 +494,8 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   __shared__ int s_last;
 
   const uint32_t rows = static_cast<uint32_t>(a.rows);
-  const int64_t row = blockIdx.x % rows;
-  const int32_t part = static_cast<int32_t>(blockIdx.x / rows);
+  const int64_t row = a.split == 1 ? blockIdx.x : blockIdx.x % rows;
+  const int32_t part = a.split == 1 ? 0 : static_cast<int32_t>(blockIdx.x / rows);
 
   int32_t shard_q = 0, shard_rem = 0;  // kShardedStarts: gs = shard_q * shards + shard_rem
   const RowPlan<E> plan = plan_row<E, MODE, SVEC>(a, row, len, start, shard_q, shard_rem);
@@ -525,7 +542,7 @@ __global__ void __launch_bounds__(W * 32, 1024 / (W * 32)) select_warp_kernel(co
 
   const RowPlan<E> plan =
       plan_unsharded<E>(static_cast<const TE*>(a.logits), a.ld, a.width, a.row_ks, a.row_ke,
-                        a.row_repeat, a.block_size, a.pin_newest, row);
+                        a.by_repeat, a.block_size, a.by_block, a.pin_newest, row);
   if (lane == 0) len[0] = plan.len_max;
   const int32_t nblk = plan.nblk;
   for (int32_t b = lane; b < nblk; b += 32) keys[b] = kKeyNegInf;
@@ -560,6 +577,8 @@ struct ScoresArgs {
   int32_t chunks;  // CTAs per row
   void* scores;        // E::T elements
   int64_t ld_scores;
+  Divisor by_repeat;
+  Divisor by_block;
 };
 
 template <typename E>
@@ -574,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 4) block_scores_kernel(const ScoresA
 
   const RowPlan<E> plan =
       plan_unsharded<E>(static_cast<const TE*>(a.logits), a.ld, a.width, a.row_ks, a.row_ke,
-                        a.row_repeat, a.block_size, a.pin_newest, row);
+                        a.by_repeat, a.block_size, a.by_block, a.pin_newest, row);
   if (threadIdx.x == 0) len[0] = plan.len_max;
   for (int32_t b = threadIdx.x; b < c1 - c0; b += blockDim.x) keys[b] = kKeyNegInf;
   __syncthreads();
@@ -868,6 +887,8 @@ dsa_status block_scores_impl(const typename E::T* logits, int64_t rows, int64_t 
   a.row_ke = row_ke;
   a.row_repeat = row_repeat;
   a.block_size = block_size;
+  a.by_repeat = make_divisor(row_repeat);
+  a.by_block = make_divisor(block_size);
   a.nb = static_cast<int32_t>(nb);
   a.pin_newest = pin_newest != 0;
   // About 64 KiB of logits per CTA, at least 32 blocks, at most 4096.
@@ -917,6 +938,8 @@ dsa_status select_impl(const typename E::T* logits, int64_t rows, int64_t width,
   a.row_ke = row_ke;
   a.row_repeat = row_repeat;
   a.block_size = block_size;
+  a.by_repeat = make_divisor(row_repeat);
+  a.by_block = make_divisor(block_size);
   a.nb = static_cast<int32_t>(nb);
   a.nb_data = a.nb;
   a.pin_newest = pin_newest != 0;
@@ -1032,6 +1055,10 @@ dsa_status select_sharded_impl(const typename E::T* logits, int32_t shards, int6
   a.row_repeat = row_repeat;
   a.block_size = lbs;
   a.global_block_size = global_block_size;
+  a.by_repeat = make_divisor(row_repeat);
+  a.by_block = make_divisor(lbs);
+  a.by_gblock = make_divisor(global_block_size);
+  a.by_shards = make_divisor(shards);
   a.nb = nbg;
   a.nb_data = static_cast<int32_t>(std::min<int64_t>((local_width + lbs - 1) / lbs, nbg));
   a.pin_newest = 0;

@@ -503,9 +503,102 @@ __host__ __device__ __forceinline__ bool lane_per_block(int32_t bs) {
   return bs >= 2 && bs <= 128 && (bs & (bs - 1)) == 0;
 }
 
+// Lane per block with 16-byte loads when the piece starts `off` bytes past a
+// 16-byte boundary (0 < off < 16; every block then starts `off` bytes into
+// a chunk, as a block is a whole number of chunks). A block covers its CH + 1
+// chunks partly: its first chunk from byte off on, chunks 1 .. CH-1 whole,
+// and its last chunk (the next block's first) below byte off. The two
+// partial chunks are complementary, so one bit-select per word (bytes below
+// off from the last chunk, the rest from the first) gives a full chunk of
+// the block's own elements. The whole chunks are visited in a lane-rotated
+// order, (c + lane % 8) mod (CH - 1), so that the 8 lanes of each 16-byte
+// load phase mostly hit 8 different bank groups.
+template <typename E, int BS, bool MERGE>
+__device__ __forceinline__ void fold_lane_blocks_vmis(const unsigned char* stage,
+                                                      const StageDesc& d, int g0, int gstep,
+                                                      uint32_t* __restrict__ keys) {
+  constexpr int ES = E::kBytes;
+  constexpr int CH = BS * ES / 16;
+  static_assert(CH >= 2 && (BS * ES) % 16 == 0, "at least two whole 16-byte chunks");
+  const int lane = threadIdx.x & 31;
+  const int32_t c0 = d.c0, n = d.n, cnt = d.cnt;
+  const uint32_t off = d.off & 15u;
+  const unsigned char* __restrict__ const base = stage + (d.off & ~15u);
+  // Byte mask of the first chunk's part in word w: bytes at or past `off`.
+  uint32_t m[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t mw = 0u;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) mw |= (4u * w + b >= off) ? (0xFFu << (8 * b)) : 0u;
+    m[w] = mw;
+  }
+  const int rot = lane & 7;
+  const int32_t ngroups = (n + 31) >> 5;
+  for (int32_t g = g0; g < ngroups; g += gstep) {
+    const int32_t blk = g * 32 + lane;
+    if (blk >= n) continue;
+    const int32_t valid = cnt - blk * BS;
+    if (valid <= 0) continue;
+    const unsigned char* pb = base + static_cast<uint32_t>(blk * BS) * ES;
+    float acc;
+    if (valid >= BS) {
+      const uint4 f = *reinterpret_cast<const uint4*>(pb);
+      const uint4 l = *reinterpret_cast<const uint4*>(pb + CH * 16);
+      uint4 e;
+      e.x = (f.x & m[0]) | (l.x & ~m[0]);
+      e.y = (f.y & m[1]) | (l.y & ~m[1]);
+      e.z = (f.z & m[2]) | (l.z & ~m[2]);
+      e.w = (f.w & m[3]) | (l.w & ~m[3]);
+      if constexpr (ES == 4) {
+        float a4[4] = {max_nan(__uint_as_float(e.x), __uint_as_float(e.y)),
+                       max_nan(__uint_as_float(e.z), __uint_as_float(e.w)), neg_inf(), neg_inf()};
+#pragma unroll
+        for (int c = 0; c < CH - 1; ++c) {
+          int t = c + rot;
+          t = t >= CH - 1 ? t - (CH - 1) : t;
+          if (CH - 1 < 8) t = (c + rot) % (CH - 1);
+          const float4 v = *reinterpret_cast<const float4*>(pb + 16 * (1 + t));
+          a4[(c & 1) * 2] = max_nan(a4[(c & 1) * 2], v.x, v.y);
+          a4[(c & 1) * 2 + 1] = max_nan(a4[(c & 1) * 2 + 1], v.z, v.w);
+        }
+        acc = max_nan(max_nan(a4[0], a4[1], a4[2]), a4[3]);
+      } else {
+        uint32_t w2[2] = {max_nan_bf16x2(e.x, e.z), max_nan_bf16x2(e.y, e.w)};
+#pragma unroll
+        for (int c = 0; c < CH - 1; ++c) {
+          int t = c + rot;
+          t = t >= CH - 1 ? t - (CH - 1) : t;
+          if (CH - 1 < 8) t = (c + rot) % (CH - 1);
+          const uint4 v = *reinterpret_cast<const uint4*>(pb + 16 * (1 + t));
+          w2[0] = max_nan_bf16x2(w2[0], v.x);
+          w2[1] = max_nan_bf16x2(w2[1], v.y);
+          w2[0] = max_nan_bf16x2(w2[0], v.z);
+          w2[1] = max_nan_bf16x2(w2[1], v.w);
+        }
+        const uint32_t mm = max_nan_bf16x2(w2[0], w2[1]);
+        acc = max_nan(__uint_as_float(mm << 16), __uint_as_float(mm & 0xFFFF0000u));
+      }
+    } else {
+      // The window's last block: only its first `valid` elements.
+      acc = neg_inf();
+      for (int32_t e = 0; e < valid; ++e) acc = max_nan(acc, stage_elem<E>(pb + off + e * ES));
+    }
+    const uint32_t key = order_key(acc);
+    if (MERGE)
+      atomicMax(&keys[c0 + blk], key);
+    else
+      keys[c0 + blk] = key;
+  }
+}
+
 // The warp's share of one stage: the lane-per-block groups (gbase + g) %
-// gstep == g0, or every gstep-th block / tile of the element path.
-template <typename E, int MODE>
+// gstep == g0, or every gstep-th block / tile of the element path. VMIS:
+// pieces off the 16-byte grid fold with 16-byte loads (fold_lane_blocks_vmis;
+// the cooperative kernel, where folding warps share the stage) rather than
+// element loads (the per-warp kernel, where the two partial chunks' bank
+// conflicts sit on the warp's own path: prefill 35.0 -> 37.5 us with them).
+template <typename E, int MODE, bool VMIS>
 __device__ __forceinline__ void fold_stage(const PipeArgs& a, const unsigned char* stage,
                                            const StageDesc& d, int g0, int gstep, uint32_t gbase,
                                            uint32_t* __restrict__ keys) {
@@ -526,6 +619,22 @@ __device__ __forceinline__ void fold_stage(const PipeArgs& a, const unsigned cha
       case 32: fold_lane_blocks_vec<E, 32, M>(stage, d, first, gstep, keys); return;
       case 64: fold_lane_blocks_vec<E, 64, M>(stage, d, first, gstep, keys); return;
       case 128: fold_lane_blocks_vec<E, 128, M>(stage, d, first, gstep, keys); return;
+      default: break;
+    }
+  }
+  if (VMIS && a.block_size * ES >= 32) {
+    // Off the 16-byte grid: 16-byte loads, the two partial chunks combined.
+    switch (a.block_size) {
+      case 8:
+        if constexpr (ES == 4) {
+          fold_lane_blocks_vmis<E, 8, M>(stage, d, first, gstep, keys);
+          return;
+        }
+        break;
+      case 16: fold_lane_blocks_vmis<E, 16, M>(stage, d, first, gstep, keys); return;
+      case 32: fold_lane_blocks_vmis<E, 32, M>(stage, d, first, gstep, keys); return;
+      case 64: fold_lane_blocks_vmis<E, 64, M>(stage, d, first, gstep, keys); return;
+      case 128: fold_lane_blocks_vmis<E, 128, M>(stage, d, first, gstep, keys); return;
       default: break;
     }
   }
@@ -615,15 +724,14 @@ constexpr int kLptClasses = 128;
 constexpr int kLptMaxRows = 4096;
 
 __host__ __device__ __forceinline__ size_t lpt_scratch_bytes(int warps, int32_t rows) {
-  return static_cast<size_t>(warps + 1) * kLptClasses * 4 + static_cast<size_t>(rows);
+  return static_cast<size_t>(warps) * kLptClasses * 4 + static_cast<size_t>(rows);
 }
 
 template <int NWARPS>
 __device__ void longest_first_order(const PipeArgs& a, uint16_t* __restrict__ order,
                                     unsigned char* __restrict__ scratch) {
   uint32_t* hist = reinterpret_cast<uint32_t*>(scratch);  // [NWARPS][kLptClasses]
-  uint32_t* start = hist + NWARPS * kLptClasses;           // [kLptClasses]
-  unsigned char* cls = reinterpret_cast<unsigned char*>(start + kLptClasses);  // [rows]
+  unsigned char* cls = reinterpret_cast<unsigned char*>(hist + NWARPS * kLptClasses);  // [rows]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < NWARPS * kLptClasses; i += blockDim.x) hist[i] = 0u;
   const int32_t rows = a.rows;
@@ -652,7 +760,8 @@ __device__ void longest_first_order(const PipeArgs& a, uint16_t* __restrict__ or
   }
   __syncthreads();
   // Each class's start in the order (an exclusive scan over classes, longest
-  // first), then each warp's start within the class.
+  // first), then each warp's start within the class; warp 0, lane l owns
+  // classes PER*l .. PER*l + PER - 1.
   if (warp == 0) {
     constexpr int PER = kLptClasses / 32;
     uint32_t t[PER], sum = 0;
@@ -668,21 +777,15 @@ __device__ void longest_first_order(const PipeArgs& a, uint16_t* __restrict__ or
       const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
-    uint32_t run = incl - sum;
+    uint32_t off = incl - sum;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      start[lane * PER + i] = run;
-      run += t[i];
-    }
-  }
-  __syncthreads();
-  for (int b = threadIdx.x; b < kLptClasses; b += blockDim.x) {
-    uint32_t off = start[b];
-    for (int w = 0; w < NWARPS; ++w) {
-      const uint32_t c = hist[w * kLptClasses + b];
-      hist[w * kLptClasses + b] = off;
-      off += c;
-    }
+    for (int i = 0; i < PER; ++i)
+      for (int w = 0; w < NWARPS; ++w) {
+        uint32_t& h = hist[w * kLptClasses + lane * PER + i];
+        const uint32_t c = h;
+        h = off;
+        off += c;
+      }
   }
   __syncthreads();
   for (int32_t c = c0; c < c1; ++c) {
@@ -757,6 +860,11 @@ __global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
     mbar_init_fence();
   }
   __syncthreads();
+  // With rows longest first, the producer claims its first row before the
+  // ordering pass, so that the claim's round trip overlaps the pass.
+  uint32_t first = 0;
+  if (MODE == kPipeUnsharded && a.lpt && warp == NW + NR && lane == 0)
+    first = atomicAdd(a.queue, 1u);
   if constexpr (MODE == kPipeUnsharded)
     if (a.lpt) longest_first_order<NW + NR + 1>(a, order, ring);
 
@@ -767,9 +875,7 @@ __global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
     // as they free up. The row's bounds were read by the order pass and are
     // cached.
     const uint32_t total = static_cast<uint32_t>(a.rows);
-    uint32_t u = 0;
-    if (lane == 0) u = atomicAdd(a.queue, 1u);
-    u = __shfl_sync(0xffffffffu, u, 0);
+    uint32_t u = __shfl_sync(0xffffffffu, first, 0);
     uint32_t k = 0;
     int ok = 1;
     while (ok && u < total) {
@@ -908,10 +1014,11 @@ __global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
                   parts = d.parts;
     uint32_t* keys = keys0 + ub * nbp;
     if (!a.own_stages)
-      fold_stage<E, MODE>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d, warp, NW, gbase,
-                          keys);
+      fold_stage<E, MODE, true>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d, warp, NW,
+                                gbase, keys);
     else if (k % NW == static_cast<uint32_t>(warp))
-      fold_stage<E, MODE>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d, 0, 1, 0u, keys);
+      fold_stage<E, MODE, true>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d, 0, 1, 0u,
+                                keys);
     gbase += stage_groups(a.block_size, d.n);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
@@ -1041,8 +1148,8 @@ __global__ void __launch_bounds__(NW * 32, 2) pipe_solo_kernel(const PipeArgs a)
     const StageDesc& d = desc[slot];
     const int32_t flags = d.flags;
     const int32_t row = d.row, nblk = d.nblk, pin = d.pin;
-    fold_stage<E, kPipeUnsharded>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d, 0, 1,
-                                  0u, keys);
+    fold_stage<E, kPipeUnsharded, false>(a, ring + static_cast<size_t>(slot) * a.stage_bytes, d,
+                                         0, 1, 0u, keys);
     __syncwarp();  // the slot and its descriptor are free for lane 0
     if (!(flags & kLast)) continue;
     topk_warp(keys, a.nb, nblk, min(a.topk, a.nb), pin, cand,
@@ -1202,14 +1309,6 @@ dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int c
                           cudaStream_t s) {
   const int sms = sm_count_now();
   const int pieces = 1;  // one piece per stage (one shard in the shard forms)
-  // A stage carries `payload` bytes of whole blocks; its buffer adds 32 bytes
-  // for the 16-byte rounding at both ends of the piece.
-  const int kb = g_over[DSA_LAUNCH_PIPE_STAGE_KB].load(std::memory_order_relaxed);
-  const int payload = (kb >= 4 && kb <= 64 ? kb : 32) * 1024;
-  a.stage_bytes = (payload + 32 * pieces + 127) & ~127;
-  a.cap = static_cast<int32_t>(payload /
-                               (static_cast<int64_t>(pieces) * a.block_size * E::kBytes));
-  if (a.cap < 1) return kPipeDeclined;
   const int slots = sms * ctas;
   // Parts per row: only when there are fewer rows than CTAs, never below
   // 64 KiB per part, at most 8; only with a workspace. (Merging parts costs
@@ -1224,18 +1323,36 @@ dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int c
   }
   a.split = split;
   a.own_stages = g_over[DSA_LAUNCH_PIPE_STAGE_OWNER].load(std::memory_order_relaxed) == 1;
-  // Longest rows first when rows outnumber the CTAs (unsharded, unsplit,
-  // through the unit counter).
+  // Longest rows first when rows outnumber the CTAs and a row can hold a
+  // CTA much longer than the ordering pass takes (about 2 us per call):
+  // rows of up to 256 KiB or more (unsharded, unsplit, through the unit
+  // counter). Measured: 512 rows of up to 256 KiB 28.8 -> 27.3 us; of up to
+  // 128 KiB 21.3 -> 24.9 us (the pass costs more than the balance gains).
   const int ord = g_over[DSA_LAUNCH_PIPE_ORDER].load(std::memory_order_relaxed);
   a.lpt = MODE == kPipeUnsharded && split == 1 && a.queue != nullptr && a.rows <= kLptMaxRows &&
-          ord != 1 && (ord == 2 || a.rows > slots);
+          ord != 1 && (ord == 2 || (a.rows > slots && max_row_bytes >= 256 * 1024));
   const size_t tail = 2 * static_cast<size_t>((a.nb + 3) & ~3) * 4 +
                       static_cast<size_t>(std::max(a.kpad, kRankMax)) * 8 +
                       (a.lpt ? ((static_cast<size_t>(a.rows) * 2 + 15) & ~static_cast<size_t>(15)) : 0);
   const size_t limit =
       smem_budget(ctas, sizeof(TopkShared) + sizeof(PieceTable) + 2 * sizeof(UnitMeta) + 128);
-  int stages = 16;
-  while (stages >= 2 && coop_keys_offset(stages, a.stage_bytes) + tail > limit) --stages;
+  // A stage carries `payload` bytes of whole blocks; its buffer adds 32 bytes
+  // for the 16-byte rounding at both ends of the piece. The largest payload
+  // of 48, 32 and 16 KiB that leaves room for two stages: fewer, larger
+  // stages measured faster (48 against 32 KiB: decode 28.0 -> 26.8 us,
+  // decode_bf16 21.2 -> 20.5 us, long 70.0 -> 69.3 us).
+  const int kb = g_over[DSA_LAUNCH_PIPE_STAGE_KB].load(std::memory_order_relaxed);
+  int stages = 0;
+  for (int p = 48; p >= 16 && stages < 2; p -= 16) {
+    const int payload = (kb >= 4 && kb <= 64 ? kb : p) * 1024;
+    a.stage_bytes = (payload + 32 * pieces + 127) & ~127;
+    a.cap = static_cast<int32_t>(payload /
+                                 (static_cast<int64_t>(pieces) * a.block_size * E::kBytes));
+    stages = 16;
+    while (stages >= 2 && coop_keys_offset(stages, a.stage_bytes) + tail > limit) --stages;
+    if (a.cap < 1) stages = 0;
+    if (kb >= 4 && kb <= 64) break;
+  }
   const int fst = g_over[DSA_LAUNCH_PIPE_STAGES].load(std::memory_order_relaxed);
   if (fst >= 2 && fst < stages) stages = fst;
   if (stages < 2) return kPipeDeclined;

@@ -72,13 +72,20 @@ __device__ __forceinline__ int32_t candidate_id(uint64_t c) {
 
 // Stores ranks of cand[0 .. n) (distinct composites): rank r < K goes to
 // out[r]; out[K .. topk) becomes -1. No barrier inside.
+// cand is 16-byte aligned: the candidates are read in pairs.
 template <typename Sync = CtaSync>
 __device__ __forceinline__ void rank_store(const uint64_t* __restrict__ cand, int32_t n, int32_t K,
                                            int32_t* __restrict__ out, int32_t topk) {
+  const ulonglong2* pairs = reinterpret_cast<const ulonglong2*>(cand);
   for (int i = Sync::tid(); i < n; i += Sync::count()) {
     const uint64_t ci = cand[i];
     int32_t r = 0;
-    for (int j = 0; j < n; ++j) r += cand[j] > ci;
+#pragma unroll 4
+    for (int j = 0; j < (n >> 1); ++j) {
+      const ulonglong2 cj = pairs[j];
+      r += (cj.x > ci) + (cj.y > ci);
+    }
+    if (n & 1) r += cand[n - 1] > ci;
     if (r < K) out[r] = candidate_id(ci);
   }
   for (int j = K + Sync::tid(); j < topk; j += Sync::count()) out[j] = -1;

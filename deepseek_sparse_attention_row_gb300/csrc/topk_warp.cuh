@@ -157,7 +157,8 @@ __device__ __forceinline__ uint32_t warp_kth_largest(uint32_t v, int R) {
 // keys: [n_live] final keys in shared memory (no other warp writes them any
 // more), 16-byte aligned, padded to a multiple of 4 words (n_live <= padded
 // size); block pin_block (if >= 0, below n_live) becomes key(+inf) here.
-// cand: [cand_cap >= 64] in shared memory. All 32 lanes call this.
+// cand: [cand_cap >= 64, even] in shared memory, 16-byte aligned. All 32
+// lanes call this.
 template <typename S>
 __device__ void topk_warp_wide(uint32_t* __restrict__ keys, int32_t nb, int32_t n_live, int32_t k,
                                int32_t pin_block, uint64_t* __restrict__ cand, int32_t cand_cap,
@@ -240,17 +241,22 @@ __device__ void topk_warp_wide(uint32_t* __restrict__ keys, int32_t nb, int32_t 
       const int b = 4 * lane + 128 * (q >> 2) + (q & 3);
       cand[pos++] = pack_candidate(keys[b], b);
     }
+    // An odd count is padded with a 0 composite (below every candidate), so
+    // that the ranking reads pairs with 16-byte loads.
+    if (lane == 0 && (n & 1)) cand[n] = 0ull;
     __syncwarp();
     // 4. Rank by counting; two candidates per lane per pass.
+    const ulonglong2* pairs = reinterpret_cast<const ulonglong2*>(cand);
     for (int i0 = 0; i0 < n; i0 += 64) {
       const int ia = i0 + lane, ib = i0 + 32 + lane;
       const uint64_t ca = ia < n ? cand[ia] : 0ull;
       const uint64_t cb = ib < n ? cand[ib] : 0ull;
       int32_t ra = 0, rb = 0;
-      for (int j = 0; j < n; ++j) {
-        const uint64_t cj = cand[j];
-        ra += cj > ca;
-        rb += cj > cb;
+#pragma unroll 4
+      for (int j = 0; j < (n + 1) >> 1; ++j) {
+        const ulonglong2 cj = pairs[j];
+        ra += (cj.x > ca) + (cj.y > ca);
+        rb += (cj.x > cb) + (cj.y > cb);
       }
       if (ia < n && ra < K) out[ra] = candidate_id(ca);
       if (ib < n && rb < K) out[rb] = candidate_id(cb);
