@@ -25,7 +25,8 @@ constexpr int kWarpCand = 128;  // candidates ranked by counting, per warp
 
 // keys: this warp's [n_live] block keys in shared memory (the pinned block,
 // if >= 0, lies below n_live and becomes +inf here). cand: [kWarpCand] in
-// shared memory. out: the row's output slots (global; unused when k == 0).
+// shared memory, 16-byte aligned. out: the row's output slots (global;
+// unused when k == 0).
 // scores: optional row of nb entries (fp32 or bf16 bits). All 32 lanes call
 // this.
 template <typename S>
@@ -96,10 +97,17 @@ __device__ void topk_warp(uint32_t* __restrict__ keys, int32_t nb, int32_t n_liv
     }
     __syncwarp();
     if (n <= kWarpCand) {
+      // Candidates read in 16-byte pairs (cand is 16-byte aligned).
+      const ulonglong2* pairs = reinterpret_cast<const ulonglong2*>(cand);
       for (int i = lane; i < n; i += 32) {
         const uint64_t ci = cand[i];
         int32_t r = 0;
-        for (int j = 0; j < n; ++j) r += cand[j] > ci;
+#pragma unroll 4
+        for (int j = 0; j < (n >> 1); ++j) {
+          const ulonglong2 cj = pairs[j];
+          r += (cj.x > ci) + (cj.y > ci);
+        }
+        if (n & 1) r += cand[n - 1] > ci;
         if (r < K) out[r] = candidate_id(ci);
       }
       for (int j = K + lane; j < topk; j += 32) out[j] = -1;
@@ -144,19 +152,18 @@ __device__ __forceinline__ uint32_t warp_kth_largest(uint32_t v, int R) {
 }
 
 // Ranked top-k of one row by one warp for rows of up to 1024 block keys
-// (32 per lane) and k <= 32; same result as topk_store. Lane l reads keys
-// 4l + 128i .. 4l + 128i + 3 with one 16-byte shared load per i (conflict
-// free) and keeps its two largest keys t1 >= t2. Bound: ceil(k/2) lanes with
-// t2 >= L hold at least k keys >= L, so every top-k key is >= L (L from t1
-// and k lanes when too few lanes have two live keys; all live keys when even
-// that fails). Keys >= L (typically k plus a few dozen) are compacted from
-// per-lane bit masks and a warp scan, and ranked by counting the composites
-// above each. More candidates than `cand_cap` (long runs of equal keys): k
-// rounds of a warp max.
+// (32 per lane) and k <= 32; same result as topk_store. Lane l holds keys
+// l, l + 32, ... (conflict-free loads; a short row still spreads over the
+// lanes) and keeps its two largest t1 >= t2. Bound: ceil(k/2) lanes with
+// t2 >= L hold at least k keys >= L, so every top-k key is >= L; when fewer
+// than ceil(k/2) lanes hold two live keys, every live key is a candidate.
+// Candidates (typically k plus a few dozen) are marked in a 32-bit mask per
+// lane, a warp scan of the mask counts gives each lane its slots, and each is
+// ranked by counting the composites above it. More candidates than
+// `cand_cap` (long runs of equal keys): k rounds of a warp max.
 //
 // keys: [n_live] final keys in shared memory (no other warp writes them any
-// more), 16-byte aligned, padded to a multiple of 4 words (n_live <= padded
-// size); block pin_block (if >= 0, below n_live) becomes key(+inf) here.
+// more); block pin_block (if >= 0, below n_live) becomes key(+inf) here.
 // cand: [cand_cap >= 64, even] in shared memory, 16-byte aligned. All 32
 // lanes call this.
 template <typename S>
@@ -173,57 +180,26 @@ __device__ void topk_warp_wide(uint32_t* __restrict__ keys, int32_t nb, int32_t 
   // 1. Each lane's two largest keys (0 stands for none: every key is >=
   // key(-inf) > 0).
   uint32_t t1 = 0u, t2 = 0u;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int base = 4 * lane + 128 * i;
-    if (base < n_live) {
-      uint4 v = *reinterpret_cast<const uint4*>(keys + base);
-      if (base + 4 > n_live) {
-        if (base + 1 >= n_live) v.y = 0u;
-        if (base + 2 >= n_live) v.z = 0u;
-        v.w = 0u;
-      }
-      t2 = max(t2, min(t1, v.x)); t1 = max(t1, v.x);
-      t2 = max(t2, min(t1, v.y)); t1 = max(t1, v.y);
-      t2 = max(t2, min(t1, v.z)); t1 = max(t1, v.z);
-      t2 = max(t2, min(t1, v.w)); t1 = max(t1, v.w);
-    }
+#pragma unroll 8
+  for (int i = 0; i < 32; ++i) {
+    const int b = lane + 32 * i;
+    const uint32_t x = b < n_live ? keys[b] : 0u;
+    t2 = max(t2, min(t1, x));
+    t1 = max(t1, x);
   }
 
-  // 2. The bound.
-  int32_t K = k;
+  // 2. The bound (key(-inf) + 1, i.e. every live key, when it fails).
   uint32_t thr = warp_kth_largest(t2, (k + 1) >> 1);
-  if (thr == 0u) thr = warp_kth_largest(t1, k);
-  if (thr == 0u) {
-    // Fewer than k lanes hold a live key: take every live key.
-    uint32_t cnt = 0;
-    for (int i = 0; i < 8; ++i)
-      for (int j = 0; j < 4; ++j) {
-        const int b = 4 * lane + 128 * i + j;
-        cnt += (b < n_live && keys[b] > kKeyNegInf) ? 1u : 0u;
-      }
-    const uint32_t total = __reduce_add_sync(0xffffffffu, cnt);
-    K = static_cast<int32_t>(min(static_cast<uint32_t>(k), total));
-    thr = kKeyNegInf + 1u;
-  }
-  if (K == 0) {
-    for (int j = lane; j < topk; j += 32) out[j] = -1;
-    return;
-  }
+  const bool take_all = thr == 0u;
+  if (take_all) thr = kKeyNegInf + 1u;
 
   // 3. Candidates: a bit per key at or above the bound, then a warp scan of
   // the counts gives each lane its slots.
   uint32_t bits = 0u;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int base = 4 * lane + 128 * i;
-    if (base < n_live) {
-      const uint4 v = *reinterpret_cast<const uint4*>(keys + base);
-      uint32_t m = (v.x >= thr ? 1u : 0u) | (v.y >= thr ? 2u : 0u) | (v.z >= thr ? 4u : 0u) |
-                   (v.w >= thr ? 8u : 0u);
-      if (base + 4 > n_live) m &= (1u << (n_live - base)) - 1u;
-      bits |= m << (4 * i);
-    }
+#pragma unroll 8
+  for (int i = 0; i < 32; ++i) {
+    const int b = lane + 32 * i;
+    bits |= (b < n_live && keys[b] >= thr) ? (1u << i) : 0u;
   }
   const uint32_t mine = __popc(bits);
   uint32_t incl = mine;
@@ -233,12 +209,17 @@ __device__ void topk_warp_wide(uint32_t* __restrict__ keys, int32_t nb, int32_t 
     if (lane >= o) incl += t;
   }
   const int32_t n = static_cast<int32_t>(__shfl_sync(0xffffffffu, incl, 31));
+  const int32_t K = take_all ? min(k, n) : k;
+  if (K == 0) {
+    for (int j = lane; j < topk; j += 32) out[j] = -1;
+    return;
+  }
   if (n <= cand_cap) {
     int32_t pos = static_cast<int32_t>(incl - mine);
     while (bits) {
       const int q = __ffs(bits) - 1;
       bits &= bits - 1u;
-      const int b = 4 * lane + 128 * (q >> 2) + (q & 3);
+      const int b = lane + 32 * q;
       cand[pos++] = pack_candidate(keys[b], b);
     }
     // An odd count is padded with a 0 composite (below every candidate), so
