@@ -1341,12 +1341,12 @@ dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int c
       smem_budget(ctas, sizeof(TopkShared) + sizeof(PieceTable) + 2 * sizeof(UnitMeta) + 128);
   // A stage carries `payload` bytes of whole blocks; its buffer adds 32 bytes
   // for the 16-byte rounding at both ends of the piece. The largest payload
-  // of 48, 32 and 16 KiB that leaves room for two stages: fewer, larger
-  // stages measured faster (48 against 32 KiB: decode 28.0 -> 26.8 us,
-  // decode_bf16 21.2 -> 20.5 us, long 70.0 -> 69.3 us).
+  // of 48 (64 at one CTA per SM), 32 and 16 KiB that leaves room for two
+  // stages: fewer, larger stages measured faster (48 against 32 KiB: decode
+  // 28.0 -> 26.8 us, decode_bf16 21.2 -> 20.5 us, long 70.0 -> 69.3 us).
   const int kb = g_over[DSA_LAUNCH_PIPE_STAGE_KB].load(std::memory_order_relaxed);
   int stages = 0;
-  for (int p = 48; p >= 16 && stages < 2; p -= 16) {
+  for (int p = ctas == 1 ? 64 : 48; p >= 16 && stages < 2; p -= 16) {
     const int payload = (kb >= 4 && kb <= 64 ? kb : p) * 1024;
     a.stage_bytes = (payload + 32 * pieces + 127) & ~127;
     a.cap = static_cast<int32_t>(payload /
@@ -1372,11 +1372,16 @@ dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int c
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ECUDA;
 }
 
+// Rows of more than 256 KiB run at one CTA per SM with 8 folding warps and
+// three 64 KiB stages (192 KiB in flight per SM, one producer): long (1024
+// rows of 256-512 KiB) 69.0 -> 65.6 us. Shorter rows keep two CTAs per SM
+// with 4 folding warps each: decode (rows of up to 256 KiB) measured 28.2
+// against 30.0 us in the one-CTA shape, decode_bf16 20.5 against 25.1 us.
 template <typename E, int MODE>
 dsa_status launch_coop(const PipeArgs& a, int64_t max_row_bytes, bool have_ws, cudaStream_t s) {
   const int warps = g_over[DSA_LAUNCH_PIPE_WARPS].load(std::memory_order_relaxed);
   const int fc = g_over[DSA_LAUNCH_PIPE_CTAS].load(std::memory_order_relaxed);
-  if (warps == 8)
+  if (warps == 8 || (warps == 0 && max_row_bytes > 256 * 1024))
     return launch_coop_nw<E, MODE, 8>(a, max_row_bytes, have_ws, 1, s);
   return launch_coop_nw<E, MODE, 4>(a, max_row_bytes, have_ws, fc >= 1 ? std::min(fc, 2) : 2, s);
 }

@@ -116,7 +116,8 @@ size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks);
  *   DSA_LAUNCH_PIPE_SCHED  pipelined kernels: 1 = rows dealt to CTAs in a
  *                          fixed order even when a workspace is given
  *   DSA_LAUNCH_PIPE_WARPS  pipelined kernels, every warp on one row: 4 or 8
- *                          consumer warps per CTA
+ *                          consumer warps per CTA (default: 8, one CTA per
+ *                          SM, for rows of more than 256 KiB; else 4)
  *   DSA_LAUNCH_PIPE_CTAS   pipelined kernels: CTAs per SM, 1..4 (at most 2
  *                          with 8 consumer warps or one row per warp)
  *   DSA_LAUNCH_PIPE_STAGE_OWNER  pipelined kernels, every warp on one row:
