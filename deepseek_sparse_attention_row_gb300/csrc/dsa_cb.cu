@@ -401,7 +401,11 @@ __device__ __forceinline__ void stream_range(const SelectArgs& a, const RowPlan<
   }
   __syncthreads();
   if constexpr (MODE == kShardedStarts) {
-    for (int d = threadIdx.x; d < a.shards; d += blockDim.x) {
+    // Shard d's tail on lane d / warps of warp d % warps: every warp takes a
+    // share, so the barrier below waits on less.
+    const int nwarps = blockDim.x >> 5;
+    for (int d = (threadIdx.x & 31) * nwarps + (threadIdx.x >> 5); d < a.shards;
+         d += 32 * nwarps) {
       const RowPlan<E> pd = plan_window<E>(plan.origin + d * a.shard_stride, start[d], len[d],
                                            a.block_size, a.by_block);
       Window<E> wd;
@@ -430,30 +434,25 @@ __device__ __forceinline__ void stream_range(const SelectArgs& a, const RowPlan<
 // blocks with k <= 32 are ranked by warp 0 alone (topk_warp_wide): the
 // other warps leave, and the ranking costs a quarter of the instructions of
 // the CTA-wide topk_store.
+// Keys [nblk, pin] were set to key(-inf) with the CTA's own blocks; the pin
+// becomes +inf inside the ranking. `merged`: the keys were just read back
+// from the workspace (a split row), so a barrier comes first.
 template <typename E>
 __device__ __forceinline__ void rank_row(const SelectArgs& a, int64_t row, int32_t nblk,
                                          int32_t pin_block, uint32_t* keys, uint64_t* cand,
-                                         TopkShared& tsh) {
+                                         TopkShared& tsh, bool merged) {
   using TE = typename E::T;
   const int32_t n_live = max(nblk, pin_block + 1);
   const int32_t k = min(a.topk, a.nb);
   int32_t* out = a.topk > 0 ? a.out + row * a.ld_out : nullptr;
   TE* scores = a.scores ? static_cast<TE*>(a.scores) + row * a.ld_scores : nullptr;
+  if (merged) __syncthreads();
   if (!a.rank_cta && k <= 32 && n_live <= 1024) {
-    // Blocks between the data and the pin are -inf; after the barrier (the
-    // last CTA of a split row may still be reading other parts' keys back)
-    // the ranking warp makes the pin +inf.
-    for (int32_t b = nblk + threadIdx.x; b < pin_block; b += blockDim.x) keys[b] = kKeyNegInf;
-    __syncthreads();
     if (threadIdx.x < 32)
       topk_warp_wide(keys, a.nb, n_live, k, pin_block, cand, max(a.kpad, kRankMax), out, a.topk,
                      scores);
     return;
   }
-  // Blocks past the data blocks up to the pin are -inf (the pin can lie past
-  // the data in the DCP form); topk_store never reads further.
-  for (int32_t b = nblk + threadIdx.x; b <= pin_block; b += blockDim.x) keys[b] = kKeyNegInf;
-  __syncthreads();
   topk_store(keys, a.nb, n_live, k, pin_block, cand, a.kpad, out, a.topk, scores, tsh);
 }
 
@@ -505,14 +504,18 @@ __global__ void __launch_bounds__(T, 1024 / T) select_kernel(const SelectArgs a)
   const int32_t b0 = part * a.chunk;
   const int32_t b1 = min(b0 + a.chunk, nblk);
 
+  // This CTA's blocks, and the blocks past the data up to the pin (which can
+  // lie past the data in the DCP form; no stream writes them), start at
+  // key(-inf).
   for (int32_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) keys[b] = kKeyNegInf;
+  for (int32_t b = nblk + threadIdx.x; b <= plan.pin_block; b += blockDim.x) keys[b] = kKeyNegInf;
   __syncthreads();
   stream_range<E, MODE, SVEC>(a, plan, shard_q, shard_rem, b0, b1, keys, len, start);
   // Publish this share, count in; only the last CTA of the row goes on.
   if (parts > 1 &&
       !merge_shares(a, row, nblk, b0, b1, 1u, static_cast<uint32_t>(parts), keys, &s_last))
     return;
-  rank_row<E>(a, row, nblk, plan.pin_block, keys, cand, tsh);
+  rank_row<E>(a, row, nblk, plan.pin_block, keys, cand, tsh, parts > 1);
 }
 
 // Shared memory per warp in select_warp_kernel: candidates, keys, length.

@@ -578,8 +578,10 @@ __device__ __forceinline__ void commit_partial_shifted(const typename E::T* orig
                                                        int32_t kbase) {
   constexpr int VEC = 16 / E::kBytes;
   const int32_t first = max(((len + r) / VEC) * VEC - r, 0);
+  const bool pow2 = (block_size & (block_size - 1)) == 0;
+  const int sh = __ffs(block_size) - 1;
   for (int32_t i = first; i < len; ++i) {
-    const int32_t blk = i / block_size;
+    const int32_t blk = pow2 ? (i >> sh) : i / block_size;
     if (blk >= b0 && blk < b1) atomicMax(&keys[blk - kbase], order_key(ld_elem(origin + i)));
   }
 }
@@ -601,7 +603,8 @@ __device__ __forceinline__ Partial load_partial(const typename E::T* shard_origi
   if (VEC == 1) return p;
   const int32_t first = (len / VEC) * VEC;
   if (first == len) return p;
-  const int32_t blk = first / block_size;
+  const int32_t blk = (block_size & (block_size - 1)) == 0 ? first >> (__ffs(block_size) - 1)
+                                                           : first / block_size;
   if (blk < b0 || blk >= b1) return p;
   for (int32_t i = first; i < len; ++i) p.v = max_nan(p.v, ld_elem(shard_origin + i));
   p.blk = blk;
