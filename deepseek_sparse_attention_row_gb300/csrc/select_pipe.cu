@@ -1152,9 +1152,9 @@ __global__ void __launch_bounds__(NW * 32, 2) pipe_solo_kernel(const PipeArgs a)
                                          0, 1, 0u, keys);
     __syncwarp();  // the slot and its descriptor are free for lane 0
     if (!(flags & kLast)) continue;
-    // The lane-maximum bound: on the warp's own path its 32-step rank of the
-    // lane maxima beats the rounds of topk_warp_wide's tighter bound (prefill
-    // 34.9 against 37.1 us).
+    // The lane-maximum bound: on the warp's own path it measured as fast as
+    // topk_warp_wide's tighter bound (prefill 34.9 against 35.4 us), whose
+    // rounds of warp maxima sit on that path.
     topk_warp(keys, a.nb, nblk, min(a.topk, a.nb), pin, cand,
               a.topk > 0 ? a.out + static_cast<int64_t>(row) * a.ld_out : nullptr, a.topk,
               score_row<E>(a, row));

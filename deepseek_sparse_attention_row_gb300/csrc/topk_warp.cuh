@@ -178,10 +178,11 @@ __device__ void topk_warp_wide(uint32_t* __restrict__ keys, int32_t nb, int32_t 
   if (k <= 0) return;
 
   // 1. Each lane's two largest keys (0 stands for none: every key is >=
-  // key(-inf) > 0).
+  // key(-inf) > 0), over the rounds of 32 keys the row has.
+  const int rounds = (n_live + 31) >> 5;
   uint32_t t1 = 0u, t2 = 0u;
 #pragma unroll 8
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < rounds; ++i) {
     const int b = lane + 32 * i;
     const uint32_t x = b < n_live ? keys[b] : 0u;
     t2 = max(t2, min(t1, x));
@@ -197,7 +198,7 @@ __device__ void topk_warp_wide(uint32_t* __restrict__ keys, int32_t nb, int32_t 
   // the counts gives each lane its slots.
   uint32_t bits = 0u;
 #pragma unroll 8
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < rounds; ++i) {
     const int b = lane + 32 * i;
     bits |= (b < n_live && keys[b] >= thr) ? (1u << i) : 0u;
   }
