@@ -859,6 +859,7 @@ dsa_status dsa_select_set_launch_override(int32_t knob, int32_t value) {
     case DSA_LAUNCH_RANK_CTA:
       if (value < 0 || value > 2) return DSA_EINVAL;
       g_rank_cta.store(value);
+      pipe_set_override(knob, value);
       return DSA_OK;
     default:
       return DSA_EINVAL;

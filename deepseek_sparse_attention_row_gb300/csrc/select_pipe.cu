@@ -118,6 +118,7 @@ struct PipeArgs {
   int32_t cap;          // blocks per stage
   int32_t own_stages;   // coop: each fold warp folds whole stages in turn
   int32_t lpt;          // coop, unsharded, S = 1: unit u is row order[u], longest first
+  int32_t rank_warp;    // coop: one rank warp ranks rows of <= 1024 blocks, k <= 32
 };
 
 // ---------------------------------------------------------------------------
@@ -724,14 +725,15 @@ constexpr int kLptClasses = 128;
 constexpr int kLptMaxRows = 4096;
 
 __host__ __device__ __forceinline__ size_t lpt_scratch_bytes(int warps, int32_t rows) {
-  return static_cast<size_t>(warps) * kLptClasses * 4 + static_cast<size_t>(rows);
+  return static_cast<size_t>(warps + 1) * kLptClasses * 4 + static_cast<size_t>(rows);
 }
 
 template <int NWARPS>
 __device__ void longest_first_order(const PipeArgs& a, uint16_t* __restrict__ order,
                                     unsigned char* __restrict__ scratch) {
   uint32_t* hist = reinterpret_cast<uint32_t*>(scratch);  // [NWARPS][kLptClasses]
-  unsigned char* cls = reinterpret_cast<unsigned char*>(hist + NWARPS * kLptClasses);  // [rows]
+  uint32_t* start = hist + NWARPS * kLptClasses;           // [kLptClasses]
+  unsigned char* cls = reinterpret_cast<unsigned char*>(start + kLptClasses);  // [rows]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < NWARPS * kLptClasses; i += blockDim.x) hist[i] = 0u;
   const int32_t rows = a.rows;
@@ -760,15 +762,23 @@ __device__ void longest_first_order(const PipeArgs& a, uint16_t* __restrict__ or
   }
   __syncthreads();
   // Each class's start in the order (an exclusive scan over classes, longest
-  // first), then each warp's start within the class; warp 0, lane l owns
-  // classes PER*l .. PER*l + PER - 1.
+  // first), then each warp's start within the class: one thread per class
+  // sums the warps' counts, warp 0 scans the sums, one thread per class
+  // turns its counts into offsets (short independent chains, not one long
+  // one).
+  for (int b = threadIdx.x; b < kLptClasses; b += blockDim.x) {
+    uint32_t t = 0;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) t += hist[w * kLptClasses + b];
+    start[b] = t;
+  }
+  __syncthreads();
   if (warp == 0) {
     constexpr int PER = kLptClasses / 32;
     uint32_t t[PER], sum = 0;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-      t[i] = 0;
-      for (int w = 0; w < NWARPS; ++w) t[i] += hist[w * kLptClasses + lane * PER + i];
+      t[i] = start[lane * PER + i];
       sum += t[i];
     }
     uint32_t incl = sum;
@@ -777,15 +787,24 @@ __device__ void longest_first_order(const PipeArgs& a, uint16_t* __restrict__ or
       const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
-    uint32_t off = incl - sum;
+    uint32_t run = incl - sum;
 #pragma unroll
-    for (int i = 0; i < PER; ++i)
-      for (int w = 0; w < NWARPS; ++w) {
-        uint32_t& h = hist[w * kLptClasses + lane * PER + i];
-        const uint32_t c = h;
-        h = off;
-        off += c;
-      }
+    for (int i = 0; i < PER; ++i) {
+      start[lane * PER + i] = run;
+      run += t[i];
+    }
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < kLptClasses; b += blockDim.x) {
+    uint32_t c[NWARPS];
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) c[w] = hist[w * kLptClasses + b];
+    uint32_t off = start[b];
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) {
+      hist[w * kLptClasses + b] = off;
+      off += c[w];
+    }
   }
   __syncthreads();
   for (int32_t c = c0; c < c1; ++c) {
@@ -969,10 +988,18 @@ __global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
         for (int32_t b = m.nblk + RankSync::tid(); b <= m.pin; b += RankSync::count())
           keys[b] = kKeyNegInf;
         RankSync::sync();
-        topk_store<typename E::T, RankSync>(
-            keys, a.nb, max(m.nblk, m.pin + 1), min(a.topk, a.nb), m.pin, cand, a.kpad,
-            a.topk > 0 ? a.out + static_cast<int64_t>(m.row) * a.ld_out : nullptr, a.topk,
-            score_row<E>(a, m.row), tsh);
+        const int32_t n_live = max(m.nblk, m.pin + 1), kk = min(a.topk, a.nb);
+        int32_t* out = a.topk > 0 ? a.out + static_cast<int64_t>(m.row) * a.ld_out : nullptr;
+        if (a.rank_warp && kk <= 32 && n_live <= 1024) {
+          // One rank warp: fewer instructions, but a longer path than four
+          // warps sharing the keys (decode 29.8 against 28.3 us).
+          if (RankSync::tid() < 32)
+            topk_warp_wide(keys, a.nb, n_live, kk, m.pin, cand, max(a.kpad, kRankMax), out,
+                           a.topk, score_row<E>(a, m.row));
+        } else {
+          topk_store<typename E::T, RankSync>(keys, a.nb, n_live, kk, m.pin, cand, a.kpad, out,
+                                              a.topk, score_row<E>(a, m.row), tsh);
+        }
       }
       RankSync::sync();  // every rank thread is done with the keys
       if (kMerge) {
@@ -1326,14 +1353,15 @@ dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int c
   }
   a.split = split;
   a.own_stages = g_over[DSA_LAUNCH_PIPE_STAGE_OWNER].load(std::memory_order_relaxed) == 1;
-  // Longest rows first when rows outnumber the CTAs and a row can hold a
-  // CTA much longer than the ordering pass takes (about 2 us per call):
-  // rows of up to 256 KiB or more (unsharded, unsplit, through the unit
-  // counter). Measured: 512 rows of up to 256 KiB 28.8 -> 27.3 us; of up to
-  // 128 KiB 21.3 -> 24.9 us (the pass costs more than the balance gains).
+  a.rank_warp = g_over[DSA_LAUNCH_RANK_CTA].load(std::memory_order_relaxed) == 2;
+  // Longest rows first only on request (unsharded, unsplit, through the unit
+  // counter): timed in turn on the same buffers, the ordering pass (about 2.5
+  // us at the start of a flushed step) costs more than the balance gains:
+  // decode 25.6 us in index order against 27.6 us longest first,
+  // decode_bf16 20.6 against 23.1 us, long 65.6 us either way.
   const int ord = g_over[DSA_LAUNCH_PIPE_ORDER].load(std::memory_order_relaxed);
   a.lpt = MODE == kPipeUnsharded && split == 1 && a.queue != nullptr && a.rows <= kLptMaxRows &&
-          ord != 1 && (ord == 2 || (a.rows > slots && max_row_bytes >= 256 * 1024));
+          ord == 2;
   const size_t tail = 2 * static_cast<size_t>((a.nb + 3) & ~3) * 4 +
                       static_cast<size_t>(std::max(a.kpad, kRankMax)) * 8 +
                       (a.lpt ? ((static_cast<size_t>(a.rows) * 2 + 15) & ~static_cast<size_t>(15)) : 0);

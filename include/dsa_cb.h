@@ -124,13 +124,15 @@ size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks);
  *                          1 = each folding warp takes whole stages in turn
  *                          (default: every stage's blocks shared by all)
  *   DSA_LAUNCH_PIPE_ORDER  pipelined kernels, every warp on one row: 1 = rows
- *                          handed out in index order, 2 = longest rows first
- *                          whenever the call allows it (default: longest
- *                          first when the rows outnumber the CTAs)
+ *                          handed out in index order (the default), 2 =
+ *                          longest rows first whenever the call allows it
  *   DSA_LAUNCH_RANK_CTA    row-per-CTA kernel: 1 = every warp of the CTA
  *                          ranks each row, 2 = one warp ranks every row of
  *                          up to 1024 live blocks with k <= 32 (default: one
- *                          warp, except the fp32 DCP form without starts)
+ *                          warp, except the fp32 DCP form without starts);
+ *                          pipelined kernel: 2 = one rank warp ranks rows
+ *                          of up to 1024 live blocks with k <= 32 (default:
+ *                          all four rank warps)
  *
  * DSA_EINVAL for an unknown knob or a value outside its range (nothing
  * changes then).

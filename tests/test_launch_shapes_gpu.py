@@ -50,6 +50,7 @@ CASES = {
     "pipe_fixed_order": ("pipeline=2,pipe_sched=1,pipe_split=2", SWEEPS, 150),
     "pipe_8_warps": ("pipeline=2,pipe_warps=8,pipe_ctas=1", SWEEPS + " or graph", 150),
     "pipe_4_warps": ("pipeline=2,pipe_warps=4", SWEEPS + " or full_size_unsharded", 150),
+    "pipe_rank_warp": ("pipeline=2,rank_cta=2", SWEEPS + " or full_size_unsharded", 150),
     "pipe_stage_owner": ("pipeline=2,pipe_stage_owner=1", SWEEPS, 150),
     "pipe_longest_first": ("pipeline=2,pipe_order=2", SWEEPS + " or graph", 150),
     "pipe_solo_small_stages": ("pipeline=3,pipe_stage_kb=4,pipe_ctas=1", "unsharded_sweep or warp",
