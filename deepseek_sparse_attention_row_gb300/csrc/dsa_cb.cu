@@ -853,7 +853,7 @@ dsa_status dsa_select_set_launch_override(int32_t knob, int32_t value) {
       pipe_set_override(knob, value);
       return DSA_OK;
     case DSA_LAUNCH_PIPE_ORDER:
-      if (value < 0 || value > 2) return DSA_EINVAL;
+      if (value < 0 || value > 3) return DSA_EINVAL;
       pipe_set_override(knob, value);
       return DSA_OK;
     case DSA_LAUNCH_RANK_CTA:

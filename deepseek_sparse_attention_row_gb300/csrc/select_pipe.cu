@@ -118,6 +118,7 @@ struct PipeArgs {
   int32_t cap;          // blocks per stage
   int32_t own_stages;   // coop: each fold warp folds whole stages in turn
   int32_t lpt;          // coop, unsharded, S = 1: unit u is row order[u], longest first
+  int32_t claim_ahead;  // coop: units claimed two ahead from the start (not as CTAs free up)
   int32_t rank_warp;    // coop: one rank warp ranks rows of <= 1024 blocks, k <= 32
 };
 
@@ -881,24 +882,28 @@ __global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
   __syncthreads();
   // With rows longest first, the producer claims its first row before the
   // ordering pass, so that the claim's round trip overlaps the pass.
+  // Whole unsharded rows from the unit counter: the producer claims a CTA's
+  // next row only when the current row's last stage is due (the ring still
+  // holds that row's last stages, which hides the claim's round trip), so
+  // rows go to CTAs as they free up. Claiming two ahead from the start fixed
+  // each CTA's rows when the launch began (on decode one CTA drew two of the
+  // longest rows, 480 KB against 194 KB on average): timed in turn, decode
+  // 25.4 -> 23.4 us, long 65.6 -> 63.3 us, decode_bf16 20.6 -> 20.4 us. The
+  // first claim overlaps the ordering pass, when there is one.
+  const bool claim_late = MODE == kPipeUnsharded && a.split == 1 && a.queue != nullptr &&
+                          !a.claim_ahead;
   uint32_t first = 0;
-  if (MODE == kPipeUnsharded && a.lpt && warp == NW + NR && lane == 0)
-    first = atomicAdd(a.queue, 1u);
+  if (claim_late && warp == NW + NR && lane == 0) first = atomicAdd(a.queue, 1u);
   if constexpr (MODE == kPipeUnsharded)
     if (a.lpt) longest_first_order<NW + NR + 1>(a, order, ring);
 
-  if (MODE == kPipeUnsharded && a.lpt && warp == NW + NR) {
-    // Producer warp, longest rows first: a CTA claims its next row only when
-    // the current row's last stage is due (the ring still holds the row's
-    // last stages, which hides the claim's round trip), so rows go to CTAs
-    // as they free up. The row's bounds were read by the order pass and are
-    // cached.
+  if (claim_late && warp == NW + NR) {
     const uint32_t total = static_cast<uint32_t>(a.rows);
     uint32_t u = __shfl_sync(0xffffffffu, first, 0);
     uint32_t k = 0;
     int ok = 1;
     while (ok && u < total) {
-      const int32_t row = order[u];
+      const int32_t row = a.lpt ? static_cast<int32_t>(order[u]) : static_cast<int32_t>(u);
       const LanePlan<E> p = plan_lane<E, MODE>(a, row, load_bounds<MODE>(a, row), lane);
       if (lane == 0) {
         pt.origin[0] = reinterpret_cast<const unsigned char*>(p.origin);
@@ -917,7 +922,8 @@ __global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
   }
 
   if (warp == NW + NR) {
-    // Producer warp. Units are fetched two ahead: while the stages of unit u
+    // Producer warp for parts of rows, the shard forms and the fixed order.
+    // Units are fetched two ahead: while the stages of unit u
     // go out, the bounds of the next unit and the index of the one after it
     // are in flight, so a unit boundary waits on no memory round trip.
     const uint32_t S = static_cast<uint32_t>(a.split);
@@ -1362,6 +1368,7 @@ dsa_status launch_coop_nw(PipeArgs a, int64_t max_row_bytes, bool have_ws, int c
   const int ord = g_over[DSA_LAUNCH_PIPE_ORDER].load(std::memory_order_relaxed);
   a.lpt = MODE == kPipeUnsharded && split == 1 && a.queue != nullptr && a.rows <= kLptMaxRows &&
           ord == 2;
+  a.claim_ahead = ord == 3;
   const size_t tail = 2 * static_cast<size_t>((a.nb + 3) & ~3) * 4 +
                       static_cast<size_t>(std::max(a.kpad, kRankMax)) * 8 +
                       (a.lpt ? ((static_cast<size_t>(a.rows) * 2 + 15) & ~static_cast<size_t>(15)) : 0);

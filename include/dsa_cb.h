@@ -125,7 +125,9 @@ size_t dsa_select_workspace_bytes(int64_t rows, int64_t nblocks);
  *                          (default: every stage's blocks shared by all)
  *   DSA_LAUNCH_PIPE_ORDER  pipelined kernels, every warp on one row: 1 = rows
  *                          handed out in index order (the default), 2 =
- *                          longest rows first whenever the call allows it
+ *                          longest rows first whenever the call allows it,
+ *                          3 = index order with each CTA's next rows claimed
+ *                          ahead from the start (not as it frees up)
  *   DSA_LAUNCH_RANK_CTA    row-per-CTA kernel: 1 = every warp of the CTA
  *                          ranks each row, 2 = one warp ranks every row of
  *                          up to 1024 live blocks with k <= 32 (default: one

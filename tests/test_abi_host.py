@@ -93,7 +93,7 @@ def test_launch_override_validation(lib):
                             (7, (0, 2, 16), (1, 17)), (8, (0, 4, 64), (3, 65)),
                             (9, (0, 1), (2, -1)), (10, (0, 4, 8), (2, 16)),
                             (11, (0, 1, 4), (5, -1)), (12, (0, 1), (2, -1)),
-                            (13, (0, 1, 2), (3, -1)), (14, (0, 1, 2), (3, -1))):
+                            (13, (0, 1, 2, 3), (4, -1)), (14, (0, 1, 2), (3, -1))):
         for v in good:
             assert set_(knob, v) == DSA_OK
         for v in bad:

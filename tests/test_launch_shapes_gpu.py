@@ -53,6 +53,7 @@ CASES = {
     "pipe_rank_warp": ("pipeline=2,rank_cta=2", SWEEPS + " or full_size_unsharded", 150),
     "pipe_stage_owner": ("pipeline=2,pipe_stage_owner=1", SWEEPS, 150),
     "pipe_longest_first": ("pipeline=2,pipe_order=2", SWEEPS + " or graph", 150),
+    "pipe_claim_ahead": ("pipeline=2,pipe_order=3", SWEEPS + " or full_size_unsharded", 150),
     "pipe_solo_small_stages": ("pipeline=3,pipe_stage_kb=4,pipe_ctas=1", "unsharded_sweep or warp",
                                80),
 }
