@@ -240,7 +240,8 @@ struct PieceTable {
 // stages: wait for the stage's slot, write its descriptor (the unit's fields
 // only on its last stage), arm its barrier and issue the one bulk copy.
 // With `claim`, the next unit is claimed from the unit counter as the last
-// stage's turn comes (before waiting for its slot). Returns false (on lane
+// stage's turn comes (before waiting for its slot); the counter hands out
+// units from gridDim.x on (CTA b starts with unit b). Returns false (on lane
 // 0) when a wait gave up.
 template <typename E>
 __device__ __forceinline__ bool emit_unit(const PipeArgs& a, const PieceTable& pt, int npieces,
@@ -256,7 +257,7 @@ __device__ __forceinline__ bool emit_unit(const PipeArgs& a, const PieceTable& p
     const bool last = c + n >= b1 && shard == npieces - 1;
     const uint32_t slot = k % static_cast<uint32_t>(stages);
     const uint32_t round = k / static_cast<uint32_t>(stages);
-    if (last && claim) *claim = atomicAdd(a.queue, 1u);
+    if (last && claim) *claim = gridDim.x + atomicAdd(a.queue, 1u);
     if (round > 0 && !mbar_wait(&empty[slot], (round - 1u) & 1u, kSiteEmpty)) return false;
     // The piece: elements [c*bs, min((c+n)*bs, len)) of the shard's window,
     // copied from the 16-byte granule holding its first element through the
@@ -885,21 +886,19 @@ __global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
   // Whole unsharded rows from the unit counter: the producer claims a CTA's
   // next row only when the current row's last stage is due (the ring still
   // holds that row's last stages, which hides the claim's round trip), so
-  // rows go to CTAs as they free up. Claiming two ahead from the start fixed
-  // each CTA's rows when the launch began (on decode one CTA drew two of the
-  // longest rows, 480 KB against 194 KB on average): timed in turn, decode
-  // 25.4 -> 23.4 us, long 65.6 -> 63.3 us, decode_bf16 20.6 -> 20.4 us. The
-  // first claim overlaps the ordering pass, when there is one.
+  // rows go to CTAs as they free up; CTA b starts with row b, so that its
+  // first bound load waits on no claim. Claiming two ahead from the start
+  // fixed each CTA's rows when the launch began (on decode one CTA drew two
+  // of the longest rows, 480 KB against 194 KB on average): timed in turn,
+  // decode 25.4 -> 23.4 us, long 65.6 -> 63.3 us, decode_bf16 20.6 -> 20.4 us.
   const bool claim_late = MODE == kPipeUnsharded && a.split == 1 && a.queue != nullptr &&
                           !a.claim_ahead;
-  uint32_t first = 0;
-  if (claim_late && warp == NW + NR && lane == 0) first = atomicAdd(a.queue, 1u);
   if constexpr (MODE == kPipeUnsharded)
     if (a.lpt) longest_first_order<NW + NR + 1>(a, order, ring);
 
   if (claim_late && warp == NW + NR) {
     const uint32_t total = static_cast<uint32_t>(a.rows);
-    uint32_t u = __shfl_sync(0xffffffffu, first, 0);
+    uint32_t u = blockIdx.x;  // the grid never exceeds the rows
     uint32_t k = 0;
     int ok = 1;
     while (ok && u < total) {
