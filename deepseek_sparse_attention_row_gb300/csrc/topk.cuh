@@ -334,12 +334,23 @@ __device__ void topk_store(uint32_t* __restrict__ keys, int32_t nb, int32_t n_li
     // 2. Candidates: keys >= L (every key above -inf when K == total).
     const uint32_t thr = (static_cast<uint32_t>(K) == total) ? kKeyNegInf + 1u : max(L, kKeyNegInf + 1u);
     const uint32_t cap = static_cast<uint32_t>(max(kpad, kRankMax));
+    // One shared atomic per warp: ballots count the warp's candidates, lane 0
+    // reserves their slots, each lane writes at its prefix.
+    uint32_t bal[KR], wn = 0;
 #pragma unroll
     for (int i = 0; i < KR; ++i) {
-      if (kr[i] >= thr) {
-        const uint32_t pos = atomicAdd(&sh.count, 1u);
-        if (pos < cap) cand[pos] = pack_candidate(kr[i], tid + i * nthreads);
-      }
+      bal[i] = __ballot_sync(0xffffffffu, kr[i] >= thr);
+      wn += __popc(bal[i]);
+    }
+    uint32_t base = 0;
+    if (lane == 0 && wn) base = atomicAdd(&sh.count, wn);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < KR; ++i) {
+      const uint32_t pos = base + __popc(bal[i] & lt);
+      if (((bal[i] >> lane) & 1u) && pos < cap) cand[pos] = pack_candidate(kr[i], tid + i * nthreads);
+      base += __popc(bal[i]);
     }
     Sync::sync();
     const uint32_t n = sh.count;
