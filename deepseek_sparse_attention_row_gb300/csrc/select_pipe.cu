@@ -713,16 +713,17 @@ __device__ __forceinline__ void retire_queue(const PipeArgs& a) {
   }
 }
 
-// Longest rows first. With rows handed out by the unit counter, CTAs that
-// start on long rows and pick up short ones when they free up finish close
-// together (greedy list scheduling in longest-first order); in index order a
-// CTA can draw two of the longest rows while others idle. Every CTA computes
+// Longest rows first (on request; index order is the default, see
+// launch_coop_nw). With rows handed out by the unit counter, CTAs that start
+// on long rows and pick up short ones when they free up finish close
+// together (greedy list scheduling in longest-first order). Every CTA computes
 // the same order: a stable counting sort of the rows by window length, cut
 // into kLptClasses classes of width/(kLptClasses - 1) elements, longest class
 // first and row index ascending within a class. Warp w sorts a contiguous
 // range of 32-row chunks; __match_any_sync gives each lane its peers in the
-// same class. Scratch (per-warp class counts and the rows' classes) lives in
-// the ring, which no copy touches before the order is built.
+// same class. Scratch (per-warp class counts, the class starts and the rows'
+// classes) lives in the ring, which no copy touches before the order is
+// built.
 constexpr int kLptClasses = 128;
 constexpr int kLptMaxRows = 4096;
 
@@ -881,8 +882,6 @@ __global__ void __launch_bounds__((NW + kRankWarps + 1) * 32, NW == 4 ? 2 : 1)
     mbar_init_fence();
   }
   __syncthreads();
-  // With rows longest first, the producer claims its first row before the
-  // ordering pass, so that the claim's round trip overlaps the pass.
   // Whole unsharded rows from the unit counter: the producer claims a CTA's
   // next row only when the current row's last stage is due (the ring still
   // holds that row's last stages, which hides the claim's round trip), so
